@@ -1,0 +1,324 @@
+/*
+ * CPU oracle for the W4A16 group-quantized linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this library. The CUDA library never includes,
+ * links or calls anything here, and this file includes nothing of it.
+ *
+ * What it computes (plain loops, written for a reader to check by eye):
+ *   - the asymmetric per-group int4 rule named in compressed-tensors PR #269
+ *     "Some fixes for AWQ" (opening comment: alignment with AutoAWQ's
+ *     pseudo_quantize_tensor): s = (max - min)/15, z = round(-min/s),
+ *     q = clamp(round(w/s) + z, 0, 15);
+ *   - dequantization (q - z)*s, rounded once to fp16;
+ *   - the W4A16 product itself: fp16 inputs times int4-quantized weights
+ *     (same PR, the reply defining "w4a16"), accumulated here in fp64 with
+ *     the per-element magnitude sum used by the tolerance;
+ *   - the packed device layout (a format of this project, specified in the
+ *     public header's comment and restated below), and its inverse.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   R-round  every "round" is round-half-to-even (IEEE default);
+ *   R-s16    q and z use the stored fp16 scale s16 (converted to fp32), so the
+ *            triple (q, s16, z) is self-consistent;
+ *   R-eps    if s16 rounds to zero (constant or near-constant group), s16 is
+ *            replaced by RNE_fp16(1e-5);
+ *   R-zclamp z is clamped to [0, 15] (zeros are uint4);
+ *   R-dq     dequant = RNE_fp16((q - z) * s16): one rounding of an exact
+ *            product;
+ *   R-acc    fp64 accumulation, order free.
+ *
+ * Arithmetic rules: float operations below are IEEE binary32 with no
+ * contraction (built with -ffp-contract=off); fp16 conversions are written
+ * out from the binary16 definition, not taken from a compiler type.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------- */
+/* binary16 <-> binary64, from the IEEE 754 binary16 definition            */
+/* (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits).           */
+/* ---------------------------------------------------------------------- */
+
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* zero or subnormal */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);     /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest binary16, ties to even; overflow -> inf. */
+uint16_t oracle_double_to_half(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return 0x7e00;
+    if (isinf(a))
+        return sign | 0x7c00;
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);                  /* a in [2^(ex-1), 2^ex) */
+    int E = ex - 1;                 /* unbiased exponent of a */
+    if (E < -14)
+        E = -14;                    /* subnormal range: spacing 2^-24 */
+    double spacing = ldexp(1.0, E - 10);
+    double r = nearbyint(a / spacing);   /* exact scaling; ties to even */
+    double v = r * spacing;              /* the rounded magnitude */
+    if (v > 65504.0)                      /* beyond the largest finite half */
+        return sign | 0x7c00;
+    if (v < ldexp(1.0, -14))             /* subnormal (or zero) */
+        return sign | (uint16_t)(v / ldexp(1.0, -24));
+    frexp(v, &ex);
+    E = ex - 1;
+    uint16_t frac = (uint16_t)(v / ldexp(1.0, E - 10) - 1024.0);
+    return sign | (uint16_t)((E + 15) << 10) | frac;
+}
+
+void oracle_doubles_to_half(const double* x, size_t n, uint16_t* out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = oracle_double_to_half(x[i]);
+}
+
+void oracle_halves_to_double(const uint16_t* h, size_t n, double* out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = oracle_half_to_double(h[i]);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Quantization (offline step).                                            */
+/* W: float32 [K][N] row-major; group divides K; G = K / group.            */
+/* Outputs q u8 [K][N], s16 fp16 bits [G][N], z u8 [G][N].                 */
+/* ---------------------------------------------------------------------- */
+
+static float clamp_0_15(float v)
+{
+    if (!(v >= 0.0f))   /* also maps NaN to 0 */
+        return 0.0f;
+    if (v > 15.0f)
+        return 15.0f;
+    return v;
+}
+
+void oracle_quantize(const float* W, int K, int N, int group,
+                     uint8_t* q, uint16_t* s16, uint8_t* z)
+{
+    const int G = K / group;
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        for (int j = 0; j < G; ++j) {
+            /* step 1: min and max over the group's k */
+            float mn = W[(size_t)(j * group) * N + n];
+            float mx = mn;
+            for (int k = j * group; k < (j + 1) * group; ++k) {
+                float w = W[(size_t)k * N + n];
+                if (w < mn) mn = w;
+                if (w > mx) mx = w;
+            }
+            /* step 2: s = (max - min) / 15 in fp32, stored as fp16 */
+            float range = mx - mn;
+            float s32 = range / 15.0f;
+            uint16_t sb = oracle_double_to_half((double)s32);
+            if ((sb & 0x7fff) == 0)                       /* R-eps */
+                sb = oracle_double_to_half((double)1e-5f);
+            float s = (float)oracle_half_to_double(sb);   /* R-s16 */
+            /* step 3: z = clamp(round(-min / s), 0, 15) */
+            float zf = clamp_0_15(nearbyintf(-mn / s));
+            /* step 4: q = clamp(round(w / s) + z, 0, 15) */
+            for (int k = j * group; k < (j + 1) * group; ++k) {
+                float w = W[(size_t)k * N + n];
+                float qf = clamp_0_15(nearbyintf(w / s) + zf);
+                q[(size_t)k * N + n] = (uint8_t)qf;
+            }
+            s16[(size_t)j * N + n] = sb;
+            z[(size_t)j * N + n] = (uint8_t)zf;
+        }
+    }
+}
+
+/* deq[k][n] = RNE_fp16((q - z) * s16), one rounding of the exact product. */
+void oracle_dequantize(const uint8_t* q, const uint16_t* s16, const uint8_t* z,
+                       int K, int N, int group, uint16_t* deq)
+{
+    #pragma omp parallel for schedule(static)
+    for (int k = 0; k < K; ++k) {
+        int j = k / group;
+        for (int n = 0; n < N; ++n) {
+            int d = (int)q[(size_t)k * N + n] - (int)z[(size_t)j * N + n];
+            double s = oracle_half_to_double(s16[(size_t)j * N + n]);
+            deq[(size_t)k * N + n] = oracle_double_to_half((double)d * s);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* The product.  A: fp16 bits [M][K]; B: fp16 bits [K][N] (the dequantized */
+/* weights).  y[m][n] = sum_k a[m][k]*b[k][n] in fp64, and                 */
+/* mag[m][n] = sum_k |a[m][k]*b[k][n]| (the tolerance's magnitude term).   */
+/* ---------------------------------------------------------------------- */
+
+static double half_table[65536];
+static int half_table_ready = 0;
+
+/* Value of every binary16 pattern, computed once from the definition. */
+static void fill_half_table(void)
+{
+    if (half_table_ready)
+        return;
+    #pragma omp critical(oracle_half_table)
+    {
+        if (!half_table_ready) {
+            for (int h = 0; h < 65536; ++h)
+                half_table[h] = oracle_half_to_double((uint16_t)h);
+            half_table_ready = 1;
+        }
+    }
+}
+
+void oracle_matmul(const uint16_t* A, const uint16_t* B, int M, int N, int K,
+                   double* y, double* mag)
+{
+    enum { NC = 64 };
+    fill_half_table();
+    /* Each (m, n) is the sum over k = 0, 1, ..., K-1 in that order; the n
+     * loop is innermost only so that rows of B are read contiguously. */
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int n0 = 0; n0 < N; n0 += NC) {
+        int n1 = n0 + NC < N ? n0 + NC : N;
+        double acc[NC], acc_abs[NC];
+        for (int m = 0; m < M; ++m) {
+            for (int n = n0; n < n1; ++n) {
+                acc[n - n0] = 0.0;
+                acc_abs[n - n0] = 0.0;
+            }
+            for (int k = 0; k < K; ++k) {
+                double a = half_table[A[(size_t)m * K + k]];
+                const uint16_t* brow = B + (size_t)k * N;
+                for (int n = n0; n < n1; ++n) {
+                    double p = a * half_table[brow[n]];
+                    acc[n - n0] += p;
+                    acc_abs[n - n0] += fabs(p);
+                }
+            }
+            for (int n = n0; n < n1; ++n) {
+                y[(size_t)m * N + n] = acc[n - n0];
+                mag[(size_t)m * N + n] = acc_abs[n - n0];
+            }
+        }
+    }
+}
+
+/* Tolerance check: ratio[i] = |y_gpu - y_ref| / (2^-9 * mag + 1e-3).      */
+/* Returns the maximum ratio; an element passes when its ratio is <= 1.    */
+double oracle_check(const uint16_t* y_gpu, const double* y_ref, const double* mag,
+                    size_t count, size_t* worst_index)
+{
+    double worst = 0.0;
+    size_t wi = 0;
+    for (size_t i = 0; i < count; ++i) {
+        double g = oracle_half_to_double(y_gpu[i]);
+        double bound = ldexp(mag[i], -9) + 1e-3;
+        double r = fabs(g - y_ref[i]) / bound;
+        if (!(r <= worst)) {    /* NaN propagates as the worst */
+            worst = r;
+            wi = i;
+            if (isnan(r))
+                break;
+        }
+    }
+    if (worst_index)
+        *worst_index = wi;
+    return worst;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Packed device layout (format of this project).                           */
+/*                                                                          */
+/* Weights: uint32 words, 8 nibbles each.  Columns are grouped in strips of */
+/* 16 (strip j = columns 16j..16j+15), K in atoms of 64 (atom a = k in      */
+/* [64a, 64a+64)).  Word offset = (j*(K/64) + a)*128 + 4*L + i, where       */
+/* L in [0,32) and i in [0,4); with g = L>>2, t = L&3, s = i>>1, r = i&1    */
+/* the word holds column n = 16j + g + 8r and the 8 values k = 64a + 32s +  */
+/* 8t + e, e = 0..7.  Value e sits in nibble p (bits 4p..4p+3) with         */
+/* p = e/2 for even e and p = 4 + (e-1)/2 for odd e.                        */
+/* Scales: fp16 at offset (j*G + grp)*16 + c for column 16j + c.            */
+/* Zeros: uint32 at offset (j*G + grp)*2 + h; nibble c holds the zero of    */
+/* column 16j + 8h + c.                                                     */
+/* ---------------------------------------------------------------------- */
+
+static int nibble_of(int e)
+{
+    return (e % 2 == 0) ? e / 2 : 4 + (e - 1) / 2;
+}
+
+static size_t word_offset(int K, int n, int k)
+{
+    int j = n / 16, c = n % 16;
+    int a = k / 64, kk = k % 64;
+    int s = kk / 32, t = (kk % 32) / 8;
+    int g = c % 8, r = c / 8;
+    int L = 4 * g + t, i = 2 * s + r;
+    return ((size_t)j * (K / 64) + a) * 128 + 4 * L + i;
+}
+
+void oracle_pack(const uint8_t* q, const uint8_t* z, const uint16_t* s16,
+                 int K, int N, int group, uint32_t* Wp, uint16_t* Sp, uint32_t* Zp)
+{
+    const int G = K / group;
+    memset(Wp, 0, (size_t)K * N / 2);
+    memset(Zp, 0, (size_t)G * N / 2);
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) {
+            uint32_t v = q[(size_t)k * N + n] & 15u;
+            Wp[word_offset(K, n, k)] |= v << (4 * nibble_of(k % 8));
+        }
+    for (int grp = 0; grp < G; ++grp)
+        for (int n = 0; n < N; ++n) {
+            int j = n / 16, c = n % 16;
+            Sp[((size_t)j * G + grp) * 16 + c] = s16[(size_t)grp * N + n];
+            uint32_t v = z[(size_t)grp * N + n] & 15u;
+            Zp[((size_t)j * G + grp) * 2 + c / 8] |= v << (4 * (c % 8));
+        }
+}
+
+void oracle_unpack(const uint32_t* Wp, const uint16_t* Sp, const uint32_t* Zp,
+                   int K, int N, int group, uint8_t* q, uint16_t* s16, uint8_t* z)
+{
+    const int G = K / group;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n)
+            q[(size_t)k * N + n] =
+                (uint8_t)((Wp[word_offset(K, n, k)] >> (4 * nibble_of(k % 8))) & 15u);
+    for (int grp = 0; grp < G; ++grp)
+        for (int n = 0; n < N; ++n) {
+            int j = n / 16, c = n % 16;
+            s16[(size_t)grp * N + n] = Sp[((size_t)j * G + grp) * 16 + c];
+            z[(size_t)grp * N + n] =
+                (uint8_t)((Zp[((size_t)j * G + grp) * 2 + c / 8] >> (4 * (c % 8))) & 15u);
+        }
+}
+
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,289 @@
+"""Pins for the CPU oracle, each against something other than the oracle.
+
+Sources of truth used here: the IEEE binary16 format (numpy's independent
+conversion), a hand-worked example (tests/golden), exact rational arithmetic
+(fractions), numpy's float64 matmul, closed forms on the int4 grid, and the
+layout text of the packed format re-implemented in this file.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            out[key] = vals
+    return out
+
+
+# --------------------------------------------------------------- binary16
+
+def test_from_half_all_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.from_half(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_to_half_matches_numpy_rounding():
+    rng = np.random.default_rng(1)
+    # random magnitudes over the whole fp16 range, subnormals and overflow
+    x = np.concatenate([
+        rng.standard_normal(20000) * np.exp2(rng.uniform(-30, 17, 20000)),
+        rng.uniform(-1e-7, 1e-7, 2000),
+        np.array([65504.0, 65519.99, 65520.0, -65520.0, 1e6, 0.0, -0.0,
+                  2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26]),
+    ])
+    # exact midpoints between adjacent halves: ties must go to even
+    h = rng.integers(0, 0x7bff, 5000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    x = np.concatenate([x, (lo + hi) / 2, -(lo + hi) / 2])
+    ours = oracle.to_half(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# --------------------------------------------------------------- worked example
+
+def test_worked_example_group_of_8():
+    g = _read_golden("quant_group8_worked.txt")
+    w = np.array([float(v) for v in g["w"]], np.float32).reshape(8, 1)
+    q, s, z = oracle.quantize(w, 8)
+    assert s[0, 0] == int(g["s16_bits"][0], 16)
+    assert oracle.from_half(s)[0, 0] == float(g["s16"][0])
+    assert z[0, 0] == int(g["z"][0])
+    assert q[:, 0].tolist() == [int(v) for v in g["q"]]
+    deq = oracle.from_half(oracle.dequantize(q, s, z, 8))[:, 0]
+    assert deq.tolist() == [float(v) for v in g["deq"]]
+    a = np.array([float(v) for v in g["a"]], np.float16).reshape(1, 8)
+    y, mag = oracle.reference(a, q, s, z, 8)
+    assert y[0, 0] == float(g["y"][0])
+    assert mag[0, 0] == float(g["mag"][0])
+
+
+# --------------------------------------------------------------- quantizer
+
+def _grid_weights(K, N, group, seed):
+    q, s, z = synthetic.grid_group_values(K, N, group, seed)
+    G = K // group
+    s64 = s.view(np.float16).astype(np.float64)
+    qi = q.astype(np.int64)
+    zi = np.repeat(z.astype(np.int64), group, axis=0)
+    w = (qi - zi) * np.repeat(s64, group, axis=0)      # exact: <= 15 bits
+    w32 = w.astype(np.float32)
+    assert np.array_equal(w32.astype(np.float64), w)
+    return w32, q, s, z, G
+
+
+@pytest.mark.parametrize("K,N,group", [(256, 32, 128), (128, 16, 32), (192, 8, 64),
+                                       (256, 24, 256), (64, 5, 8)])
+def test_grid_weights_round_trip_exactly(K, N, group):
+    w, q, s, z, _ = _grid_weights(K, N, group, seed=K + N + group)
+    q2, s2, z2 = oracle.quantize(w, group)
+    assert np.array_equal(s2, s)
+    assert np.array_equal(z2, z)
+    assert np.array_equal(q2, q)
+    # (q - z)*s16 is exact in fp32 (at most 15 significant bits); its fp16
+    # rounding is what dequantization must return
+    deq = oracle.dequantize(q2, s2, z2, group)
+    assert np.array_equal(deq, w.astype(np.float16).view(np.uint16))
+
+
+def test_quantize_error_bound_random_weights():
+    K, N, group = 1024, 96, 128
+    w = synthetic.small_weights(K, N, seed=3)
+    q, s, z = oracle.quantize(w, group)
+    G = K // group
+    wg = w.reshape(G, group, N)
+    mn, mx = wg.min(axis=1), wg.max(axis=1)
+    assert np.all(mn <= 0) and np.all(mx >= 0)
+    s32 = ((mx - mn) / np.float32(15)).astype(np.float64)
+    s16 = oracle.from_half(s)
+    assert np.all(np.abs(s16 - s32) <= s32 * 2.0 ** -11)       # one fp16 rounding
+    assert np.all((z >= 0) & (z <= 15)) and np.all(q <= 15)
+    recon = (q.astype(np.float64).reshape(G, group, N) - z[:, None, :]) * s16[:, None, :]
+    err = np.abs(wg - recon)
+    bound = 0.5 * s16 + 15 * np.abs(s32 - s16) + 2.0 ** -20 * s16
+    assert np.all(err <= bound[:, None, :])
+    # the max element of each group maps to q=15 or its neighbour, the min to q=0 or 1
+    deq = oracle.from_half(oracle.dequantize(q, s, z, group)).reshape(G, group, N)
+    exact = recon
+    ulp_half = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -14))) - 11)
+    assert np.all(np.abs(deq - exact) <= ulp_half)
+
+
+def test_groups_are_independent():
+    """Quantizing [W1; W2] with group g equals quantizing W1 and W2 alone."""
+    w = synthetic.small_weights(384, 40, seed=4)
+    q, s, z = oracle.quantize(w, 128)
+    for j in range(3):
+        qj, sj, zj = oracle.quantize(w[128 * j:128 * (j + 1)], 128)
+        assert np.array_equal(q[128 * j:128 * (j + 1)], qj)
+        assert np.array_equal(s[j:j + 1], sj)
+        assert np.array_equal(z[j:j + 1], zj)
+
+
+def test_constant_group_uses_floor_scale():
+    w = np.zeros((128, 16), np.float32)
+    w[:, 3] = 0.25
+    w[:, 4] = -0.125
+    q, s, z = oracle.quantize(w, 128)
+    floor_bits = np.array([1e-5], np.float64).astype(np.float16).view(np.uint16)[0]
+    assert np.all(s == floor_bits)
+    assert np.all(z[0, [0, 1, 2, 5]] == 0) and np.all(q[:, 0] == 0)
+    # a positive constant is clipped at 15*s (z clamps to 0), a negative one at 0*s
+    assert np.all(q[:, 3] == 15) and z[0, 3] == 0
+    assert np.all(q[:, 4] == 0) and z[0, 4] == 15
+
+
+# --------------------------------------------------------------- matmul
+
+def _exact_dot(a, b):
+    acc = Fraction(0)
+    mag = Fraction(0)
+    for x, y in zip(a, b):
+        p = Fraction(float(x)) * Fraction(float(y))
+        acc += p
+        mag += abs(p)
+    return acc, mag
+
+
+def test_matmul_brute_force_tiny():
+    rng = np.random.default_rng(5)
+    for (M, K, N) in [(1, 1, 1), (2, 3, 4), (3, 8, 5), (4, 17, 3)]:
+        A = rng.standard_normal((M, K)).astype(np.float16)
+        B = (rng.standard_normal((K, N)) * 0.1).astype(np.float16)
+        y, mag = oracle.matmul(A, B)
+        for m in range(M):
+            for n in range(N):
+                ex, exm = _exact_dot(A[m], B[:, n])
+                assert abs(y[m, n] - float(ex)) <= 1e-13 * float(exm) + 1e-300
+                assert abs(mag[m, n] - float(exm)) <= 1e-13 * float(exm)
+
+
+def test_matmul_matches_numpy_float64():
+    A = synthetic.small_activations(5, 300, seed=6)
+    B = (np.random.default_rng(7).standard_normal((300, 70)) * 0.02).astype(np.float16)
+    y, mag = oracle.matmul(A, B)
+    ref = A.astype(np.float64) @ B.astype(np.float64)
+    refmag = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))
+    assert np.allclose(y, ref, rtol=0, atol=1e-12 * refmag.max())
+    assert np.allclose(mag, refmag, rtol=1e-12, atol=0)
+
+
+def test_integer_closed_form():
+    """s = 1, z = 8 and small integer activations give an exact integer product."""
+    K, N, M, group = 256, 24, 3, 128
+    rng = np.random.default_rng(8)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 0x3C00, np.uint16)          # 1.0
+    A = rng.integers(-4, 5, (M, K)).astype(np.float16)
+    y, _ = oracle.reference(A, q, s, z, group)
+    exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.array_equal(y, exact.astype(np.float64))
+
+
+def test_zero_when_codes_equal_zero_points():
+    K, N, group = 256, 16, 128
+    z = np.random.default_rng(9).integers(0, 16, (K // group, N)).astype(np.uint8)
+    q = np.repeat(z, group, axis=0)
+    s = np.full(z.shape, 0x2A66, np.uint16)
+    A = synthetic.small_activations(4, K, seed=9)
+    y, mag = oracle.reference(A, q, s, z, group)
+    assert np.all(y == 0) and np.all(mag == 0)
+
+
+def test_linear_in_activations():
+    K, N, group = 256, 32, 128
+    w = synthetic.small_weights(K, N, seed=10)
+    q, s, z = oracle.quantize(w, group)
+    rng = np.random.default_rng(11)
+    A1 = rng.integers(-8, 9, (2, K)).astype(np.float16)
+    A2 = rng.integers(-8, 9, (2, K)).astype(np.float16)
+    y1, m1 = oracle.reference(A1, q, s, z, group)
+    y2, m2 = oracle.reference(A2, q, s, z, group)
+    y12, _ = oracle.reference((A1.astype(np.float32) + A2).astype(np.float16), q, s, z, group)
+    assert np.allclose(y12, y1 + y2, rtol=0, atol=1e-12 * (m1 + m2).max())
+
+
+def test_check_accepts_rounded_reference_and_rejects_errors():
+    K, N, group = 256, 32, 128
+    q, s, z = oracle.quantize(synthetic.small_weights(K, N, seed=12), group)
+    A = synthetic.small_activations(3, K, seed=12)
+    y, mag = oracle.reference(A, q, s, z, group)
+    Y = oracle.to_half(y)
+    r, _ = oracle.check(Y, y, mag)
+    assert r <= 0.5
+    bad = Y.copy()
+    bad[1, 5] = oracle.to_half(oracle.from_half(bad[1, 5]) + 0.01 * mag[1, 5] + 0.01)
+    r, i = oracle.check(bad, y, mag)
+    assert r > 1 and i == 1 * N + 5
+
+
+# --------------------------------------------------------------- packed layout
+
+def _spec_decode(Wp, K, N):
+    """Decode q[k][n] from the packed words using the layout text alone."""
+    q = np.empty((K, N), np.uint8)
+    natoms = K // 64
+    for n in range(N):
+        j, c = divmod(n, 16)
+        g, r = c % 8, c // 8
+        for k in range(K):
+            a, kk = divmod(k, 64)
+            s_, rem = divmod(kk, 32)
+            t, e = divmod(rem, 8)
+            word = (j * natoms + a) * 128 + 4 * (4 * g + t) + 2 * s_ + r
+            p = e // 2 if e % 2 == 0 else 4 + (e - 1) // 2
+            q[k, n] = (int(Wp[word]) >> (4 * p)) & 15
+    return q
+
+
+def test_pack_single_nibble_position():
+    K, N = 64, 16
+    q = np.zeros((K, N), np.uint8)
+    q[9, 3] = 0xA          # atom 0, s=0, t=1, e=1 -> nibble 4; g=3, r=0 -> lane 13, i=0
+    z = np.zeros((1, N), np.uint8)
+    z[0, 11] = 0x7         # h=1, c=3 -> word 1, nibble 3
+    s = np.zeros((1, N), np.uint16)
+    s[0, 11] = 0x1234
+    Wp, Sp, Zp = oracle.pack(q, z, s, 64)
+    expect = np.zeros(K * N // 8, np.uint32)
+    expect[4 * 13 + 0] = 0xA << 16
+    assert np.array_equal(Wp, expect)
+    assert Zp.tolist() == [0, 0x7 << 12]
+    assert Sp[11] == 0x1234 and np.count_nonzero(Sp) == 1
+
+
+@pytest.mark.parametrize("K,N,group", [(128, 32, 128), (192, 48, 64), (256, 16, 256)])
+def test_pack_follows_layout_text_and_round_trips(K, N, group):
+    q, s, z = synthetic.random_codes(K, N, group, seed=K + N)
+    Wp, Sp, Zp = oracle.pack(q, z, s, group)
+    assert np.array_equal(_spec_decode(Wp, K, N), q)
+    G = K // group
+    for n in range(N):
+        j, c = divmod(n, 16)
+        for grp in range(G):
+            assert Sp[(j * G + grp) * 16 + c] == s[grp, n]
+            word = int(Zp[(j * G + grp) * 2 + c // 8])
+            assert (word >> (4 * (c % 8))) & 15 == z[grp, n]
+    q2, s2, z2 = oracle.unpack(Wp, Sp, Zp, K, N, group)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s) and np.array_equal(z2, z)
