@@ -1,0 +1,213 @@
+"""GB300 (sm_103a) W4A16 group-quantized linear layer: Python binding.
+
+A thin ctypes layer over the C ABI in include/w4a16.h (libw4a16.so, built
+in-tree by ``build.build()``). PyTorch supplies device memory and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels. There is no fallback: if the library is missing or a call
+fails, an exception is raised.
+
+The operation (compressed-tensors PR #269 "Some fixes for AWQ", reply
+defining w4a16): Y[M,N] fp16 = A[M,K] fp16 . dequant(W)[K,N], with W
+quantized asymmetrically per group of `group` input channels (the AWQ-g128
+format of vLLM PR #1032 "Implement AWQ quantization support for LLaMA").
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from .build import LIB as LIB_PATH
+
+PATH_AUTO, PATH_DECODE, PATH_TENSOR = 0, 1, 2
+_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR}
+
+ERRORS = {
+    -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
+    -4: "WORKSPACE_TOO_SMALL", -5: "CUDA_ERROR", -6: "DEVICE_CHECK",
+}
+
+# every symbol declared in include/w4a16.h, with its ctypes signature
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_PSZ = ctypes.POINTER(ctypes.c_size_t)
+_PI = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "w4a16_last_error": (ctypes.c_char_p, []),
+    "w4a16_version": (_I, []),
+    "w4a16_packed_sizes": (_I, [_I, _I, _I, _PSZ, _PSZ, _PSZ]),
+    "w4a16_quantize": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
+    "w4a16_pack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "w4a16_unpack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "w4a16_dequantize": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "w4a16_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
+    "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _I, _I, _P]),
+    "w4a16_plan": (_I, [_I, _I, _I, _I, _PI, _PI]),
+    "w4a16_device_status": (_I, [_P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, code: int, where: str, message: str):
+        self.code = code
+        super().__init__(f"{where}: {ERRORS.get(code, code)}: {message}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libw4a16.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m bit_weight_only_g128_gb300.build` (needs nvcc)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        msg = lib().w4a16_last_error().decode(errors="replace")
+        raise W4A16Error(rc, where, msg)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+@dataclasses.dataclass
+class PackedWeight:
+    """Packed int4 weight of one linear layer, resident on the device."""
+    Wq: torch.Tensor       # int32 [K*N/8]
+    Sp: torch.Tensor       # float16 [K/group * N]
+    Zp: torch.Tensor       # int32 [K/group * N / 8]
+    K: int
+    N: int
+    group: int
+
+    @property
+    def nbytes(self) -> int:
+        return self.Wq.numel() * 4 + self.Sp.numel() * 2 + self.Zp.numel() * 4
+
+
+def packed_sizes(K: int, N: int, group: int) -> Tuple[int, int, int]:
+    w, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().w4a16_packed_sizes(K, N, group, ctypes.byref(w), ctypes.byref(s),
+                                    ctypes.byref(z)), "w4a16_packed_sizes")
+    return w.value, s.value, z.value
+
+
+def quantize(W: torch.Tensor, group: int, stream=None):
+    """fp32 W [K, N] (device) -> (q uint8 [K,N], s fp16 [G,N], z uint8 [G,N])."""
+    K, N = W.shape
+    G = K // group if group > 0 else 0
+    q = torch.empty((K, N), dtype=torch.uint8, device=W.device)
+    s = torch.empty((G, N), dtype=torch.float16, device=W.device)
+    z = torch.empty((G, N), dtype=torch.uint8, device=W.device)
+    _check(lib().w4a16_quantize(_dev(W, torch.float32, "W"), K, N, group, q.data_ptr(),
+                                s.data_ptr(), z.data_ptr(), _stream(stream)), "w4a16_quantize")
+    return q, s, z
+
+
+def pack(q: torch.Tensor, s: torch.Tensor, z: torch.Tensor, group: int, stream=None) -> PackedWeight:
+    """Interchange (q, s, z) -> PackedWeight in the library's device layout."""
+    K, N = q.shape
+    wb, sb, zb = packed_sizes(K, N, group)
+    dev = q.device
+    Wq = torch.empty(wb // 4, dtype=torch.int32, device=dev)
+    Sp = torch.empty(sb // 2, dtype=torch.float16, device=dev)
+    Zp = torch.empty(zb // 4, dtype=torch.int32, device=dev)
+    _check(lib().w4a16_pack(_dev(q, torch.uint8, "q"), _dev(s, torch.float16, "s"),
+                            _dev(z, torch.uint8, "z"), K, N, group, Wq.data_ptr(),
+                            Sp.data_ptr(), Zp.data_ptr(), _stream(stream)), "w4a16_pack")
+    return PackedWeight(Wq, Sp, Zp, K, N, group)
+
+
+def quantize_pack(W: torch.Tensor, group: int, stream=None) -> PackedWeight:
+    q, s, z = quantize(W, group, stream)
+    return pack(q, s, z, group, stream)
+
+
+def unpack(pw: PackedWeight, stream=None):
+    dev = pw.Wq.device
+    G = pw.K // pw.group
+    q = torch.empty((pw.K, pw.N), dtype=torch.uint8, device=dev)
+    s = torch.empty((G, pw.N), dtype=torch.float16, device=dev)
+    z = torch.empty((G, pw.N), dtype=torch.uint8, device=dev)
+    _check(lib().w4a16_unpack(pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(), pw.K, pw.N,
+                              pw.group, q.data_ptr(), s.data_ptr(), z.data_ptr(),
+                              _stream(stream)), "w4a16_unpack")
+    return q, s, z
+
+
+def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
+    deq = torch.empty((pw.K, pw.N), dtype=torch.float16, device=pw.Wq.device)
+    _check(lib().w4a16_dequantize(pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(), pw.K,
+                                  pw.N, pw.group, deq.data_ptr(), _stream(stream)),
+           "w4a16_dequantize")
+    return deq
+
+
+def workspace_size(M: int, N: int, K: int, group: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().w4a16_workspace_size(M, N, K, group, ctypes.byref(b)), "w4a16_workspace_size")
+    return b.value
+
+
+def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
+    p, s = ctypes.c_int(), ctypes.c_int()
+    _check(lib().w4a16_plan(M, N, K, group, ctypes.byref(p), ctypes.byref(s)), "w4a16_plan")
+    return {v: k for k, v in _PATHS.items()}[p.value], s.value
+
+
+def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
+         path: str = "auto", split: int = 0, workspace: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream."""
+    M, K = A.shape
+    if K != pw.K:
+        raise ValueError(f"A has K={K}, weight has K={pw.K}")
+    if out is None:
+        out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
+    ws_ptr, ws_bytes = None, 0
+    need = workspace_size(M, pw.N, pw.K, pw.group)
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
+                               pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
+                               _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
+                               _PATHS[path], split, _stream(stream)), "w4a16_gemm")
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronize and raise if a kernel reported an error on the device."""
+    _check(lib().w4a16_device_status(_stream(stream)), "w4a16_device_status")

@@ -1,0 +1,224 @@
+// C ABI of the W4A16 library: argument checks, path choice, launches.
+// Declarations and the contract of every entry point: include/w4a16.h.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+
+__device__ int g_device_error = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int ok() {
+  t_last_error.clear();
+  return W4A16_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxDim = 1 << 20;
+
+// Shape rules shared by every entry point that takes K, N, group.
+int check_kn(int K, int N, int group) {
+  if (K <= 0 || N <= 0 || group <= 0)
+    return fail(W4A16_ERR_INVALID_ARG, "K=%d, N=%d, group=%d must be positive", K, N, group);
+  if (K > kMaxDim || N > kMaxDim)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "K=%d or N=%d above %d", K, N, kMaxDim);
+  if (N % kStripCols)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 16", N);
+  if (K % kAtomK) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", K);
+  if (group % kAtomK)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "group=%d is not a multiple of 64", group);
+  if (K % group) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "group=%d does not divide K=%d", group, K);
+  return W4A16_OK;
+}
+
+// SM count of the current device (cached per device; 148 if unknown).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 148;
+  if (dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+// Split of K for the decode kernel: enough CTAs to cover every SM about
+// twice, while each warp keeps at least 8 atoms (4 KiB of weights per warp).
+int decode_split(int N, int K) {
+  const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
+  const int natoms = K / kAtomK;
+  const int target = 2 * sm_count();
+  int split = 1;
+  while (split < kDecodeMaxSplit && nblk * split < target && natoms / (2 * split) >= 8) split *= 2;
+  return split;
+}
+
+int choose_path(int M) { return W4A16_PATH_DECODE; (void)M; }
+
+int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
+              const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
+              void* workspace, size_t workspace_bytes, int path, int split,
+              cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
+  if (M > kMaxDim) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "M=%d above %d", M, kMaxDim);
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (M == 0) return ok();
+  if (!A || !Wq || !scales || !zeros || !Y)
+    return fail(W4A16_ERR_INVALID_ARG, "null pointer (A=%p Wq=%p scales=%p zeros=%p Y=%p)", A, Wq,
+                scales, zeros, Y);
+  if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(scales, 16) || !aligned(Y, 16) ||
+      !aligned(zeros, 8))
+    return fail(W4A16_ERR_MISALIGNED,
+                "alignment: A, Wq, scales, Y need 16 bytes and zeros 8 bytes");
+  if (path == W4A16_PATH_AUTO) path = choose_path(M);
+  if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+  if (path == W4A16_PATH_TENSOR)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "tensor-core path not available in this build");
+  if (split < 0 || split > kDecodeMaxSplit)
+    return fail(W4A16_ERR_INVALID_ARG, "split=%d outside 0..%d", split, kDecodeMaxSplit);
+  if (split == 0) split = decode_split(N, K);
+  if (split > K / kAtomK)
+    return fail(W4A16_ERR_INVALID_ARG, "split=%d exceeds the %d atoms of K", split, K / kAtomK);
+  // 16 rows per launch; larger M re-streams the weights once per 16 rows
+  for (int r0 = 0; r0 < M; r0 += 16) {
+    const int rows = M - r0 < 16 ? M - r0 : 16;
+    cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N,
+                                  rows, N, K, group, split, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
+  return ok();
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char* w4a16_last_error(void) { return t_last_error.c_str(); }
+
+int w4a16_version(void) { return 100; }
+
+int w4a16_packed_sizes(int K, int N, int group, size_t* wq_bytes, size_t* sp_bytes,
+                       size_t* zp_bytes) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!wq_bytes || !sp_bytes || !zp_bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  const size_t G = (size_t)(K / group);
+  *wq_bytes = (size_t)K * N / 2;
+  *sp_bytes = 2 * G * N;
+  *zp_bytes = G * N / 2;
+  return ok();
+}
+
+int w4a16_quantize(const float* W, int K, int N, int group, uint8_t* q, uint16_t* s, uint8_t* z,
+                   void* stream) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!W || !q || !s || !z) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  cudaError_t e = launch_quantize(W, K, N, group, q, s, z, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
+  return ok();
+}
+
+int w4a16_pack(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K, int N, int group,
+               uint32_t* Wq, uint16_t* Sp, uint32_t* Zp, void* stream) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!q || !s || !z || !Wq || !Sp || !Zp) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(Wq, 16) || !aligned(Sp, 16) || !aligned(Zp, 8))
+    return fail(W4A16_ERR_MISALIGNED, "alignment: Wq, Sp need 16 bytes and Zp 8 bytes");
+  cudaError_t e = launch_pack(q, s, z, K, N, group, Wq, Sp, Zp, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
+  return ok();
+}
+
+int w4a16_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K, int N,
+                 int group, uint8_t* q, uint16_t* s, uint8_t* z, void* stream) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!q || !s || !z || !Wq || !Sp || !Zp) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  cudaError_t e = launch_unpack(Wq, Sp, Zp, K, N, group, q, s, z, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "unpack kernel launch");
+  return ok();
+}
+
+int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K, int N,
+                     int group, uint16_t* deq, void* stream) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!Wq || !Sp || !Zp || !deq) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  cudaError_t e = launch_dequantize(Wq, Sp, Zp, K, N, group, deq, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel launch");
+  return ok();
+}
+
+int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes) {
+  if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  *bytes = 0;
+  return ok();
+}
+
+int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales, const uint32_t* zeros,
+               int M, int N, int K, int group, uint16_t* Y, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  return gemm_impl(A, Wq, scales, zeros, M, N, K, group, Y, workspace, workspace_bytes,
+                   W4A16_PATH_AUTO, 0, (cudaStream_t)stream);
+}
+
+int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
+                  const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
+                  void* workspace, size_t workspace_bytes, int path, int split, void* stream) {
+  return gemm_impl(A, Wq, scales, zeros, M, N, K, group, Y, workspace, workspace_bytes, path,
+                   split, (cudaStream_t)stream);
+}
+
+int w4a16_plan(int M, int N, int K, int group, int* path, int* split) {
+  if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!path || !split) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  *path = choose_path(M);
+  *split = decode_split(N, K);
+  return ok();
+}
+
+int w4a16_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int flag = 0;
+  e = cudaMemcpyFromSymbol(&flag, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (flag != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return fail(W4A16_ERR_DEVICE_CHECK, "device error word = 0x%08x", flag);
+  }
+  return ok();
+}
+
+}  // extern "C"

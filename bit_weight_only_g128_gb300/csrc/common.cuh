@@ -1,0 +1,107 @@
+// Device helpers shared by the W4A16 kernels (sm_103a).
+//
+// Packed format (see include/w4a16.h): a word holds 8 consecutive k of one
+// column with the codes of k-offsets 0,2,4,6 in nibbles 0..3 and 1,3,5,7 in
+// nibbles 4..7, so one mask pulls out the pair (2p, 2p+1) into the two fp16
+// halves of a register.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/w4a16.h"
+
+namespace w4a16 {
+
+constexpr int kStripCols = 16;   // columns per strip
+constexpr int kAtomK = 64;       // k per atom
+constexpr int kAtomWords = 128;  // 32-bit words per atom (16 * 64 / 8)
+
+// ------------------------------------------------------------------ fp16x2
+
+__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Per (group, column) constants of the dequantization of one column.
+struct DeqConst {
+  uint32_t zb;    // fp16x2 (1024 + z): subtracted from (1024 + q)
+  uint32_t nzb4;  // fp16x2 -(64 + z): added to (1024 + 16 q)/16
+  uint32_t s2;    // fp16x2 (s, s)
+};
+
+__device__ __forceinline__ DeqConst make_deq_const(uint32_t z, uint16_t s_bits) {
+  DeqConst c;
+  c.zb = (0x6400u + z) * 0x00010001u;           // 1024 + z, exact (ulp 1)
+  c.nzb4 = (0xD400u + 16u * z) * 0x00010001u;   // -(64 + z), exact (ulp 1/16)
+  c.s2 = (uint32_t)s_bits * 0x00010001u;
+  return c;
+}
+
+// One packed word -> four fp16x2 values out[p] = (deq[2p], deq[2p+1]) with
+// deq = RNE_fp16((q - z) * s). The subtraction is exact (integers below
+// 2048 in fp16, or an fma whose exact result is the integer q - z), so the
+// multiply by s is the only rounding, as in the definition.
+__device__ __forceinline__ void dequant_word(uint32_t w, const DeqConst& c, uint32_t out[4]) {
+  const uint32_t kMagic = 0x64006400u;      // fp16x2 (1024, 1024)
+  const uint32_t kSixteenth = 0x2C002C00u;  // fp16x2 (1/16, 1/16)
+  const uint32_t w8 = w >> 8;
+  const uint32_t x0 = (w & 0x000F000Fu) | kMagic;    // 1024 + q0,    1024 + q1
+  const uint32_t x1 = (w & 0x00F000F0u) | kMagic;    // 1024 + 16 q2, 1024 + 16 q3
+  const uint32_t x2 = (w8 & 0x000F000Fu) | kMagic;   // 1024 + q4,    1024 + q5
+  const uint32_t x3 = (w8 & 0x00F000F0u) | kMagic;   // 1024 + 16 q6, 1024 + 16 q7
+  out[0] = hmul2_rn(hsub2_rn(x0, c.zb), c.s2);
+  out[1] = hmul2_rn(hfma2_rn(x1, kSixteenth, c.nzb4), c.s2);
+  out[2] = hmul2_rn(hsub2_rn(x2, c.zb), c.s2);
+  out[3] = hmul2_rn(hfma2_rn(x3, kSixteenth, c.nzb4), c.s2);
+}
+
+// ------------------------------------------------------------------ loads
+
+// Streaming 16-byte load of packed weights: read once, keep out of L1.
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// 16-byte load of activations, cached in L1 (shared by the CTA's warps).
+__device__ __forceinline__ uint4 ldg_keep(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ mma.sync
+
+// D (16x8 f32) += A (16x16 f16, row) * B (16x8 f16, col).
+__device__ __forceinline__ void mma_16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace w4a16

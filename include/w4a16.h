@@ -1,0 +1,144 @@
+/*
+ * w4a16.h - C ABI of the GB300 (sm_103a) W4A16 group-quantized linear layer.
+ *
+ * The operation (compressed-tensors PR #269 "Some fixes for AWQ", the reply
+ * defining w4a16): fp16 activations are multiplied by int4-quantized weights
+ * to give fp16 outputs. Weights are quantized asymmetrically per group of
+ * `group` consecutive input channels (128 in the "w4-g128" / "AWQ-g128"
+ * checkpoints of vLLM PR #1032 "Implement AWQ quantization support for LLaMA"
+ * and the lmdeploy issue #2274 tables; group == K is the per-channel variant)
+ * with the rule that PR #269 aligns with AutoAWQ's pseudo_quantize_tensor:
+ *     s = (max - min)/15,  z = round(-min/s),  q = clamp(round(w/s) + z, 0, 15),
+ * and are dequantized inside the kernels as (q - z)*s, rounded once to fp16.
+ * Products accumulate in fp32; Y is rounded to fp16 (ties to even).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *     owned by the caller. The library never allocates, frees or keeps device
+ *     memory, and never synchronizes: work is enqueued on `stream` (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream).
+ *   - fp16 values are passed as uint16_t bit patterns (IEEE binary16).
+ *   - Return value: W4A16_OK (0) or a negative W4A16_ERR_* code. On error no
+ *     kernel has been launched (except W4A16_ERR_CUDA, which reports a failed
+ *     launch), and w4a16_last_error() returns a message for the calling
+ *     thread. No C++ exception crosses this interface.
+ *   - Shapes: N % 16 == 0, K % 64 == 0, group % 64 == 0 and K % group == 0;
+ *     M >= 0 (M == 0 is a no-op). Other shapes return
+ *     W4A16_ERR_UNSUPPORTED_SHAPE. 1 <= N, K <= 1<<20 and M <= 1<<20.
+ *
+ * Interchange (logical) layouts, as in the transposed AWQ format quoted in
+ * vLLM PR #1032 (the Triton variant: qw (K/pack, N), scales (K/group, N),
+ * qzeros (K/group/pack, N)), unpacked to one byte per code here:
+ *     q     uint8  [K][N]   codes 0..15 (row k, column n)
+ *     s     fp16   [G][N]   scales, G = K / group
+ *     z     uint8  [G][N]   zero points 0..15
+ *     A     fp16   [M][K]   activations, row-major
+ *     Y     fp16   [M][N]   outputs, row-major
+ *
+ * Packed device layout (this library's own format; built by w4a16_pack):
+ *   Wq: uint32 words, K*N/8 of them, 8 codes per word. Columns form strips
+ *     of 16 (strip j = columns 16j..16j+15); K forms atoms of 64 (atom a =
+ *     k in [64a, 64a+64)). The word at offset (j*(K/64) + a)*128 + 4*L + i,
+ *     L in [0,32), i in [0,4), with g = L>>2, t = L&3, s = i>>1, r = i&1,
+ *     holds column n = 16j + g + 8r at k = 64a + 32s + 8t + e, e = 0..7;
+ *     code e sits in nibble p (bits 4p..4p+3), p = e/2 for even e and
+ *     p = 4 + (e-1)/2 for odd e. So (word >> 4p) & 0x000F000F holds the
+ *     codes of k-offsets (2p, 2p+1) in its two 16-bit halves, and each lane
+ *     L of a warp reads its four words of an atom with one 16-byte load.
+ *   Sp: fp16, N*G of them; offset (j*G + grp)*16 + c is the scale of
+ *     column 16j + c in group grp.
+ *   Zp: uint32, N*G/8 of them; offset (j*G + grp)*2 + h holds in nibble c
+ *     the zero point of column 16j + 8h + c in group grp.
+ *   Sizes: w4a16_packed_sizes(). Alignment: Wq, Sp, A and Y 16-byte aligned,
+ *   Zp 8-byte aligned (W4A16_ERR_MISALIGNED otherwise).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_OK 0
+#define W4A16_ERR_INVALID_ARG (-1)         /* null pointer, negative size  */
+#define W4A16_ERR_UNSUPPORTED_SHAPE (-2)   /* shape rules above violated   */
+#define W4A16_ERR_MISALIGNED (-3)          /* pointer alignment violated   */
+#define W4A16_ERR_WORKSPACE_TOO_SMALL (-4) /* workspace below the size query */
+#define W4A16_ERR_CUDA (-5)                /* CUDA runtime/launch failure  */
+#define W4A16_ERR_DEVICE_CHECK (-6)        /* a kernel reported an error   */
+
+/* Paths for w4a16_gemm_ex. */
+#define W4A16_PATH_AUTO 0
+#define W4A16_PATH_DECODE 1   /* split-K register-dequant GEMV, M <= 16 */
+#define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char* w4a16_last_error(void);
+
+/* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
+int w4a16_version(void);
+
+/* Byte sizes of the packed buffers for a K x N weight with group `group`:
+ * Wq = K*N/2, Sp = 2*N*(K/group), Zp = N*(K/group)/2. Host-only. */
+int w4a16_packed_sizes(int K, int N, int group,
+                       size_t* wq_bytes, size_t* sp_bytes, size_t* zp_bytes);
+
+/* Offline step: quantize fp32 W [K][N] per group along K with the rule
+ * above (R-eps: a scale that rounds to zero in fp16 is replaced by
+ * RNE_fp16(1e-5)). q/z must use the stored fp16 scale, all divisions and
+ * roundings are IEEE fp32 round-to-nearest-even. W must be finite.
+ * Outputs: q [K][N], s [G][N] (fp16 bits), z [G][N]. */
+int w4a16_quantize(const float* W, int K, int N, int group,
+                   uint8_t* q, uint16_t* s, uint8_t* z, void* stream);
+
+/* Offline step: interchange (q, s, z) -> packed (Wq, Sp, Zp), layout above.
+ * Codes and zero points above 15 keep only their low 4 bits. */
+int w4a16_pack(const uint8_t* q, const uint16_t* s, const uint8_t* z,
+               int K, int N, int group,
+               uint32_t* Wq, uint16_t* Sp, uint32_t* Zp, void* stream);
+
+/* Inverse of w4a16_pack (for checks and debugging). */
+int w4a16_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
+                 int K, int N, int group,
+                 uint8_t* q, uint16_t* s, uint8_t* z, void* stream);
+
+/* deq [K][N] fp16 = RNE_fp16((q - z)*s) computed from the packed buffers
+ * with the same device routine the GEMM kernels use (for checks). */
+int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
+                     int K, int N, int group, uint16_t* deq, void* stream);
+
+/* Scratch bytes w4a16_gemm needs for this problem (0 when none). Host-only. */
+int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
+
+/* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
+ * The path (decode GEMV or tensor-core GEMM) and its split of K are chosen
+ * from M, N, K and the device's SM count. `workspace` may be NULL when
+ * w4a16_workspace_size reports 0. Y must not overlap the inputs. */
+int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
+               const uint32_t* zeros, int M, int N, int K, int group,
+               uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* As w4a16_gemm with the path and split forced (0 = automatic choice).
+ * W4A16_PATH_DECODE needs M <= 16; split is the number of K ranges whose
+ * partial sums are reduced inside a thread-block cluster (1..8). */
+int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
+                  const uint32_t* zeros, int M, int N, int K, int group,
+                  uint16_t* Y, void* workspace, size_t workspace_bytes,
+                  int path, int split, void* stream);
+
+/* The path and split w4a16_gemm would use on the current device. Host-only. */
+int w4a16_plan(int M, int N, int K, int group, int* path, int* split);
+
+/* Synchronizes `stream`, then reads and clears the library's device error
+ * word (set by a kernel that gave up a bounded wait or failed a self-check).
+ * Returns W4A16_OK or W4A16_ERR_DEVICE_CHECK (message: which check, where). */
+int w4a16_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no kernel runs here, no GPU needed).
+
+The library must load, export every entry point declared in
+include/w4a16.h, and reject bad arguments on the host with the documented
+codes before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_weight_only_g128_gb300 as w4
+from bit_weight_only_g128_gb300 import build as wbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wbuild.build()
+    return w4.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("w4a16_pack", "w4a16_gemm", "w4a16_quantize", "w4a16_unpack",
+                 "w4a16_workspace_size", "w4a16_last_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_the_header():
+    assert sorted(w4.SIGNATURES) == declared_symbols()
+
+
+def test_header_compiles_as_c_and_cpp(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "w4a16.h"\nint main(void){return W4A16_OK;}\n')
+    import subprocess
+    for comp, ext in (("gcc", "c"), ("g++", "cpp")):
+        f = tmp_path / f"t.{ext}"
+        f.write_text(src.read_text())
+        subprocess.run([comp, "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-c", str(f), "-o", str(tmp_path / f"t_{ext}.o")], check=True)
+
+
+def test_packed_sizes(lib):
+    assert w4.packed_sizes(4096, 4096, 128) == (4096 * 4096 // 2, 2 * 32 * 4096, 32 * 4096 // 2)
+    assert w4.packed_sizes(8192, 64, 8192) == (8192 * 64 // 2, 2 * 64, 32)
+
+
+@pytest.mark.parametrize("K,N,group,code", [
+    (4096, 4096, 0, -1), (0, 16, 64, -1), (64, 0, 64, -1),
+    (4096, 4100, 128, -2), (4000, 4096, 128, -2), (4096, 4096, 96, -2),
+    (4096, 4096, 32, -2), (4096 + 64, 4096, 128, -2), (1 << 21, 16, 64, -2),
+])
+def test_shape_rules(lib, K, N, group, code):
+    w, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    rc = lib.w4a16_packed_sizes(K, N, group, ctypes.byref(w), ctypes.byref(s), ctypes.byref(z))
+    assert rc == code
+    assert lib.w4a16_last_error()
+
+
+def _gemm(lib, A=16, W=16, S=16, Z=16, Y=16, M=1, N=64, K=128, group=128, path=0, split=0):
+    # fake (never dereferenced) addresses: every failure below is decided on the host
+    return lib.w4a16_gemm_ex(A and 0x10000 + A % 16, W and 0x20000 + W % 16,
+                             S and 0x30000 + S % 16, Z and 0x40000 + Z % 16, M, N, K, group,
+                             Y and 0x50000 + Y % 16, None, 0, path, split, None)
+
+
+def test_gemm_argument_errors(lib):
+    assert _gemm(lib, A=0) == -1
+    assert _gemm(lib, Y=0) == -1
+    assert _gemm(lib, M=-1) == -1
+    assert _gemm(lib, N=40) == -2
+    assert _gemm(lib, K=100) == -2
+    assert _gemm(lib, group=48) == -2
+    assert _gemm(lib, A=2) == -3
+    assert _gemm(lib, Y=8) == -3
+    assert _gemm(lib, Z=4) == -3
+    assert _gemm(lib, path=7) == -1
+    assert _gemm(lib, split=9) == -1
+    assert _gemm(lib, M=17, path=1, split=4, K=128) == -1   # split above the 2 atoms of K
+
+
+def test_gemm_m_zero_is_a_noop(lib):
+    # M == 0 returns before any pointer is used or any kernel is launched
+    assert lib.w4a16_gemm(None, None, None, None, 0, 64, 128, 128, None, None, 0, None) == 0
+
+
+def test_workspace_size_is_zero(lib):
+    assert w4.workspace_size(16, 4096, 4096, 128) == 0

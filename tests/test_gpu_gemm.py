@@ -1,0 +1,91 @@
+"""GEMM parity: CUDA library vs CPU oracle, element by element.
+
+Tolerance (per element): |y - y_ref| <= 2^-9 * sum_k |a_k w_kn| + 1e-3, with
+y_ref the fp64 product of the same fp16 activations and the same
+fp16-dequantized weights. Shapes span several CTAs and ragged tails in N (at
+the 16-column granularity of the format), in M and in the K split.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_only_g128_gb300 as w4
+import oracle
+import synthetic
+from gpu_util import cuda, guarded_output, check_guard, half_bits, prepare, run_and_check
+
+pytestmark = pytest.mark.gpu
+
+DECODE_CASES = [
+    # M, K, N, group, split
+    (1, 64, 16, 64, 1),
+    (1, 128, 16, 128, 2),
+    (3, 256, 48, 128, 0),
+    (8, 512, 144, 128, 4),
+    (9, 640, 272, 64, 3),
+    (16, 1024, 256, 1024, 8),
+    (16, 4096, 512, 128, 0),
+    (2, 4096, 4096, 128, 0),
+    (5, 896, 160, 128, 8),
+    (7, 1280, 400, 128, 5),
+    (12, 2048, 1040, 2048, 2),
+    (4, 11008, 256, 128, 0),
+]
+
+
+@pytest.mark.parametrize("M,K,N,group,split", DECODE_CASES)
+def test_decode_path(M, K, N, group, split):
+    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", split=split)
+
+
+@pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (16, 4096, 256, 128),
+                                         (17, 256, 64, 128), (33, 384, 80, 128)])
+def test_auto_path(M, K, N, group):
+    run_and_check(M, K, N, group, seed=M + K + N)
+
+
+def test_outlier_activation_columns():
+    run_and_check(4, 4096, 256, 128, seed=5, outliers=True)
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 8])
+def test_every_split_gives_the_same_tolerance(split):
+    run_and_check(8, 2048, 128, 128, seed=11, path="decode", split=split)
+
+
+def test_integer_product_is_exact():
+    """s = 1, z = 8 and integer activations: the exact integer result fits fp16."""
+    K, N, M, group = 512, 64, 4, 128
+    rng = np.random.default_rng(8)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 1.0, np.float16)
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.abs(exact).max() < 2048
+    pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
+    for split in (1, 4):
+        Y = w4.gemm(cuda(A), pw, path="decode", split=split)
+        assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
+
+
+def test_zero_rows_is_a_noop():
+    pw = prepare(synthetic.small_weights(128, 32, seed=1), 128)[1]
+    full, Y, pad = guarded_output(0, 32)
+    w4.gemm(torch.empty((0, 128), dtype=torch.float16, device="cuda"), pw, out=Y)
+    w4.device_status()
+    check_guard(full, 0, 32, pad)
+
+
+def test_stream_ordering_on_a_side_stream():
+    W = synthetic.small_weights(1024, 256, seed=2)
+    A = synthetic.small_activations(4, 1024, seed=2)
+    (q, s, z), pw = prepare(W, 128)
+    side = torch.cuda.Stream()
+    Ad = cuda(A)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        Y = w4.gemm(Ad, pw)
+    side.synchronize()
+    y, mag = oracle.reference(A, q, s, z, 128)
+    assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
