@@ -303,13 +303,16 @@ def capture_step(torch, w4, cases, weights, a_views, y_views, stream):
 
 
 def time_graphs(torch, graphs, steps, stream):
+    """Seconds for `steps` graph replays, timed with events on the stream the
+    graphs are replayed on (CUDAGraph.replay launches on the current stream)."""
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(steps):
-        graphs[i % len(graphs)].replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / 1e3
 
@@ -323,8 +326,7 @@ def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
                 w4.gemm(A, rot[r % len(rot)][c.key], out=Y)
-        for _ in range(3):
-            g.replay()
+        time_graphs(torch, [g], 3, stream)
         secs = time_graphs(torch, [g], 5, stream) / (5 * reps)
         out.append(secs)
         del g
@@ -349,9 +351,7 @@ def run_ours(args, wl, dist, rank, world, local):
     step_flops = sum(flops(c.M, c.K, c.N) for c in cases)
     step_roof_us = sum(roofline_us(c.M, c.K, c.N, c.group, pk)[0] for c in cases)
 
-    for i in range(args.warmup):
-        graphs[i % len(graphs)].replay()
-    torch.cuda.synchronize()
+    time_graphs(torch, graphs, args.warmup, stream)
     barrier(dist)
     with ClockSampler(local) as clk:
         secs = time_graphs(torch, graphs, args.steps, stream)
@@ -373,8 +373,7 @@ def run_ours(args, wl, dist, rank, world, local):
                 w4.gemm(A, r[c.key], out=Y)
             y_host.copy_(y_flat, non_blocking=True)
         e2e_graphs.append(g)
-    for i in range(args.warmup):
-        e2e_graphs[i % len(e2e_graphs)].replay()
+    time_graphs(torch, e2e_graphs, args.warmup, stream)
     barrier(dist)
     e2e_secs = max_over_ranks(dist, time_graphs(torch, e2e_graphs, args.steps, stream))
 

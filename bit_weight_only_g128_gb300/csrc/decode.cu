@@ -31,46 +31,76 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
+constexpr int kChunkAtoms = 16;                   // activation k staged per chunk: 1024
+constexpr int kPrefetch = 8;                      // weight atoms in flight per warp
 
-// MT: token octets (1: M <= 8, 2: M <= 16). U: atoms in flight per warp.
-template <int MT, int U>
-__global__ void __launch_bounds__(kThreads)
+// Bytes of one activation row of a chunk in shared memory. The extra 64
+// bytes put consecutive rows in opposite halves of the 32 banks, so the
+// 16-byte fragment loads of a quarter-warp (two rows x 64 bytes) never
+// collide.
+constexpr int kActRowBytes = kChunkAtoms * kAtomK * 2 + 64;
+
+template <int MT>
+__host__ __device__ constexpr int act_buffer_bytes() { return MT * 8 * kActRowBytes; }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Copy the activations of atoms [a0, a1) (rows 0..M-1) into a chunk buffer.
+__device__ __forceinline__ void stage_activations(uint32_t buf, const uint16_t* __restrict__ A,
+                                                  int M, int K, int a0, int a1) {
+  const int units = (a1 - a0) * (kAtomK / 8);  // 16-byte units per row
+  for (int idx = threadIdx.x; idx < M * units; idx += kThreads) {
+    const int row = idx / units, u = idx % units;
+    cp_async16(buf + row * kActRowBytes + u * 16, A + (size_t)row * K + (size_t)a0 * kAtomK + u * 8);
+  }
+}
+
+// MT: token octets (1: M <= 8, 2: M <= 16).
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
               const uint16_t* __restrict__ Sp, const uint2* __restrict__ Zp,
               uint16_t* __restrict__ Y, int M, int N, int K, int group, int split) {
-  __shared__ float red[MT * 8 * kRedStride];
+  constexpr int U = kPrefetch;
+  constexpr int kBuf = act_buffer_bytes<MT>();
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;  // mma groupID / thread-in-group
   const int nstrips = N / kStripCols;
   const int strip = blockIdx.y * kWarps + warp;
+  const bool active = strip < nstrips;
   const int natoms = K / kAtomK;
   const int a_begin = (int)(((long long)blockIdx.x * natoms) / split);
   const int a_end = (int)(((long long)(blockIdx.x + 1) * natoms) / split);
   const int G = K / group;
   const int apg = group / kAtomK;  // atoms per group
 
-  float acc[MT][4];
-#pragma unroll
-  for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
+  const uint4* wp = Wq + (size_t)(active ? strip : 0) * natoms * 32 + lane;
+  const uint16_t* sp = Sp + (size_t)(active ? strip : 0) * G * 16 + gq;
+  const uint2* zp = Zp + (size_t)(active ? strip : 0) * G;
 
-  if (strip < nstrips) {
-    const uint4* wp = Wq + (size_t)strip * natoms * 32 + lane;
-    const uint16_t* sp = Sp + (size_t)strip * G * 16 + gq;
-    const uint2* zp = Zp + (size_t)strip * G;
-    const uint16_t* arow[MT];
-    bool aval[MT];
-#pragma unroll
-    for (int o = 0; o < MT; ++o) {
-      const int m = 8 * o + gq;
-      aval[o] = m < M;
-      arow[o] = A + (size_t)(aval[o] ? m : 0) * K + 8 * t;
-    }
-
-    // weights and per-group constants of the atoms in flight
-    uint4 w[U];
-    uint32_t sv[U];
-    uint2 zv[U];
+  // weights and per-group constants of the atoms in flight (slot u holds the
+  // atom a with (a - a_begin) % U == u)
+  uint4 w[U];
+  uint32_t sv[U];
+  uint2 zv[U];
+  if (active) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int au = a_begin + u;
@@ -81,61 +111,88 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
         zv[u] = zp[grp];
       }
     }
+  }
 
-    for (int a = a_begin; a < a_end; a += U) {
+  float acc[2][MT][4];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int au = a + u;
-        if (au < a_end) {
-          const uint4 cw = w[u];
-          const uint32_t cs = sv[u];
-          const uint2 cz = zv[u];
-          const int nx = au + U;
-          if (nx < a_end) {  // refill this slot with the atom U ahead
-            const int grp = nx / apg;
-            w[u] = ldg_stream(wp + (size_t)nx * 32);
-            sv[u] = (uint32_t)sp[grp * 16] | ((uint32_t)sp[grp * 16 + 8] << 16);
-            zv[u] = zp[grp];
-          }
-          // activations of this atom: lane holds k = 64au + 32s + 8t .. +7 of token 8o+gq
-          uint4 act[2][MT];
+  for (int s = 0; s < 2; ++s)
 #pragma unroll
-          for (int o = 0; o < MT; ++o) {
+    for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
+
+  const int nchunks = (a_end - a_begin + kChunkAtoms - 1) / kChunkAtoms;
+  stage_activations(sbase, A, M, K, a_begin, min(a_end, a_begin + kChunkAtoms));
+  cp_async_commit();
+  for (int c = 0; c < nchunks; ++c) {
+    const int c0 = a_begin + c * kChunkAtoms;
+    const int c1 = min(a_end, c0 + kChunkAtoms);
+    if (c + 1 < nchunks) {  // next chunk into the other buffer
+      stage_activations(sbase + ((c + 1) & 1) * kBuf, A, M, K, c1, min(a_end, c1 + kChunkAtoms));
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    // lane's fragment row and column inside the chunk buffer
+    const uint32_t abuf = sbase + (c & 1) * kBuf + gq * kActRowBytes + 16 * t;
+    if (active) {
+      for (int a = c0; a < c1; a += U) {
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-              act[s][o] = aval[o] ? ldg_keep(arow[o] + (size_t)au * kAtomK + 32 * s)
-                                  : make_uint4(0u, 0u, 0u, 0u);
-          }
-          const DeqConst d0 = make_deq_const((cz.x >> (4 * gq)) & 15u, (uint16_t)(cs & 0xffffu));
-          const DeqConst d1 = make_deq_const((cz.y >> (4 * gq)) & 15u, (uint16_t)(cs >> 16));
-          uint32_t p[4][4];
-          dequant_word(cw.x, d0, p[0]);  // k-half 0, column gq
-          dequant_word(cw.y, d1, p[1]);  // k-half 0, column gq + 8
-          dequant_word(cw.z, d0, p[2]);  // k-half 1, column gq
-          dequant_word(cw.w, d1, p[3]);  // k-half 1, column gq + 8
+        for (int u = 0; u < U; ++u) {
+          const int au = a + u;
+          if (au < c1) {
+            const uint4 cw = w[u];
+            const uint32_t cs = sv[u];
+            const uint2 cz = zv[u];
+            const int nx = au + U;
+            if (nx < a_end) {  // refill this slot with the atom U ahead
+              const int grp = nx / apg;
+              w[u] = ldg_stream(wp + (size_t)nx * 32);
+              sv[u] = (uint32_t)sp[grp * 16] | ((uint32_t)sp[grp * 16 + 8] << 16);
+              zv[u] = zp[grp];
+            }
+            // B fragments: token 8o+gq, k = 64au + 32s + 8t .. +7
+            uint4 act[2][MT];
 #pragma unroll
-          for (int o = 0; o < MT; ++o) {
+            for (int o = 0; o < MT; ++o)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              const uint32_t* lo = p[2 * s];
-              const uint32_t* hi = p[2 * s + 1];
-              mma_16816(acc[o], lo[0], hi[0], lo[1], hi[1], act[s][o].x, act[s][o].y);
-              mma_16816(acc[o], lo[2], hi[2], lo[3], hi[3], act[s][o].z, act[s][o].w);
+              for (int s = 0; s < 2; ++s)
+                act[s][o] = lds128(abuf + o * 8 * kActRowBytes + ((au - c0) * kAtomK + 32 * s) * 2);
+            const DeqConst d0 = make_deq_const((cz.x >> (4 * gq)) & 15u, (uint16_t)(cs & 0xffffu));
+            const DeqConst d1 = make_deq_const((cz.y >> (4 * gq)) & 15u, (uint16_t)(cs >> 16));
+            uint32_t p[4][4];
+            dequant_word(cw.x, d0, p[0]);  // k-half 0, column gq
+            dequant_word(cw.y, d1, p[1]);  // k-half 0, column gq + 8
+            dequant_word(cw.z, d0, p[2]);  // k-half 1, column gq
+            dequant_word(cw.w, d1, p[3]);  // k-half 1, column gq + 8
+#pragma unroll
+            for (int o = 0; o < MT; ++o) {
+#pragma unroll
+              for (int s = 0; s < 2; ++s) {
+                const uint32_t* lo = p[2 * s];
+                const uint32_t* hi = p[2 * s + 1];
+                mma_16816(acc[s][o], lo[0], hi[0], lo[1], hi[1], act[s][o].x, act[s][o].y);
+                mma_16816(acc[s][o], lo[2], hi[2], lo[3], hi[3], act[s][o].z, act[s][o].w);
+              }
             }
           }
         }
       }
     }
+    __syncthreads();  // buffer (c & 1) is refilled by the copies issued next iteration
+  }
 
-    // accumulator fragment: rows = columns gq / gq+8 of the strip, cols = tokens 2t, 2t+1
+  // partial tile [token][column] (reuses activation buffer 0)
+  float* red = reinterpret_cast<float*>(smem);
+  if (active) {
 #pragma unroll
     for (int o = 0; o < MT; ++o) {
       const int tok = 8 * o + 2 * t;
       const int col = kStripCols * warp + gq;
-      red[tok * kRedStride + col] = acc[o][0];
-      red[(tok + 1) * kRedStride + col] = acc[o][1];
-      red[tok * kRedStride + col + 8] = acc[o][2];
-      red[(tok + 1) * kRedStride + col + 8] = acc[o][3];
+      red[tok * kRedStride + col] = acc[0][o][0] + acc[1][o][0];
+      red[(tok + 1) * kRedStride + col] = acc[0][o][1] + acc[1][o][1];
+      red[tok * kRedStride + col + 8] = acc[0][o][2] + acc[1][o][2];
+      red[(tok + 1) * kRedStride + col + 8] = acc[0][o][3] + acc[1][o][3];
     }
   }
 
@@ -172,11 +229,19 @@ template <int MT>
 cudaError_t launch_mt(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                       const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group, int split,
                       cudaStream_t stream) {
-  constexpr int U = 8;
+  constexpr int smem_bytes = 2 * act_buffer_bytes<MT>();
+  static_assert(MT * 8 * kRedStride * 4 <= act_buffer_bytes<MT>(), "partial tile must fit");
+  static bool attr_set = false;  // per process; identical for every device
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)split, (unsigned)((N + kDecodeBlockCols - 1) / kDecodeBlockCols), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -185,7 +250,7 @@ cudaError_t launch_mt(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, U>, A, reinterpret_cast<const uint4*>(Wq), Sp,
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, A, reinterpret_cast<const uint4*>(Wq), Sp,
                             reinterpret_cast<const uint2*>(Zp), Y, M, N, K, group, split);
 }
 
