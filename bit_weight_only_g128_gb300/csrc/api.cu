@@ -8,9 +8,6 @@
 #include "kernels.h"
 
 namespace w4a16 {
-
-__device__ int g_device_error = 0;
-
 namespace {
 
 thread_local std::string t_last_error;
@@ -66,18 +63,32 @@ int sm_count() {
   return sms;
 }
 
-// Split of K for the decode kernel: enough CTAs to cover every SM about
-// twice, while each warp keeps at least 8 atoms (4 KiB of weights per warp).
-int decode_split(int N, int K) {
+// Split of K for the decode kernel. A launch has ceil(N/128) * split CTAs;
+// the split (1..8) is chosen to fill the resident CTA slots of the device in
+// whole waves (the fraction of slot-time doing work is highest), keeping at
+// least 4 atoms (256 k) per CTA. Ties go to the smaller split (fewer partial
+// sums to reduce).
+int decode_split(int M, int N, int K) {
   const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
   const int natoms = K / kAtomK;
-  const int target = 2 * sm_count();
-  int split = 1;
-  while (split < kDecodeMaxSplit && nblk * split < target && natoms / (2 * split) >= 8) split *= 2;
-  return split;
+  const long slots = (long)sm_count() * decode_ctas_per_sm(M);
+  int best = 1;
+  double best_eff = -1.0;
+  for (int split = 1; split <= kDecodeMaxSplit; ++split) {
+    if (split > 1 && natoms / split < 4) break;
+    const long total = (long)nblk * split;
+    const long waves = (total + slots - 1) / slots;
+    const double eff = (double)total / (double)(waves * slots);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = split;
+    }
+  }
+  return best;
 }
 
-int choose_path(int M) { return W4A16_PATH_DECODE; (void)M; }
+// Decode GEMV up to 16 rows; tensor-core GEMM above.
+int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
 
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
               const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
@@ -99,11 +110,15 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  if (path == W4A16_PATH_TENSOR)
-    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "tensor-core path not available in this build");
+  if (path == W4A16_PATH_TENSOR) {
+    if (split > 1) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no split (got %d)", split);
+    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+    return ok();
+  }
   if (split < 0 || split > kDecodeMaxSplit)
     return fail(W4A16_ERR_INVALID_ARG, "split=%d outside 0..%d", split, kDecodeMaxSplit);
-  if (split == 0) split = decode_split(N, K);
+  if (split == 0) split = decode_split(M < 16 ? M : 16, N, K);
   if (split > K / kAtomK)
     return fail(W4A16_ERR_INVALID_ARG, "split=%d exceeds the %d atoms of K", split, K / kAtomK);
   // 16 rows per launch; larger M re-streams the weights once per 16 rows
@@ -203,7 +218,7 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* split) {
   if (int rc = check_kn(K, N, group)) return rc;
   if (!path || !split) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   *path = choose_path(M);
-  *split = decode_split(N, K);
+  *split = *path == W4A16_PATH_DECODE ? decode_split(M < 16 ? M : 16, N, K) : 1;
   return ok();
 }
 
@@ -211,13 +226,13 @@ int w4a16_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
   int flag = 0;
-  e = cudaMemcpyFromSymbol(&flag, g_device_error, sizeof(int));
+  e = read_and_clear_device_error(&flag);
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  if (flag != 0) {
-    const int zero = 0;
-    cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
-    return fail(W4A16_ERR_DEVICE_CHECK, "device error word = 0x%08x", flag);
-  }
+  if (flag != 0)
+    return fail(W4A16_ERR_DEVICE_CHECK,
+                "device error word = 0x%x (bits: 1 producer, 2 MMA, 4 dequant, 8 epilogue waits "
+                "timed out; 16 drain timed out)",
+                flag);
   return ok();
 }
 

@@ -31,17 +31,18 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
-constexpr int kChunkAtoms = 16;                   // activation k staged per chunk: 1024
 constexpr int kPrefetch = 8;                      // weight atoms in flight per warp
 
-// Bytes of one activation row of a chunk in shared memory. The extra 64
-// bytes put consecutive rows in opposite halves of the 32 banks, so the
-// 16-byte fragment loads of a quarter-warp (two rows x 64 bytes) never
-// collide.
-constexpr int kActRowBytes = kChunkAtoms * kAtomK * 2 + 64;
-
+// Activation atoms staged per chunk (1024 or 2048 k), and the bytes of one
+// staged row. The extra 64 bytes put consecutive rows in opposite halves of
+// the 32 banks, so the 16-byte fragment loads of a quarter-warp (two rows x
+// 64 bytes) never collide.
 template <int MT>
-__host__ __device__ constexpr int act_buffer_bytes() { return MT * 8 * kActRowBytes; }
+__host__ __device__ constexpr int chunk_atoms() { return MT == 1 ? 32 : 16; }
+template <int MT>
+__host__ __device__ constexpr int act_row_bytes() { return chunk_atoms<MT>() * kAtomK * 2 + 64; }
+template <int MT>
+__host__ __device__ constexpr int act_buffer_bytes() { return MT * 8 * act_row_bytes<MT>(); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -60,12 +61,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // Copy the activations of atoms [a0, a1) (rows 0..M-1) into a chunk buffer.
+template <int MT>
 __device__ __forceinline__ void stage_activations(uint32_t buf, const uint16_t* __restrict__ A,
                                                   int M, int K, int a0, int a1) {
   const int units = (a1 - a0) * (kAtomK / 8);  // 16-byte units per row
   for (int idx = threadIdx.x; idx < M * units; idx += kThreads) {
     const int row = idx / units, u = idx % units;
-    cp_async16(buf + row * kActRowBytes + u * 16, A + (size_t)row * K + (size_t)a0 * kAtomK + u * 8);
+    cp_async16(buf + row * act_row_bytes<MT>() + u * 16,
+               A + (size_t)row * K + (size_t)a0 * kAtomK + u * 8);
   }
 }
 
@@ -73,9 +76,11 @@ __device__ __forceinline__ void stage_activations(uint32_t buf, const uint16_t* 
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
-              const uint16_t* __restrict__ Sp, const uint2* __restrict__ Zp,
+              const uint32_t* __restrict__ Sp2, const uint2* __restrict__ Zp,
               uint16_t* __restrict__ Y, int M, int N, int K, int group, int split) {
   constexpr int U = kPrefetch;
+  constexpr int CH = chunk_atoms<MT>();
+  constexpr int kRow = act_row_bytes<MT>();
   constexpr int kBuf = act_buffer_bytes<MT>();
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
@@ -92,26 +97,32 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
   const int apg = group / kAtomK;  // atoms per group
 
   const uint4* wp = Wq + (size_t)(active ? strip : 0) * natoms * 32 + lane;
-  const uint16_t* sp = Sp + (size_t)(active ? strip : 0) * G * 16 + gq;
+  const uint32_t* sp = Sp2 + (size_t)(active ? strip : 0) * G * 8 + gq;  // (s[gq], s[gq+8])
   const uint2* zp = Zp + (size_t)(active ? strip : 0) * G;
 
-  // weights and per-group constants of the atoms in flight (slot u holds the
-  // atom a with (a - a_begin) % U == u)
+  // Slot u holds the atom a with (a - a_begin) % U == u: its weights, and the
+  // scale pair / zero words of its group when it is the first atom of a group
+  // (or of the range). The load stream runs U atoms ahead of consumption.
   uint4 w[U];
-  uint32_t sv[U];
-  uint2 zv[U];
+  uint32_t ms[U];
+  uint2 mz[U];
+  int l_atom = a_begin, l_grp = a_begin / apg, l_rem = a_begin % apg;
   if (active) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int au = a_begin + u;
-      if (au < a_end) {
-        const int grp = au / apg;
-        w[u] = ldg_stream(wp + (size_t)au * 32);
-        sv[u] = (uint32_t)sp[grp * 16] | ((uint32_t)sp[grp * 16 + 8] << 16);
-        zv[u] = zp[grp];
+      if (l_atom < a_end) {
+        w[u] = ldg_stream(wp + (size_t)l_atom * 32);
+        if (u == 0 || l_rem == 0) {
+          ms[u] = __ldg(sp + (size_t)l_grp * 8);
+          mz[u] = __ldg(zp + l_grp);
+        }
+        ++l_atom;
+        if (++l_rem == apg) { l_rem = 0; ++l_grp; }
       }
     }
   }
+  int c_rem = a_begin % apg;  // position of the consumed atom inside its group
+  DeqConst d0 = {}, d1 = {};
 
   float acc[2][MT][4];
 #pragma unroll
@@ -119,14 +130,14 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
 #pragma unroll
     for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
 
-  const int nchunks = (a_end - a_begin + kChunkAtoms - 1) / kChunkAtoms;
-  stage_activations(sbase, A, M, K, a_begin, min(a_end, a_begin + kChunkAtoms));
+  const int nchunks = (a_end - a_begin + CH - 1) / CH;
+  stage_activations<MT>(sbase, A, M, K, a_begin, min(a_end, a_begin + CH));
   cp_async_commit();
   for (int c = 0; c < nchunks; ++c) {
-    const int c0 = a_begin + c * kChunkAtoms;
-    const int c1 = min(a_end, c0 + kChunkAtoms);
+    const int c0 = a_begin + c * CH;
+    const int c1 = min(a_end, c0 + CH);
     if (c + 1 < nchunks) {  // next chunk into the other buffer
-      stage_activations(sbase + ((c + 1) & 1) * kBuf, A, M, K, c1, min(a_end, c1 + kChunkAtoms));
+      stage_activations<MT>(sbase + ((c + 1) & 1) * kBuf, A, M, K, c1, min(a_end, c1 + CH));
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -134,22 +145,28 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
     }
     __syncthreads();
     // lane's fragment row and column inside the chunk buffer
-    const uint32_t abuf = sbase + (c & 1) * kBuf + gq * kActRowBytes + 16 * t;
+    const uint32_t abuf = sbase + (c & 1) * kBuf + gq * kRow + 16 * t;
     if (active) {
       for (int a = c0; a < c1; a += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int au = a + u;
-          if (au < c1) {
+          if (au < c1) {  // warp-uniform; false only in the last batch of the range
             const uint4 cw = w[u];
-            const uint32_t cs = sv[u];
-            const uint2 cz = zv[u];
-            const int nx = au + U;
-            if (nx < a_end) {  // refill this slot with the atom U ahead
-              const int grp = nx / apg;
-              w[u] = ldg_stream(wp + (size_t)nx * 32);
-              sv[u] = (uint32_t)sp[grp * 16] | ((uint32_t)sp[grp * 16 + 8] << 16);
-              zv[u] = zp[grp];
+            if (c_rem == 0 || au == a_begin) {  // first atom of a group: new constants
+              const uint32_t z0 = (mz[u].x >> (4 * gq)) & 15u, z1 = (mz[u].y >> (4 * gq)) & 15u;
+              d0 = make_deq_const(z0, (uint16_t)(ms[u] & 0xffffu));
+              d1 = make_deq_const(z1, (uint16_t)(ms[u] >> 16));
+            }
+            if (++c_rem == apg) c_rem = 0;
+            if (l_atom < a_end) {  // refill this slot with the atom U ahead
+              w[u] = ldg_stream(wp + (size_t)l_atom * 32);
+              if (l_rem == 0) {
+                ms[u] = __ldg(sp + (size_t)l_grp * 8);
+                mz[u] = __ldg(zp + l_grp);
+              }
+              ++l_atom;
+              if (++l_rem == apg) { l_rem = 0; ++l_grp; }
             }
             // B fragments: token 8o+gq, k = 64au + 32s + 8t .. +7
             uint4 act[2][MT];
@@ -157,9 +174,7 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
             for (int o = 0; o < MT; ++o)
 #pragma unroll
               for (int s = 0; s < 2; ++s)
-                act[s][o] = lds128(abuf + o * 8 * kActRowBytes + ((au - c0) * kAtomK + 32 * s) * 2);
-            const DeqConst d0 = make_deq_const((cz.x >> (4 * gq)) & 15u, (uint16_t)(cs & 0xffffu));
-            const DeqConst d1 = make_deq_const((cz.y >> (4 * gq)) & 15u, (uint16_t)(cs >> 16));
+                act[s][o] = lds128(abuf + o * 8 * kRow + ((au - c0) * kAtomK + 32 * s) * 2);
             uint32_t p[4][4];
             dequant_word(cw.x, d0, p[0]);  // k-half 0, column gq
             dequant_word(cw.y, d1, p[1]);  // k-half 0, column gq + 8
@@ -225,19 +240,52 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
   }
 }
 
+}  // namespace
+
+namespace {
+
+// Opt both kernel variants into their dynamic shared memory (once per process).
+cudaError_t prepare_decode_kernels() {
+  static cudaError_t state = cudaErrorNotReady;
+  if (state == cudaErrorNotReady) {
+    state = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 2 * act_buffer_bytes<1>());
+    if (state == cudaSuccess)
+      state = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   2 * act_buffer_bytes<2>());
+  }
+  return state;
+}
+
+}  // namespace
+
+// CTAs of the decode kernel variant for M rows that fit on one SM.
+int decode_ctas_per_sm(int M) {
+  static int cache[2] = {0, 0};
+  const int v = M <= 8 ? 0 : 1;
+  if (cache[v] == 0) {
+    int n = 0;
+    if (prepare_decode_kernels() != cudaSuccess) return 2;
+    cudaError_t e = v == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_kernel<1>, kThreads, 2 * act_buffer_bytes<1>())
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, decode_kernel<2>, kThreads, 2 * act_buffer_bytes<2>());
+    if (e != cudaSuccess || n <= 0) return 2;
+    cache[v] = n;
+  }
+  return cache[v];
+}
+
+namespace {
+
 template <int MT>
 cudaError_t launch_mt(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                       const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group, int split,
                       cudaStream_t stream) {
   constexpr int smem_bytes = 2 * act_buffer_bytes<MT>();
   static_assert(MT * 8 * kRedStride * 4 <= act_buffer_bytes<MT>(), "partial tile must fit");
-  static bool attr_set = false;  // per process; identical for every device
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t prep = prepare_decode_kernels();
+  if (prep != cudaSuccess) return prep;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)split, (unsigned)((N + kDecodeBlockCols - 1) / kDecodeBlockCols), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -250,7 +298,8 @@ cudaError_t launch_mt(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, A, reinterpret_cast<const uint4*>(Wq), Sp,
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, A, reinterpret_cast<const uint4*>(Wq),
+                            reinterpret_cast<const uint32_t*>(Sp),
                             reinterpret_cast<const uint2*>(Zp), Y, M, N, K, group, split);
 }
 

@@ -24,6 +24,21 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int split, cudaStream_t stream);
 
+// tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile.
+cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
+                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
+                           cudaStream_t stream);
+// Token tile (MMA N) used for M rows, and the dynamic shared memory it needs.
+int tc_token_tile(int M);
+size_t tc_smem_bytes(int bt, int* stages);
+
+// Reads the device error word (bounded waits that gave up, self-checks) and
+// clears it if set.
+cudaError_t read_and_clear_device_error(int* flag);
+
+// CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
+int decode_ctas_per_sm(int M);
+
 // Largest split the decode kernel accepts (cluster size).
 constexpr int kDecodeMaxSplit = 8;
 // Output columns per decode CTA.

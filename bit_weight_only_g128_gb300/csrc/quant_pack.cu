@@ -95,7 +95,7 @@ __global__ void pack_meta_kernel(const uint16_t* __restrict__ s, const uint8_t* 
   for (int c = 0; c < 8; ++c) {
     const int n = kStripCols * j + 8 * h + c;
     word |= (uint32_t)(z[(size_t)grp * N + n] & 15u) << (4 * c);
-    Sp[jg * 16 + 8 * h + c] = s[(size_t)grp * N + n];
+    Sp[jg * 16 + 2 * c + h] = s[(size_t)grp * N + n];
   }
   Zp[idx] = word;
 }
@@ -126,7 +126,7 @@ __global__ void unpack_meta_kernel(const uint16_t* __restrict__ Sp, const uint32
   for (int c = 0; c < 8; ++c) {
     const int n = kStripCols * j + 8 * h + c;
     z[(size_t)grp * N + n] = (uint8_t)((word >> (4 * c)) & 15u);
-    s[(size_t)grp * N + n] = Sp[jg * 16 + 8 * h + c];
+    s[(size_t)grp * N + n] = Sp[jg * 16 + 2 * c + h];
   }
 }
 
@@ -143,7 +143,7 @@ __global__ void dequantize_kernel(const uint32_t* __restrict__ Wq, const uint16_
   const int grp = k0 / group;
   const size_t jg = (size_t)j * G + grp;
   const uint32_t zw = Zp[jg * 2 + (c >> 3)];
-  const DeqConst dc = make_deq_const((zw >> (4 * (c & 7))) & 15u, Sp[jg * 16 + c]);
+  const DeqConst dc = make_deq_const((zw >> (4 * (c & 7))) & 15u, Sp[jg * 16 + 2 * (c & 7) + (c >> 3)]);
   uint32_t pairs[4];
   dequant_word(Wq[widx], dc, pairs);
 #pragma unroll

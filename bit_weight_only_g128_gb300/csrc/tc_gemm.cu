@@ -1,0 +1,484 @@
+// Tensor-core path of the W4A16 linear layer (sm_103a, tcgen05 + TMEM + TMA).
+//
+// At large M the layer is a dense contraction ("the rest is normal FP16
+// operations" once dequantized, vLLM PR #1032 thread), so the int4 weights
+// are dequantized into shared memory and fed to tcgen05.mma kind::f16 with
+// fp32 accumulation in tensor memory.
+//
+// Orientation: D[n][m] = sum_k Wdeq[n][k] * A[m][k] (the weight tile is the
+// 128-row MMA operand, the tokens are the MMA's N dimension). Each
+// dequantized weight then serves up to 256 tokens, which halves the dequant
+// work per FLOP compared with putting the tokens on the 128-row side, and
+// token tiles of 16..256 cover the middle band of M as well.
+//
+// CTA (one output tile: 128 columns x BT tokens, full K):
+//   warp 0      TMA producer: activations tile [BT x 64] (128B swizzle) and
+//               the packed int4 atoms of 8 strips [8 x 512 B] per k-stage;
+//   warp 1      TMEM allocation; one thread issues 4 MMAs (K=16) per stage;
+//   warps 2..9  dequantize the packed atoms of a stage into the 128B-swizzled
+//               K-major operand tile, then run the epilogue (TMEM -> fp16 Y).
+// Stages form a ring guarded by mbarriers: full_tma (TMA bytes landed),
+// full_dq (256 dequant threads done), empty (MMAs of the stage completed).
+// Every wait is bounded; a wait that gives up sets the library's device
+// error word and the CTA drains and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kTileN = 128;        // output columns per CTA (MMA M)
+constexpr int kStageK = 64;        // k per pipeline stage (one 128-byte swizzle row)
+constexpr int kDqWarps = 8;
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kThreads = 64 + kDqThreads;
+constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
+constexpr int kPackedBytes = kTileN * kStageK / 2;  // 4 KiB packed codes
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// error codes written to g_device_error (one bit per role)
+constexpr int kErrProducer = 1, kErrMma = 2, kErrDequant = 4, kErrEpilogue = 8, kErrDrain = 16;
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity`. Returns false if the CTA is
+// aborting (another role gave up) or if this wait exceeded the limit, in
+// which case it raises the abort flag and records `code` in the error word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int code) {
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(&g_device_error, code);
+      return false;
+    }
+  }
+}
+
+// Wait used only while aborting: for this CTA's own asynchronous work (copies
+// or MMAs already issued) to finish, ignoring the abort flag, bounded by a
+// shorter limit.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs / 10) {
+      atomicOr(&g_device_error, kErrDrain);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the canonical
+// 128-byte-swizzle layout: rows of 128 bytes (64 fp16 of k), 8-row groups
+// 1024 bytes apart (stride byte offset), tile base 1024-byte aligned.
+// Fields: start address >> 4 [0,14), leading byte offset >> 4 [16,30)
+// (unused for this layout, set to 1), stride byte offset >> 4 [32,46),
+// descriptor version 1 [46,48), swizzle mode 2 = 128B [61,64).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 D [4,6) = 1, fp16 A
+// and B [7,10) = [10,13) = 0, both K-major [15] = [16] = 0, N >> 3 at
+// [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct TcParams {
+  const uint16_t* Sp;
+  const uint32_t* Zp;
+  uint16_t* Y;
+  int M, N, K, group;
+  int bt;       // token tile (MMA N): multiple of 16, 16..256
+  int stages;   // pipeline depth
+  int tmem_cols;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+               const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const int bt = p.bt, stages = p.stages;
+  const uint32_t act_bytes = (uint32_t)bt * 128u;
+  const uint32_t stage_bytes = act_bytes + kWdqBytes + kPackedBytes;
+  // stage s: [activations | dequantized weights | packed codes], 1024-aligned
+  const uint32_t bars = base + (uint32_t)stages * stage_bytes;
+  auto full_tma = [&](int s) { return bars + 8u * s; };
+  auto full_dq = [&](int s) { return bars + 8u * (stages + s); };
+  auto empty = [&](int s) { return bars + 8u * (2 * stages + s); };
+  const uint32_t accum_bar = bars + 8u * (3 * stages);
+  const uint32_t tmem_slot = accum_bar + 8u;
+  uint8_t* gen_base = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 4u - base));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kTileN;
+  const int m0 = blockIdx.y * bt;
+  const int nk = p.K / kStageK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full_tma(s), 1);
+      mbar_init(full_dq(s), kDqThreads);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(accum_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gen_base + (tmem_slot - base));
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % stages;
+        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
+        const uint32_t st = base + (uint32_t)s * stage_bytes;
+        mbar_expect_tx(full_tma(s), act_bytes + kPackedBytes);
+        tma_load_2d(st, &tmA, kb * kStageK, m0, full_tma(s));
+        tma_load_2d(st + act_bytes + kWdqBytes, &tmW, kb * 128, n0 / kStripCols, full_tma(s));
+        ++issued;
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA exits
+        for (int kb = (issued > stages ? issued - stages : 0); kb < issued; ++kb)
+          mbar_drain(full_tma(kb % stages), (uint32_t)(kb / stages) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(kTileN, bt);
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % stages;
+        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+        ok = mbar_wait(full_tma(s), ph, abort_flag, kErrMma) &&
+             mbar_wait(full_dq(s), ph, abort_flag, kErrMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = base + (uint32_t)s * stage_bytes;
+        const uint64_t bdesc = sw128_kmajor_desc(st);
+        const uint64_t adesc = sw128_kmajor_desc(st + act_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes of k per MMA
+          tc_mma_f16(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+        tc_commit(empty(s));
+      }
+      tc_commit(accum_bar);  // fires once every MMA issued above has completed
+      if (!ok) mbar_drain(accum_bar, 0);  // no MMA may run past the TMEM release
+    }
+  } else {
+    // ---------------------------------------------------------- dequant + epilogue
+    const int dw = warp - 2;                 // strip of the tile handled by this warp
+    const int gq = lane >> 2, t = lane & 3;
+    const int strip = n0 / kStripCols + dw;
+    const bool valid = strip < p.N / kStripCols;
+    const int G = p.K / p.group;
+    const uint32_t* sp = reinterpret_cast<const uint32_t*>(p.Sp) + (size_t)(valid ? strip : 0) * G * 8 + gq;
+    const uint32_t* zp = p.Zp + (size_t)(valid ? strip : 0) * G * 2;
+    // process the lane's words in an order that keeps the 16-byte stores of
+    // each quarter-warp on distinct banks (odd rows take the other k-half first)
+    const uint32_t flip = (uint32_t)(gq & 1);
+    uint32_t pre_s = 0, pre_z0 = 0, pre_z1 = 0;  // next group's constants, prefetched
+    if (valid) {
+      pre_s = sp[0];  // (s[gq], s[gq + 8])
+      pre_z0 = zp[0];
+      pre_z1 = zp[1];
+    }
+    DeqConst d0 = {}, d1 = {};
+    int cur_grp = -1;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % stages;
+      const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+      if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
+      const uint32_t st = base + (uint32_t)s * stage_bytes;
+      if (valid) {
+        const int grp = kb * kStageK / p.group;
+        if (grp != cur_grp) {
+          d0 = make_deq_const((pre_z0 >> (4 * gq)) & 15u, (uint16_t)(pre_s & 0xffffu));
+          d1 = make_deq_const((pre_z1 >> (4 * gq)) & 15u, (uint16_t)(pre_s >> 16));
+          cur_grp = grp;
+          if (grp + 1 < G) {
+            pre_s = sp[(grp + 1) * 8];
+            pre_z0 = zp[(grp + 1) * 2];
+            pre_z1 = zp[(grp + 1) * 2 + 1];
+          }
+        }
+        const uint4 v = lds128(st + act_bytes + kWdqBytes + dw * 512 + lane * 16);
+        const uint32_t wdq = st + act_bytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t ks = (uint32_t)(i >> 1) ^ flip;  // k-half of this word
+          const uint32_t r = (uint32_t)(i & 1);           // column gq or gq + 8
+          const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
+          uint32_t o[4];
+          dequant_word(word, r ? d1 : d0, o);
+          // row n = 16 dw + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
+          const uint32_t row = 16u * dw + gq + 8u * r;
+          const uint32_t kw = 4u * ks + t;
+          sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4), o[0],
+                 o[1], o[2], o[3]);
+        }
+      }
+      fence_async_shared();  // generic-proxy stores -> visible to the tensor core
+      mbar_arrive(full_dq(s));
+    }
+
+    // epilogue: TMEM lanes 32q..32q+31 are output columns, TMEM columns are tokens
+    const bool have_accum = mbar_wait(accum_bar, 0, abort_flag, kErrEpilogue);
+    __syncwarp();
+    if (__all_sync(0xffffffffu, have_accum)) {  // warp-uniform: tcgen05.ld is .aligned
+      tc_fence_after();
+      const int q = warp & 3;
+      const int half = dw >> 2;  // two warpgroups split the token chunks
+      const int n = n0 + 32 * q + lane;
+      for (int c = half; c < bt / 16; c += 2) {
+        uint32_t r[16];
+        tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * c), r);
+        tmem_wait_ld();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = m0 + 16 * c + j;
+            if (tok < p.M)
+              p.Y[(size_t)tok * p.N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+int tc_token_tile(int M) {
+  if (M >= 256) return 256;
+  return (M + 15) / 16 * 16;
+}
+
+size_t tc_smem_bytes(int bt, int* stages_out) {
+  const size_t stage = (size_t)bt * 128 + kWdqBytes + kPackedBytes;
+  const size_t budget = 227 * 1024 - 1024 - 256;
+  int stages = (int)(budget / stage);
+  if (stages > 8) stages = 8;
+  if (stages_out) *stages_out = stages;
+  return (size_t)stages * stage + 1024 + 256;
+}
+
+cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
+                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
+                           cudaStream_t stream) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  const int bt = tc_token_tile(M);
+  CUtensorMap tmA, tmW;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)bt};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / kAtomK) * kAtomWords, (cuuint64_t)(N / kStripCols)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / kAtomK) * kAtomWords * 4};
+    const cuuint32_t box[2] = {kAtomWords, kTileN / kStripCols};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(Wq), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  TcParams prm;
+  prm.Sp = Sp;
+  prm.Zp = Zp;
+  prm.Y = Y;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.group = group;
+  prm.bt = bt;
+  const size_t smem = tc_smem_bytes(bt, &prm.stages);
+  prm.tmem_cols = pow2_at_least(bt);
+  static size_t attr_bytes = 0;
+  if (attr_bytes < smem) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(227 * 1024));
+    if (e != cudaSuccess) return e;
+    attr_bytes = 227 * 1024;
+  }
+  const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt), 1);
+  tc_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_error(int* flag) {
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
+  if (e != cudaSuccess || *flag == 0) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+}
+
+}  // namespace w4a16

@@ -45,8 +45,9 @@
  *     p = 4 + (e-1)/2 for odd e. So (word >> 4p) & 0x000F000F holds the
  *     codes of k-offsets (2p, 2p+1) in its two 16-bit halves, and each lane
  *     L of a warp reads its four words of an atom with one 16-byte load.
- *   Sp: fp16, N*G of them; offset (j*G + grp)*16 + c is the scale of
- *     column 16j + c in group grp.
+ *   Sp: fp16, N*G of them; offset (j*G + grp)*16 + 2c + h is the scale of
+ *     column 16j + 8h + c (c in [0,8), h in {0,1}) in group grp, so the two
+ *     columns g and g + 8 that one lane dequantizes share one 32-bit word.
  *   Zp: uint32, N*G/8 of them; offset (j*G + grp)*2 + h holds in nibble c
  *     the zero point of column 16j + 8h + c in group grp.
  *   Sizes: w4a16_packed_sizes(). Alignment: Wq, Sp, A and Y 16-byte aligned,

@@ -1,0 +1,73 @@
+"""Parity of the tcgen05/TMEM tensor-core path against the CPU oracle.
+
+Same tolerance as the decode path; shapes cover token tiles of 16..256,
+ragged M inside a token tile, several 128-column tiles with a ragged last
+tile (N a multiple of 16 only), K from one stage (64) to thousands, and
+groups 64, 128 and K (per-channel).
+"""
+import numpy as np
+import pytest
+
+import bit_weight_only_g128_gb300 as w4
+import oracle
+import synthetic
+from gpu_util import cuda, half_bits, prepare, run_and_check
+
+pytestmark = pytest.mark.gpu
+
+TENSOR_CASES = [
+    # M, K, N, group
+    (16, 128, 128, 128),
+    (32, 64, 128, 64),
+    (128, 256, 256, 128),
+    (17, 640, 144, 64),
+    (100, 1024, 272, 1024),
+    (256, 512, 384, 128),
+    (300, 768, 512, 256),
+    (64, 4096, 1024, 128),
+    (513, 1024, 400, 128),
+    (1024, 2048, 1280, 128),
+    (8, 256, 16, 128),
+    (1, 128, 32, 128),
+]
+
+
+@pytest.mark.parametrize("M,K,N,group", TENSOR_CASES)
+def test_tensor_path(M, K, N, group):
+    run_and_check(M, K, N, group, seed=M * 7 + N, path="tensor")
+
+
+def test_tensor_outliers():
+    run_and_check(512, 4096, 512, 128, seed=3, path="tensor", outliers=True)
+
+
+@pytest.mark.parametrize("M", [16, 32, 48])
+def test_decode_and_tensor_agree(M):
+    """Both paths within tolerance of the oracle and within twice it of each other."""
+    K, N, group = 2048, 256, 128
+    W = synthetic.small_weights(K, N, seed=M)
+    A = synthetic.small_activations(M, K, seed=M)
+    (q, s, z), pw = prepare(W, group)
+    y, mag = oracle.reference(A, q, s, z, group)
+    Ad = cuda(A)
+    Yd = half_bits(w4.gemm(Ad, pw, path="decode"))
+    Yt = half_bits(w4.gemm(Ad, pw, path="tensor"))
+    w4.device_status()
+    assert oracle.check(Yd, y, mag)[0] <= 1.0
+    assert oracle.check(Yt, y, mag)[0] <= 1.0
+    diff = np.abs(oracle.from_half(Yd) - oracle.from_half(Yt))
+    assert np.all(diff <= 2 * (2.0 ** -9 * mag + 1e-3))
+
+
+def test_integer_product_is_exact_on_tensor_cores():
+    K, N, M, group = 512, 128, 64, 128
+    rng = np.random.default_rng(8)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 1.0, np.float16)
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
+    pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
+    Y = w4.gemm(cuda(A), pw, path="tensor")
+    w4.device_status()
+    assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)

@@ -270,7 +270,7 @@ def test_pack_single_nibble_position():
     expect[4 * 13 + 0] = 0xA << 16
     assert np.array_equal(Wp, expect)
     assert Zp.tolist() == [0, 0x7 << 12]
-    assert Sp[11] == 0x1234 and np.count_nonzero(Sp) == 1
+    assert Sp[7] == 0x1234 and np.count_nonzero(Sp) == 1   # column 11 = 8*1 + 3 -> 2*3 + 1
 
 
 @pytest.mark.parametrize("K,N,group", [(128, 32, 128), (192, 48, 64), (256, 16, 256)])
@@ -282,7 +282,7 @@ def test_pack_follows_layout_text_and_round_trips(K, N, group):
     for n in range(N):
         j, c = divmod(n, 16)
         for grp in range(G):
-            assert Sp[(j * G + grp) * 16 + c] == s[grp, n]
+            assert Sp[(j * G + grp) * 16 + 2 * (c % 8) + c // 8] == s[grp, n]
             word = int(Zp[(j * G + grp) * 2 + c // 8])
             assert (word >> (4 * (c % 8))) & 15 == z[grp, n]
     q2, s2, z2 = oracle.unpack(Wp, Sp, Zp, K, N, group)
