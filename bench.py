@@ -268,6 +268,10 @@ def build_gpu_workload(wl, torch, w4, device, copies=None):
                                        pw.group) for k, pw in layers.items()})
     a_flat, a_views = _aligned_views(torch, [(c.M, c.K) for c in cases], torch.float16, device)
     y_flat, y_views = _aligned_views(torch, [(c.M, c.N) for c in cases], torch.float16, device)
+    # one workspace serves every call: they run one after another on one stream
+    ws = w4.new_workspace(max(w4.workspace_size(c.M, c.N, c.K, c.group) for c in cases), device)
+    for r in rot:
+        r["workspace"] = ws
     for c, av in zip(cases, a_views):
         av.copy_(torch.from_numpy(synthetic.activations(wl.cfg, c.M, c.K, c.N,
                                                         outliers=wl.outliers)))
@@ -282,7 +286,7 @@ def sanity_check(wl, cases, rot, a_views, y_views, torch, w4):
         if c.key in seen:
             continue
         seen.add(c.key)
-        w4.gemm(A, rot[0][c.key], out=Y)
+        w4.gemm(A, rot[0][c.key], out=Y, workspace=rot[0]["workspace"])
         torch.cuda.synchronize()
         cols = synthetic.sample_indices(c.N, 32, seed=0, salt=c.N)
         W = synthetic.weights(wl.cfg, c.K, c.N)[:, cols]
@@ -298,7 +302,7 @@ def capture_step(torch, w4, cases, weights, a_views, y_views, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for c, A, Y in zip(cases, a_views, y_views):
-            w4.gemm(A, weights[c.key], out=Y)
+            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"])
     return g
 
 
@@ -325,7 +329,7 @@ def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
-                w4.gemm(A, rot[r % len(rot)][c.key], out=Y)
+                w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=rot[0]["workspace"])
         time_graphs(torch, [g], 3, stream)
         secs = time_graphs(torch, [g], 5, stream) / (5 * reps)
         out.append(secs)
@@ -370,7 +374,7 @@ def run_ours(args, wl, dist, rank, world, local):
         with torch.cuda.graph(g, stream=stream):
             a_flat.copy_(a_host, non_blocking=True)
             for c, A, Y in zip(cases, a_views, y_views):
-                w4.gemm(A, r[c.key], out=Y)
+                w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"])
             y_host.copy_(y_flat, non_blocking=True)
         e2e_graphs.append(g)
     time_graphs(torch, e2e_graphs, args.warmup, stream)
@@ -407,10 +411,10 @@ def run_ours(args, wl, dist, rank, world, local):
         with open(args.sweep, "a") as f:
             for c, t in zip(cases, times):
                 roof, bound = roofline_us(c.M, c.K, c.N, c.group, pk)
-                path, split = w4.plan(c.M, c.N, c.K, c.group)
+                path, ctas = w4.plan(c.M, c.N, c.K, c.group)
                 f.write(json.dumps({
                     "workload": wl.name, "layer": c.layer, "M": c.M, "K": c.K, "N": c.N,
-                    "group": c.group, "path": path, "split": split, "us": 1e6 * t,
+                    "group": c.group, "path": path, "ctas": ctas, "us": 1e6 * t,
                     "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
                     "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
                     "bound": bound, "frac": roof / (1e6 * t)}) + "\n")

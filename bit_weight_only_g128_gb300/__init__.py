@@ -46,6 +46,7 @@ SIGNATURES = {
     "w4a16_unpack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "w4a16_dequantize": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "w4a16_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
+    "w4a16_workspace_size_ex": (_I, [_I, _I, _I, _I, _I, _I, _PSZ]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _I, _I, _P]),
     "w4a16_plan": (_I, [_I, _I, _I, _I, _PI, _PI]),
@@ -174,37 +175,49 @@ def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
     return deq
 
 
-def workspace_size(M: int, N: int, K: int, group: int) -> int:
+def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", ctas: int = 0) -> int:
+    """Scratch bytes a gemm call needs (0 for the tensor-core path)."""
     b = ctypes.c_size_t()
-    _check(lib().w4a16_workspace_size(M, N, K, group, ctypes.byref(b)), "w4a16_workspace_size")
+    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], ctas, ctypes.byref(b)),
+           "w4a16_workspace_size")
     return b.value
 
 
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled, 256-byte aligned workspace (every call leaves it zeroed)."""
+    return torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device or "cuda")
+
+
 def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
-    p, s = ctypes.c_int(), ctypes.c_int()
-    _check(lib().w4a16_plan(M, N, K, group, ctypes.byref(p), ctypes.byref(s)), "w4a16_plan")
-    return {v: k for k, v in _PATHS.items()}[p.value], s.value
+    """(path, decode CTA count) the library picks for this problem."""
+    p, c = ctypes.c_int(), ctypes.c_int()
+    _check(lib().w4a16_plan(M, N, K, group, ctypes.byref(p), ctypes.byref(c)), "w4a16_plan")
+    return {v: k for k, v in _PATHS.items()}[p.value], c.value
 
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
-         path: str = "auto", split: int = 0, workspace: Optional[torch.Tensor] = None,
+         path: str = "auto", ctas: int = 0, workspace: Optional[torch.Tensor] = None,
          stream=None) -> torch.Tensor:
-    """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream."""
+    """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
+
+    `workspace` must be zero-filled before its first use (new_workspace);
+    without one, a fresh zeroed buffer is allocated for this call.
+    """
     M, K = A.shape
     if K != pw.K:
         raise ValueError(f"A has K={K}, weight has K={pw.K}")
     if out is None:
         out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, ctas)
     if need:
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+            workspace = new_workspace(need, A.device)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
-                               _PATHS[path], split, _stream(stream)), "w4a16_gemm")
+                               _PATHS[path], ctas, _stream(stream)), "w4a16_gemm")
     return out
 
 

@@ -63,39 +63,30 @@ int sm_count() {
   return sms;
 }
 
-// Split of K for the decode kernel. A launch has ceil(N/128) * split CTAs;
-// the split (1..8) is chosen to fill the resident CTA slots of the device in
-// whole waves (the fraction of slot-time doing work is highest), keeping at
-// least 4 atoms (256 k) per CTA. Ties go to the smaller split (fewer partial
-// sums to reduce).
-int decode_split(int M, int N, int K) {
-  const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
-  const int natoms = K / kAtomK;
-  const long slots = (long)sm_count() * decode_ctas_per_sm(M);
-  int best = 1;
-  double best_eff = -1.0;
-  for (int split = 1; split <= kDecodeMaxSplit; ++split) {
-    if (split > 1 && natoms / split < 4) break;
-    const long total = (long)nblk * split;
-    const long waves = (total + slots - 1) / slots;
-    const double eff = (double)total / (double)(waves * slots);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = split;
-    }
-  }
-  return best;
+// Persistent CTAs of the decode kernel: every resident slot of the device,
+// but never more than the T work units (each CTA must own at least one).
+int decode_ctas(int M, int N, int K, int requested) {
+  const long long T = (long long)((N + kDecodeBlockCols - 1) / kDecodeBlockCols) * (K / kAtomK);
+  long long c = requested > 0 ? requested : (long long)sm_count() * decode_ctas_per_sm(M);
+  if (c > T) c = T;
+  return (int)c;
 }
 
 // Decode GEMV up to 16 rows; tensor-core GEMM above.
 int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
 
+// Scratch bytes of a (path, ctas) choice: the decode path's counters and
+// partial tiles (16-row chunks share one workspace); none for tensor cores.
+size_t workspace_for(int M, int N, int K, int path, int ctas) {
+  if (M == 0 || path != W4A16_PATH_DECODE) return 0;
+  const int rows = M < 16 ? M : 16;
+  return decode_workspace_bytes(rows, N, decode_ctas(rows, N, K, ctas));
+}
+
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
               const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-              void* workspace, size_t workspace_bytes, int path, int split,
+              void* workspace, size_t workspace_bytes, int path, int ctas,
               cudaStream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (M > kMaxDim) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "M=%d above %d", M, kMaxDim);
   if (int rc = check_kn(K, N, group)) return rc;
@@ -110,22 +101,23 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
   if (path == W4A16_PATH_TENSOR) {
-    if (split > 1) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no split (got %d)", split);
+    if (ctas > 0) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no CTA count");
     cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return ok();
   }
-  if (split < 0 || split > kDecodeMaxSplit)
-    return fail(W4A16_ERR_INVALID_ARG, "split=%d outside 0..%d", split, kDecodeMaxSplit);
-  if (split == 0) split = decode_split(M < 16 ? M : 16, N, K);
-  if (split > K / kAtomK)
-    return fail(W4A16_ERR_INVALID_ARG, "split=%d exceeds the %d atoms of K", split, K / kAtomK);
+  const size_t need = workspace_for(M, N, K, path, ctas);
+  if (!workspace || workspace_bytes < need)
+    return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
+                need, workspace ? workspace_bytes : (size_t)0);
+  if (!aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
   // 16 rows per launch; larger M re-streams the weights once per 16 rows
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
-    cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N,
-                                  rows, N, K, group, split, stream);
+    cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, rows,
+                                  N, K, group, decode_ctas(rows, N, K, ctas), workspace, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   return ok();
@@ -192,10 +184,18 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 }
 
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes) {
+  return w4a16_workspace_size_ex(M, N, K, group, W4A16_PATH_AUTO, 0, bytes);
+}
+
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas, size_t* bytes) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
+  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
-  *bytes = 0;
+  if (path == W4A16_PATH_AUTO) path = choose_path(M);
+  if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
+  *bytes = workspace_for(M, N, K, path, ctas);
   return ok();
 }
 
@@ -208,17 +208,18 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales, co
 
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-                  void* workspace, size_t workspace_bytes, int path, int split, void* stream) {
+                  void* workspace, size_t workspace_bytes, int path, int ctas, void* stream) {
   return gemm_impl(A, Wq, scales, zeros, M, N, K, group, Y, workspace, workspace_bytes, path,
-                   split, (cudaStream_t)stream);
+                   ctas, (cudaStream_t)stream);
 }
 
-int w4a16_plan(int M, int N, int K, int group, int* path, int* split) {
+int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (int rc = check_kn(K, N, group)) return rc;
-  if (!path || !split) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  if (!path || !ctas) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   *path = choose_path(M);
-  *split = *path == W4A16_PATH_DECODE ? decode_split(M < 16 ? M : 16, N, K) : 1;
+  const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
+  *ctas = *path == W4A16_PATH_DECODE ? decode_ctas(rows, N, K, 0) : 0;
   return ok();
 }
 

@@ -18,11 +18,16 @@ cudaError_t launch_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t
 cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
                               int N, int group, uint16_t* deq, cudaStream_t stream);
 
-// Split-K register-dequant GEMV for M <= 16 rows of A (one launch); `split`
-// CTAs of one thread-block cluster share each block of 128 output columns.
+// Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
+// persistent CTAs, 1 <= ctas <= ceil(N/128) * K/64). `workspace` holds the
+// per-block counters (zero before the first call, left zero by every call)
+// followed by the partial tiles; see decode_workspace_bytes.
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int split, cudaStream_t stream);
+                          int ctas, void* workspace, cudaStream_t stream);
+size_t decode_workspace_bytes(int M, int N, int ctas);
+// Bytes of the counter area at the start of the decode workspace.
+size_t decode_counter_bytes(int N);
 
 // tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile.
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
@@ -39,8 +44,6 @@ cudaError_t read_and_clear_device_error(int* flag);
 // CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
 int decode_ctas_per_sm(int M);
 
-// Largest split the decode kernel accepts (cluster size).
-constexpr int kDecodeMaxSplit = 8;
 // Output columns per decode CTA.
 constexpr int kDecodeBlockCols = 128;
 

@@ -1,9 +1,10 @@
 // Tensor-core path of the W4A16 linear layer (sm_103a, tcgen05 + TMEM + TMA).
 //
-// At large M the layer is a dense contraction ("the rest is normal FP16
-// operations" once dequantized, vLLM PR #1032 thread), so the int4 weights
-// are dequantized into shared memory and fed to tcgen05.mma kind::f16 with
-// fp32 accumulation in tensor memory.
+// At large M the layer is a dense contraction: once the weights are
+// dequantized, what remains is an ordinary fp16 matrix product (the point made
+// in the vLLM PR #1032 thread). So the int4 weights are dequantized into
+// shared memory and fed to tcgen05.mma kind::f16 with fp32 accumulation in
+// tensor memory.
 //
 // Orientation: D[n][m] = sum_k Wdeq[n][k] * A[m][k] (the weight tile is the
 // 128-row MMA operand, the tokens are the MMA's N dimension). Each

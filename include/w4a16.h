@@ -73,7 +73,7 @@ extern "C" {
 
 /* Paths for w4a16_gemm_ex. */
 #define W4A16_PATH_AUTO 0
-#define W4A16_PATH_DECODE 1   /* split-K register-dequant GEMV, M <= 16 */
+#define W4A16_PATH_DECODE 1   /* stream-K register-dequant GEMV         */
 #define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
 
 /* Message for the last error returned on the calling thread ("" if none). */
@@ -111,27 +111,44 @@ int w4a16_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int K, int N, int group, uint16_t* deq, void* stream);
 
-/* Scratch bytes w4a16_gemm needs for this problem (0 when none). Host-only. */
+/* Scratch bytes w4a16_gemm needs for this problem on the current device
+ * (0 when none: the tensor-core path). The decode path (M <= 16 rows per
+ * launch) finishes output blocks split between CTAs through this workspace:
+ * a counter area followed by fp32 partial tiles. The workspace must be
+ * zero-filled before its first use; every call leaves it zero-filled again,
+ * so one buffer serves any number of calls that run one after another.
+ * Calls that may run concurrently (other streams) need separate workspaces.
+ * Host-only. */
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
 
+/* As w4a16_workspace_size for a forced path and CTA count (see
+ * w4a16_gemm_ex). Host-only. */
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas,
+                            size_t* bytes);
+
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
- * The path (decode GEMV or tensor-core GEMM) and its split of K are chosen
- * from M, N, K and the device's SM count. `workspace` may be NULL when
- * w4a16_workspace_size reports 0. Y must not overlap the inputs. */
+ * The path (decode GEMV for M <= 16, tensor-core GEMM above) and its grid
+ * are chosen from M, N, K and the device's SM count. `workspace` (256-byte
+ * aligned, zero-filled before first use) may be NULL when
+ * w4a16_workspace_size reports 0; W4A16_ERR_WORKSPACE_TOO_SMALL otherwise.
+ * Y must not overlap the inputs. */
 int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                const uint32_t* zeros, int M, int N, int K, int group,
                uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream);
 
-/* As w4a16_gemm with the path and split forced (0 = automatic choice).
- * W4A16_PATH_DECODE needs M <= 16; split is the number of K ranges whose
- * partial sums are reduced inside a thread-block cluster (1..8). */
+/* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and, for
+ * the decode path, the number of persistent CTAs that share the work
+ * (0 = automatic; clamped to the number of 128-column x 64-k work units).
+ * The decode path handles any M in launches of 16 rows (it streams the
+ * weights once per launch); the tensor path takes ctas = 0. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,
-                  int path, int split, void* stream);
+                  int path, int ctas, void* stream);
 
-/* The path and split w4a16_gemm would use on the current device. Host-only. */
-int w4a16_plan(int M, int N, int K, int group, int* path, int* split);
+/* The path and decode CTA count w4a16_gemm would use on the current device
+ * (ctas = 0 for the tensor-core path). Host-only. */
+int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas);
 
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word (set by a kernel that gave up a bounded wait or failed a self-check).

@@ -73,11 +73,13 @@ def test_shape_rules(lib, K, N, group, code):
     assert lib.w4a16_last_error()
 
 
-def _gemm(lib, A=16, W=16, S=16, Z=16, Y=16, M=1, N=64, K=128, group=128, path=0, split=0):
+def _gemm(lib, A=16, W=16, S=16, Z=16, Y=16, M=1, N=64, K=128, group=128, path=0, ctas=0,
+          ws=256, ws_bytes=1 << 20):
     # fake (never dereferenced) addresses: every failure below is decided on the host
     return lib.w4a16_gemm_ex(A and 0x10000 + A % 16, W and 0x20000 + W % 16,
                              S and 0x30000 + S % 16, Z and 0x40000 + Z % 16, M, N, K, group,
-                             Y and 0x50000 + Y % 16, None, 0, path, split, None)
+                             Y and 0x50000 + Y % 16, ws and 0x100000 + ws % 256, ws_bytes,
+                             path, ctas, None)
 
 
 def test_gemm_argument_errors(lib):
@@ -91,8 +93,11 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Y=8) == -3
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
-    assert _gemm(lib, split=9) == -1
-    assert _gemm(lib, M=17, path=1, split=4, K=128) == -1   # split above the 2 atoms of K
+    assert _gemm(lib, ctas=-1) == -1
+    assert _gemm(lib, path=2, ctas=4) == -1          # the tensor path takes no CTA count
+    assert _gemm(lib, path=1, ws=0) == -4             # decode needs a workspace
+    assert _gemm(lib, path=1, ws_bytes=16) == -4
+    assert _gemm(lib, path=1, ws=8) == -3             # workspace not 256-byte aligned
 
 
 def test_gemm_m_zero_is_a_noop(lib):
@@ -100,5 +105,12 @@ def test_gemm_m_zero_is_a_noop(lib):
     assert lib.w4a16_gemm(None, None, None, None, 0, 64, 128, 128, None, None, 0, None) == 0
 
 
-def test_workspace_size_is_zero(lib):
-    assert w4.workspace_size(16, 4096, 4096, 128) == 0
+def test_workspace_sizes(lib):
+    # tensor-core path: none; decode path: counters + two fp32 tiles per CTA
+    assert w4.workspace_size(64, 4096, 4096, 128) == 0
+    assert w4.workspace_size(0, 4096, 4096, 128) == 0
+    one = w4.workspace_size(1, 4096, 4096, 128, path="decode", ctas=10)
+    assert one == 256 + 2 * 10 * 8 * 128 * 4
+    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", ctas=10) == 256 + 2 * 10 * 16 * 128 * 4
+    # the CTA count is clamped to the 32 x 2 = 64 work units of this problem
+    assert w4.workspace_size(1, 4096, 128, 128, path="decode", ctas=1000) == 256 + 2 * 64 * 8 * 128 * 4

@@ -17,7 +17,7 @@ from gpu_util import cuda, guarded_output, check_guard, half_bits, prepare, run_
 pytestmark = pytest.mark.gpu
 
 DECODE_CASES = [
-    # M, K, N, group, split
+    # M, K, N, group, ctas (0: automatic)
     (1, 64, 16, 64, 1),
     (1, 128, 16, 128, 2),
     (3, 256, 48, 128, 0),
@@ -33,9 +33,9 @@ DECODE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,K,N,group,split", DECODE_CASES)
-def test_decode_path(M, K, N, group, split):
-    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", split=split)
+@pytest.mark.parametrize("M,K,N,group,ctas", DECODE_CASES)
+def test_decode_path(M, K, N, group, ctas):
+    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", ctas=ctas)
 
 
 @pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (16, 4096, 256, 128),
@@ -48,9 +48,25 @@ def test_outlier_activation_columns():
     run_and_check(4, 4096, 256, 128, seed=5, outliers=True)
 
 
-@pytest.mark.parametrize("split", [1, 2, 3, 4, 8])
-def test_every_split_gives_the_same_tolerance(split):
-    run_and_check(8, 2048, 128, 128, seed=11, path="decode", split=split)
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 31, 32, 33, 1000])
+def test_every_cta_count_meets_the_tolerance(ctas):
+    """1 CTA (every block whole), blocks split unevenly, one unit per CTA, clamping."""
+    run_and_check(8, 2048, 272, 128, seed=11, path="decode", ctas=ctas)
+
+
+def test_workspace_is_left_zeroed_and_reusable():
+    K, N, group = 1024, 400, 128
+    W = synthetic.small_weights(K, N, seed=4)
+    (q, s, z), pw = prepare(W, group)
+    ws = w4.new_workspace(w4.workspace_size(16, N, K, group, path="decode", ctas=9))
+    for M in (1, 5, 16, 3):
+        A = synthetic.small_activations(M, K, seed=M)
+        Y = w4.gemm(cuda(A), pw, path="decode", ctas=9, workspace=ws)
+        w4.device_status()
+        y, mag = oracle.reference(A, q, s, z, group)
+        assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
+        counters = ws[:256].view(torch.int32).cpu().numpy()
+        assert np.all(counters == 0), "counters must be left at zero"
 
 
 def test_integer_product_is_exact():
@@ -64,8 +80,8 @@ def test_integer_product_is_exact():
     exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
     assert np.abs(exact).max() < 2048
     pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
-    for split in (1, 4):
-        Y = w4.gemm(cuda(A), pw, path="decode", split=split)
+    for ctas in (1, 4, 0):
+        Y = w4.gemm(cuda(A), pw, path="decode", ctas=ctas)
         assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
 
 
