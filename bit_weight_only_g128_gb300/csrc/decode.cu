@@ -347,9 +347,13 @@ int decode_ctas_per_sm(int M) {
   return cache[v];
 }
 
+// The counter area has room for the largest legal N (2^20 columns = 8192
+// blocks), whatever N this call has: a workspace can then serve calls of any
+// shape in turn, since no call's partial tiles ever land on another call's
+// counters.
 size_t decode_counter_bytes(int N) {
-  const size_t nblk = (size_t)((N + kDecodeBlockCols - 1) / kDecodeBlockCols);
-  return (nblk * sizeof(int) + 255) / 256 * 256;
+  (void)N;
+  return (size_t)((1 << 20) / kDecodeBlockCols) * sizeof(int);
 }
 
 size_t decode_workspace_bytes(int M, int N, int ctas) {

@@ -114,10 +114,11 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 /* Scratch bytes w4a16_gemm needs for this problem on the current device
  * (0 when none: the tensor-core path). The decode path (M <= 16 rows per
  * launch) finishes output blocks split between CTAs through this workspace:
- * a counter area followed by fp32 partial tiles. The workspace must be
- * zero-filled before its first use; every call leaves it zero-filled again,
- * so one buffer serves any number of calls that run one after another.
- * Calls that may run concurrently (other streams) need separate workspaces.
+ * a 32 KiB counter area (room for any N) followed by fp32 partial tiles. The
+ * counter area must be zero-filled before the first use; every call leaves it
+ * zero-filled again, so one buffer serves any number of calls, of any shape
+ * that fits, that run one after another. Calls that may run concurrently
+ * (other streams) need separate workspaces.
  * Host-only. */
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
 

@@ -109,8 +109,9 @@ def test_workspace_sizes(lib):
     # tensor-core path: none; decode path: counters + two fp32 tiles per CTA
     assert w4.workspace_size(64, 4096, 4096, 128) == 0
     assert w4.workspace_size(0, 4096, 4096, 128) == 0
+    head = 32768   # counters for up to 2^20 / 128 column blocks
     one = w4.workspace_size(1, 4096, 4096, 128, path="decode", ctas=10)
-    assert one == 256 + 2 * 10 * 8 * 128 * 4
-    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", ctas=10) == 256 + 2 * 10 * 16 * 128 * 4
+    assert one == head + 2 * 10 * 8 * 128 * 4
+    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", ctas=10) == head + 2 * 10 * 16 * 128 * 4
     # the CTA count is clamped to the 32 x 2 = 64 work units of this problem
-    assert w4.workspace_size(1, 4096, 128, 128, path="decode", ctas=1000) == 256 + 2 * 64 * 8 * 128 * 4
+    assert w4.workspace_size(1, 4096, 128, 128, path="decode", ctas=1000) == head + 2 * 64 * 8 * 128 * 4

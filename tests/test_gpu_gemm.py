@@ -65,8 +65,24 @@ def test_workspace_is_left_zeroed_and_reusable():
         w4.device_status()
         y, mag = oracle.reference(A, q, s, z, group)
         assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
-        counters = ws[:256].view(torch.int32).cpu().numpy()
+        counters = ws[:32768].view(torch.int32).cpu().numpy()
         assert np.all(counters == 0), "counters must be left at zero"
+
+
+def test_one_workspace_serves_calls_of_different_shapes():
+    """Calls of different N, M and CTA count in turn share one workspace."""
+    shapes = [(1, 1024, 2816), (16, 512, 256), (4, 2048, 1024), (1, 1024, 2816), (9, 640, 4096)]
+    ws = w4.new_workspace(max(w4.workspace_size(16, N, K, 128, path="decode", ctas=300)
+                              for (_, K, N) in shapes))
+    for i, (M, K, N) in enumerate(shapes):
+        W = synthetic.small_weights(K, N, seed=40 + i)
+        A = synthetic.small_activations(M, K, seed=40 + i)
+        (q, s, z), pw = prepare(W, 128)
+        for ctas in (300, 0, 37):
+            Y = w4.gemm(cuda(A), pw, path="decode", ctas=ctas, workspace=ws)
+            w4.device_status()
+            y, mag = oracle.reference(A, q, s, z, 128)
+            assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0, (M, K, N, ctas)
 
 
 def test_integer_product_is_exact():
