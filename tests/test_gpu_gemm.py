@@ -72,8 +72,8 @@ def test_workspace_is_left_zeroed_and_reusable():
 def test_one_workspace_serves_calls_of_different_shapes():
     """Calls of different N, M and CTA count in turn share one workspace."""
     shapes = [(1, 1024, 2816), (16, 512, 256), (4, 2048, 1024), (1, 1024, 2816), (9, 640, 4096)]
-    ws = w4.new_workspace(max(w4.workspace_size(16, N, K, 128, path="decode", ctas=300)
-                              for (_, K, N) in shapes))
+    ws = w4.new_workspace(max(w4.workspace_size(16, N, K, 128, path="decode", ctas=c)
+                              for (_, K, N) in shapes for c in (300, 0, 37)))
     for i, (M, K, N) in enumerate(shapes):
         W = synthetic.small_weights(K, N, seed=40 + i)
         A = synthetic.small_activations(M, K, seed=40 + i)
