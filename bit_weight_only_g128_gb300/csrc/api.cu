@@ -113,6 +113,9 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
                 need, workspace ? workspace_bytes : (size_t)0);
   if (!aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+  if (decode_group_shift(K, group) < 0)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
+                "decode path: group=%d must be K or 64 times a power of two", group);
   // 16 rows per launch; larger M re-streams the weights once per 16 rows
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;

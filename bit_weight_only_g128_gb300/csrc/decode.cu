@@ -34,49 +34,17 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
-constexpr int kPrefetch = 8;                      // weight atoms in flight per warp
 
-// Activation atoms staged per chunk (2048 or 1024 k), and the bytes of one
-// staged row. The extra 64 bytes put consecutive rows in opposite halves of
-// the 32 banks, so the 16-byte fragment loads of a quarter-warp (two rows x
-// 64 bytes) never collide.
+// Weight atoms in flight per warp (even: activations use a 2-deep ring).
 template <int MT>
-__host__ __device__ constexpr int chunk_atoms() { return MT == 1 ? 32 : 16; }
+__host__ __device__ constexpr int prefetch_atoms() { return MT == 1 ? 8 : 4; }
 template <int MT>
-__host__ __device__ constexpr int act_row_bytes() { return chunk_atoms<MT>() * kAtomK * 2 + 64; }
-template <int MT>
-__host__ __device__ constexpr int act_buffer_bytes() { return MT * 8 * act_row_bytes<MT>(); }
-template <int MT>
-__host__ __device__ constexpr int red_bytes() { return MT * 8 * kRedStride * 4; }
-template <int MT>
-__host__ __device__ constexpr int smem_bytes() { return 2 * act_buffer_bytes<MT>() + red_bytes<MT>(); }
+__host__ __device__ constexpr int smem_bytes() { return MT * 8 * kRedStride * 4; }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-// Copy the activations of atoms [a0, a1) (rows 0..M-1) into a chunk buffer.
-template <int MT>
-__device__ __forceinline__ void stage_activations(uint32_t buf, const uint16_t* __restrict__ A,
-                                                  int M, int K, int a0, int a1) {
-  const int units = (a1 - a0) * (kAtomK / 8);  // 16-byte units per row
-  for (int idx = threadIdx.x; idx < M * units; idx += kThreads) {
-    const int row = idx / units, u = idx % units;
-    cp_async16(buf + row * act_row_bytes<MT>() + u * 16,
-               A + (size_t)row * K + (size_t)a0 * kAtomK + u * 8);
-  }
+// 16-byte activation load, kept in L1: the 8 warps of a CTA read the same
+// activations (same atoms, different strips).
+__device__ __forceinline__ uint4 ldg_act(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
 // CTA that owns unit u when T units are split among C CTAs.
@@ -84,166 +52,170 @@ __device__ __forceinline__ int owner_cta(long long u, long long T, int C) {
   return (int)(((u + 1) * C - 1) / T);
 }
 
-// Partial sums of strip `strip` over atoms [a_begin, a_end) for this lane's
-// fragment: acc[s][o] (two independent accumulator chains, s = k-half).
+struct DecodeArgs {
+  const uint16_t* A;
+  const uint4* Wq;
+  const uint32_t* Sp2;  // scale pairs (s[c], s[c+8])
+  const uint8_t* Zp;    // zero-point pairs z[c] | z[c+8] << 4
+  uint16_t* Y;
+  int* counters;
+  float* tiles;
+  int M, N, K;
+  int gshift;  // group index of atom a is a >> gshift
+};
+
+// MT: token octets (1: M <= 8, 2: M <= 16).
 template <int MT>
-__device__ __forceinline__ void segment_mainloop(
-    float (&acc)[2][MT][4], const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
-    const uint32_t* __restrict__ Sp2, const uint2* __restrict__ Zp, int M, int K, int group,
-    int strip, bool active, int a_begin, int a_end, uint32_t sbase) {
-  constexpr int U = kPrefetch;
-  constexpr int CH = chunk_atoms<MT>();
-  constexpr int kRow = act_row_bytes<MT>();
-  constexpr int kBuf = act_buffer_bytes<MT>();
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p) {
+  constexpr int U = prefetch_atoms<MT>();
+  extern __shared__ __align__(16) float red[];  // partial tile [token][column]
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;  // mma groupID / thread-in-group
+  const int N = p.N, K = p.K, M = p.M;
+  const int nstrips = N / kStripCols;
+  const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
   const int natoms = K / kAtomK;
-  const int G = K / group;
-  const int apg = group / kAtomK;  // atoms per group
+  const int gshift = p.gshift;
+  const int gmask = (1 << gshift) - 1;
+  const int groups = (natoms + gmask) >> gshift;  // groups per strip (1 when per-channel)
+  const int C = gridDim.x;
+  const int T = nblk * natoms;  // < 2^27 for legal shapes
+  const int u_begin = (int)((long long)blockIdx.x * T / C);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * T / C);
+  const int first_blk = u_begin / natoms;
+  constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;  // one partial tile in the workspace
 
-  const uint4* wp = Wq + (size_t)(active ? strip : 0) * natoms * 32 + lane;
-  const uint32_t* sp = Sp2 + (size_t)(active ? strip : 0) * G * 8 + gq;  // (s[gq], s[gq+8])
-  const uint2* zp = Zp + (size_t)(active ? strip : 0) * G;
-
+  // activation rows of this lane's fragment (rows >= M read row M-1; their
+  // products land in accumulator columns that are never stored)
+  const uint16_t* arow[MT];
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
-#pragma unroll
-    for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
+  for (int o = 0; o < MT; ++o) arow[o] = p.A + (size_t)min(8 * o + gq, M - 1) * K + 8 * t;
 
-  // Slot u holds the atom a with (a - a_begin) % U == u: its weights, and the
-  // scale pair / zero words of its group when it is the first atom of a group
-  // (or of the range). The load stream runs U atoms ahead of consumption.
+  // ---- load stream: units u_begin.. in order, U units ahead of consumption
+  int l_unit = u_begin;
+  int l_blk = first_blk;
+  int l_atom = u_begin - first_blk * natoms;
+  int l_strip = l_blk * kWarps + warp;
+  bool l_active = l_strip < nstrips;
+  const uint4* l_ptr = p.Wq + ((size_t)(l_active ? l_strip : 0) * natoms + l_atom) * 32 + lane;
+  const uint32_t* l_sp = p.Sp2 + (size_t)(l_active ? l_strip : 0) * groups * 8 + gq;
+  const uint8_t* l_zp = p.Zp + (size_t)(l_active ? l_strip : 0) * groups * 8 + gq;
+
   uint4 w[U];
   uint32_t ms[U];
-  uint2 mz[U];
-  int l_atom = a_begin, l_grp = a_begin / apg, l_rem = a_begin % apg;
-  if (active) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (l_atom < a_end) {
-        w[u] = ldg_stream(wp + (size_t)l_atom * 32);
-        if (u == 0 || l_rem == 0) {
-          ms[u] = __ldg(sp + (size_t)l_grp * 8);
-          mz[u] = __ldg(zp + l_grp);
-        }
-        ++l_atom;
-        if (++l_rem == apg) {
-          l_rem = 0;
-          ++l_grp;
+  uint32_t mz[U];
+  // advance the load stream by one unit into slot `u`; group constants are
+  // fetched at group starts and for the first unit of the run
+  auto refill = [&](int u, bool first) {
+    if (l_unit < u_end) {
+      if (l_active) {
+        w[u] = ldg_stream(l_ptr);
+        if (first || (l_atom & gmask) == 0) {
+          const int g = l_atom >> gshift;
+          ms[u] = __ldg(l_sp + (size_t)g * 8);
+          mz[u] = __ldg(l_zp + (size_t)g * 8);
         }
       }
+      ++l_unit;
+      l_ptr += 32;
+      if (++l_atom == natoms) {  // next block: strip `warp` of it
+        l_atom = 0;
+        ++l_blk;
+        l_strip = l_blk * kWarps + warp;
+        l_active = l_strip < nstrips;
+        l_ptr = p.Wq + (size_t)(l_active ? l_strip : 0) * natoms * 32 + lane;
+        l_sp = p.Sp2 + (size_t)(l_active ? l_strip : 0) * groups * 8 + gq;
+        l_zp = p.Zp + (size_t)(l_active ? l_strip : 0) * groups * 8 + gq;
+      }
     }
-  }
-  int c_rem = a_begin % apg;  // position of the consumed atom inside its group
-  DeqConst d0 = {}, d1 = {};
+  };
+#pragma unroll
+  for (int u = 0; u < U; ++u) refill(u, u == 0);
 
-  const int nchunks = (a_end - a_begin + CH - 1) / CH;
-  stage_activations<MT>(sbase, A, M, K, a_begin, min(a_end, a_begin + CH));
-  cp_async_commit();
-  for (int c = 0; c < nchunks; ++c) {
-    const int c0 = a_begin + c * CH;
-    const int c1 = min(a_end, c0 + CH);
-    if (c + 1 < nchunks) {  // next chunk into the other buffer
-      stage_activations<MT>(sbase + ((c + 1) & 1) * kBuf, A, M, K, c1, min(a_end, c1 + CH));
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    // lane's fragment row and column inside the chunk buffer
-    const uint32_t abuf = sbase + (c & 1) * kBuf + gq * kRow + 16 * t;
-    if (active) {
-      for (int a = c0; a < c1; a += U) {
+  // ---- activation ring: unit x uses act[(x - u_begin) & 1]; 2 units ahead
+  uint4 act[2][2][MT];
+  auto load_act = [&](int slot, int atom) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int au = a + u;
-          if (au < c1) {  // warp-uniform; false only in the last batch of the range
-            const uint4 cw = w[u];
-            if (c_rem == 0 || au == a_begin) {  // first atom of a group: new constants
-              const uint32_t z0 = (mz[u].x >> (4 * gq)) & 15u, z1 = (mz[u].y >> (4 * gq)) & 15u;
-              d0 = make_deq_const(z0, (uint16_t)(ms[u] & 0xffffu));
-              d1 = make_deq_const(z1, (uint16_t)(ms[u] >> 16));
+    for (int o = 0; o < MT; ++o)
+#pragma unroll
+      for (int s = 0; s < 2; ++s) act[slot][s][o] = ldg_act(arow[o] + (size_t)atom * kAtomK + 32 * s);
+  };
+  {
+    const int a0 = u_begin - first_blk * natoms;
+    load_act(0, a0);
+    if (u_begin + 1 < u_end) load_act(1, a0 + 1 < natoms ? a0 + 1 : 0);
+  }
+
+  for (int s0 = u_begin; s0 < u_end;) {
+    // segment [s0, s1): atoms [a0, a1) of block b
+    const int b = s0 / natoms;
+    const int a0 = s0 - b * natoms;
+    const int s1 = min(u_end, (b + 1) * natoms);
+    const int a1 = s1 - b * natoms;
+    const bool active = b * kWarps + warp < nstrips;
+
+    float acc[2][MT][4];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
+    int cur_grp = -1;
+    DeqConst d0 = {}, d1 = {};
+    int c_atom = a0;  // atom of the unit being consumed
+
+    // batches aligned to the run start keep slot indices compile-time constants
+    for (int ub = u_begin + (s0 - u_begin) / U * U; ub < s1; ub += U) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int x = ub + u;
+        if (x >= s0 && x < s1) {  // warp-uniform
+          const uint4 cw = w[u];
+          const uint32_t cms = ms[u];
+          const uint32_t cmz = mz[u];
+          refill(u, false);
+          uint4 ca[2][MT];
+#pragma unroll
+          for (int o = 0; o < MT; ++o) {
+            ca[0][o] = act[u & 1][0][o];
+            ca[1][o] = act[u & 1][1][o];
+          }
+          if (x + 2 < u_end) {  // atom of unit x + 2 (the run may wrap into the next block)
+            int na = c_atom + 2;
+            if (na >= natoms) na -= natoms;
+            if (na >= natoms) na -= natoms;  // K = 64: one atom per block
+            load_act(u & 1, na);
+          }
+          if (active) {
+            const int grp = c_atom >> gshift;
+            if (grp != cur_grp) {  // first atom of a group (or of the segment)
+              cur_grp = grp;
+              d0 = make_deq_const(cmz & 15u, (uint16_t)(cms & 0xffffu));
+              d1 = make_deq_const((cmz >> 4) & 15u, (uint16_t)(cms >> 16));
             }
-            if (++c_rem == apg) c_rem = 0;
-            if (l_atom < a_end) {  // refill this slot with the atom U ahead
-              w[u] = ldg_stream(wp + (size_t)l_atom * 32);
-              if (l_rem == 0) {
-                ms[u] = __ldg(sp + (size_t)l_grp * 8);
-                mz[u] = __ldg(zp + l_grp);
-              }
-              ++l_atom;
-              if (++l_rem == apg) {
-                l_rem = 0;
-                ++l_grp;
-              }
-            }
-            // B fragments: token 8o+gq, k = 64au + 32s + 8t .. +7
-            uint4 act[2][MT];
-#pragma unroll
-            for (int o = 0; o < MT; ++o)
-#pragma unroll
-              for (int s = 0; s < 2; ++s)
-                act[s][o] = lds128(abuf + o * 8 * kRow + ((au - c0) * kAtomK + 32 * s) * 2);
-            uint32_t p[4][4];
-            dequant_word(cw.x, d0, p[0]);  // k-half 0, column gq
-            dequant_word(cw.y, d1, p[1]);  // k-half 0, column gq + 8
-            dequant_word(cw.z, d0, p[2]);  // k-half 1, column gq
-            dequant_word(cw.w, d1, p[3]);  // k-half 1, column gq + 8
+            uint32_t q[4][4];
+            dequant_word(cw.x, d0, q[0]);  // k-half 0, column gq
+            dequant_word(cw.y, d1, q[1]);  // k-half 0, column gq + 8
+            dequant_word(cw.z, d0, q[2]);  // k-half 1, column gq
+            dequant_word(cw.w, d1, q[3]);  // k-half 1, column gq + 8
 #pragma unroll
             for (int o = 0; o < MT; ++o) {
 #pragma unroll
               for (int s = 0; s < 2; ++s) {
-                const uint32_t* lo = p[2 * s];
-                const uint32_t* hi = p[2 * s + 1];
-                mma_16816(acc[s][o], lo[0], hi[0], lo[1], hi[1], act[s][o].x, act[s][o].y);
-                mma_16816(acc[s][o], lo[2], hi[2], lo[3], hi[3], act[s][o].z, act[s][o].w);
+                const uint32_t* lo = q[2 * s];
+                const uint32_t* hi = q[2 * s + 1];
+                mma_16816(acc[s][o], lo[0], hi[0], lo[1], hi[1], ca[s][o].x, ca[s][o].y);
+                mma_16816(acc[s][o], lo[2], hi[2], lo[3], hi[3], ca[s][o].z, ca[s][o].w);
               }
             }
           }
+          ++c_atom;
         }
       }
     }
-    __syncthreads();  // buffer (c & 1) is refilled by the copies issued next iteration
-  }
-}
 
-// MT: token octets (1: M <= 8, 2: M <= 16).
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2)
-decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
-              const uint32_t* __restrict__ Sp2, const uint2* __restrict__ Zp,
-              uint16_t* __restrict__ Y, int M, int N, int K, int group, int* __restrict__ counters,
-              float* __restrict__ tiles) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  float* red = reinterpret_cast<float*>(smem + 2 * act_buffer_bytes<MT>());
-  __shared__ int s_last;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, t = lane & 3;
-  const int nstrips = N / kStripCols;
-  const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
-  const int natoms = K / kAtomK;
-  const int C = gridDim.x;
-  const long long T = (long long)nblk * natoms;
-  const long long u_begin = (long long)blockIdx.x * T / C;
-  const long long u_end = (long long)(blockIdx.x + 1) * T / C;
-  const int first_blk = (int)(u_begin / natoms);
-  constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;  // one partial tile in the workspace
-
-  for (long long u = u_begin; u < u_end;) {
-    const int b = (int)(u / natoms);
-    const int a0 = (int)(u - (long long)b * natoms);
-    const int a1 = (int)min((long long)natoms, u_end - (long long)b * natoms);
-    u = (long long)(b + 1) * natoms;
-
-    const int strip = b * kWarps + warp;
-    const bool active = strip < nstrips;
-    float acc[2][MT][4];
-    segment_mainloop<MT>(acc, A, Wq, Sp2, Zp, M, K, group, strip, active, a0, a1, sbase);
-
-    // partial tile [token][column] of this segment
+    // ---- segment epilogue: partial tile [token][column] in shared memory
     if (active) {
 #pragma unroll
       for (int o = 0; o < MT; ++o) {
@@ -262,13 +234,13 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
       for (int e = threadIdx.x; e < total; e += kThreads) {
         const int tok = e / kDecodeBlockCols, col = e % kDecodeBlockCols;
         if (col0 + col < N)
-          Y[(size_t)tok * N + col0 + col] =
+          p.Y[(size_t)tok * N + col0 + col] =
               __half_as_ushort(__float2half_rn(red[tok * kRedStride + col]));
       }
     } else {
       // publish the partial tile, then count this CTA in
       const int slot = 2 * blockIdx.x + (b == first_blk ? 0 : 1);
-      float* my = tiles + (size_t)slot * kTileFloats;
+      float* my = p.tiles + (size_t)slot * kTileFloats;
       for (int e = threadIdx.x; e < total; e += kThreads) {
         const int tok = e / kDecodeBlockCols, col = e % kDecodeBlockCols;
         my[e] = red[tok * kRedStride + col];
@@ -278,7 +250,7 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
       const int c_first = owner_cta((long long)b * natoms, T, C);
       const int c_last = owner_cta((long long)b * natoms + natoms - 1, T, C);
       if (threadIdx.x == 0) {
-        const int old = atomicAdd(counters + b, 1);
+        const int old = atomicAdd(p.counters + b, 1);
         s_last = (old == c_last - c_first);
       }
       __syncthreads();
@@ -291,15 +263,16 @@ decode_kernel(const uint16_t* __restrict__ A, const uint4* __restrict__ Wq,
           for (int c = c_first; c <= c_last; ++c) {  // fixed order: deterministic
             const int cfirst_blk = (int)(((long long)c * T / C) / natoms);
             const int cslot = 2 * c + (b == cfirst_blk ? 0 : 1);
-            sum += __ldcg(tiles + (size_t)cslot * kTileFloats + e);
+            sum += __ldcg(p.tiles + (size_t)cslot * kTileFloats + e);
           }
           const int tok = e / kDecodeBlockCols;
-          Y[(size_t)tok * N + col0 + col] = __half_as_ushort(__float2half_rn(sum));
+          p.Y[(size_t)tok * N + col0 + col] = __half_as_ushort(__float2half_rn(sum));
         }
-        if (threadIdx.x == 0) counters[b] = 0;  // ready for the next call
+        if (threadIdx.x == 0) p.counters[b] = 0;  // ready for the next call
       }
     }
     __syncthreads();  // the partial tile buffer is reused by the next segment
+    s0 = s1;
   }
 }
 
@@ -312,19 +285,21 @@ cudaError_t prepare_decode_kernels() {
     if (state == cudaSuccess)
       state = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    smem_bytes<2>());
+    if (state == cudaSuccess)
+      state = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxL1);
+    if (state == cudaSuccess)
+      state = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxL1);
   }
   return state;
 }
 
 template <int MT>
-cudaError_t launch_mt(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
-                      const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group, int ctas,
-                      int* counters, float* tiles, cudaStream_t stream) {
+cudaError_t launch_mt(const DecodeArgs& args, int ctas, cudaStream_t stream) {
   const cudaError_t prep = prepare_decode_kernels();
   if (prep != cudaSuccess) return prep;
-  decode_kernel<MT><<<ctas, kThreads, smem_bytes<MT>(), stream>>>(
-      A, reinterpret_cast<const uint4*>(Wq), reinterpret_cast<const uint32_t*>(Sp),
-      reinterpret_cast<const uint2*>(Zp), Y, M, N, K, group, counters, tiles);
+  decode_kernel<MT><<<ctas, kThreads, smem_bytes<MT>(), stream>>>(args);
   return cudaGetLastError();
 }
 
@@ -365,11 +340,33 @@ size_t decode_workspace_bytes(int M, int N, int ctas) {
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int ctas, void* workspace, cudaStream_t stream) {
-  int* counters = static_cast<int*>(workspace);
-  float* tiles =
-      reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + decode_counter_bytes(N));
-  if (M <= 8) return launch_mt<1>(A, Wq, Sp, Zp, Y, M, N, K, group, ctas, counters, tiles, stream);
-  return launch_mt<2>(A, Wq, Sp, Zp, Y, M, N, K, group, ctas, counters, tiles, stream);
+  DecodeArgs args;
+  args.A = A;
+  args.Wq = reinterpret_cast<const uint4*>(Wq);
+  args.Sp2 = reinterpret_cast<const uint32_t*>(Sp);
+  args.Zp = reinterpret_cast<const uint8_t*>(Zp);
+  args.Y = Y;
+  args.counters = static_cast<int*>(workspace);
+  args.tiles = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + decode_counter_bytes(N));
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.gshift = decode_group_shift(K, group);
+  if (args.gshift < 0) return cudaErrorInvalidValue;
+  if (M <= 8) return launch_mt<1>(args, ctas, stream);
+  return launch_mt<2>(args, ctas, stream);
+}
+
+// Group index of atom a is a >> shift: log2(group/64) for power-of-two
+// groups, 30 (always group 0) for one group per column; -1 otherwise.
+int decode_group_shift(int K, int group) {
+  const int apg = group / kAtomK;
+  if (apg > 0 && (apg & (apg - 1)) == 0) {
+    int sh = 0;
+    while ((1 << sh) < apg) ++sh;
+    return sh;
+  }
+  return group == K ? 30 : -1;
 }
 
 }  // namespace w4a16

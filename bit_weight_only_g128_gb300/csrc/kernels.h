@@ -28,6 +28,9 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
 size_t decode_workspace_bytes(int M, int N, int ctas);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
+// Shift that maps an atom index to its group (see decode.cu); -1 if the
+// group size is not supported by the decode kernel.
+int decode_group_shift(int K, int group);
 
 // tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile.
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,

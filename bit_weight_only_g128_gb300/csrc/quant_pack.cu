@@ -80,7 +80,9 @@ __global__ void pack_weights_kernel(const uint8_t* __restrict__ q, int K, int N,
   Wq[widx] = word;
 }
 
-// One thread per (strip, group, half): 8 zero points and 8 scales.
+// One thread per (strip, group, half h): the 8 scales of columns 16j+8h+c
+// (interleaved with the other half), and zero-point word h, whose bytes
+// 4h..4h+3 pair the zero points of columns 16j+c and 16j+8+c.
 __global__ void pack_meta_kernel(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z,
                                  int K, int N, int group, uint16_t* __restrict__ Sp,
                                  uint32_t* __restrict__ Zp) {
@@ -94,8 +96,13 @@ __global__ void pack_meta_kernel(const uint16_t* __restrict__ s, const uint8_t* 
   uint32_t word = 0;
   for (int c = 0; c < 8; ++c) {
     const int n = kStripCols * j + 8 * h + c;
-    word |= (uint32_t)(z[(size_t)grp * N + n] & 15u) << (4 * c);
     Sp[jg * 16 + 2 * c + h] = s[(size_t)grp * N + n];
+  }
+  for (int b = 0; b < 4; ++b) {
+    const int c = 4 * h + b;  // byte c of the record
+    const uint32_t lo = z[(size_t)grp * N + kStripCols * j + c] & 15u;
+    const uint32_t hi = z[(size_t)grp * N + kStripCols * j + 8 + c] & 15u;
+    word |= (lo | (hi << 4)) << (8 * b);
   }
   Zp[idx] = word;
 }
@@ -125,8 +132,13 @@ __global__ void unpack_meta_kernel(const uint16_t* __restrict__ Sp, const uint32
   const uint32_t word = Zp[idx];
   for (int c = 0; c < 8; ++c) {
     const int n = kStripCols * j + 8 * h + c;
-    z[(size_t)grp * N + n] = (uint8_t)((word >> (4 * c)) & 15u);
     s[(size_t)grp * N + n] = Sp[jg * 16 + 2 * c + h];
+  }
+  for (int b = 0; b < 4; ++b) {
+    const int c = 4 * h + b;
+    const uint32_t byte = (word >> (8 * b)) & 0xffu;
+    z[(size_t)grp * N + kStripCols * j + c] = (uint8_t)(byte & 15u);
+    z[(size_t)grp * N + kStripCols * j + 8 + c] = (uint8_t)(byte >> 4);
   }
 }
 
@@ -142,8 +154,8 @@ __global__ void dequantize_kernel(const uint32_t* __restrict__ Wq, const uint16_
   const int j = n / kStripCols, c = n % kStripCols;
   const int grp = k0 / group;
   const size_t jg = (size_t)j * G + grp;
-  const uint32_t zw = Zp[jg * 2 + (c >> 3)];
-  const DeqConst dc = make_deq_const((zw >> (4 * (c & 7))) & 15u, Sp[jg * 16 + 2 * (c & 7) + (c >> 3)]);
+  const uint32_t zbyte = reinterpret_cast<const uint8_t*>(Zp)[jg * 8 + (c & 7)];
+  const DeqConst dc = make_deq_const((zbyte >> (4 * (c >> 3))) & 15u, Sp[jg * 16 + 2 * (c & 7) + (c >> 3)]);
   uint32_t pairs[4];
   dequant_word(Wq[widx], dc, pairs);
 #pragma unroll

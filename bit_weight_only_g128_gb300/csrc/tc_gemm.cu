@@ -305,15 +305,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool valid = strip < p.N / kStripCols;
     const int G = p.K / p.group;
     const uint32_t* sp = reinterpret_cast<const uint32_t*>(p.Sp) + (size_t)(valid ? strip : 0) * G * 8 + gq;
-    const uint32_t* zp = p.Zp + (size_t)(valid ? strip : 0) * G * 2;
+    const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp) + (size_t)(valid ? strip : 0) * G * 8 + gq;
     // process the lane's words in an order that keeps the 16-byte stores of
     // each quarter-warp on distinct banks (odd rows take the other k-half first)
     const uint32_t flip = (uint32_t)(gq & 1);
-    uint32_t pre_s = 0, pre_z0 = 0, pre_z1 = 0;  // next group's constants, prefetched
+    uint32_t pre_s = 0, pre_z = 0;  // next group's (s[gq], s[gq+8]) and zero-point pair
     if (valid) {
-      pre_s = sp[0];  // (s[gq], s[gq + 8])
-      pre_z0 = zp[0];
-      pre_z1 = zp[1];
+      pre_s = sp[0];
+      pre_z = zp[0];
     }
     DeqConst d0 = {}, d1 = {};
     int cur_grp = -1;
@@ -325,13 +324,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (valid) {
         const int grp = kb * kStageK / p.group;
         if (grp != cur_grp) {
-          d0 = make_deq_const((pre_z0 >> (4 * gq)) & 15u, (uint16_t)(pre_s & 0xffffu));
-          d1 = make_deq_const((pre_z1 >> (4 * gq)) & 15u, (uint16_t)(pre_s >> 16));
+          d0 = make_deq_const(pre_z & 15u, (uint16_t)(pre_s & 0xffffu));
+          d1 = make_deq_const((pre_z >> 4) & 15u, (uint16_t)(pre_s >> 16));
           cur_grp = grp;
           if (grp + 1 < G) {
             pre_s = sp[(grp + 1) * 8];
-            pre_z0 = zp[(grp + 1) * 2];
-            pre_z1 = zp[(grp + 1) * 2 + 1];
+            pre_z = zp[(grp + 1) * 8];
           }
         }
         const uint4 v = lds128(st + act_bytes + kWdqBytes + dw * 512 + lane * 16);

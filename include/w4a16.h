@@ -48,8 +48,10 @@
  *   Sp: fp16, N*G of them; offset (j*G + grp)*16 + 2c + h is the scale of
  *     column 16j + 8h + c (c in [0,8), h in {0,1}) in group grp, so the two
  *     columns g and g + 8 that one lane dequantizes share one 32-bit word.
- *   Zp: uint32, N*G/8 of them; offset (j*G + grp)*2 + h holds in nibble c
- *     the zero point of column 16j + 8h + c in group grp.
+ *   Zp: bytes, N*G/2 of them (addressed as uint32 words); byte
+ *     (j*G + grp)*8 + c holds the zero point of column 16j + c in its low
+ *     nibble and that of column 16j + 8 + c in its high nibble (c in [0,8)),
+ *     again the two columns one lane dequantizes.
  *   Sizes: w4a16_packed_sizes(). Alignment: Wq, Sp, A and Y 16-byte aligned,
  *   Zp 8-byte aligned (W4A16_ERR_MISALIGNED otherwise).
  */
@@ -141,7 +143,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * the decode path, the number of persistent CTAs that share the work
  * (0 = automatic; clamped to the number of 128-column x 64-k work units).
  * The decode path handles any M in launches of 16 rows (it streams the
- * weights once per launch); the tensor path takes ctas = 0. */
+ * weights once per launch) and needs group == K or group = 64 * 2^j
+ * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise); the tensor path takes ctas = 0. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,

@@ -258,8 +258,8 @@ double oracle_check(const uint16_t* y_gpu, const double* y_ref, const double* ma
 /* 8t + e, e = 0..7.  Value e sits in nibble p (bits 4p..4p+3) with         */
 /* p = e/2 for even e and p = 4 + (e-1)/2 for odd e.                        */
 /* Scales: fp16 at offset (j*G + grp)*16 + 2*(c%8) + c/8 for column 16j+c. */
-/* Zeros: uint32 at offset (j*G + grp)*2 + h; nibble c holds the zero of    */
-/* column 16j + 8h + c.                                                     */
+/* Zeros: bytes; byte (j*G + grp)*8 + c (c < 8) holds the zero of column    */
+/* 16j + c in its low nibble and of column 16j + 8 + c in its high nibble.  */
 /* ---------------------------------------------------------------------- */
 
 static int nibble_of(int e)
@@ -293,7 +293,8 @@ void oracle_pack(const uint8_t* q, const uint8_t* z, const uint16_t* s16,
             int j = n / 16, c = n % 16;
             Sp[((size_t)j * G + grp) * 16 + 2 * (c % 8) + c / 8] = s16[(size_t)grp * N + n];
             uint32_t v = z[(size_t)grp * N + n] & 15u;
-            Zp[((size_t)j * G + grp) * 2 + c / 8] |= v << (4 * (c % 8));
+            /* byte (j*G + grp)*8 + c%8 of the little-endian word array, nibble c/8 */
+            Zp[((size_t)j * G + grp) * 2 + (c % 8) / 4] |= v << (8 * ((c % 8) % 4) + 4 * (c / 8));
         }
 }
 
@@ -310,7 +311,8 @@ void oracle_unpack(const uint32_t* Wp, const uint16_t* Sp, const uint32_t* Zp,
             int j = n / 16, c = n % 16;
             s16[(size_t)grp * N + n] = Sp[((size_t)j * G + grp) * 16 + 2 * (c % 8) + c / 8];
             z[(size_t)grp * N + n] =
-                (uint8_t)((Zp[((size_t)j * G + grp) * 2 + c / 8] >> (4 * (c % 8))) & 15u);
+                (uint8_t)((Zp[((size_t)j * G + grp) * 2 + (c % 8) / 4] >>
+                           (8 * ((c % 8) % 4) + 4 * (c / 8))) & 15u);
         }
 }
 

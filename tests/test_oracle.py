@@ -262,14 +262,14 @@ def test_pack_single_nibble_position():
     q = np.zeros((K, N), np.uint8)
     q[9, 3] = 0xA          # atom 0, s=0, t=1, e=1 -> nibble 4; g=3, r=0 -> lane 13, i=0
     z = np.zeros((1, N), np.uint8)
-    z[0, 11] = 0x7         # h=1, c=3 -> word 1, nibble 3
+    z[0, 11] = 0x7         # column 8 + 3 -> byte 3 (word 0, bits 24..31), high nibble
     s = np.zeros((1, N), np.uint16)
     s[0, 11] = 0x1234
     Wp, Sp, Zp = oracle.pack(q, z, s, 64)
     expect = np.zeros(K * N // 8, np.uint32)
     expect[4 * 13 + 0] = 0xA << 16
     assert np.array_equal(Wp, expect)
-    assert Zp.tolist() == [0, 0x7 << 12]
+    assert Zp.tolist() == [0x7 << 28, 0]
     assert Sp[7] == 0x1234 and np.count_nonzero(Sp) == 1   # column 11 = 8*1 + 3 -> 2*3 + 1
 
 
@@ -283,7 +283,8 @@ def test_pack_follows_layout_text_and_round_trips(K, N, group):
         j, c = divmod(n, 16)
         for grp in range(G):
             assert Sp[(j * G + grp) * 16 + 2 * (c % 8) + c // 8] == s[grp, n]
-            word = int(Zp[(j * G + grp) * 2 + c // 8])
-            assert (word >> (4 * (c % 8))) & 15 == z[grp, n]
+            zbytes = Zp.view(np.uint8)   # little-endian bytes of the word array
+            byte = int(zbytes[(j * G + grp) * 8 + c % 8])
+            assert (byte >> (4 * (c // 8))) & 15 == z[grp, n]
     q2, s2, z2 = oracle.unpack(Wp, Sp, Zp, K, N, group)
     assert np.array_equal(q2, q) and np.array_equal(s2, s) and np.array_equal(z2, z)
