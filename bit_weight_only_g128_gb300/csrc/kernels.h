@@ -18,19 +18,21 @@ cudaError_t launch_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t
 cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
                               int N, int group, uint16_t* deq, cudaStream_t stream);
 
-// Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
-// persistent CTAs, 1 <= ctas <= ceil(N/128) * K/64). `workspace` holds the
-// per-block counters (zero before the first call, left zero by every call)
-// followed by the partial tiles; see decode_workspace_bytes.
+// Split-K register-dequant GEMV for M <= 16 rows of A (one launch, grid
+// (split, N/128)). With split > 1, `workspace` holds the per-block counters
+// (zero before the first call, left zero by every call) followed by the
+// partial tiles; see decode_workspace_bytes (0 when split == 1).
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int ctas, void* workspace, cudaStream_t stream);
-size_t decode_workspace_bytes(int M, int N, int ctas);
+                          int split, void* workspace, cudaStream_t stream);
+size_t decode_workspace_bytes(int M, int N, int split);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
-// Shift that maps an atom index to its group (see decode.cu); -1 if the
-// group size is not supported by the decode kernel.
-int decode_group_shift(int K, int group);
+// Largest split of K the decode kernel supports for this group size (0: the
+// group size is not supported by the decode kernel).
+int decode_max_split(int K, int group);
+// CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
+int decode_ctas_per_sm(int M);
 
 // tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile.
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
@@ -43,9 +45,6 @@ size_t tc_smem_bytes(int bt, int* stages);
 // Reads the device error word (bounded waits that gave up, self-checks) and
 // clears it if set.
 cudaError_t read_and_clear_device_error(int* flag);
-
-// CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
-int decode_ctas_per_sm(int M);
 
 // Output columns per decode CTA.
 constexpr int kDecodeBlockCols = 128;
