@@ -175,10 +175,10 @@ def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
     return deq
 
 
-def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", split: int = 0) -> int:
-    """Scratch bytes a gemm call needs (0 for the tensor-core path or no split)."""
+def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", ctas: int = 0) -> int:
+    """Scratch bytes a gemm call needs (0 for the tensor-core path)."""
     b = ctypes.c_size_t()
-    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], split, ctypes.byref(b)),
+    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], ctas, ctypes.byref(b)),
            "w4a16_workspace_size")
     return b.value
 
@@ -189,14 +189,14 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
 
 
 def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
-    """(path, decode split of K) the library picks for this problem."""
+    """(path, decode CTA count) the library picks for this problem."""
     p, c = ctypes.c_int(), ctypes.c_int()
     _check(lib().w4a16_plan(M, N, K, group, ctypes.byref(p), ctypes.byref(c)), "w4a16_plan")
     return {v: k for k, v in _PATHS.items()}[p.value], c.value
 
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
-         path: str = "auto", split: int = 0, workspace: Optional[torch.Tensor] = None,
+         path: str = "auto", ctas: int = 0, workspace: Optional[torch.Tensor] = None,
          stream=None) -> torch.Tensor:
     """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
 
@@ -209,7 +209,7 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     if out is None:
         out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group, path, split)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, ctas)
     if need:
         if workspace is None:
             workspace = new_workspace(need, A.device)
@@ -217,7 +217,7 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
-                               _PATHS[path], split, _stream(stream)), "w4a16_gemm")
+                               _PATHS[path], ctas, _stream(stream)), "w4a16_gemm")
     return out
 
 

@@ -63,52 +63,31 @@ int sm_count() {
   return sms;
 }
 
-// Split of K for the decode kernel (grid: split x ceil(N/128) CTAs). Among
-// splits that keep at least 8 atoms (512 k) per range, take the one whose
-// CTAs fill the device's resident slots best: whole waves (total / (waves *
-// slots)) times the evenness of the ranges (mean / longest). Ties (within
-// 2%) go to the smaller split: fewer partial tiles to reduce. A requested
-// split is clamped to the ranges K can be cut into.
-int decode_split(int M, int N, int K, int group, int requested) {
-  const int max_split = decode_max_split(K, group);
-  if (max_split <= 0) return 0;
-  if (requested > 0) return requested < max_split ? requested : max_split;
-  const int natoms = K / kAtomK;
-  const int gran = natoms / max_split;
-  const long nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
-  const long slots = (long)sm_count() * decode_ctas_per_sm(M);
-  int best = 1;
-  double best_eff = -1.0;
-  for (int split = 1; split <= max_split && split <= 64; ++split) {
-    if (split > 1 && natoms / split < 8) break;
-    const long total = nblk * split;
-    const long waves = (total + slots - 1) / slots;
-    const int longest = (max_split + split - 1) / split * gran;
-    const double eff = ((double)total / (double)(waves * slots)) *
-                       ((double)natoms / split / (double)longest);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = split;
-    }
-  }
-  return best;
+// Persistent CTAs of the decode kernel: every resident slot of the device,
+// but never more than the work units (each CTA must own at least one).
+int decode_ctas(int M, int N, int K, int group, int requested) {
+  const long T = decode_units(N, K, group);
+  if (T <= 0) return 0;
+  long c = requested > 0 ? requested : (long)sm_count() * decode_ctas_per_sm(M);
+  if (c > T) c = T;
+  return (int)c;
 }
 
 // Decode GEMV up to 16 rows; tensor-core GEMM above.
 int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
 
-// Scratch bytes of a (path, split) choice: the decode path's counters and
-// partial tiles when it splits K (16-row chunks share one workspace); none
-// for tensor cores.
-size_t workspace_for(int M, int N, int K, int group, int path, int split) {
+// Scratch bytes of a (path, ctas) choice: the decode path's counters and
+// partial tiles (16-row chunks share one workspace); none for tensor cores.
+size_t workspace_for(int M, int N, int K, int group, int path, int ctas) {
   if (M == 0 || path != W4A16_PATH_DECODE) return 0;
   const int rows = M < 16 ? M : 16;
-  return decode_workspace_bytes(rows, N, decode_split(rows, N, K, group, split));
+  const int c = decode_ctas(rows, N, K, group, ctas);
+  return c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
 }
 
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
               const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-              void* workspace, size_t workspace_bytes, int path, int split,
+              void* workspace, size_t workspace_bytes, int path, int ctas,
               cudaStream_t stream) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (M > kMaxDim) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "M=%d above %d", M, kMaxDim);
@@ -124,30 +103,26 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  if (split < 0) return fail(W4A16_ERR_INVALID_ARG, "split=%d is negative", split);
+  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
   if (path == W4A16_PATH_TENSOR) {
-    if (split > 0) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no split");
+    if (ctas > 0) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no CTA count");
     cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return ok();
   }
-  if (decode_max_split(K, group) <= 0)
+  if (decode_units(N, K, group) <= 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
                 "decode path: group=%d must be K or 64 times a power of two", group);
-  const size_t need = workspace_for(M, N, K, group, path, split);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need)
-      return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
-                  "decode path needs a workspace of %zu bytes (got %zu)", need,
-                  workspace ? workspace_bytes : (size_t)0);
-    if (!aligned(workspace, 256))
-      return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
-  }
+  const size_t need = workspace_for(M, N, K, group, path, ctas);
+  if (!workspace || workspace_bytes < need)
+    return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
+                need, workspace ? workspace_bytes : (size_t)0);
+  if (!aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
   // 16 rows per launch; larger M re-streams the weights once per 16 rows
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
     cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, rows,
-                                  N, K, group, decode_split(rows, N, K, group, split), workspace,
+                                  N, K, group, decode_ctas(rows, N, K, group, ctas), workspace,
                                   stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
@@ -218,15 +193,15 @@ int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes) {
   return w4a16_workspace_size_ex(M, N, K, group, W4A16_PATH_AUTO, 0, bytes);
 }
 
-int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int split, size_t* bytes) {
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas, size_t* bytes) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
-  if (split < 0) return fail(W4A16_ERR_INVALID_ARG, "split=%d is negative", split);
+  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  *bytes = workspace_for(M, N, K, group, path, split);
+  *bytes = workspace_for(M, N, K, group, path, ctas);
   return ok();
 }
 
@@ -239,18 +214,18 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales, co
 
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-                  void* workspace, size_t workspace_bytes, int path, int split, void* stream) {
+                  void* workspace, size_t workspace_bytes, int path, int ctas, void* stream) {
   return gemm_impl(A, Wq, scales, zeros, M, N, K, group, Y, workspace, workspace_bytes, path,
-                   split, (cudaStream_t)stream);
+                   ctas, (cudaStream_t)stream);
 }
 
-int w4a16_plan(int M, int N, int K, int group, int* path, int* split) {
+int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (int rc = check_kn(K, N, group)) return rc;
-  if (!path || !split) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  if (!path || !ctas) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   *path = choose_path(M);
   const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
-  *split = *path == W4A16_PATH_DECODE ? decode_split(rows, N, K, group, 0) : 0;
+  *ctas = *path == W4A16_PATH_DECODE ? decode_ctas(rows, N, K, group, 0) : 0;
   return ok();
 }
 

@@ -18,19 +18,19 @@ cudaError_t launch_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t
 cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
                               int N, int group, uint16_t* deq, cudaStream_t stream);
 
-// Split-K register-dequant GEMV for M <= 16 rows of A (one launch, grid
-// (split, N/128)). With split > 1, `workspace` holds the per-block counters
-// (zero before the first call, left zero by every call) followed by the
-// partial tiles; see decode_workspace_bytes (0 when split == 1).
+// Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
+// persistent CTAs, 1 <= ctas <= decode_units). `workspace` holds the
+// per-block counters (zero before the first call, left zero by every call)
+// followed by the partial tiles; see decode_workspace_bytes.
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int split, void* workspace, cudaStream_t stream);
-size_t decode_workspace_bytes(int M, int N, int split);
+                          int ctas, void* workspace, cudaStream_t stream);
+size_t decode_workspace_bytes(int M, int N, int ctas);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
-// Largest split of K the decode kernel supports for this group size (0: the
-// group size is not supported by the decode kernel).
-int decode_max_split(int K, int group);
+// Work units (128 columns x 512 k) of a problem; 0 if the decode kernel does
+// not support the group size.
+long decode_units(int N, int K, int group);
 // CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
 int decode_ctas_per_sm(int M);
 

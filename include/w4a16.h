@@ -75,7 +75,7 @@ extern "C" {
 
 /* Paths for w4a16_gemm_ex. */
 #define W4A16_PATH_AUTO 0
-#define W4A16_PATH_DECODE 1   /* split-K register-dequant GEMV          */
+#define W4A16_PATH_DECODE 1   /* stream-K register-dequant GEMV         */
 #define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
 
 /* Message for the last error returned on the calling thread ("" if none). */
@@ -114,19 +114,19 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int K, int N, int group, uint16_t* deq, void* stream);
 
 /* Scratch bytes w4a16_gemm needs for this problem on the current device
- * (0 when none: the tensor-core path, or a decode launch that does not split
- * K). When the decode path (M <= 16 rows per launch) splits K, the partial
- * sums of a 128-column block are combined through this workspace: a 32 KiB
- * counter area (room for any N) followed by fp32 partial tiles. The counter
+ * (0 when none: the tensor-core path). The decode path (M <= 16 rows per
+ * launch) combines the partial sums of 128-column blocks shared by several
+ * CTAs through this workspace: a 32 KiB counter area (room for any N)
+ * followed by two fp32 partial tiles per CTA. The counter
  * area must be zero-filled before the first use; every call leaves it
  * zero-filled again, so one buffer serves any number of calls, of any shape
  * that fits, that run one after another. Calls that may run concurrently
  * (other streams) need separate workspaces. Host-only. */
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
 
-/* As w4a16_workspace_size for a forced path and split (see w4a16_gemm_ex).
- * Host-only. */
-int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int split,
+/* As w4a16_workspace_size for a forced path and CTA count (see
+ * w4a16_gemm_ex). Host-only. */
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas,
                             size_t* bytes);
 
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
@@ -140,19 +140,20 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and, for
- * the decode path, the number of K ranges (`split`, 0 = automatic; clamped to
- * the number of group-aligned ranges K can be cut into). The decode path
- * handles any M in launches of 16 rows (it streams the weights once per
- * launch) and needs group == K or group = 64 * 2^j
- * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise); the tensor path takes split = 0. */
+ * the decode path, the number of persistent CTAs that share the work
+ * (`ctas`, 0 = one per resident CTA slot of the device; clamped to the number
+ * of 128-column x 512-k work units). The decode path handles any M in
+ * launches of 16 rows (it streams the weights once per launch) and needs
+ * group == K or group = 64 * 2^j (W4A16_ERR_UNSUPPORTED_SHAPE otherwise);
+ * the tensor path takes ctas = 0. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,
-                  int path, int split, void* stream);
+                  int path, int ctas, void* stream);
 
-/* The path and decode split w4a16_gemm would use on the current device
- * (split = 0 for the tensor-core path). Host-only. */
-int w4a16_plan(int M, int N, int K, int group, int* path, int* split);
+/* The path and decode CTA count w4a16_gemm would use on the current device
+ * (ctas = 0 for the tensor-core path). Host-only. */
+int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas);
 
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word (set by a kernel that gave up a bounded wait or failed a self-check).
