@@ -50,6 +50,7 @@ SIGNATURES = {
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _I, _I, _P]),
     "w4a16_plan": (_I, [_I, _I, _I, _I, _PI, _PI]),
+    "w4a16_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "w4a16_device_status": (_I, [_P]),
 }
 
@@ -218,6 +219,22 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
                                _PATHS[path], ctas, _stream(stream)), "w4a16_gemm")
+    return out
+
+
+def gemm_noalloc(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """Decode-path Y = A . dequant(pw) through w4a16_gemm_noalloc: no workspace;
+    the library's own device scratch array is used instead (see the header)."""
+    M, K = A.shape
+    if K != pw.K:
+        raise ValueError(f"A has K={K}, weight has K={pw.K}")
+    if out is None:
+        out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
+    _check(lib().w4a16_gemm_noalloc(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(),
+                                    pw.Sp.data_ptr(), pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
+                                    _dev(out, torch.float16, "out"), _stream(stream)),
+           "w4a16_gemm_noalloc")
     return out
 
 

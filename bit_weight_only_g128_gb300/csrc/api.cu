@@ -130,6 +130,12 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
 }
 
 }  // namespace
+
+// Record an error (or success) for w4a16_last_error from other translation
+// units of the library.
+int report_error(int code, const char* message) { return fail(code, "%s", message); }
+int report_ok() { return ok(); }
+
 }  // namespace w4a16
 
 using namespace w4a16;

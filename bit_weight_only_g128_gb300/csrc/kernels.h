@@ -46,6 +46,10 @@ size_t tc_smem_bytes(int bt, int* stages);
 // clears it if set.
 cudaError_t read_and_clear_device_error(int* flag);
 
+// Set (or clear) the calling thread's w4a16_last_error message; returns code.
+int report_error(int code, const char* message);
+int report_ok();
+
 // Output columns per decode CTA.
 constexpr int kDecodeBlockCols = 128;
 

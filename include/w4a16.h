@@ -155,6 +155,26 @@ int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * (ctas = 0 for the tensor-core path). Host-only. */
 int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas);
 
+/* The decode-path GEMM (same kernel, same results as w4a16_gemm_ex with
+ * W4A16_PATH_DECODE and the automatic CTA count) for callers that cannot
+ * allocate device memory: code that must not allocate once running (a fixed
+ * memory budget), plugins without access to their host's allocator, or loops
+ * that cannot afford an allocation. The pages have no counterpart of it.
+ * It takes no workspace: its scratch is a device array inside the library,
+ * 32 KiB of counters plus 8 MiB of partial tiles, which every GPU that loads
+ * the library holds until the process exits. Shapes whose partial tiles do
+ * not fit (more than 512 CTAs for 9..16 rows, 1024 for up to 8) are rejected
+ * with W4A16_ERR_UNSUPPORTED_SHAPE; the decode path's group rule applies.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls that overlap on the GPU
+ * (other streams, other host threads) race and give wrong results. Each call
+ * clears the counters it uses before its kernels run. Any M is taken, in
+ * launches of 16 rows. */
+int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
+                       const uint32_t* zeros, int M, int N, int K, int group,
+                       uint16_t* Y, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device error
  * word (set by a kernel that gave up a bounded wait or failed a self-check).
  * Returns W4A16_OK or W4A16_ERR_DEVICE_CHECK (message: which check, where). */
