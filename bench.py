@@ -411,10 +411,10 @@ def run_ours(args, wl, dist, rank, world, local):
         with open(args.sweep, "a") as f:
             for c, t in zip(cases, times):
                 roof, bound = roofline_us(c.M, c.K, c.N, c.group, pk)
-                path, ctas = w4.plan(c.M, c.N, c.K, c.group)
+                path, parts = w4.plan(c.M, c.N, c.K, c.group)
                 f.write(json.dumps({
                     "workload": wl.name, "layer": c.layer, "M": c.M, "K": c.K, "N": c.N,
-                    "group": c.group, "path": path, "ctas": ctas, "us": 1e6 * t,
+                    "group": c.group, "path": path, "parts": parts, "us": 1e6 * t,
                     "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
                     "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
                     "bound": bound, "frac": roof / (1e6 * t)}) + "\n")

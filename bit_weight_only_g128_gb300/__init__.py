@@ -176,10 +176,10 @@ def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
     return deq
 
 
-def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", ctas: int = 0) -> int:
+def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0) -> int:
     """Scratch bytes a gemm call needs (0 for the tensor-core path)."""
     b = ctypes.c_size_t()
-    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], ctas, ctypes.byref(b)),
+    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], parts, ctypes.byref(b)),
            "w4a16_workspace_size")
     return b.value
 
@@ -197,7 +197,7 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
 
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
-         path: str = "auto", ctas: int = 0, workspace: Optional[torch.Tensor] = None,
+         path: str = "auto", parts: int = 0, workspace: Optional[torch.Tensor] = None,
          stream=None) -> torch.Tensor:
     """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
 
@@ -210,7 +210,7 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     if out is None:
         out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group, path, ctas)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts)
     if need:
         if workspace is None:
             workspace = new_workspace(need, A.device)
@@ -218,7 +218,7 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
-                               _PATHS[path], ctas, _stream(stream)), "w4a16_gemm")
+                               _PATHS[path], parts, _stream(stream)), "w4a16_gemm")
     return out
 
 

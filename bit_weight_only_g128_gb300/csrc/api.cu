@@ -76,18 +76,28 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 // Decode GEMV up to 16 rows; tensor-core GEMM above.
 int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
 
-// Scratch bytes of a (path, ctas) choice: the decode path's counters and
+// Scratch bytes of a (path, parts) choice: the decode path's counters and
 // partial tiles (16-row chunks share one workspace); none for tensor cores.
-size_t workspace_for(int M, int N, int K, int group, int path, int ctas) {
-  if (M == 0 || path != W4A16_PATH_DECODE) return 0;
+// K split of the tensor-core path (requested, else chosen from the tiles).
+int tc_split(int M, int N, int K, int requested) {
+  const int nk = K / kAtomK;
+  int s = requested > 0 ? requested : tc_choose_split(M, N, K, sm_count());
+  if (s > nk) s = nk;
+  return s < 1 ? 1 : s;
+}
+
+size_t workspace_for(int M, int N, int K, int group, int path, int parts) {
+  if (M == 0) return 0;
+  if (path == W4A16_PATH_TENSOR) return tc_workspace_bytes(M, N, tc_split(M, N, K, parts));
+  if (path != W4A16_PATH_DECODE) return 0;
   const int rows = M < 16 ? M : 16;
-  const int c = decode_ctas(rows, N, K, group, ctas);
+  const int c = decode_ctas(rows, N, K, group, parts);
   return c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
 }
 
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
               const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-              void* workspace, size_t workspace_bytes, int path, int ctas,
+              void* workspace, size_t workspace_bytes, int path, int parts,
               cudaStream_t stream) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (M > kMaxDim) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "M=%d above %d", M, kMaxDim);
@@ -103,17 +113,25 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
+  if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (path == W4A16_PATH_TENSOR) {
-    if (ctas > 0) return fail(W4A16_ERR_INVALID_ARG, "the tensor-core path takes no CTA count");
-    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, stream);
+    const int split = tc_split(M, N, K, parts);
+    const size_t need = tc_workspace_bytes(M, N, split);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+      return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
+                  "tensor-core path (K split %d) needs a workspace of %zu bytes (got %zu)", split,
+                  need, workspace ? workspace_bytes : (size_t)0);
+    if (need > 0 && !aligned(workspace, 256))
+      return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, split,
+                                   need > 0 ? workspace : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     return ok();
   }
   if (decode_units(N, K, group) <= 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
                 "decode path: group=%d must be K or 64 times a power of two", group);
-  const size_t need = workspace_for(M, N, K, group, path, ctas);
+  const size_t need = workspace_for(M, N, K, group, path, parts);
   if (!workspace || workspace_bytes < need)
     return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
                 need, workspace ? workspace_bytes : (size_t)0);
@@ -122,7 +140,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
     cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, rows,
-                                  N, K, group, decode_ctas(rows, N, K, group, ctas), workspace,
+                                  N, K, group, decode_ctas(rows, N, K, group, parts), workspace,
                                   stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
@@ -199,15 +217,15 @@ int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes) {
   return w4a16_workspace_size_ex(M, N, K, group, W4A16_PATH_AUTO, 0, bytes);
 }
 
-int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas, size_t* bytes) {
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts, size_t* bytes) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
-  if (ctas < 0) return fail(W4A16_ERR_INVALID_ARG, "ctas=%d is negative", ctas);
+  if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  *bytes = workspace_for(M, N, K, group, path, ctas);
+  *bytes = workspace_for(M, N, K, group, path, parts);
   return ok();
 }
 
@@ -220,18 +238,18 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales, co
 
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group, uint16_t* Y,
-                  void* workspace, size_t workspace_bytes, int path, int ctas, void* stream) {
+                  void* workspace, size_t workspace_bytes, int path, int parts, void* stream) {
   return gemm_impl(A, Wq, scales, zeros, M, N, K, group, Y, workspace, workspace_bytes, path,
-                   ctas, (cudaStream_t)stream);
+                   parts, (cudaStream_t)stream);
 }
 
-int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas) {
+int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (int rc = check_kn(K, N, group)) return rc;
-  if (!path || !ctas) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  if (!path || !parts) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   *path = choose_path(M);
   const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
-  *ctas = *path == W4A16_PATH_DECODE ? decode_ctas(rows, N, K, group, 0) : 0;
+  *parts = *path == W4A16_PATH_DECODE ? decode_ctas(rows, N, K, group, 0) : tc_split(M, N, K, 0);
   return ok();
 }
 

@@ -34,10 +34,14 @@ long decode_units(int N, int K, int group);
 // CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
 int decode_ctas_per_sm(int M);
 
-// tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile.
+// tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile
+// x K range (`split` ranges; with split > 1 the workspace holds the tile
+// counters, zero between calls, and the fp32 partial tiles).
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           cudaStream_t stream);
+                           int split, void* workspace, cudaStream_t stream);
+size_t tc_workspace_bytes(int M, int N, int split);
+int tc_choose_split(int M, int N, int K, int sms);
 // Token tile (MMA N) used for M rows, and the dynamic shared memory it needs.
 int tc_token_tile(int M);
 size_t tc_smem_bytes(int bt, int* stages);

@@ -42,6 +42,7 @@ constexpr int kThreads = 64 + kDqThreads;
 constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
 constexpr int kPackedBytes = kTileN * kStageK / 2;  // 4 KiB packed codes
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr size_t kTcCounterBytes = 32768;          // tile counters of a K-split launch
 
 // error codes written to g_device_error (one bit per role)
 constexpr int kErrProducer = 1, kErrMma = 2, kErrDequant = 4, kErrEpilogue = 8, kErrDrain = 16;
@@ -205,11 +206,17 @@ struct TcParams {
   const uint16_t* Sp;
   const uint32_t* Zp;
   uint16_t* Y;
+  int* counters;  // split > 1: one per output tile, zero between calls
+  float* tiles;   // split > 1: fp32 partial tiles [tile][split][bt][128]
   int M, N, K, group;
-  int bt;       // token tile (MMA N): multiple of 16, 16..256
-  int stages;   // pipeline depth
+  int bt;         // token tile (MMA N): multiple of 16, 16..256
+  int stages;     // pipeline depth
   int tmem_cols;
+  int split;      // K ranges per output tile (grid z)
 };
+
+// named barrier of the 8 dequant/epilogue warps
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -229,11 +236,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem_slot = accum_bar + 8u;
   uint8_t* gen_base = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 4u - base));
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 8u - base));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kTileN;
   const int m0 = blockIdx.y * bt;
-  const int nk = p.K / kStageK;
+  // this CTA's K range: stages [kb0, kb0 + nk)
+  const int nk_all = p.K / kStageK;
+  const int kb0 = (int)((long long)blockIdx.z * nk_all / p.split);
+  const int nk = (int)((long long)(blockIdx.z + 1) * nk_all / p.split) - kb0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -264,8 +275,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
         const uint32_t st = base + (uint32_t)s * stage_bytes;
         mbar_expect_tx(full_tma(s), act_bytes + kPackedBytes);
-        tma_load_2d(st, &tmA, kb * kStageK, m0, full_tma(s));
-        tma_load_2d(st + act_bytes + kWdqBytes, &tmW, kb * 128, n0 / kStripCols, full_tma(s));
+        tma_load_2d(st, &tmA, (kb0 + kb) * kStageK, m0, full_tma(s));
+        tma_load_2d(st + act_bytes + kWdqBytes, &tmW, (kb0 + kb) * 128, n0 / kStripCols, full_tma(s));
         ++issued;
       }
       if (*abort_flag) {
@@ -309,27 +320,42 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // process the lane's words in an order that keeps the 16-byte stores of
     // each quarter-warp on distinct banks (odd rows take the other k-half first)
     const uint32_t flip = (uint32_t)(gq & 1);
-    uint32_t pre_s = 0, pre_z = 0;  // next group's (s[gq], s[gq+8]) and zero-point pair
-    if (valid) {
-      pre_s = sp[0];
-      pre_z = zp[0];
+    // (s[gq], s[gq+8]) and zero-point pairs of the next kMetaAhead groups,
+    // fetched well before use: each group is used once per tile, so these
+    // loads usually come from HBM
+    constexpr int kMetaAhead = 4;
+    const int g0 = kb0 * kStageK / p.group;
+    uint32_t ring_s[kMetaAhead], ring_z[kMetaAhead];
+#pragma unroll
+    for (int i = 0; i < kMetaAhead; ++i) {
+      ring_s[i] = 0;
+      ring_z[i] = 0;
+      if (valid && g0 + i < G) {
+        ring_s[i] = sp[(g0 + i) * 8];
+        ring_z[i] = zp[(g0 + i) * 8];
+      }
     }
     DeqConst d0 = {}, d1 = {};
-    int cur_grp = -1;
+    int cur_grp = g0 - 1;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % stages;
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
       if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
       if (valid) {
-        const int grp = kb * kStageK / p.group;
-        if (grp != cur_grp) {
-          d0 = make_deq_const(pre_z & 15u, (uint16_t)(pre_s & 0xffffu));
-          d1 = make_deq_const((pre_z >> 4) & 15u, (uint16_t)(pre_s >> 16));
+        const int grp = (kb0 + kb) * kStageK / p.group;
+        if (grp != cur_grp) {  // groups advance one at a time
+          d0 = make_deq_const(ring_z[0] & 15u, (uint16_t)(ring_s[0] & 0xffffu));
+          d1 = make_deq_const((ring_z[0] >> 4) & 15u, (uint16_t)(ring_s[0] >> 16));
           cur_grp = grp;
-          if (grp + 1 < G) {
-            pre_s = sp[(grp + 1) * 8];
-            pre_z = zp[(grp + 1) * 8];
+#pragma unroll
+          for (int i = 0; i + 1 < kMetaAhead; ++i) {
+            ring_s[i] = ring_s[i + 1];
+            ring_z[i] = ring_z[i + 1];
+          }
+          if (grp + kMetaAhead < G) {
+            ring_s[kMetaAhead - 1] = sp[(grp + kMetaAhead) * 8];
+            ring_z[kMetaAhead - 1] = zp[(grp + kMetaAhead) * 8];
           }
         }
         const uint4 v = lds128(st + act_bytes + kWdqBytes + dw * 512 + lane * 16);
@@ -360,11 +386,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int q = warp & 3;
       const int half = dw >> 2;  // two warpgroups split the token chunks
       const int n = n0 + 32 * q + lane;
+      float* part = p.tiles + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * p.split + blockIdx.z) *
+                                  (size_t)bt * kTileN;
       for (int c = half; c < bt / 16; c += 2) {
         uint32_t r[16];
         tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * c), r);
         tmem_wait_ld();
-        if (n < p.N) {
+        if (p.split > 1) {  // fp32 partial tile [token][column]
+#pragma unroll
+          for (int j = 0; j < 16; ++j) part[(16 * c + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
+        } else if (n < p.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = m0 + 16 * c + j;
@@ -372,6 +403,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               p.Y[(size_t)tok * p.N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
           }
         }
+      }
+    }
+    if (p.split > 1) {
+      // K split: the last of the tile's CTAs to arrive sums the partial tiles in
+      // split order (deterministic), writes Y and resets the tile's counter
+      const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+      __threadfence();
+      epilogue_bar();
+      if (dw == 0 && lane == 0)
+        *last_flag = (*abort_flag == 0) && atomicAdd(p.counters + tile, 1) == p.split - 1;
+      epilogue_bar();
+      if (*last_flag) {
+        __threadfence();
+        const float* tb = p.tiles + (size_t)tile * p.split * bt * kTileN;
+        for (int e = dw * 32 + lane; e < bt * kTileN; e += kDqThreads) {
+          const int tok = m0 + e / kTileN, n = n0 + e % kTileN;
+          if (tok >= p.M || n >= p.N) continue;
+          float sum = 0.f;
+          for (int z = 0; z < p.split; ++z) sum += __ldcg(tb + (size_t)z * bt * kTileN + e);
+          p.Y[(size_t)tok * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+        }
+        if (dw == 0 && lane == 0) p.counters[tile] = 0;
       }
     }
   }
@@ -422,9 +475,43 @@ size_t tc_smem_bytes(int bt, int* stages_out) {
   return (size_t)stages * stage + 1024 + 256;
 }
 
+size_t tc_workspace_bytes(int M, int N, int split) {
+  if (split <= 1) return 0;
+  const int bt = tc_token_tile(M);
+  const size_t tiles = (size_t)((N + kTileN - 1) / kTileN) * ((M + bt - 1) / bt);
+  return kTcCounterBytes + tiles * (size_t)split * bt * kTileN * sizeof(float);
+}
+
+// K split of the tensor-core GEMM: only when the output tiles cannot fill the
+// SMs. Among splits that keep >= 8 stages (512 k) per CTA, the score is the
+// wave efficiency times the share of weight bytes in the traffic once the
+// fp32 partial tiles (written and read back) are counted.
+int tc_choose_split(int M, int N, int K, int sms) {
+  const int bt = tc_token_tile(M);
+  const long tiles = (long)((N + kTileN - 1) / kTileN) * ((M + bt - 1) / bt);
+  if (tiles >= sms) return 1;
+  if (tiles > (long)(kTcCounterBytes / sizeof(int))) return 1;
+  const int nk = K / kStageK;
+  const double wbytes = (double)K * N / 2 + 2.0 * M * K;
+  int best = 1;
+  double best_score = -1.0;
+  for (int split = 1; split <= 16 && nk / split >= 8; ++split) {
+    const long total = tiles * split;
+    const long waves = (total + sms - 1) / sms;
+    const double eff = (double)total / (double)(waves * sms);
+    const double part = split > 1 ? 2.0 * tiles * split * bt * kTileN * 4.0 : 0.0;
+    const double score = eff * wbytes / (wbytes + part);
+    if (score > best_score + 0.01) {
+      best_score = score;
+      best = split;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           cudaStream_t stream) {
+                           int split, void* workspace, cudaStream_t stream) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const int bt = tc_token_tile(M);
@@ -459,6 +546,10 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.K = K;
   prm.group = group;
   prm.bt = bt;
+  prm.split = split < 1 ? 1 : split;
+  prm.counters = static_cast<int*>(workspace);
+  prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
+                        : nullptr;
   const size_t smem = tc_smem_bytes(bt, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
   static size_t attr_bytes = 0;
@@ -468,7 +559,8 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
     if (e != cudaSuccess) return e;
     attr_bytes = 227 * 1024;
   }
-  const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt), 1);
+  const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
+                  (unsigned)prm.split);
   tc_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
   return cudaGetLastError();
 }

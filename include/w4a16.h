@@ -114,19 +114,20 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int K, int N, int group, uint16_t* deq, void* stream);
 
 /* Scratch bytes w4a16_gemm needs for this problem on the current device
- * (0 when none: the tensor-core path). The decode path (M <= 16 rows per
- * launch) combines the partial sums of 128-column blocks shared by several
- * CTAs through this workspace: a 32 KiB counter area (room for any N)
- * followed by two fp32 partial tiles per CTA. The counter
+ * (0 when none). Work split across CTAs is combined through it: the decode
+ * path (M <= 16 rows per launch) shares 128-column blocks between CTAs, and
+ * the tensor-core path splits K when its output tiles cannot fill the SMs.
+ * Layout: a 32 KiB counter area followed by fp32 partial tiles. The counter
  * area must be zero-filled before the first use; every call leaves it
  * zero-filled again, so one buffer serves any number of calls, of any shape
  * that fits, that run one after another. Calls that may run concurrently
- * (other streams) need separate workspaces. Host-only. */
+ * (other streams) need separate workspaces. After W4A16_ERR_DEVICE_CHECK,
+ * zero it again. Host-only. */
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
 
-/* As w4a16_workspace_size for a forced path and CTA count (see
+/* As w4a16_workspace_size for a forced path and work partition (see
  * w4a16_gemm_ex). Host-only. */
-int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int ctas,
+int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
                             size_t* bytes);
 
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
@@ -139,21 +140,21 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                const uint32_t* zeros, int M, int N, int K, int group,
                uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream);
 
-/* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and, for
- * the decode path, the number of persistent CTAs that share the work
- * (`ctas`, 0 = one per resident CTA slot of the device; clamped to the number
- * of 128-column x 512-k work units). The decode path handles any M in
- * launches of 16 rows (it streams the weights once per launch) and needs
- * group == K or group = 64 * 2^j (W4A16_ERR_UNSUPPORTED_SHAPE otherwise);
- * the tensor path takes ctas = 0. */
+/* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and the
+ * work partition forced (`parts`, 0 = automatic): for the decode path the
+ * number of persistent CTAs (clamped to the 128-column x 512-k work units),
+ * for the tensor-core path the number of K ranges per output tile (clamped to
+ * K/64). The decode path handles any M in launches of 16 rows (it streams the
+ * weights once per launch) and needs group == K or group = 64 * 2^j
+ * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,
-                  int path, int ctas, void* stream);
+                  int path, int parts, void* stream);
 
-/* The path and decode CTA count w4a16_gemm would use on the current device
- * (ctas = 0 for the tensor-core path). Host-only. */
-int w4a16_plan(int M, int N, int K, int group, int* path, int* ctas);
+/* The path and work partition w4a16_gemm would use on the current device
+ * (parts: decode CTAs, or tensor-core K ranges). Host-only. */
+int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
 
 /* The decode-path GEMM (same kernel, same results as w4a16_gemm_ex with
  * W4A16_PATH_DECODE and the automatic CTA count) for callers that cannot

@@ -42,7 +42,7 @@ def check_guard(full: torch.Tensor, M: int, N: int, pad: int):
     assert np.all(bits[pad + M * N:] == 0x7E5A), "write after Y"
 
 
-def run_and_check(M, K, N, group, seed, path="auto", ctas=0, outliers=False, repeat=2):
+def run_and_check(M, K, N, group, seed, path="auto", parts=0, outliers=False, repeat=2):
     W = synthetic.small_weights(K, N, seed)
     A = synthetic.small_activations(M, K, seed, outliers=outliers)
     (q, s, z), pw = prepare(W, group)
@@ -50,7 +50,7 @@ def run_and_check(M, K, N, group, seed, path="auto", ctas=0, outliers=False, rep
     outs = []
     for _ in range(repeat):
         full, Y, pad = guarded_output(M, N)
-        w4.gemm(Ad, pw, out=Y, path=path, ctas=ctas)
+        w4.gemm(Ad, pw, out=Y, path=path, parts=parts)
         w4.device_status()
         check_guard(full, M, N, pad)
         outs.append(half_bits(Y).copy())

@@ -73,13 +73,13 @@ def test_shape_rules(lib, K, N, group, code):
     assert lib.w4a16_last_error()
 
 
-def _gemm(lib, A=16, W=16, S=16, Z=16, Y=16, M=1, N=64, K=128, group=128, path=0, ctas=0,
+def _gemm(lib, A=16, W=16, S=16, Z=16, Y=16, M=1, N=64, K=128, group=128, path=0, parts=0,
           ws=256, ws_bytes=1 << 20):
     # fake (never dereferenced) addresses: every failure below is decided on the host
     return lib.w4a16_gemm_ex(A and 0x10000 + A % 16, W and 0x20000 + W % 16,
                              S and 0x30000 + S % 16, Z and 0x40000 + Z % 16, M, N, K, group,
                              Y and 0x50000 + Y % 16, ws and 0x100000 + ws % 256, ws_bytes,
-                             path, ctas, None)
+                             path, parts, None)
 
 
 def test_gemm_argument_errors(lib):
@@ -93,8 +93,8 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Y=8) == -3
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
-    assert _gemm(lib, ctas=-1) == -1
-    assert _gemm(lib, path=2, ctas=4) == -1          # the tensor path takes no CTA count
+    assert _gemm(lib, parts=-1) == -1
+    assert _gemm(lib, path=2, parts=4, ws=0) == -4      # a K-split tensor launch needs a workspace
     assert _gemm(lib, path=1, ws=0) == -4             # decode needs a workspace
     assert _gemm(lib, path=1, ws_bytes=16) == -4
     assert _gemm(lib, path=1, ws=8) == -3             # workspace not 256-byte aligned
@@ -107,12 +107,15 @@ def test_gemm_m_zero_is_a_noop(lib):
 
 
 def test_workspace_sizes(lib):
-    # tensor-core path: none; decode path: counters + two fp32 tiles
-    # (8 or 16 tokens x 128 columns) per CTA
+    # decode path: counters + two fp32 tiles (8 or 16 tokens x 128 columns)
+    # per CTA; tensor path: counters + one fp32 tile (token tile x 128) per
+    # output tile and K range, none without a split
     head = 32768   # counters for up to 2^20 / 128 column blocks
-    assert w4.workspace_size(64, 4096, 4096, 128) == 0
     assert w4.workspace_size(0, 4096, 4096, 128) == 0
-    assert w4.workspace_size(1, 4096, 4096, 128, path="decode", ctas=10) == head + 2 * 10 * 8 * 128 * 4
-    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", ctas=10) == head + 2 * 10 * 16 * 128 * 4
+    assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=1) == 0
+    assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=3) == head + 32 * 3 * 64 * 128 * 4
+    assert w4.workspace_size(300, 256, 4096, 128, path="tensor", parts=2) == head + 4 * 2 * 256 * 128 * 4
+    assert w4.workspace_size(1, 4096, 4096, 128, path="decode", parts=10) == head + 2 * 10 * 8 * 128 * 4
+    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", parts=10) == head + 2 * 10 * 16 * 128 * 4
     # the CTA count is clamped to the work units: 32 blocks x 1 batch of 8 atoms
-    assert w4.workspace_size(1, 4096, 512, 128, path="decode", ctas=1000) == head + 2 * 32 * 8 * 128 * 4
+    assert w4.workspace_size(1, 4096, 512, 128, path="decode", parts=1000) == head + 2 * 32 * 8 * 128 * 4

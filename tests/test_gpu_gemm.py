@@ -33,9 +33,9 @@ DECODE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,K,N,group,ctas", DECODE_CASES)
-def test_decode_path(M, K, N, group, ctas):
-    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", ctas=ctas)
+@pytest.mark.parametrize("M,K,N,group,parts", DECODE_CASES)
+def test_decode_path(M, K, N, group, parts):
+    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", parts=parts)
 
 
 @pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (16, 4096, 256, 128),
@@ -48,31 +48,31 @@ def test_outlier_activation_columns():
     run_and_check(4, 4096, 256, 128, seed=5, outliers=True)
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 11, 12, 13, 1000])
-def test_every_cta_count_meets_the_tolerance(ctas):
+@pytest.mark.parametrize("parts", [1, 2, 3, 7, 11, 12, 13, 1000])
+def test_every_cta_count_meets_the_tolerance(parts):
     """One CTA (every block whole), blocks shared unevenly, one unit per CTA,
     clamping to the 3 x 4 = 12 units."""
-    run_and_check(8, 2048, 272, 128, seed=11, path="decode", ctas=ctas)
+    run_and_check(8, 2048, 272, 128, seed=11, path="decode", parts=parts)
 
 
-@pytest.mark.parametrize("M,K,N,group,ctas", [(3, 512, 64, 64, 1), (5, 1024, 144, 256, 3),
+@pytest.mark.parametrize("M,K,N,group,parts", [(3, 512, 64, 64, 1), (5, 1024, 144, 256, 3),
                                               (9, 2048, 128, 512, 2), (2, 1536, 32, 1536, 2),
                                               (16, 4096, 160, 1024, 3), (1, 320, 48, 320, 1),
                                               (4, 1600, 400, 1600, 5), (7, 704, 96, 64, 0)])
-def test_group_sizes(M, K, N, group, ctas):
+def test_group_sizes(M, K, N, group, parts):
     """Groups of 1, 4, 8 and 16 atoms and per-channel groups of any length
     (short last batches of 1..7 atoms at 320, 704, 1600)."""
-    run_and_check(M, K, N, group, seed=M + K + group, path="decode", ctas=ctas)
+    run_and_check(M, K, N, group, seed=M + K + group, path="decode", parts=parts)
 
 
 def test_workspace_is_left_zeroed_and_reusable():
     K, N, group = 1024, 400, 128
     W = synthetic.small_weights(K, N, seed=4)
     (q, s, z), pw = prepare(W, group)
-    ws = w4.new_workspace(w4.workspace_size(16, N, K, group, path="decode", ctas=9))
+    ws = w4.new_workspace(w4.workspace_size(16, N, K, group, path="decode", parts=9))
     for M in (1, 5, 16, 3):
         A = synthetic.small_activations(M, K, seed=M)
-        Y = w4.gemm(cuda(A), pw, path="decode", ctas=9, workspace=ws)
+        Y = w4.gemm(cuda(A), pw, path="decode", parts=9, workspace=ws)
         w4.device_status()
         y, mag = oracle.reference(A, q, s, z, group)
         assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
@@ -83,17 +83,17 @@ def test_workspace_is_left_zeroed_and_reusable():
 def test_one_workspace_serves_calls_of_different_shapes():
     """Calls of different N, M and CTA count in turn share one workspace."""
     shapes = [(1, 1024, 2816), (16, 512, 256), (4, 2048, 1024), (1, 1024, 2816), (9, 640, 4096)]
-    ws = w4.new_workspace(max(w4.workspace_size(16, N, K, 128, path="decode", ctas=c)
+    ws = w4.new_workspace(max(w4.workspace_size(16, N, K, 128, path="decode", parts=c)
                               for (_, K, N) in shapes for c in (300, 0, 37)))
     for i, (M, K, N) in enumerate(shapes):
         W = synthetic.small_weights(K, N, seed=40 + i)
         A = synthetic.small_activations(M, K, seed=40 + i)
         (q, s, z), pw = prepare(W, 128)
-        for ctas in (300, 0, 37):
-            Y = w4.gemm(cuda(A), pw, path="decode", ctas=ctas, workspace=ws)
+        for parts in (300, 0, 37):
+            Y = w4.gemm(cuda(A), pw, path="decode", parts=parts, workspace=ws)
             w4.device_status()
             y, mag = oracle.reference(A, q, s, z, 128)
-            assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0, (M, K, N, ctas)
+            assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0, (M, K, N, parts)
 
 
 def test_integer_product_is_exact():
@@ -107,8 +107,8 @@ def test_integer_product_is_exact():
     exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
     assert np.abs(exact).max() < 2048
     pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
-    for ctas in (1, 4, 0):
-        Y = w4.gemm(cuda(A), pw, path="decode", ctas=ctas)
+    for parts in (1, 4, 0):
+        Y = w4.gemm(cuda(A), pw, path="decode", parts=parts)
         assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
 
 

@@ -7,6 +7,7 @@ groups 64, 128 and K (per-channel).
 """
 import numpy as np
 import pytest
+import torch
 
 import bit_weight_only_g128_gb300 as w4
 import oracle
@@ -71,3 +72,24 @@ def test_integer_product_is_exact_on_tensor_cores():
     Y = w4.gemm(cuda(A), pw, path="tensor")
     w4.device_status()
     assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
+
+
+@pytest.mark.parametrize("M,K,N,group,parts", [(64, 4096, 256, 128, 4), (100, 2048, 400, 128, 3),
+                                               (300, 1024, 144, 1024, 2), (17, 1280, 48, 64, 5),
+                                               (64, 5120, 640, 128, 0), (128, 3072, 1024, 256, 0)])
+def test_tensor_k_split(M, K, N, group, parts):
+    """K split across CTAs with the last-arriving CTA summing the fp32 tiles."""
+    run_and_check(M, K, N, group, seed=M + N + parts, path="tensor", parts=parts)
+
+
+def test_tensor_split_workspace_is_left_zeroed():
+    K, N, group = 2048, 256, 128
+    (q, s, z), pw = prepare(synthetic.small_weights(K, N, seed=9), group)
+    ws = w4.new_workspace(w4.workspace_size(64, N, K, group, path="tensor", parts=4))
+    for M in (64, 40, 64):
+        A = synthetic.small_activations(M, K, seed=M)
+        Y = w4.gemm(cuda(A), pw, path="tensor", parts=4, workspace=ws)
+        w4.device_status()
+        y, mag = oracle.reference(A, q, s, z, group)
+        assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
+        assert int(ws[:32768].view(torch.int32).abs().sum()) == 0
