@@ -16,10 +16,13 @@
 //   warp 0      TMA producer: activations tile [BT x 64] (128B swizzle) and
 //               the packed int4 atoms of 8 strips [8 x 512 B] per k-stage;
 //   warp 1      TMEM allocation; one thread issues 4 MMAs (K=16) per stage;
-//   warps 2..9  dequantize the packed atoms of a stage into the 128B-swizzled
-//               K-major operand tile, then run the epilogue (TMEM -> fp16 Y).
+//   warps 2..9  dequantize the packed atoms into the 128B-swizzled K-major
+//               operand tile (4 pairs of warps, each pair on every 4th stage,
+//               so 4 stages are converted concurrently), then run the
+//               epilogue (TMEM -> fp16 Y).
 // Stages form a ring guarded by mbarriers: full_tma (TMA bytes landed),
-// full_dq (256 dequant threads done), empty (MMAs of the stage completed).
+// full_dq (the stage's 64 dequant threads done), empty (MMAs of the stage
+// completed).
 // Every wait is bounded; a wait that gives up sets the library's device
 // error word and the CTA drains and exits.
 #include <cuda.h>
@@ -37,6 +40,7 @@ namespace {
 constexpr int kTileN = 128;        // output columns per CTA (MMA M)
 constexpr int kStageK = 64;        // k per pipeline stage (one 128-byte swizzle row)
 constexpr int kDqWarps = 8;
+constexpr int kDqGroups = 4;  // dequant warp pairs working on different stages
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kThreads = 64 + kDqThreads;
 constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
@@ -218,7 +222,7 @@ struct TcParams {
 // named barrier of the 8 dequant/epilogue warps
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -249,7 +253,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_tma(s), 1);
-      mbar_init(full_dq(s), kDqThreads);
+      mbar_init(full_dq(s), 64);  // the two warps of the stage's dequant group
       mbar_init(empty(s), 1);
     }
     mbar_init(accum_bar, 1);
@@ -310,72 +314,73 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ---------------------------------------------------------- dequant + epilogue
-    const int dw = warp - 2;                 // strip of the tile handled by this warp
+    // The 8 warps form kDqGroups groups of 2; group g dequantizes the stages
+    // kb = g, g + kDqGroups, ... so several stages are converted at once,
+    // and within a stage warp `sub` converts strips 4*sub .. 4*sub+3.
+    const int dw = warp - 2;
+    const int dg = dw >> 1, sub = dw & 1;
     const int gq = lane >> 2, t = lane & 3;
-    const int strip = n0 / kStripCols + dw;
-    const bool valid = strip < p.N / kStripCols;
+    const int nstrips = p.N / kStripCols;
     const int G = p.K / p.group;
-    const uint32_t* sp = reinterpret_cast<const uint32_t*>(p.Sp) + (size_t)(valid ? strip : 0) * G * 8 + gq;
-    const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp) + (size_t)(valid ? strip : 0) * G * 8 + gq;
+    const uint32_t* sp2 = reinterpret_cast<const uint32_t*>(p.Sp);
+    const uint8_t* zpb = reinterpret_cast<const uint8_t*>(p.Zp);
     // process the lane's words in an order that keeps the 16-byte stores of
     // each quarter-warp on distinct banks (odd rows take the other k-half first)
     const uint32_t flip = (uint32_t)(gq & 1);
-    // (s[gq], s[gq+8]) and zero-point pairs of the next kMetaAhead groups,
-    // fetched well before use: each group is used once per tile, so these
-    // loads usually come from HBM
-    constexpr int kMetaAhead = 4;
-    const int g0 = kb0 * kStageK / p.group;
-    uint32_t ring_s[kMetaAhead], ring_z[kMetaAhead];
+    // (s[gq], s[gq+8]) and zero-point pairs of this warp's 4 strips for a stage
+    auto load_meta = [&](int kb, uint32_t (&ms)[4], uint32_t (&mz)[4]) {
+      const int grp = (int)((long long)(kb0 + kb) * kStageK / p.group);
 #pragma unroll
-    for (int i = 0; i < kMetaAhead; ++i) {
-      ring_s[i] = 0;
-      ring_z[i] = 0;
-      if (valid && g0 + i < G) {
-        ring_s[i] = sp[(g0 + i) * 8];
-        ring_z[i] = zp[(g0 + i) * 8];
+      for (int i = 0; i < 4; ++i) {
+        const int strip = n0 / kStripCols + 4 * sub + i;
+        ms[i] = 0;
+        mz[i] = 0;
+        if (strip < nstrips) {
+          const size_t off = ((size_t)strip * G + grp) * 8 + gq;
+          ms[i] = sp2[off];
+          mz[i] = zpb[off];
+        }
       }
-    }
-    DeqConst d0 = {}, d1 = {};
-    int cur_grp = g0 - 1;
-    for (int kb = 0; kb < nk; ++kb) {
+    };
+    uint32_t ms[4], mz[4];
+    if (dg < nk) load_meta(dg, ms, mz);
+    for (int kb = dg; kb < nk; kb += kDqGroups) {
       const int s = kb % stages;
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+      uint32_t nms[4] = {0, 0, 0, 0}, nmz[4] = {0, 0, 0, 0};
+      if (kb + kDqGroups < nk) load_meta(kb + kDqGroups, nms, nmz);  // this warp's next stage
       if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
-      if (valid) {
-        const int grp = (kb0 + kb) * kStageK / p.group;
-        if (grp != cur_grp) {  // groups advance one at a time
-          d0 = make_deq_const(ring_z[0] & 15u, (uint16_t)(ring_s[0] & 0xffffu));
-          d1 = make_deq_const((ring_z[0] >> 4) & 15u, (uint16_t)(ring_s[0] >> 16));
-          cur_grp = grp;
+      const uint32_t wdq = st + act_bytes;
 #pragma unroll
-          for (int i = 0; i + 1 < kMetaAhead; ++i) {
-            ring_s[i] = ring_s[i + 1];
-            ring_z[i] = ring_z[i + 1];
-          }
-          if (grp + kMetaAhead < G) {
-            ring_s[kMetaAhead - 1] = sp[(grp + kMetaAhead) * 8];
-            ring_z[kMetaAhead - 1] = zp[(grp + kMetaAhead) * 8];
-          }
-        }
-        const uint4 v = lds128(st + act_bytes + kWdqBytes + dw * 512 + lane * 16);
-        const uint32_t wdq = st + act_bytes;
+      for (int i = 0; i < 4; ++i) {
+        const int ls = 4 * sub + i;  // strip within the tile
+        if (n0 / kStripCols + ls < nstrips) {
+          const DeqConst d0 = make_deq_const(mz[i] & 15u, (uint16_t)(ms[i] & 0xffffu));
+          const DeqConst d1 = make_deq_const((mz[i] >> 4) & 15u, (uint16_t)(ms[i] >> 16));
+          const uint4 v = lds128(st + act_bytes + kWdqBytes + ls * 512 + lane * 16);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t ks = (uint32_t)(i >> 1) ^ flip;  // k-half of this word
-          const uint32_t r = (uint32_t)(i & 1);           // column gq or gq + 8
-          const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
-          uint32_t o[4];
-          dequant_word(word, r ? d1 : d0, o);
-          // row n = 16 dw + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
-          const uint32_t row = 16u * dw + gq + 8u * r;
-          const uint32_t kw = 4u * ks + t;
-          sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4), o[0],
-                 o[1], o[2], o[3]);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
+            const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
+            const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
+            uint32_t o[4];
+            dequant_word(word, r ? d1 : d0, o);
+            // row n = 16 ls + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
+            const uint32_t row = 16u * ls + gq + 8u * r;
+            const uint32_t kw = 4u * ks + t;
+            sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4), o[0],
+                   o[1], o[2], o[3]);
+          }
         }
       }
       fence_async_shared();  // generic-proxy stores -> visible to the tensor core
       mbar_arrive(full_dq(s));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ms[i] = nms[i];
+        mz[i] = nmz[i];
+      }
     }
 
     // epilogue: TMEM lanes 32q..32q+31 are output columns, TMEM columns are tokens
@@ -466,9 +471,14 @@ int tc_token_tile(int M) {
   return (M + 15) / 16 * 16;
 }
 
+// CTAs per SM the tensor-core kernel is sized for: two when the token tile is
+// at most 128 (smem and TMEM allow it; more CTAs for the small tile counts of
+// the middle band of M), else one with the deepest pipeline that fits.
+int tc_ctas_per_sm(int bt) { return bt <= 128 ? 2 : 1; }
+
 size_t tc_smem_bytes(int bt, int* stages_out) {
   const size_t stage = (size_t)bt * 128 + kWdqBytes + kPackedBytes;
-  const size_t budget = 227 * 1024 - 1024 - 256;
+  const size_t budget = (tc_ctas_per_sm(bt) == 2 ? 113 * 1024 : 227 * 1024) - 1024 - 256;
   int stages = (int)(budget / stage);
   if (stages > 8) stages = 8;
   if (stages_out) *stages_out = stages;
@@ -489,7 +499,8 @@ size_t tc_workspace_bytes(int M, int N, int split) {
 int tc_choose_split(int M, int N, int K, int sms) {
   const int bt = tc_token_tile(M);
   const long tiles = (long)((N + kTileN - 1) / kTileN) * ((M + bt - 1) / bt);
-  if (tiles >= sms) return 1;
+  const long slots = (long)sms * tc_ctas_per_sm(bt);
+  if (tiles >= slots) return 1;
   if (tiles > (long)(kTcCounterBytes / sizeof(int))) return 1;
   const int nk = K / kStageK;
   const double wbytes = (double)K * N / 2 + 2.0 * M * K;
@@ -497,8 +508,8 @@ int tc_choose_split(int M, int N, int K, int sms) {
   double best_score = -1.0;
   for (int split = 1; split <= 16 && nk / split >= 8; ++split) {
     const long total = tiles * split;
-    const long waves = (total + sms - 1) / sms;
-    const double eff = (double)total / (double)(waves * sms);
+    const long waves = (total + slots - 1) / slots;
+    const double eff = (double)total / (double)(waves * slots);
     const double part = split > 1 ? 2.0 * tiles * split * bt * kTileN * 4.0 : 0.0;
     const double score = eff * wbytes / (wbytes + part);
     if (score > best_score + 0.01) {
