@@ -17,11 +17,11 @@
 //               the packed int4 atoms of 8 strips [8 x 512 B] per k-stage;
 //   warp 1      TMEM allocation; one thread issues 4 MMAs (K=16) per stage;
 //   warps 2..9  dequantize the packed atoms into the 128B-swizzled K-major
-//               operand tile (4 pairs of warps, each pair on every 4th stage,
-//               so 4 stages are converted concurrently), then run the
-//               epilogue (TMEM -> fp16 Y).
+//               operand tile (usually 4 pairs of warps, each pair on every
+//               4th stage, so 4 stages are converted concurrently), then run
+//               the epilogue (TMEM -> fp16 Y).
 // Stages form a ring guarded by mbarriers: full_tma (TMA bytes landed),
-// full_dq (the stage's 64 dequant threads done), empty (MMAs of the stage
+// full_dq (the stage's dequant group done), empty (MMAs of the stage
 // completed).
 // Every wait is bounded; a wait that gives up sets the library's device
 // error word and the CTA drains and exits.
@@ -40,7 +40,6 @@ namespace {
 constexpr int kTileN = 128;        // output columns per CTA (MMA M)
 constexpr int kStageK = 64;        // k per pipeline stage (one 128-byte swizzle row)
 constexpr int kDqWarps = 8;
-constexpr int kDqGroups = 4;  // dequant warp pairs working on different stages
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kThreads = 64 + kDqThreads;
 constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
@@ -217,6 +216,7 @@ struct TcParams {
   int stages;     // pipeline depth
   int tmem_cols;
   int split;      // K ranges per output tile (grid z)
+  int dq_groups;  // dequant warp groups (4, 2 or 1), dividing `stages`
 };
 
 // named barrier of the 8 dequant/epilogue warps
@@ -253,7 +253,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_tma(s), 1);
-      mbar_init(full_dq(s), 64);  // the two warps of the stage's dequant group
+      mbar_init(full_dq(s), 32 * (kDqWarps / p.dq_groups));  // the stage's dequant group
       mbar_init(empty(s), 1);
     }
     mbar_init(accum_bar, 1);
@@ -314,11 +314,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ---------------------------------------------------------- dequant + epilogue
-    // The 8 warps form kDqGroups groups of 2; group g dequantizes the stages
-    // kb = g, g + kDqGroups, ... so several stages are converted at once,
-    // and within a stage warp `sub` converts strips 4*sub .. 4*sub+3.
+    // The 8 warps form `groups` groups (4, 2 or 1); group g dequantizes the
+    // stages kb = g, g + groups, ... so several stages are converted at once;
+    // within a stage each of the group's warps converts `groups` strips.
+    // `stages` is a multiple of `groups`, so a ring slot is always converted
+    // by the same group, which has waited for the slot's previous round: a
+    // parity wait can then never run more than one phase ahead of its
+    // barrier (where it would take an older phase for the awaited one).
+    const int groups = p.dq_groups;
+    const int wpg = kDqWarps / groups;  // warps per group
     const int dw = warp - 2;
-    const int dg = dw >> 1, sub = dw & 1;
+    const int dg = dw / wpg, sub = dw % wpg;
     const int gq = lane >> 2, t = lane & 3;
     const int nstrips = p.N / kStripCols;
     const int G = p.K / p.group;
@@ -327,15 +333,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // process the lane's words in an order that keeps the 16-byte stores of
     // each quarter-warp on distinct banks (odd rows take the other k-half first)
     const uint32_t flip = (uint32_t)(gq & 1);
-    // (s[gq], s[gq+8]) and zero-point pairs of this warp's 4 strips for a stage
+    // (s[gq], s[gq+8]) and zero-point pairs of this warp's strips for a stage
     auto load_meta = [&](int kb, uint32_t (&ms)[4], uint32_t (&mz)[4]) {
       const int grp = (int)((long long)(kb0 + kb) * kStageK / p.group);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int strip = n0 / kStripCols + 4 * sub + i;
+        const int strip = n0 / kStripCols + groups * sub + i;
         ms[i] = 0;
         mz[i] = 0;
-        if (strip < nstrips) {
+        if (i < groups && strip < nstrips) {
           const size_t off = ((size_t)strip * G + grp) * 8 + gq;
           ms[i] = sp2[off];
           mz[i] = zpb[off];
@@ -344,18 +350,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     };
     uint32_t ms[4], mz[4];
     if (dg < nk) load_meta(dg, ms, mz);
-    for (int kb = dg; kb < nk; kb += kDqGroups) {
+    for (int kb = dg; kb < nk; kb += groups) {
       const int s = kb % stages;
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
       uint32_t nms[4] = {0, 0, 0, 0}, nmz[4] = {0, 0, 0, 0};
-      if (kb + kDqGroups < nk) load_meta(kb + kDqGroups, nms, nmz);  // this warp's next stage
+      if (kb + groups < nk) load_meta(kb + groups, nms, nmz);  // this warp's next stage
       if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
       const uint32_t wdq = st + act_bytes;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int ls = 4 * sub + i;  // strip within the tile
-        if (n0 / kStripCols + ls < nstrips) {
+        const int ls = groups * sub + i;  // strip within the tile
+        if (i < groups && n0 / kStripCols + ls < nstrips) {
           const DeqConst d0 = make_deq_const(mz[i] & 15u, (uint16_t)(ms[i] & 0xffffu));
           const DeqConst d1 = make_deq_const((mz[i] >> 4) & 15u, (uint16_t)(ms[i] >> 16));
           const uint4 v = lds128(st + act_bytes + kWdqBytes + ls * 512 + lane * 16);
@@ -472,15 +478,17 @@ int tc_token_tile(int M) {
 }
 
 // CTAs per SM the tensor-core kernel is sized for: two when the token tile is
-// at most 128 (smem and TMEM allow it; more CTAs for the small tile counts of
-// the middle band of M), else one with the deepest pipeline that fits.
-int tc_ctas_per_sm(int bt) { return bt <= 128 ? 2 : 1; }
+// at most 48 (four stages still fit in half the shared memory; more CTAs for
+// the small tile counts of the middle band of M), else one with the deepest
+// pipeline that fits.
+int tc_ctas_per_sm(int bt) { return bt <= 48 ? 2 : 1; }
 
 size_t tc_smem_bytes(int bt, int* stages_out) {
   const size_t stage = (size_t)bt * 128 + kWdqBytes + kPackedBytes;
   const size_t budget = (tc_ctas_per_sm(bt) == 2 ? 113 * 1024 : 227 * 1024) - 1024 - 256;
   int stages = (int)(budget / stage);
   if (stages > 8) stages = 8;
+  if (stages >= 4) stages &= ~3;  // a multiple of the 4 dequant groups
   if (stages_out) *stages_out = stages;
   return (size_t)stages * stage + 1024 + 256;
 }
@@ -563,6 +571,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
                         : nullptr;
   const size_t smem = tc_smem_bytes(bt, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
+  prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
   static size_t attr_bytes = 0;
   if (attr_bytes < smem) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
