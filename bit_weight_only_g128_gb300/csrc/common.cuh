@@ -11,7 +11,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 
 namespace w4a16 {
 
