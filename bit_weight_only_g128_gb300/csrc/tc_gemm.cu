@@ -80,11 +80,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity`. Returns false if the CTA is
 // aborting (another role gave up) or if this wait exceeded the limit, in
 // which case it raises the abort flag and records `code` in the error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int code) {
+  if (mbar_test(bar, parity)) return true;  // already complete: no suspend
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -273,15 +287,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       int issued = 0;
+      int s = 0;
+      uint32_t ph = 0;
       for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % stages;
-        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
         if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
         const uint32_t st = base + (uint32_t)s * stage_bytes;
         mbar_expect_tx(full_tma(s), act_bytes + kPackedBytes);
         tma_load_2d(st, &tmA, (kb0 + kb) * kStageK, m0, full_tma(s));
         tma_load_2d(st + act_bytes + kWdqBytes, &tmW, (kb0 + kb) * 128, n0 / kStripCols, full_tma(s));
         ++issued;
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA exits
@@ -294,20 +312,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       const uint32_t idesc = f16_idesc(kTileN, bt);
       bool ok = true;
+      int s = 0;
+      uint32_t ph = 0;
+      // descriptors of stage 0; stage s adds s * stage_bytes >> 4
+      const uint64_t bdesc0 = sw128_kmajor_desc(base);
+      const uint64_t adesc0 = sw128_kmajor_desc(base + act_bytes);
       for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % stages;
-        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-        ok = mbar_wait(full_tma(s), ph, abort_flag, kErrMma) &&
-             mbar_wait(full_dq(s), ph, abort_flag, kErrMma);
+        // the dequant group arrives only after it saw the stage's TMA bytes land,
+        // so the second wait normally passes at the first test
+        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma) &&
+             mbar_wait(full_tma(s), ph, abort_flag, kErrMma);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = base + (uint32_t)s * stage_bytes;
-        const uint64_t bdesc = sw128_kmajor_desc(st);
-        const uint64_t adesc = sw128_kmajor_desc(st + act_bytes);
+        const uint64_t soff = (uint64_t)((uint32_t)s * (stage_bytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes of k per MMA
-          tc_mma_f16(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+          tc_mma_f16(tmem_base, adesc0 + soff + 2u * kk, bdesc0 + soff + 2u * kk, idesc,
+                     (kb | kk) != 0);
         tc_commit(empty(s));
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       tc_commit(accum_bar);  // fires once every MMA issued above has completed
       if (!ok) mbar_drain(accum_bar, 0);  // no MMA may run past the TMEM release
