@@ -60,6 +60,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// atomicAdd with acquire-release semantics at device scope: the caller's
+// earlier stores (and those it observed through a CTA barrier) are visible to
+// whoever observes the new value, and the caller observes everything that
+// the earlier adders released.
+__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // CTA that owns unit u when T units are split among C CTAs.
 __device__ __forceinline__ int owner_cta(long long u, long long T, int C) {
   return (int)(((u + 1) * C - 1) / T);
@@ -257,33 +267,43 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
                 __half_as_ushort(__float2half_rn(red[tok * kRedStride + col]));
         }
       } else {
-        // publish the partial tile, then count this CTA in
+        // publish the partial tile, then count this CTA in (one release
+        // atomic after the CTA barrier covers every thread's tile stores)
         constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;
+        constexpr int kPerThread = (kTileFloats + kThreads - 1) / kThreads;
         const int slot = 2 * blockIdx.x + (b == first_blk ? 0 : 1);
         float* my = p.tiles + (size_t)slot * kTileFloats;
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e / kDecodeBlockCols, col = e - tok * kDecodeBlockCols;
           my[e] = red[tok * kRedStride + col];
         }
-        __threadfence();
         __syncthreads();
         const int c_first = owner_cta((long long)b * nbb, T, C);
         const int c_last = owner_cta((long long)b * nbb + nbb - 1, T, C);
-        if (threadIdx.x == 0) s_last = (atomicAdd(p.counters + b, 1) == c_last - c_first);
+        if (threadIdx.x == 0) s_last = (atomic_add_acq_rel(p.counters + b, 1) == c_last - c_first);
         __syncthreads();
         if (s_last) {  // every other contributor has published: finish the block
-          __threadfence();
-          for (int e = threadIdx.x; e < total; e += kThreads) {
-            const int col = e % kDecodeBlockCols;
-            if (col0 + col >= N) continue;
-            float sum = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {  // fixed order: deterministic
-              const int cfirst_blk = (int)(((long long)c * T / C) / nbb);
-              const int cslot = 2 * c + (b == cfirst_blk ? 0 : 1);
-              sum += __ldcg(p.tiles + (size_t)cslot * kTileFloats + e);
+          // sum the contributors' tiles in CTA order (deterministic); every
+          // thread keeps its elements' sums in registers and issues the loads
+          // of one contributor at once
+          float sum[kPerThread];
+#pragma unroll
+          for (int k = 0; k < kPerThread; ++k) sum[k] = 0.f;
+          for (int c = c_first; c <= c_last; ++c) {
+            const int cfirst_blk = (int)(((long long)c * T / C) / nbb);
+            const float* tile = p.tiles + (size_t)(2 * c + (b == cfirst_blk ? 0 : 1)) * kTileFloats;
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+              const int e = threadIdx.x + k * kThreads;
+              if (e < total) sum[k] += __ldcg(tile + e);
             }
-            p.Y[(size_t)(e / kDecodeBlockCols) * N + col0 + col] =
-                __half_as_ushort(__float2half_rn(sum));
+          }
+#pragma unroll
+          for (int k = 0; k < kPerThread; ++k) {
+            const int e = threadIdx.x + k * kThreads;
+            const int col = e % kDecodeBlockCols;
+            if (e < total && col0 + col < N)
+              p.Y[(size_t)(e / kDecodeBlockCols) * N + col0 + col] = __half_as_ushort(__float2half_rn(sum[k]));
           }
           if (threadIdx.x == 0) p.counters[b] = 0;  // ready for the next call
         }

@@ -446,13 +446,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // K split: the last of the tile's CTAs to arrive sums the partial tiles in
       // split order (deterministic), writes Y and resets the tile's counter
       const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-      __threadfence();
-      epilogue_bar();
-      if (dw == 0 && lane == 0)
-        *last_flag = (*abort_flag == 0) && atomicAdd(p.counters + tile, 1) == p.split - 1;
+      epilogue_bar();  // every partial store issued; one release atomic covers them
+      if (dw == 0 && lane == 0) {
+        int old = 0;
+        if (*abort_flag == 0)
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                       : "=r"(old)
+                       : "l"(p.counters + tile)
+                       : "memory");
+        *last_flag = (*abort_flag == 0) && old == p.split - 1;
+      }
       epilogue_bar();
       if (*last_flag) {
-        __threadfence();
         const float* tb = p.tiles + (size_t)tile * p.split * bt * kTileN;
         for (int e = dw * 32 + lane; e < bt * kTileN; e += kDqThreads) {
           const int tok = m0 + e / kTileN, n = n0 + e % kTileN;
