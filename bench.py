@@ -302,7 +302,7 @@ def capture_step(torch, w4, cases, weights, a_views, y_views, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for c, A, Y in zip(cases, a_views, y_views):
-            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"])
+            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"], static_weights=True)
     return g
 
 
@@ -329,7 +329,8 @@ def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
-                w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=rot[0]["workspace"])
+                w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=rot[0]["workspace"],
+                        static_weights=True)
         time_graphs(torch, [g], 3, stream)
         secs = time_graphs(torch, [g], 5, stream) / (5 * reps)
         out.append(secs)
@@ -374,7 +375,7 @@ def run_ours(args, wl, dist, rank, world, local):
         with torch.cuda.graph(g, stream=stream):
             a_flat.copy_(a_host, non_blocking=True)
             for c, A, Y in zip(cases, a_views, y_views):
-                w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"])
+                w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"], static_weights=True)
             y_host.copy_(y_flat, non_blocking=True)
         e2e_graphs.append(g)
     time_graphs(torch, e2e_graphs, args.warmup, stream)
@@ -393,6 +394,7 @@ def run_ours(args, wl, dist, rank, world, local):
                    "layers": [f"{n} K={k} N={nn}" for (n, k, nn) in wl.layers],
                    "M": list(wl.ms), "group": list(wl.groups),
                    "gemms_per_step": len(cases),
+                   "static_weights": True,
                    "l2": (f"inputs larger than L2: {len(rot)} rotating copies of the packed "
                           f"weights, {len(rot) * packed_bytes / 2**20:.0f} MiB")},
         "tflops": world * step_flops * args.steps / secs / 1e12,

@@ -25,6 +25,7 @@ from .build import LIB as LIB_PATH
 
 PATH_AUTO, PATH_DECODE, PATH_TENSOR = 0, 1, 2
 _PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR}
+STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
 
 ERRORS = {
     -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
@@ -198,11 +199,14 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
          path: str = "auto", parts: int = 0, workspace: Optional[torch.Tensor] = None,
-         stream=None) -> torch.Tensor:
+         stream=None, static_weights: bool = False) -> torch.Tensor:
     """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
 
     `workspace` must be zero-filled before its first use (new_workspace);
     without one, a fresh zeroed buffer is allocated for this call.
+    `static_weights` (W4A16_STATIC_WEIGHTS): the kernel may read pw while the
+    work queued before it on the stream drains; pw must not be written by
+    that work.
     """
     M, K = A.shape
     if K != pw.K:
@@ -218,7 +222,8 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
-                               _PATHS[path], parts, _stream(stream)), "w4a16_gemm")
+                               _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0), parts,
+                               _stream(stream)), "w4a16_gemm")
     return out
 
 

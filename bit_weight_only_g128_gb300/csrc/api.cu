@@ -110,6 +110,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
       !aligned(zeros, 8))
     return fail(W4A16_ERR_MISALIGNED,
                 "alignment: A, Wq, scales, Y need 16 bytes and zeros 8 bytes");
+  const bool static_weights = (path & W4A16_STATIC_WEIGHTS) != 0;
+  path &= ~W4A16_STATIC_WEIGHTS;
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
@@ -141,7 +143,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     const int rows = M - r0 < 16 ? M - r0 : 16;
     cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, rows,
                                   N, K, group, decode_ctas(rows, N, K, group, parts), workspace,
-                                  stream);
+                                  static_weights, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   return ok();

@@ -1,9 +1,11 @@
 // Device helpers shared by the W4A16 kernels (sm_103a).
 //
 // Packed format (see include/w4a16.h): a word holds 8 consecutive k of one
-// column with the codes of k-offsets 0,2,4,6 in nibbles 0..3 and 1,3,5,7 in
-// nibbles 4..7, so one mask pulls out the pair (2p, 2p+1) into the two fp16
-// halves of a register.
+// column; nibble p holds k-offset rev3(p), i.e. nibbles 0..7 hold k-offsets
+// 0 4 2 6 1 5 3 7, so one mask on the word (or on the word shifted by 8)
+// pulls a pair of consecutive k-offsets into the two fp16 halves of a
+// register: (0,1) and (4,5) from the word, (2,3) and (6,7) from word >> 8,
+// the second pair of each one nibble higher.
 #pragma once
 
 #include <cstddef>
@@ -63,12 +65,12 @@ __device__ __forceinline__ void dequant_word(uint32_t w, const DeqConst& c, uint
   const uint32_t kSixteenth = 0x2C002C00u;  // fp16x2 (1/16, 1/16)
   const uint32_t w8 = w >> 8;
   const uint32_t x0 = (w & 0x000F000Fu) | kMagic;    // 1024 + q0,    1024 + q1
-  const uint32_t x1 = (w & 0x00F000F0u) | kMagic;    // 1024 + 16 q2, 1024 + 16 q3
-  const uint32_t x2 = (w8 & 0x000F000Fu) | kMagic;   // 1024 + q4,    1024 + q5
+  const uint32_t x1 = (w8 & 0x000F000Fu) | kMagic;   // 1024 + q2,    1024 + q3
+  const uint32_t x2 = (w & 0x00F000F0u) | kMagic;    // 1024 + 16 q4, 1024 + 16 q5
   const uint32_t x3 = (w8 & 0x00F000F0u) | kMagic;   // 1024 + 16 q6, 1024 + 16 q7
   out[0] = hmul2_rn(hsub2_rn(x0, c.zb), c.s2);
-  out[1] = hmul2_rn(hfma2_rn(x1, kSixteenth, c.nzb4), c.s2);
-  out[2] = hmul2_rn(hsub2_rn(x2, c.zb), c.s2);
+  out[1] = hmul2_rn(hsub2_rn(x1, c.zb), c.s2);
+  out[2] = hmul2_rn(hfma2_rn(x2, kSixteenth, c.nzb4), c.s2);
   out[3] = hmul2_rn(hfma2_rn(x3, kSixteenth, c.nzb4), c.s2);
 }
 

@@ -15,23 +15,36 @@
 //   * Warp w handles strip w of each unit's block. Each lane streams its four
 //     words of an atom with one 16-byte load (L1 bypassed); the next unit's
 //     atoms are loaded while the current one is computed (8 atoms, 4 KiB per
-//     warp, always in flight), across block boundaries too. The next unit's
-//     activations are copied into a two-slot shared-memory ring (cp.async)
-//     meanwhile, one CTA barrier per unit.
-//   * Group boundaries fall at fixed positions of a unit (groups are 1, 2, 4
-//     or >= 8 atoms and units start at multiples of 8 atoms), so the code that
-//     rebuilds the dequantization constants is placed at compile time.
-//   * Dequantization in registers (LOP3 + exact fp16 subtract + one fp16
-//     multiply per pair of codes) feeds mma.sync m16n8k16 with the weights as
-//     the 16-row operand (output columns) and up to 8 tokens as the 8-column
-//     operand. k inside each MMA is permuted identically on both operands (a
-//     lane holds 4 consecutive k), which leaves the sum unchanged.
+//     warp, always in flight), across block boundaries too. Activations go
+//     through a three-slot shared-memory ring (cp.async), two units ahead,
+//     with one CTA barrier per unit.
+//   * Codes enter the tensor core as they are. A 4-bit code q masked into the
+//     low nibble of an fp16 half is the subnormal q * 2^-24, exact; masked
+//     one nibble higher it is 16 q * 2^-24. So one AND per pair of codes
+//     feeds mma.sync m16n8k16 (weights as the 16-row operand, tokens as the
+//     8 columns), with the "low nibble" and "high nibble" pairs accumulated
+//     separately (fp32) and the latter divided by 16 at the group's end. k
+//     inside each MMA is permuted identically on both operands, which leaves
+//     the sum unchanged.
+//   * Scale and zero point are applied once per group in fp32: with
+//     P = sum_k q_k a_k over the group and S = sum_k a_k (per token, from one
+//     extra MMA per atom against a ones operand, computed once per CTA), the
+//     group adds s * (P - z * S) = sum_k (q_k - z) s a_k. The product of a
+//     code and an activation is exact, so the only roundings are fp32 ones;
+//     the fp16 rounding of each dequantized weight that a dequantize-then-
+//     multiply kernel performs is not made (the result moves by at most
+//     2^-11 sum |a w|, a quarter of the accuracy bound).
 //   * A run's piece of one block ("segment") that covers the whole block
 //     writes Y directly. A block shared by several CTAs is finished by the
 //     last of them to arrive: each writes its fp32 partial tile to the
 //     workspace, then bumps the block's counter; the one that completes the
 //     count sums the tiles in CTA order (deterministic), writes Y and resets
 //     the counter to zero. No CTA ever waits for another.
+//   * Launched with programmatic stream serialization: the grid may start
+//     while the previous kernel on the stream drains. Everything that grid
+//     may write (A, Y, the workspace) is touched only after the grid-
+//     dependency wait; on request the first unit's weights are read before
+//     it (weights that the preceding work does not write).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,23 +55,47 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
 constexpr int kBatch = 8;                         // atoms per unit
+constexpr int kSlots = 3;                         // activation ring slots
 // One staged activation row of a unit: 8 atoms x 64 k x 2 bytes, padded by
 // 64 bytes so that consecutive rows fall in opposite halves of the 32 banks
 // (a quarter-warp's 16-byte fragment loads cover two rows x 64 bytes).
 constexpr int kActRow = kBatch * kAtomK * 2 + 64;
+constexpr int kActRowVec = kActRow / 16;  // the same in 16-byte vectors
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Dynamic shared memory of the kernel for MT token octets and NG groups per
+// unit. A ring slot holds one unit's activations (MT*8 rows) and the scale and
+// zero-point pairs of its 8 strips.
+template <int MT, int NG>
+struct Smem {
+  static constexpr int kActVecs = MT * 8 * kActRowVec;
+  static constexpr int kSpVecs = kWarps * NG * 2;         // 32 bytes per (strip, group)
+  static constexpr int kZpVecs = (kWarps * NG + 1) / 2;   // 8 bytes per (strip, group)
+  static constexpr int kSlotVecs = kActVecs + kSpVecs + kZpVecs;
+  static constexpr int kRingBytes = kSlots * kSlotVecs * 16;
+  static constexpr int kSumFloats = kBatch * MT * 8;  // one buffer: [atom][token]
+  static constexpr int kSumBytes = 2 * kSumFloats * 4;
+  static constexpr int kRedBytes = MT * 8 * kRedStride * 4;
+  static constexpr int kTotal = kRingBytes + kSumBytes + kRedBytes;
+};
+
+__device__ __forceinline__ void cp_async16(const void* dst_smem, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst_smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(const void* dst_smem, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst_smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
+
+// Programmatic dependent launch: let the next grid on the stream be
+// scheduled, and wait until the previous grid has completed and its writes
+// are visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // atomicAdd with acquire-release semantics at device scope: the caller's
 // earlier stores (and those it observed through a CTA barrier) are visible to
@@ -68,6 +105,38 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
   return old;
+}
+
+// D (16x8 f32) += A (16x16 f16) * B (16x8 f16), and the same with D = A * B.
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// The four code pairs of one packed word (nibble p holds k-offset rev3(p)) as
+// fp16x2 subnormals: c[0] = (k 0,1) and c[1] = (k 2,3) hold q * 2^-24,
+// c[2] = (k 4,5) and c[3] = (k 6,7) hold 16 q * 2^-24.
+__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&c)[4]) {
+  const uint32_t w8 = w >> 8;
+  c[0] = w & 0x000F000Fu;
+  c[1] = w8 & 0x000F000Fu;
+  c[2] = w & 0x00F000F0u;
+  c[3] = w8 & 0x00F000F0u;
+}
+
+// A small non-negative integer as fp32 (exact, no conversion unit).
+__device__ __forceinline__ float small_int_float(uint32_t v) {
+  return __uint_as_float(0x4B000000u | v) - 8388608.0f;
 }
 
 // CTA that owns unit u when T units are split among C CTAs.
@@ -84,7 +153,8 @@ struct DecodeArgs {
   int* counters;
   float* tiles;
   int M, N, K;
-  int gshift;  // group of atom a is a >> gshift (30: a single group per column)
+  int gshift;         // group of atom a is a >> gshift (30: a single group per column)
+  int early_weights;  // read the first unit's weights before the grid-dependency wait
 };
 
 // Where one unit's data lives for this warp/lane.
@@ -94,32 +164,179 @@ struct Unit {
   int n;         // atoms in the unit (1..8)
   bool active;   // this warp's strip exists (N tail)
   const uint4* wp;
-  const uint32_t* sp;
-  const uint8_t* zp;
 };
 
-__device__ __forceinline__ Unit unit_at(const DecodeArgs& p, int x, int natoms, int nbb, int groups,
-                                        int warp, int lane, int gq) {
+__device__ __forceinline__ Unit make_unit(const DecodeArgs& p, int blk, int a0, int natoms,
+                                          int nstrips, int warp, int lane) {
   Unit u;
-  u.blk = x / nbb;
-  u.a0 = (x - u.blk * nbb) * kBatch;
-  u.n = min(kBatch, natoms - u.a0);
-  const int strip = u.blk * kWarps + warp;
-  u.active = strip < p.N / kStripCols;
+  u.blk = blk;
+  u.a0 = a0;
+  u.n = min(kBatch, natoms - a0);
+  const int strip = blk * kWarps + warp;
+  u.active = strip < nstrips;
   const int st = u.active ? strip : 0;
-  u.wp = p.Wq + ((size_t)st * natoms + u.a0) * 32 + lane;
-  u.sp = p.Sp2 + (size_t)st * groups * 8 + gq;
-  u.zp = p.Zp + (size_t)st * groups * 8 + gq;
+  u.wp = p.Wq + ((size_t)st * natoms + a0) * 32 + lane;
   return u;
 }
 
-// Activations of a unit (rows 0..M-1, atoms a0..a0+n-1) into a ring slot.
-__device__ __forceinline__ void stage_act(uint32_t slot, const uint16_t* __restrict__ A, int M,
-                                          int K, int a0, int n) {
-  const int units = n * (kAtomK / 8);  // 16-byte pieces per row
-  for (int idx = threadIdx.x; idx < M * units; idx += kThreads) {
-    const int row = idx / units, c = idx - row * units;
-    cp_async16(slot + row * kActRow + c * 16, A + (size_t)row * K + (size_t)a0 * kAtomK + c * 8);
+// Next unit position in block-major order.
+__device__ __forceinline__ void advance(int& blk, int& a0, int natoms) {
+  a0 += kBatch;
+  if (a0 >= natoms) {
+    a0 = 0;
+    ++blk;
+  }
+}
+
+// One unit into a ring slot: activations (rows 0..M-1, atoms a0..a0+n-1),
+// then the scale pairs and zero-point pairs of the groups it touches for the
+// block's existing strips.
+template <int MT, int NG, int APG>
+__device__ __forceinline__ void stage_unit(uint4* slot, const DecodeArgs& p, int blk, int a0, int n,
+                                           int nstrips, int groups) {
+  using SM = Smem<MT, NG>;
+  const int pieces = n * (kAtomK / 8);  // 16-byte pieces per row
+  for (int idx = threadIdx.x; idx < p.M * (kBatch * kAtomK / 8); idx += kThreads) {
+    const int row = idx >> 6, c = idx & 63;
+    if (c < pieces)
+      cp_async16(slot + row * kActRowVec + c, p.A + (size_t)row * p.K + (size_t)a0 * kAtomK + c * 8);
+  }
+  const int ng = APG < kBatch ? n / APG : 1;  // groups present in the unit
+  const int grp0 = a0 >> p.gshift;
+  const int strips = min(kWarps, nstrips - blk * kWarps);
+  const uint4* sp_src = reinterpret_cast<const uint4*>(p.Sp2);
+  const uint2* zp_src = reinterpret_cast<const uint2*>(p.Zp);
+  uint4* sp_dst = slot + SM::kActVecs;
+  uint2* zp_dst = reinterpret_cast<uint2*>(slot + SM::kActVecs + SM::kSpVecs);
+  for (int idx = threadIdx.x; idx < strips * NG * 3; idx += kThreads) {
+    const int w = idx / (NG * 3), r = idx - w * (NG * 3);
+    const size_t base = (size_t)(blk * kWarps + w) * groups + grp0;
+    if (r < 2 * NG) {  // scale pairs: two 16-byte pieces per group
+      if ((r >> 1) < ng) cp_async16(sp_dst + w * NG * 2 + r, sp_src + base * 2 + r);
+    } else {           // zero-point pairs: 8 bytes per group
+      const int g = r - 2 * NG;
+      if (g < ng) cp_async8(zp_dst + w * NG + g, zp_src + base + g);
+    }
+  }
+}
+
+// sum_k 2^-24 a[k] over one atom of a staged unit, per token, into the sum
+// buffer (the ones operand is the fp16 subnormal 2^-24).
+template <int MT>
+__device__ __forceinline__ void atom_sums(const uint4* slot, float* sb, int atom, int gq, int t) {
+  constexpr uint32_t kOnes = 0x00010001u;
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const uint4* f = slot + (8 * o + gq) * kActRowVec + atom * 8 + t;
+    const uint4 b0 = f[0], b1 = f[4];
+    float d[4];
+    mma_first(d, kOnes, kOnes, kOnes, kOnes, b0.x, b0.y);
+    mma_acc(d, kOnes, kOnes, kOnes, kOnes, b0.z, b0.w);
+    mma_acc(d, kOnes, kOnes, kOnes, kOnes, b1.x, b1.y);
+    mma_acc(d, kOnes, kOnes, kOnes, kOnes, b1.z, b1.w);
+    if (gq == 0) *reinterpret_cast<float2*>(sb + atom * MT * 8 + 8 * o + 2 * t) = make_float2(d[0], d[1]);
+  }
+}
+
+// One atom: the code pairs of the lane's four words (x, y: columns gq and
+// gq + 8 in the first 32 k; z, v: the same columns in the last 32 k) against
+// the staged activations. pe collects the q * 2^-24 pairs, po the
+// 16 q * 2^-24 ones; each MMA's B operand is one adjacent register pair of a
+// 16-byte fragment load.
+template <int MT, bool kFirst>
+__device__ __forceinline__ void atom_mma(float (&pe)[MT][4], float (&po)[MT][4],
+                                         const uint32_t (&x)[4], const uint32_t (&y)[4],
+                                         const uint32_t (&z)[4], const uint32_t (&v)[4],
+                                         const uint4* frag) {
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const uint4 b = frag[o * 8 * kActRowVec];
+    if (kFirst) {
+      mma_first(pe[o], x[0], y[0], x[1], y[1], b.x, b.y);
+      mma_first(po[o], x[2], y[2], x[3], y[3], b.z, b.w);
+    } else {
+      mma_acc(pe[o], x[0], y[0], x[1], y[1], b.x, b.y);
+      mma_acc(po[o], x[2], y[2], x[3], y[3], b.z, b.w);
+    }
+  }
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const uint4 b = frag[o * 8 * kActRowVec + 4];
+    mma_acc(pe[o], z[0], v[0], z[1], v[1], b.x, b.y);
+    mma_acc(po[o], z[2], v[2], z[3], v[3], b.z, b.w);
+  }
+}
+
+// End of a group of `na` atoms starting at atom a: acc += s * (P - z * S),
+// with the group's scale pair sp (s[c], s[c+8]) and zero-point pair zp.
+template <int MT>
+__device__ __forceinline__ void apply_group(float (&acc)[MT][4], const float (&pe)[MT][4],
+                                            const float (&po)[MT][4], uint32_t sp, uint32_t zp,
+                                            const float* sb, int a, int na, int t) {
+  const float s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xffffu)));
+  const float s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
+  const float nsz0 = -s0 * small_int_float(zp & 15u);
+  const float nsz1 = -s1 * small_int_float((zp >> 4) & 15u);
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const float* col = sb + a * MT * 8 + 8 * o + 2 * t;
+    float2 S = *reinterpret_cast<const float2*>(col);
+#pragma unroll
+    for (int j = 1; j < kBatch; ++j)
+      if (j < na) {
+        const float2 v = *reinterpret_cast<const float2*>(col + j * MT * 8);
+        S.x += v.x;
+        S.y += v.y;
+      }
+    const float p0 = fmaf(po[o][0], 0.0625f, pe[o][0]);
+    const float p1 = fmaf(po[o][1], 0.0625f, pe[o][1]);
+    const float p2 = fmaf(po[o][2], 0.0625f, pe[o][2]);
+    const float p3 = fmaf(po[o][3], 0.0625f, pe[o][3]);
+    acc[o][0] = fmaf(nsz0, S.x, fmaf(s0, p0, acc[o][0]));  // column gq,     token 2t
+    acc[o][1] = fmaf(nsz0, S.y, fmaf(s0, p1, acc[o][1]));  // column gq,     token 2t+1
+    acc[o][2] = fmaf(nsz1, S.x, fmaf(s1, p2, acc[o][2]));  // column gq + 8, token 2t
+    acc[o][3] = fmaf(nsz1, S.y, fmaf(s1, p3, acc[o][3]));  // column gq + 8, token 2t+1
+  }
+}
+
+// One unit of this warp's strip, from ring slot `slot` (activations, group
+// pairs) and the unit's atom sums `sb`. kFull: all 8 atoms present, the strip
+// exists and the next unit (if refilled) is full too, so nothing is
+// predicated; otherwise atoms past cu.n are skipped and the refill loads
+// only the next unit's atoms.
+template <int MT, int APG, bool kFull>
+__device__ __forceinline__ void unit_compute(float (&acc)[MT][4], uint4 (&w)[kBatch],
+                                             const Unit& cu, const Unit& nu, bool refill,
+                                             const uint4* slot, const float* sb, int warp,
+                                             int gq, int t) {
+  constexpr int NG = kBatch / APG;
+  using SM = Smem<MT, NG>;
+  const uint4* frag = slot + gq * kActRowVec + t;  // B fragments: row gq, k-octet t
+  const uint32_t* sps = reinterpret_cast<const uint32_t*>(slot + SM::kActVecs) + warp * NG * 8 + gq;
+  const uint8_t* zps = reinterpret_cast<const uint8_t*>(slot + SM::kActVecs + SM::kSpVecs) + warp * NG * 8 + gq;
+  float pe[MT][4], po[MT][4];
+  const bool compute = kFull || cu.active;
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    // the codes leave w[u] before the next unit's atom u is loaded into it
+    uint32_t x[4], y[4], z[4], v[4];
+    code_pairs(w[u].x, x);
+    code_pairs(w[u].y, y);
+    code_pairs(w[u].z, z);
+    code_pairs(w[u].w, v);
+    if (refill && (kFull || u < nu.n)) w[u] = ldg_stream(nu.wp + u * 32);
+    if (compute && (kFull || u < cu.n)) {
+      if (u % APG == 0)
+        atom_mma<MT, true>(pe, po, x, y, z, v, frag + u * 8);
+      else
+        atom_mma<MT, false>(pe, po, x, y, z, v, frag + u * 8);
+      if (APG < kBatch) {
+        if (u % APG == APG - 1)
+          apply_group<MT>(acc, pe, po, sps[(u / APG) * 8], zps[(u / APG) * 8], sb, u + 1 - APG, APG, t);
+      } else if (kFull ? u == kBatch - 1 : u == cu.n - 1) {
+        apply_group<MT>(acc, pe, po, sps[0], zps[0], sb, 0, kFull ? kBatch : cu.n, t);
+      }
+    }
   }
 }
 
@@ -129,15 +346,20 @@ __device__ __forceinline__ void stage_act(uint32_t slot, const uint16_t* __restr
 template <int MT, int APG>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p) {
   constexpr int NG = kBatch / APG;  // groups per unit
-  __shared__ __align__(16) uint8_t act_ring[2][MT * 8 * kActRow];
-  __shared__ float red[MT * 8 * kRedStride];
+  using SM = Smem<MT, NG>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint4* ring = reinterpret_cast<uint4*>(smem);
+  float* sums = reinterpret_cast<float*>(smem + SM::kRingBytes);
+  float* red = reinterpret_cast<float*>(smem + SM::kRingBytes + SM::kSumBytes);
   __shared__ int s_last;
 
+  allow_dependent_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;  // mma groupID / thread-in-group
   const int N = p.N, K = p.K, M = p.M;
   const int natoms = K / kAtomK;
   const int nbb = (natoms + kBatch - 1) / kBatch;  // units per block
+  const int nstrips = N / kStripCols;
   const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
   const int groups = (natoms + (1 << p.gshift) - 1) >> p.gshift;
   const int C = gridDim.x;
@@ -145,123 +367,99 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
   const int u_begin = (int)((long long)blockIdx.x * T / C);
   const int u_end = (int)((long long)(blockIdx.x + 1) * T / C);
   const int first_blk = u_begin / nbb;
-  const uint32_t ring = (uint32_t)__cvta_generic_to_shared(&act_ring[0][0]);
-  constexpr uint32_t kSlot = MT * 8 * kActRow;
-  // this lane's B-fragment position inside a ring slot: row gq, k-octet t
-  const uint32_t frag = (uint32_t)gq * kActRow + 16u * t;
 
-  // ---- first unit: weights, group pairs, activations
-  Unit cu = unit_at(p, u_begin, natoms, nbb, groups, warp, lane, gq);
+  // unit cursors: the current unit, the next one, and the one two ahead
+  // (activation staging)
+  int sblk = first_blk, sa0 = (u_begin - first_blk * nbb) * kBatch;
+  Unit cu = make_unit(p, sblk, sa0, natoms, nstrips, warp, lane);
   uint4 w[kBatch];
-  uint32_t ms[NG], mz[NG];
-  if (cu.active) {
+  if (p.early_weights && cu.active) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u)
       if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
-#pragma unroll
-    for (int g = 0; g < NG; ++g)
-      if (g * APG < cu.n) {
-        const int grp = (cu.a0 + g * APG) >> p.gshift;
-        ms[g] = __ldg(cu.sp + (size_t)grp * 8);
-        mz[g] = __ldg(cu.zp + (size_t)grp * 8);
-      }
   }
-  stage_act(ring, p.A, M, K, cu.a0, cu.n);
-  cp_async_commit();
+  grid_dependency_wait();
+  if (!p.early_weights && cu.active) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
+  }
 
-  float acc[2][MT][4];
+  // token rows past M stay zero (never staged)
+  if (M < MT * 8) {
+    const int per = (MT * 8 - M) * kActRowVec;
+    for (int idx = threadIdx.x; idx < kSlots * per; idx += kThreads) {
+      const int s = idx / per, r = idx - s * per;
+      ring[s * SM::kSlotVecs + M * kActRowVec + r] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  stage_unit<MT, NG, APG>(ring, p, sblk, sa0, cu.n, nstrips, groups);
+  cp_async_commit();
+  advance(sblk, sa0, natoms);
+  if (u_begin + 1 < u_end)
+    stage_unit<MT, NG, APG>(ring + SM::kSlotVecs, p, sblk, sa0, min(kBatch, natoms - sa0), nstrips, groups);
+  cp_async_commit();
+  advance(sblk, sa0, natoms);
+  cp_async_wait_all();
+  __syncthreads();
+  if (warp < cu.n) atom_sums<MT>(ring, sums, warp, gq, t);
+
+  float acc[MT][4];
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
-#pragma unroll
-    for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
+  for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
   int seg_a0 = cu.a0;  // first atom of the current segment
-  DeqConst d0 = {}, d1 = {};
+  int slot = 0;        // ring slot of the current unit
+  int nblk_c = cu.blk, na0 = cu.a0;
 
   for (int x = u_begin; x < u_end; ++x) {
     const int i = x - u_begin;
     const bool has_next = x + 1 < u_end;
-    const Unit nu = unit_at(p, has_next ? x + 1 : x, natoms, nbb, groups, warp, lane, gq);
+    advance(nblk_c, na0, natoms);
+    const Unit nu = has_next ? make_unit(p, nblk_c, na0, natoms, nstrips, warp, lane) : cu;
+    const int slot1 = slot == kSlots - 1 ? 0 : slot + 1;
+    const int slot2 = slot1 == kSlots - 1 ? 0 : slot1 + 1;
     cp_async_wait_all();
-    __syncthreads();  // unit x's activations landed; everyone is done with unit x-1's slot
-    if (has_next) stage_act(ring + ((i + 1) & 1) * kSlot, p.A, M, K, nu.a0, nu.n);
+    __syncthreads();  // unit x+1's slot and unit x's sums are visible; slot x-1 is free
+    if (x + 2 < u_end)
+      stage_unit<MT, NG, APG>(ring + slot2 * SM::kSlotVecs, p, sblk, sa0, min(kBatch, natoms - sa0),
+                              nstrips, groups);
     cp_async_commit();
-    const uint32_t abuf = ring + (i & 1) * kSlot + frag;
+    advance(sblk, sa0, natoms);
+    if (has_next && warp < nu.n)
+      atom_sums<MT>(ring + slot1 * SM::kSlotVecs, sums + ((i + 1) & 1) * SM::kSumFloats, warp, gq, t);
 
-    // group pairs of the next unit
-    uint32_t nms[NG], nmz[NG];
-    if (has_next && nu.active) {
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-        if (g * APG < nu.n) {
-          const int grp = (nu.a0 + g * APG) >> p.gshift;
-          nms[g] = __ldg(nu.sp + (size_t)grp * 8);
-          nmz[g] = __ldg(nu.zp + (size_t)grp * 8);
-        }
-    }
     const bool refill = has_next && nu.active;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const uint4 cw = w[u];
-      if (refill && u < nu.n) w[u] = ldg_stream(nu.wp + u * 32);  // same slot, next unit
-      if (cu.active && u < cu.n) {  // warp-uniform
-        if (u % APG == 0) {  // first atom of a group
-          const uint32_t zz = mz[u / APG], ss = ms[u / APG];
-          d0 = make_deq_const(zz & 15u, (uint16_t)(ss & 0xffffu));
-          d1 = make_deq_const((zz >> 4) & 15u, (uint16_t)(ss >> 16));
-        }
-        uint4 act[2][MT];
-#pragma unroll
-        for (int o = 0; o < MT; ++o)
-#pragma unroll
-          for (int s = 0; s < 2; ++s) act[s][o] = lds128(abuf + o * 8 * kActRow + (u * kAtomK + 32 * s) * 2);
-        uint32_t q[4][4];
-        dequant_word(cw.x, d0, q[0]);  // k-half 0, column gq
-        dequant_word(cw.y, d1, q[1]);  // k-half 0, column gq + 8
-        dequant_word(cw.z, d0, q[2]);  // k-half 1, column gq
-        dequant_word(cw.w, d1, q[3]);  // k-half 1, column gq + 8
-#pragma unroll
-        for (int o = 0; o < MT; ++o) {
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            const uint32_t* lo = q[2 * s];
-            const uint32_t* hi = q[2 * s + 1];
-            mma_16816(acc[s][o], lo[0], hi[0], lo[1], hi[1], act[s][o].x, act[s][o].y);
-            mma_16816(acc[s][o], lo[2], hi[2], lo[3], hi[3], act[s][o].z, act[s][o].w);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      ms[g] = nms[g];
-      mz[g] = nmz[g];
-    }
+    const uint4* cur = ring + slot * SM::kSlotVecs;
+    const float* sb = sums + (i & 1) * SM::kSumFloats;
+    if (cu.active && cu.n == kBatch && refill && nu.n == kBatch)
+      unit_compute<MT, APG, true>(acc, w, cu, nu, true, cur, sb, warp, gq, t);
+    else
+      unit_compute<MT, APG, false>(acc, w, cu, nu, refill, cur, sb, warp, gq, t);
 
     if (!has_next || nu.blk != cu.blk) {
       // ---- end of a segment: atoms [seg_a0, cu.a0 + cu.n) of block cu.blk
       const int b = cu.blk;
       const bool whole = seg_a0 == 0 && cu.a0 + cu.n == natoms;
       if (cu.active) {
+        constexpr float kUnscale = 16777216.0f;  // 2^24: codes entered as q * 2^-24
 #pragma unroll
         for (int o = 0; o < MT; ++o) {
           const int tok = 8 * o + 2 * t;
           const int col = kStripCols * warp + gq;
-          red[tok * kRedStride + col] = acc[0][o][0] + acc[1][o][0];
-          red[(tok + 1) * kRedStride + col] = acc[0][o][1] + acc[1][o][1];
-          red[tok * kRedStride + col + 8] = acc[0][o][2] + acc[1][o][2];
-          red[(tok + 1) * kRedStride + col + 8] = acc[0][o][3] + acc[1][o][3];
+          red[tok * kRedStride + col] = acc[o][0] * kUnscale;
+          red[(tok + 1) * kRedStride + col] = acc[o][1] * kUnscale;
+          red[tok * kRedStride + col + 8] = acc[o][2] * kUnscale;
+          red[(tok + 1) * kRedStride + col + 8] = acc[o][3] * kUnscale;
         }
       }
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int o = 0; o < MT; ++o) acc[s][o][0] = acc[s][o][1] = acc[s][o][2] = acc[s][o][3] = 0.f;
+      for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
       __syncthreads();
       const int col0 = b * kDecodeBlockCols;
       const int total = M * kDecodeBlockCols;
       if (whole) {
         for (int e = threadIdx.x; e < total; e += kThreads) {
-          const int tok = e / kDecodeBlockCols, col = e - tok * kDecodeBlockCols;
+          const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
           if (col0 + col < N)
             p.Y[(size_t)tok * N + col0 + col] =
                 __half_as_ushort(__float2half_rn(red[tok * kRedStride + col]));
@@ -271,10 +469,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         // atomic after the CTA barrier covers every thread's tile stores)
         constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;
         constexpr int kPerThread = (kTileFloats + kThreads - 1) / kThreads;
-        const int slot = 2 * blockIdx.x + (b == first_blk ? 0 : 1);
-        float* my = p.tiles + (size_t)slot * kTileFloats;
+        float* my = p.tiles + (size_t)(2 * blockIdx.x + (b == first_blk ? 0 : 1)) * kTileFloats;
         for (int e = threadIdx.x; e < total; e += kThreads) {
-          const int tok = e / kDecodeBlockCols, col = e - tok * kDecodeBlockCols;
+          const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
           my[e] = red[tok * kRedStride + col];
         }
         __syncthreads();
@@ -283,27 +480,41 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         if (threadIdx.x == 0) s_last = (atomic_add_acq_rel(p.counters + b, 1) == c_last - c_first);
         __syncthreads();
         if (s_last) {  // every other contributor has published: finish the block
-          // sum the contributors' tiles in CTA order (deterministic); every
-          // thread keeps its elements' sums in registers and issues the loads
-          // of one contributor at once
+          // Tiles: a CTA after the first starts its run inside block b, so b
+          // is its first block (slot 0); the first contributor used slot 0
+          // only if its run starts at the block's start.
+          const int first_slot =
+              2 * c_first + ((int)((long long)c_first * T / C) == b * nbb ? 0 : 1);
+          // sum the contributors' tiles in CTA order (deterministic), loading
+          // the values of kAhead contributors at a time
+          constexpr int kAhead = 4 / MT;
           float sum[kPerThread];
 #pragma unroll
           for (int k = 0; k < kPerThread; ++k) sum[k] = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int cfirst_blk = (int)(((long long)c * T / C) / nbb);
-            const float* tile = p.tiles + (size_t)(2 * c + (b == cfirst_blk ? 0 : 1)) * kTileFloats;
+          for (int c0 = c_first; c0 <= c_last; c0 += kAhead) {
+            float v[kAhead][kPerThread];
 #pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-              const int e = threadIdx.x + k * kThreads;
-              if (e < total) sum[k] += __ldcg(tile + e);
+            for (int j = 0; j < kAhead; ++j) {
+              const int c = c0 + j;
+              const float* tile = p.tiles + (size_t)(c == c_first ? first_slot : 2 * c) * kTileFloats;
+#pragma unroll
+              for (int k = 0; k < kPerThread; ++k) {
+                const int e = threadIdx.x + k * kThreads;
+                v[j][k] = (c <= c_last && e < total) ? __ldcg(tile + e) : 0.f;
+              }
             }
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j)
+              if (c0 + j <= c_last)
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) sum[k] += v[j][k];
           }
 #pragma unroll
           for (int k = 0; k < kPerThread; ++k) {
             const int e = threadIdx.x + k * kThreads;
-            const int col = e % kDecodeBlockCols;
+            const int col = e & (kDecodeBlockCols - 1);
             if (e < total && col0 + col < N)
-              p.Y[(size_t)(e / kDecodeBlockCols) * N + col0 + col] = __half_as_ushort(__float2half_rn(sum[k]));
+              p.Y[(size_t)(e >> 7) * N + col0 + col] = __half_as_ushort(__float2half_rn(sum[k]));
           }
           if (threadIdx.x == 0) p.counters[b] = 0;  // ready for the next call
         }
@@ -312,13 +523,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
       seg_a0 = nu.a0;
     }
     cu = nu;
+    slot = slot1;
   }
 }
 
 template <int MT, int APG>
 cudaError_t launch_variant(const DecodeArgs& args, int ctas, cudaStream_t stream) {
-  decode_kernel<MT, APG><<<ctas, kThreads, 0, stream>>>(args);
-  return cudaGetLastError();
+  auto kern = decode_kernel<MT, APG>;
+  constexpr int kSmem = Smem<MT, kBatch / APG>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 template <int MT>
@@ -355,14 +580,22 @@ bool group_shape(int K, int group, int* apg_t, int* gshift) {
 }  // namespace
 
 // CTAs of the decode kernel that fit on one SM (occupancy query, M <= 8 or
-// 9..16 rows; the group size does not change the resources).
+// 9..16 rows, for the variant with the most shared memory: groups of 64).
 int decode_ctas_per_sm(int M) {
   static int cache[2] = {0, 0};
   const int v = M <= 8 ? 0 : 1;
   if (cache[v] == 0) {
     int n = 0;
-    cudaError_t e = v == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<1, 2>, kThreads, 0)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<2, 2>, kThreads, 0);
+    cudaError_t e;
+    if (v == 0) {
+      e = cudaFuncSetAttribute(decode_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<1, 8>::kTotal);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<1, 1>, kThreads, Smem<1, 8>::kTotal);
+    } else {
+      e = cudaFuncSetAttribute(decode_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<2, 8>::kTotal);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<2, 1>, kThreads, Smem<2, 8>::kTotal);
+    }
     if (e != cudaSuccess || n <= 0) return 1;
     cache[v] = n;
   }
@@ -395,7 +628,7 @@ size_t decode_workspace_bytes(int M, int N, int ctas) {
 
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int ctas, void* workspace, cudaStream_t stream) {
+                          int ctas, void* workspace, bool early_weights, cudaStream_t stream) {
   DecodeArgs args;
   int apg_t = 0;
   if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
@@ -409,6 +642,7 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
   args.M = M;
   args.N = N;
   args.K = K;
+  args.early_weights = early_weights ? 1 : 0;
   if (M <= 8) return launch_mt<1>(args, apg_t, ctas, stream);
   return launch_mt<2>(args, apg_t, ctas, stream);
 }

@@ -21,10 +21,11 @@ cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint
 // Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
 // persistent CTAs, 1 <= ctas <= decode_units). `workspace` holds the
 // per-block counters (zero before the first call, left zero by every call)
-// followed by the partial tiles; see decode_workspace_bytes.
+// followed by the partial tiles; see decode_workspace_bytes. With
+// early_weights the first weights are read before the grid-dependency wait.
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int ctas, void* workspace, cudaStream_t stream);
+                          int ctas, void* workspace, bool early_weights, cudaStream_t stream);
 size_t decode_workspace_bytes(int M, int N, int ctas);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);

@@ -64,8 +64,8 @@ __device__ __forceinline__ void word_position(size_t widx, int K, int* n, int* k
   *k0 = kAtomK * a + 32 * sh + 8 * t;
 }
 
-// Nibble position of k-offset e within a word.
-__device__ __forceinline__ int nibble_of(int e) { return (e & 1) ? 4 + (e >> 1) : (e >> 1); }
+// Nibble position of k-offset e within a word: the 3-bit reversal of e.
+__device__ __forceinline__ int nibble_of(int e) { return ((e & 1) << 2) | (e & 2) | (e >> 2); }
 
 __global__ void pack_weights_kernel(const uint8_t* __restrict__ q, int K, int N,
                                     uint32_t* __restrict__ Wq) {

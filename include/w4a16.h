@@ -41,10 +41,12 @@
  *     k in [64a, 64a+64)). The word at offset (j*(K/64) + a)*128 + 4*L + i,
  *     L in [0,32), i in [0,4), with g = L>>2, t = L&3, s = i>>1, r = i&1,
  *     holds column n = 16j + g + 8r at k = 64a + 32s + 8t + e, e = 0..7;
- *     code e sits in nibble p (bits 4p..4p+3), p = e/2 for even e and
- *     p = 4 + (e-1)/2 for odd e. So (word >> 4p) & 0x000F000F holds the
- *     codes of k-offsets (2p, 2p+1) in its two 16-bit halves, and each lane
- *     L of a warp reads its four words of an atom with one 16-byte load.
+ *     code e sits in nibble p (bits 4p..4p+3), p = the 3-bit reversal of e
+ *     (e = 4 e2 + 2 e1 + e0 -> p = 4 e0 + 2 e1 + e2: nibbles 0..7 hold
+ *     k-offsets 0 4 2 6 1 5 3 7). So (word >> 4p) & 0x000F000F holds the
+ *     codes of k-offsets (0,1), (4,5), (2,3), (6,7) for p = 0, 1, 2, 3 in its
+ *     two 16-bit halves, and each lane L of a warp reads its four words of an
+ *     atom with one 16-byte load.
  *   Sp: fp16, N*G of them; offset (j*G + grp)*16 + 2c + h is the scale of
  *     column 16j + 8h + c (c in [0,8), h in {0,1}) in group grp, so the two
  *     columns g and g + 8 that one lane dequantizes share one 32-bit word.
@@ -77,6 +79,15 @@ extern "C" {
 #define W4A16_PATH_AUTO 0
 #define W4A16_PATH_DECODE 1   /* stream-K register-dequant GEMV         */
 #define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
+/* Flag OR-ed into the path of w4a16_gemm_ex: the weights (Wq, scales, zeros)
+ * are not written by the work queued just before this call on the stream, so
+ * the kernel may read them while that work drains. Every kernel of the
+ * library is launched with programmatic stream serialization and touches A,
+ * Y and the workspace only after the previous grid has completed; with this
+ * flag the decode kernel also loads its first weights before that point,
+ * which hides the gap between back-to-back layers. Without it the ordering is
+ * that of a plain launch. */
+#define W4A16_STATIC_WEIGHTS 0x100
 
 /* Message for the last error returned on the calling thread ("" if none). */
 const char* w4a16_last_error(void);
@@ -146,7 +157,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * for the tensor-core path the number of K ranges per output tile (clamped to
  * K/64). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
- * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). */
+ * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
+ * W4A16_STATIC_WEIGHTS (see above); any other bit is W4A16_ERR_INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,

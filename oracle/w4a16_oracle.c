@@ -255,8 +255,8 @@ double oracle_check(const uint16_t* y_gpu, const double* y_ref, const double* ma
 /* [64a, 64a+64)).  Word offset = (j*(K/64) + a)*128 + 4*L + i, where       */
 /* L in [0,32) and i in [0,4); with g = L>>2, t = L&3, s = i>>1, r = i&1    */
 /* the word holds column n = 16j + g + 8r and the 8 values k = 64a + 32s +  */
-/* 8t + e, e = 0..7.  Value e sits in nibble p (bits 4p..4p+3) with         */
-/* p = e/2 for even e and p = 4 + (e-1)/2 for odd e.                        */
+/* 8t + e, e = 0..7.  Value e sits in nibble p (bits 4p..4p+3), p = the    */
+/* 3-bit reversal of e (nibbles 0..7 hold e = 0 4 2 6 1 5 3 7).             */
 /* Scales: fp16 at offset (j*G + grp)*16 + 2*(c%8) + c/8 for column 16j+c. */
 /* Zeros: bytes; byte (j*G + grp)*8 + c (c < 8) holds the zero of column    */
 /* 16j + c in its low nibble and of column 16j + 8 + c in its high nibble.  */
@@ -264,7 +264,7 @@ double oracle_check(const uint16_t* y_gpu, const double* y_ref, const double* ma
 
 static int nibble_of(int e)
 {
-    return (e % 2 == 0) ? e / 2 : 4 + (e - 1) / 2;
+    return 4 * (e % 2) + 2 * ((e / 2) % 2) + e / 4;
 }
 
 static size_t word_offset(int K, int n, int k)

@@ -93,12 +93,19 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Y=8) == -3
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
+    assert _gemm(lib, path=0x200 | 1) == -1           # unknown flag bit
     assert _gemm(lib, parts=-1) == -1
     assert _gemm(lib, path=2, parts=4, ws=0) == -4      # a K-split tensor launch needs a workspace
     assert _gemm(lib, path=1, ws=0) == -4             # decode needs a workspace
     assert _gemm(lib, path=1, ws_bytes=16) == -4
     assert _gemm(lib, path=1, ws=8) == -3             # workspace not 256-byte aligned
     assert _gemm(lib, path=1, K=768, group=192) == -2  # decode: group 64 * 2^j or K
+
+
+def test_static_weights_flag_matches_the_header():
+    text = open(HEADER).read()
+    assert re.search(r"#define W4A16_STATIC_WEIGHTS 0x100\b", text)
+    assert w4.STATIC_WEIGHTS == 0x100
 
 
 def test_gemm_m_zero_is_a_noop(lib):

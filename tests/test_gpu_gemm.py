@@ -12,7 +12,7 @@ import torch
 import bit_weight_only_g128_gb300 as w4
 import oracle
 import synthetic
-from gpu_util import cuda, guarded_output, check_guard, half_bits, prepare, run_and_check
+from gpu_util import cuda, guarded_output, check_guard, half_bits, host, prepare, run_and_check
 
 pytestmark = pytest.mark.gpu
 
@@ -132,3 +132,40 @@ def test_stream_ordering_on_a_side_stream():
     side.synchronize()
     y, mag = oracle.reference(A, q, s, z, 128)
     assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
+
+
+def test_static_weights_keeps_the_order_of_a_layer_chain():
+    """With W4A16_STATIC_WEIGHTS the kernel reads its weights while the previous
+    kernel drains, but its activations only after that kernel is done: a chain
+    of layers fed by each other (and by a plain torch kernel in between) gives
+    the same bits as the same calls made one at a time."""
+    K = N = 1024
+    M = 5
+    pws, refs = [], []
+    for seed in (21, 22, 23):
+        (q, s, z), pw = prepare(synthetic.small_weights(K, N, seed), 128)
+        pws.append(pw)
+        refs.append((q, s, z))
+    A = cuda(synthetic.small_activations(M, K, seed=21))
+
+    def chain(static):
+        x = A
+        outs = []
+        for i, pw in enumerate(pws):
+            x = w4.gemm(x, pw, path="decode", static_weights=static)
+            outs.append(x)
+            if i == 0:
+                x = x * 0.5      # a kernel of another library between two layers
+            if not static:
+                torch.cuda.synchronize()
+        return outs
+
+    plain = [half_bits(y).copy() for y in chain(False)]
+    for _ in range(3):
+        fast = chain(True)
+        w4.device_status()
+        for a, b in zip(plain, fast):
+            assert np.array_equal(a, half_bits(b)), "static-weights chain differs"
+    # and the first layer against the oracle
+    y, mag = oracle.reference(host(A), *refs[0], 128)
+    assert oracle.check(plain[0], y, mag)[0] <= 1.0

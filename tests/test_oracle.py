@@ -252,7 +252,7 @@ def _spec_decode(Wp, K, N):
             s_, rem = divmod(kk, 32)
             t, e = divmod(rem, 8)
             word = (j * natoms + a) * 128 + 4 * (4 * g + t) + 2 * s_ + r
-            p = e // 2 if e % 2 == 0 else 4 + (e - 1) // 2
+            p = int(f"{e:03b}"[::-1], 2)      # nibble = 3-bit reversal of e
             q[k, n] = (int(Wp[word]) >> (4 * p)) & 15
     return q
 
@@ -271,6 +271,24 @@ def test_pack_single_nibble_position():
     assert np.array_equal(Wp, expect)
     assert Zp.tolist() == [0x7 << 28, 0]
     assert Sp[7] == 0x1234 and np.count_nonzero(Sp) == 1   # column 11 = 8*1 + 3 -> 2*3 + 1
+
+
+def test_pack_nibble_order_is_the_bit_reversal_of_the_k_offset():
+    # one code per k-offset e = 0..7 of word 0 (column 0, k = e): nibble p
+    # must hold e = rev3(p), i.e. nibbles 0..7 hold k-offsets 0 4 2 6 1 5 3 7
+    K, N = 64, 16
+    q = np.zeros((K, N), np.uint8)
+    for e in range(8):
+        q[e, 0] = e + 8                      # distinct codes 8..15
+    Wp, _, _ = oracle.pack(q, np.zeros((1, N), np.uint8), np.zeros((1, N), np.uint16), 64)
+    nibbles = [(int(Wp[0]) >> (4 * p)) & 15 for p in range(8)]
+    assert nibbles == [8 + e for e in (0, 4, 2, 6, 1, 5, 3, 7)]
+    # so the pair masks of the kernels see consecutive k-offsets
+    w = int(Wp[0])
+    assert (w & 0xF, (w >> 16) & 0xF) == (8, 9)               # k 0, 1
+    assert ((w >> 8) & 0xF, (w >> 24) & 0xF) == (10, 11)      # k 2, 3
+    assert ((w >> 4) & 0xF, (w >> 20) & 0xF) == (12, 13)      # k 4, 5
+    assert ((w >> 12) & 0xF, (w >> 28) & 0xF) == (14, 15)     # k 6, 7
 
 
 @pytest.mark.parametrize("K,N,group", [(128, 32, 128), (192, 48, 64), (256, 16, 256)])
