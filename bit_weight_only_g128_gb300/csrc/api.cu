@@ -70,6 +70,7 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
   if (T <= 0) return 0;
   long c = requested > 0 ? requested : (long)sm_count() * decode_ctas_per_sm(M);
   if (c > T) c = T;
+  if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
   return (int)c;
 }
 
@@ -264,7 +265,7 @@ int w4a16_device_status(void* stream) {
   if (flag != 0)
     return fail(W4A16_ERR_DEVICE_CHECK,
                 "device error word = 0x%x (bits: 1 producer, 2 MMA, 4 dequant, 8 epilogue waits "
-                "timed out; 16 drain timed out)",
+                "timed out; 16 drain timed out; 32 decode fix-up wait timed out)",
                 flag);
   return ok();
 }

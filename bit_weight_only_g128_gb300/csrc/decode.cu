@@ -7,16 +7,17 @@
 // instruction per weight counts.
 //
 // Design (sm_103a):
-//   * Work unit: one 128-column block (8 strips of 16 columns) x one batch of
-//     8 atoms (512 k; the last batch of a block may be shorter). Units are
-//     ordered block-major; the grid is persistent and CTA c takes the run
-//     [c*T/C, (c+1)*T/C) of the T units (stream-K), so every CTA streams the
-//     same number of bytes in one long, uninterrupted pass.
+//   * Work: the atoms (64 k) of every 128-column block (8 strips of 16
+//     columns), block-major, are split among the persistent CTAs in equal
+//     runs (stream-K). Runs start at group boundaries (multiples of a
+//     group's atoms, up to 8; any atom with one group per column), so every
+//     CTA streams the same number of bytes, to within one group. A run is
+//     walked in units of up to 8 atoms, a unit never crossing a block.
 //   * Warp w handles strip w of each unit's block. Each lane streams its four
 //     words of an atom with one 16-byte load (L1 bypassed); the next unit's
-//     atoms are loaded while the current one is computed (8 atoms, 4 KiB per
-//     warp, always in flight), across block boundaries too. Activations go
-//     through a three-slot shared-memory ring (cp.async), two units ahead,
+//     atoms are loaded while the current one is computed, across block
+//     boundaries too. Activations and the units' scale and zero-point pairs
+//     go through a three-slot shared-memory ring (cp.async), two units ahead,
 //     with one CTA barrier per unit.
 //   * Codes enter the tensor core as they are. A 4-bit code q masked into the
 //     low nibble of an fp16 half is the subnormal q * 2^-24, exact; masked
@@ -35,16 +36,20 @@
 //     multiply kernel performs is not made (the result moves by at most
 //     2^-11 sum |a w|, a quarter of the accuracy bound).
 //   * A run's piece of one block ("segment") that covers the whole block
-//     writes Y directly. A block shared by several CTAs is finished by the
-//     last of them to arrive: each writes its fp32 partial tile to the
-//     workspace, then bumps the block's counter; the one that completes the
-//     count sums the tiles in CTA order (deterministic), writes Y and resets
-//     the counter to zero. No CTA ever waits for another.
+//     writes Y directly. Otherwise the block is shared: a run that starts
+//     inside a block contributes its first segment as an fp32 partial tile
+//     (workspace slot of the CTA) and raises the CTA's flag; the CTA holding
+//     the block's first atom, whose segment of it ends its run, waits for the
+//     flags of the later contributors (raised at the start of their runs, so
+//     the wait is normally over at once; bounded, with an error bit when it
+//     runs out), adds their tiles to its own partial in CTA order
+//     (deterministic), writes Y and lowers the flags for the next call.
 //   * Launched with programmatic stream serialization: the grid may start
 //     while the previous kernel on the stream drains. Everything that grid
 //     may write (A, Y, the workspace) is touched only after the grid-
-//     dependency wait; on request the first unit's weights are read before
-//     it (weights that the preceding work does not write).
+//     dependency wait; on request the first units' weights, scales and zero
+//     points are read before it (weights that the preceding work does not
+//     write).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -56,6 +61,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
 constexpr int kBatch = 8;                         // atoms per unit
 constexpr int kSlots = 3;                         // activation ring slots
+constexpr int kDecodeWaitTimedOut = 32;           // device error bit
 // One staged activation row of a unit: 8 atoms x 64 k x 2 bytes, padded by
 // 64 bytes so that consecutive rows fall in opposite halves of the 32 banks
 // (a quarter-warp's 16-byte fragment loads cover two rows x 64 bytes).
@@ -97,14 +103,30 @@ __device__ __forceinline__ void allow_dependent_launch() {
 }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// atomicAdd with acquire-release semantics at device scope: the caller's
-// earlier stores (and those it observed through a CTA barrier) are visible to
-// whoever observes the new value, and the caller observes everything that
-// the earlier adders released.
-__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
-  return old;
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits (at most about a second) until *flag is non-zero; false if it never
+// became so.
+__device__ __forceinline__ bool wait_flag(const int* flag) {
+  if (ld_acquire(flag) != 0) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire(flag) != 0) return true;
+    if (global_ns() - t0 > 1000000000ull) return false;
+  }
 }
 
 // D (16x8 f32) += A (16x16 f16) * B (16x8 f16), and the same with D = A * B.
@@ -139,7 +161,8 @@ __device__ __forceinline__ float small_int_float(uint32_t v) {
   return __uint_as_float(0x4B000000u | v) - 8388608.0f;
 }
 
-// CTA that owns unit u when T units are split among C CTAs.
+// CTA whose run holds granule u when T granules are split among C CTAs
+// (CTA c takes granules [floor(c T / C), floor((c + 1) T / C))).
 __device__ __forceinline__ int owner_cta(long long u, long long T, int C) {
   return (int)(((u + 1) * C - 1) / T);
 }
@@ -150,11 +173,13 @@ struct DecodeArgs {
   const uint32_t* Sp2;  // scale pairs (s[c], s[c+8])
   const uint8_t* Zp;    // zero-point pairs z[c] | z[c+8] << 4
   uint16_t* Y;
-  int* counters;
-  float* tiles;
+  int* flags;   // one per CTA: its partial tile is published
+  float* tiles;  // one partial tile per CTA
+  int* err;      // device error word
   int M, N, K;
   int gshift;         // group of atom a is a >> gshift (30: a single group per column)
-  int early_weights;  // read the first unit's weights before the grid-dependency wait
+  int granule;        // atoms per split granule (runs start at multiples of it)
+  int early_weights;  // read the first units' weights before the grid-dependency wait
 };
 
 // Where one unit's data lives for this warp/lane.
@@ -166,12 +191,12 @@ struct Unit {
   const uint4* wp;
 };
 
-__device__ __forceinline__ Unit make_unit(const DecodeArgs& p, int blk, int a0, int natoms,
+__device__ __forceinline__ Unit make_unit(const DecodeArgs& p, int blk, int a0, int n, int natoms,
                                           int nstrips, int warp, int lane) {
   Unit u;
   u.blk = blk;
   u.a0 = a0;
-  u.n = min(kBatch, natoms - a0);
+  u.n = n;
   const int strip = blk * kWarps + warp;
   u.active = strip < nstrips;
   const int st = u.active ? strip : 0;
@@ -179,28 +204,41 @@ __device__ __forceinline__ Unit make_unit(const DecodeArgs& p, int blk, int a0, 
   return u;
 }
 
-// Next unit position in block-major order.
-__device__ __forceinline__ void advance(int& blk, int& a0, int natoms) {
-  a0 += kBatch;
-  if (a0 >= natoms) {
-    a0 = 0;
-    ++blk;
+// Position of a unit: block, first atom, global atom index (blk * natoms + a0).
+struct Pos {
+  int blk, a0, g;
+};
+
+// Atoms of the unit starting at q: up to 8, within the block and the run.
+__device__ __forceinline__ int unit_len(const Pos& q, int natoms, int run_end) {
+  return min(kBatch, min(natoms - q.a0, run_end - q.g));
+}
+
+__device__ __forceinline__ void step(Pos& q, int n, int natoms) {
+  q.g += n;
+  q.a0 += n;
+  if (q.a0 == natoms) {
+    q.a0 = 0;
+    ++q.blk;
   }
 }
 
-// One unit into a ring slot: activations (rows 0..M-1, atoms a0..a0+n-1),
-// then the scale pairs and zero-point pairs of the groups it touches for the
-// block's existing strips.
-template <int MT, int NG, int APG>
-__device__ __forceinline__ void stage_unit(uint4* slot, const DecodeArgs& p, int blk, int a0, int n,
-                                           int nstrips, int groups) {
-  using SM = Smem<MT, NG>;
+// Activations of a unit (rows 0..M-1, atoms a0..a0+n-1) into a ring slot.
+__device__ __forceinline__ void stage_act(uint4* slot, const DecodeArgs& p, int a0, int n) {
   const int pieces = n * (kAtomK / 8);  // 16-byte pieces per row
   for (int idx = threadIdx.x; idx < p.M * (kBatch * kAtomK / 8); idx += kThreads) {
     const int row = idx >> 6, c = idx & 63;
     if (c < pieces)
       cp_async16(slot + row * kActRowVec + c, p.A + (size_t)row * p.K + (size_t)a0 * kAtomK + c * 8);
   }
+}
+
+// The scale pairs and zero-point pairs of the groups a unit touches, for the
+// block's existing strips, into the ring slot after the activations.
+template <int MT, int NG, int APG>
+__device__ __forceinline__ void stage_meta(uint4* slot, const DecodeArgs& p, int blk, int a0, int n,
+                                           int nstrips, int groups) {
+  using SM = Smem<MT, NG>;
   const int ng = APG < kBatch ? n / APG : 1;  // groups present in the unit
   const int grp0 = a0 >> p.gshift;
   const int strips = min(kWarps, nstrips - blk * kWarps);
@@ -351,39 +389,45 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
   uint4* ring = reinterpret_cast<uint4*>(smem);
   float* sums = reinterpret_cast<float*>(smem + SM::kRingBytes);
   float* red = reinterpret_cast<float*>(smem + SM::kRingBytes + SM::kSumBytes);
-  __shared__ int s_last;
 
   allow_dependent_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;  // mma groupID / thread-in-group
   const int N = p.N, K = p.K, M = p.M;
   const int natoms = K / kAtomK;
-  const int nbb = (natoms + kBatch - 1) / kBatch;  // units per block
   const int nstrips = N / kStripCols;
   const int nblk = (N + kDecodeBlockCols - 1) / kDecodeBlockCols;
   const int groups = (natoms + (1 << p.gshift) - 1) >> p.gshift;
   const int C = gridDim.x;
-  const int T = nblk * nbb;
-  const int u_begin = (int)((long long)blockIdx.x * T / C);
-  const int u_end = (int)((long long)(blockIdx.x + 1) * T / C);
-  const int first_blk = u_begin / nbb;
+  const int gr = p.granule;
+  const long long T = (long long)nblk * natoms / gr;  // granules
+  const int run_begin = (int)((long long)blockIdx.x * T / C) * gr;
+  const int run_end = (int)((long long)(blockIdx.x + 1) * T / C) * gr;
 
-  // unit cursors: the current unit, the next one, and the one two ahead
-  // (activation staging)
-  int sblk = first_blk, sa0 = (u_begin - first_blk * nbb) * kBatch;
-  Unit cu = make_unit(p, sblk, sa0, natoms, nstrips, warp, lane);
+  // unit cursors: the current unit, the next one (weights), and the one two
+  // ahead (activation staging)
+  Pos sq;
+  sq.blk = run_begin / natoms;
+  sq.a0 = run_begin - sq.blk * natoms;
+  sq.g = run_begin;
+  Pos nq = sq;
+  Unit cu = make_unit(p, sq.blk, sq.a0, unit_len(sq, natoms, run_end), natoms, nstrips, warp, lane);
+  step(nq, cu.n, natoms);
+  const bool two = nq.g < run_end;  // the run has a second unit
+  const int n1 = two ? unit_len(nq, natoms, run_end) : 0;
   uint4 w[kBatch];
-  if (p.early_weights && cu.active) {
+  auto load_first = [&]() {
+    if (cu.active) {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
-  }
+      for (int u = 0; u < kBatch; ++u)
+        if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
+    }
+    stage_meta<MT, NG, APG>(ring, p, sq.blk, sq.a0, cu.n, nstrips, groups);
+    if (two) stage_meta<MT, NG, APG>(ring + SM::kSlotVecs, p, nq.blk, nq.a0, n1, nstrips, groups);
+  };
+  if (p.early_weights) load_first();
   grid_dependency_wait();
-  if (!p.early_weights && cu.active) {
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
-  }
+  if (!p.early_weights) load_first();
 
   // token rows past M stay zero (never staged)
   if (M < MT * 8) {
@@ -393,13 +437,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
       ring[s * SM::kSlotVecs + M * kActRowVec + r] = make_uint4(0, 0, 0, 0);
     }
   }
-  stage_unit<MT, NG, APG>(ring, p, sblk, sa0, cu.n, nstrips, groups);
+  stage_act(ring, p, sq.a0, cu.n);
+  if (two) stage_act(ring + SM::kSlotVecs, p, nq.a0, n1);
   cp_async_commit();
-  advance(sblk, sa0, natoms);
-  if (u_begin + 1 < u_end)
-    stage_unit<MT, NG, APG>(ring + SM::kSlotVecs, p, sblk, sa0, min(kBatch, natoms - sa0), nstrips, groups);
-  cp_async_commit();
-  advance(sblk, sa0, natoms);
+  step(sq, cu.n, natoms);
+  if (two) step(sq, n1, natoms);  // sq: two units ahead of the current one
   cp_async_wait_all();
   __syncthreads();
   if (warp < cu.n) atom_sums<MT>(ring, sums, warp, gq, t);
@@ -409,22 +451,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
   for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
   int seg_a0 = cu.a0;  // first atom of the current segment
   int slot = 0;        // ring slot of the current unit
-  int nblk_c = cu.blk, na0 = cu.a0;
 
-  for (int x = u_begin; x < u_end; ++x) {
-    const int i = x - u_begin;
-    const bool has_next = x + 1 < u_end;
-    advance(nblk_c, na0, natoms);
-    const Unit nu = has_next ? make_unit(p, nblk_c, na0, natoms, nstrips, warp, lane) : cu;
+  for (int i = 0;; ++i) {
+    const bool has_next = nq.g < run_end;
+    const Unit nu = has_next ? make_unit(p, nq.blk, nq.a0, unit_len(nq, natoms, run_end), natoms,
+                                         nstrips, warp, lane)
+                             : cu;
     const int slot1 = slot == kSlots - 1 ? 0 : slot + 1;
     const int slot2 = slot1 == kSlots - 1 ? 0 : slot1 + 1;
     cp_async_wait_all();
-    __syncthreads();  // unit x+1's slot and unit x's sums are visible; slot x-1 is free
-    if (x + 2 < u_end)
-      stage_unit<MT, NG, APG>(ring + slot2 * SM::kSlotVecs, p, sblk, sa0, min(kBatch, natoms - sa0),
-                              nstrips, groups);
+    __syncthreads();  // the next unit's slot and this unit's sums are visible; slot i-1 is free
+    if (sq.g < run_end) {
+      const int n2 = unit_len(sq, natoms, run_end);
+      stage_meta<MT, NG, APG>(ring + slot2 * SM::kSlotVecs, p, sq.blk, sq.a0, n2, nstrips, groups);
+      stage_act(ring + slot2 * SM::kSlotVecs, p, sq.a0, n2);
+      step(sq, n2, natoms);
+    }
     cp_async_commit();
-    advance(sblk, sa0, natoms);
     if (has_next && warp < nu.n)
       atom_sums<MT>(ring + slot1 * SM::kSlotVecs, sums + ((i + 1) & 1) * SM::kSumFloats, warp, gq, t);
 
@@ -439,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
     if (!has_next || nu.blk != cu.blk) {
       // ---- end of a segment: atoms [seg_a0, cu.a0 + cu.n) of block cu.blk
       const int b = cu.blk;
-      const bool whole = seg_a0 == 0 && cu.a0 + cu.n == natoms;
+      const bool head = seg_a0 == 0;  // holds the block's first atom
+      const bool whole = head && cu.a0 + cu.n == natoms;
       if (cu.active) {
         constexpr float kUnscale = 16777216.0f;  // 2^24: codes entered as q * 2^-24
 #pragma unroll
@@ -454,76 +498,85 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
       }
 #pragma unroll
       for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
-      __syncthreads();
+      constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;
       const int col0 = b * kDecodeBlockCols;
       const int total = M * kDecodeBlockCols;
       if (whole) {
+        __syncthreads();
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
           if (col0 + col < N)
             p.Y[(size_t)tok * N + col0 + col] =
                 __half_as_ushort(__float2half_rn(red[tok * kRedStride + col]));
         }
-      } else {
-        // publish the partial tile, then count this CTA in (one release
-        // atomic after the CTA barrier covers every thread's tile stores)
-        constexpr int kTileFloats = MT * 8 * kDecodeBlockCols;
+      } else if (head) {
+        // finish the block: the later contributors' tiles, in CTA order
+        const int c_last = owner_cta(((long long)(b + 1) * natoms - 1) / gr, T, C);
+        const int others = c_last - (int)blockIdx.x;
+        bool ok = true;
+        for (int j = threadIdx.x; j < others; j += kThreads) {
+          int* f = p.flags + blockIdx.x + 1 + j;
+          if (wait_flag(f))
+            *f = 0;  // lowered for the next call
+          else
+            ok = false;
+        }
+        if (!ok) atomicOr(p.err, kDecodeWaitTimedOut);
+        __syncthreads();  // (acquire by the waiting threads, then the barrier)
+        // own partial first, then the tiles in CTA order (deterministic); the
+        // values of kAhead contributors are loaded at a time
         constexpr int kPerThread = (kTileFloats + kThreads - 1) / kThreads;
-        float* my = p.tiles + (size_t)(2 * blockIdx.x + (b == first_blk ? 0 : 1)) * kTileFloats;
+        constexpr int kAhead = 4 / MT;
+        float v[kPerThread];
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+          const int e = threadIdx.x + k * kThreads;
+          v[k] = e < total ? red[(e >> 7) * kRedStride + (e & (kDecodeBlockCols - 1))] : 0.f;
+        }
+        for (int j0 = 1; j0 <= others; j0 += kAhead) {
+          float tv[kAhead][kPerThread];
+#pragma unroll
+          for (int jj = 0; jj < kAhead; ++jj) {
+            const float* tile = p.tiles + (size_t)(blockIdx.x + j0 + jj) * kTileFloats;
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+              const int e = threadIdx.x + k * kThreads;
+              tv[jj][k] = (j0 + jj <= others && e < total) ? __ldcg(tile + e) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int jj = 0; jj < kAhead; ++jj)
+            if (j0 + jj <= others)
+#pragma unroll
+              for (int k = 0; k < kPerThread; ++k) v[k] += tv[jj][k];
+        }
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+          const int e = threadIdx.x + k * kThreads;
+          const int col = e & (kDecodeBlockCols - 1);
+          if (e < total && col0 + col < N)
+            p.Y[(size_t)(e >> 7) * N + col0 + col] = __half_as_ushort(__float2half_rn(v[k]));
+        }
+      } else {
+        // a run that starts inside block b: publish the partial tile, then
+        // raise the flag (release after the CTA barrier covers every
+        // thread's tile stores)
+        __syncthreads();
+        float* my = p.tiles + (size_t)blockIdx.x * kTileFloats;
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
           my[e] = red[tok * kRedStride + col];
         }
         __syncthreads();
-        const int c_first = owner_cta((long long)b * nbb, T, C);
-        const int c_last = owner_cta((long long)b * nbb + nbb - 1, T, C);
-        if (threadIdx.x == 0) s_last = (atomic_add_acq_rel(p.counters + b, 1) == c_last - c_first);
-        __syncthreads();
-        if (s_last) {  // every other contributor has published: finish the block
-          // Tiles: a CTA after the first starts its run inside block b, so b
-          // is its first block (slot 0); the first contributor used slot 0
-          // only if its run starts at the block's start.
-          const int first_slot =
-              2 * c_first + ((int)((long long)c_first * T / C) == b * nbb ? 0 : 1);
-          // sum the contributors' tiles in CTA order (deterministic), loading
-          // the values of kAhead contributors at a time
-          constexpr int kAhead = 4 / MT;
-          float sum[kPerThread];
-#pragma unroll
-          for (int k = 0; k < kPerThread; ++k) sum[k] = 0.f;
-          for (int c0 = c_first; c0 <= c_last; c0 += kAhead) {
-            float v[kAhead][kPerThread];
-#pragma unroll
-            for (int j = 0; j < kAhead; ++j) {
-              const int c = c0 + j;
-              const float* tile = p.tiles + (size_t)(c == c_first ? first_slot : 2 * c) * kTileFloats;
-#pragma unroll
-              for (int k = 0; k < kPerThread; ++k) {
-                const int e = threadIdx.x + k * kThreads;
-                v[j][k] = (c <= c_last && e < total) ? __ldcg(tile + e) : 0.f;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < kAhead; ++j)
-              if (c0 + j <= c_last)
-#pragma unroll
-                for (int k = 0; k < kPerThread; ++k) sum[k] += v[j][k];
-          }
-#pragma unroll
-          for (int k = 0; k < kPerThread; ++k) {
-            const int e = threadIdx.x + k * kThreads;
-            const int col = e & (kDecodeBlockCols - 1);
-            if (e < total && col0 + col < N)
-              p.Y[(size_t)(e >> 7) * N + col0 + col] = __half_as_ushort(__float2half_rn(sum[k]));
-          }
-          if (threadIdx.x == 0) p.counters[b] = 0;  // ready for the next call
-        }
+        if (threadIdx.x == 0) st_release(p.flags + blockIdx.x, 1);
       }
       __syncthreads();  // the partial tile buffer is reused by the next segment
       seg_a0 = nu.a0;
     }
+    if (!has_next) break;
     cu = nu;
     slot = slot1;
+    step(nq, cu.n, natoms);
   }
 }
 
@@ -602,28 +655,32 @@ int decode_ctas_per_sm(int M) {
   return cache[v];
 }
 
-// Work units (128 columns x 8 atoms) of a problem; 0 if the group size is not
-// supported by the decode kernel.
+// Atoms per split granule: runs start at group boundaries (a group's atoms,
+// 8 for groups of 8 atoms or more) or anywhere with one group per column.
+int split_granule(int apg_t, int gshift) { return gshift == 30 ? 1 : apg_t; }
+
+// Split granules of a problem (the most CTAs a launch can use); 0 if the
+// group size is not supported by the decode kernel.
 long decode_units(int N, int K, int group) {
   int apg_t, gshift;
   if (!group_shape(K, group, &apg_t, &gshift)) return 0;
   const long natoms = K / kAtomK;
-  return (long)((N + kDecodeBlockCols - 1) / kDecodeBlockCols) * ((natoms + kBatch - 1) / kBatch);
+  return (long)((N + kDecodeBlockCols - 1) / kDecodeBlockCols) * natoms / split_granule(apg_t, gshift);
 }
 
-// The counter area has room for the largest legal N (2^20 columns = 8192
-// blocks), whatever N this call has: a workspace can then serve calls of any
-// shape in turn, since no call's partial tiles ever land on another call's
-// counters.
+// The flag area has room for the most CTAs a launch may have (8192), whatever
+// this call's shape: a workspace can then serve calls of any shape in turn.
 size_t decode_counter_bytes(int N) {
   (void)N;
-  return (size_t)((1 << 20) / kDecodeBlockCols) * sizeof(int);
+  return (size_t)kDecodeMaxCtas * sizeof(int);
 }
 
+// Flags, then one fp32 partial tile (M rows padded to 8 or 16 x 128 columns)
+// per CTA.
 size_t decode_workspace_bytes(int M, int N, int ctas) {
   const int mt = M <= 8 ? 1 : 2;
   const size_t tile_bytes = (size_t)mt * 8 * kDecodeBlockCols * sizeof(float);
-  return decode_counter_bytes(N) + 2 * (size_t)ctas * tile_bytes;
+  return decode_counter_bytes(N) + (size_t)ctas * tile_bytes;
 }
 
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
@@ -637,8 +694,11 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
   args.Sp2 = reinterpret_cast<const uint32_t*>(Sp);
   args.Zp = reinterpret_cast<const uint8_t*>(Zp);
   args.Y = Y;
-  args.counters = static_cast<int*>(workspace);
+  args.flags = static_cast<int*>(workspace);
   args.tiles = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + decode_counter_bytes(N));
+  args.granule = split_granule(apg_t, args.gshift);
+  cudaError_t e = device_error_word(&args.err);
+  if (e != cudaSuccess) return e;
   args.M = M;
   args.N = N;
   args.K = K;

@@ -19,18 +19,19 @@ cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint
                               int N, int group, uint16_t* deq, cudaStream_t stream);
 
 // Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
-// persistent CTAs, 1 <= ctas <= decode_units). `workspace` holds the
-// per-block counters (zero before the first call, left zero by every call)
-// followed by the partial tiles; see decode_workspace_bytes. With
-// early_weights the first weights are read before the grid-dependency wait.
+// persistent CTAs, 1 <= ctas <= min(decode_units, kDecodeMaxCtas)).
+// `workspace` holds the per-CTA flags (zero before the first call, left zero
+// by every call) followed by the partial tiles; see decode_workspace_bytes.
+// With early_weights the first weights are read before the grid-dependency
+// wait.
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int ctas, void* workspace, bool early_weights, cudaStream_t stream);
 size_t decode_workspace_bytes(int M, int N, int ctas);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
-// Work units (128 columns x 512 k) of a problem; 0 if the decode kernel does
-// not support the group size.
+// Split granules (128 columns x a group's atoms, at most 8) of a problem: the
+// most CTAs a decode launch can use; 0 if the group size is not supported.
 long decode_units(int N, int K, int group);
 // CTAs of the decode kernel for M rows that fit on one SM (occupancy query).
 int decode_ctas_per_sm(int M);
@@ -57,5 +58,11 @@ int report_ok();
 
 // Output columns per decode CTA.
 constexpr int kDecodeBlockCols = 128;
+// Most CTAs of one decode launch (the size of its flag area).
+constexpr int kDecodeMaxCtas = 8192;
+
+// Device address of the library's error word (bits set by kernels whose
+// bounded waits ran out), for kernels that take it as an argument.
+cudaError_t device_error_word(int** ptr);
 
 }  // namespace w4a16

@@ -8,7 +8,7 @@
 // which combines partial sums through scratch memory.
 //
 // The scratch lives in one file-scope device array below: every GPU that
-// loads the library reserves it (32 KiB of counters plus 8 MiB of partial
+// loads the library reserves it (32 KiB of flags plus 8 MiB of partial
 // tiles) until the process exits. Host code cannot pass the array's name to
 // a kernel (on the host it only stands for the symbol); its device address is
 // looked up once per device, on the first call made with that device current.
@@ -93,14 +93,14 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const u
   const int rows = M < 16 ? M : 16;
   long ctas = (long)sms * decode_ctas_per_sm(rows);
   if (ctas > units) ctas = units;
+  if (ctas > kDecodeMaxCtas) ctas = kDecodeMaxCtas;
   const size_t need = decode_workspace_bytes(rows, N, (int)ctas);
   if (need > kScratchBytes)
     return fail_fmt(W4A16_ERR_UNSUPPORTED_SHAPE,
                     "needs %ld scratch bytes, above the %ld this entry point holds", (long)need,
                     (long)kScratchBytes);
-  // the block counters must start at zero (the kernel leaves them at zero)
-  const size_t nblk = (size_t)((N + kDecodeBlockCols - 1) / kDecodeBlockCols);
-  e = cudaMemsetAsync(scratch, 0, nblk * sizeof(int), (cudaStream_t)stream);
+  // the per-CTA flags must start at zero (the kernel leaves them at zero)
+  e = cudaMemsetAsync(scratch, 0, (size_t)ctas * sizeof(int), (cudaStream_t)stream);
   for (int r0 = 0; e == cudaSuccess && r0 < M; r0 += 16) {
     const int r = M - r0 < 16 ? M - r0 : 16;
     e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, r, N, K, group,

@@ -616,6 +616,23 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   return cudaGetLastError();
 }
 
+cudaError_t device_error_word(int** ptr) {
+  static int* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev]) {
+    *ptr = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_device_error);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = static_cast<int*>(p);
+  *ptr = static_cast<int*>(p);
+  return cudaSuccess;
+}
+
 cudaError_t read_and_clear_device_error(int* flag) {
   cudaError_t e = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
   if (e != cudaSuccess || *flag == 0) return e;

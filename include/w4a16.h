@@ -128,7 +128,7 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
  * (0 when none). Work split across CTAs is combined through it: the decode
  * path (M <= 16 rows per launch) shares 128-column blocks between CTAs, and
  * the tensor-core path splits K when its output tiles cannot fill the SMs.
- * Layout: a 32 KiB counter area followed by fp32 partial tiles. The counter
+ * Layout: a 32 KiB flag/counter area followed by fp32 partial tiles. That
  * area must be zero-filled before the first use; every call leaves it
  * zero-filled again, so one buffer serves any number of calls, of any shape
  * that fits, that run one after another. Calls that may run concurrently
@@ -153,7 +153,9 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
 
 /* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and the
  * work partition forced (`parts`, 0 = automatic): for the decode path the
- * number of persistent CTAs (clamped to the 128-column x 512-k work units),
+ * number of persistent CTAs (clamped to 8192 and to the split granules:
+ * 128-column blocks x groups of K, a group counted as at most 512 k and
+ * K split anywhere on 64-k boundaries when group == K),
  * for the tensor-core path the number of K ranges per output tile (clamped to
  * K/64). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
@@ -174,15 +176,15 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
  * memory budget), plugins without access to their host's allocator, or loops
  * that cannot afford an allocation. The pages have no counterpart of it.
  * It takes no workspace: its scratch is a device array inside the library,
- * 32 KiB of counters plus 8 MiB of partial tiles, which every GPU that loads
+ * 32 KiB of flags plus 8 MiB of partial tiles, which every GPU that loads
  * the library holds until the process exits. Shapes whose partial tiles do
- * not fit (more than 512 CTAs for 9..16 rows, 1024 for up to 8) are rejected
+ * not fit (more than 1024 CTAs for 9..16 rows, 2048 for up to 8) are rejected
  * with W4A16_ERR_UNSUPPORTED_SHAPE; the decode path's group rule applies.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
  * Every call on a device shares the one array: calls that overlap on the GPU
  * (other streams, other host threads) race and give wrong results. Each call
- * clears the counters it uses before its kernels run. Any M is taken, in
+ * clears the flags it uses before its kernels run. Any M is taken, in
  * launches of 16 rows. */
 int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                        const uint32_t* zeros, int M, int N, int K, int group,

@@ -114,15 +114,24 @@ def test_gemm_m_zero_is_a_noop(lib):
 
 
 def test_workspace_sizes(lib):
-    # decode path: counters + two fp32 tiles (8 or 16 tokens x 128 columns)
-    # per CTA; tensor path: counters + one fp32 tile (token tile x 128) per
+    # decode path: flags + one fp32 tile (8 or 16 tokens x 128 columns) per
+    # CTA; tensor path: counters + one fp32 tile (token tile x 128) per
     # output tile and K range, none without a split
-    head = 32768   # counters for up to 2^20 / 128 column blocks
+    head = 32768   # flags for up to 8192 CTAs / counters for 2^20 / 128 column blocks
     assert w4.workspace_size(0, 4096, 4096, 128) == 0
     assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=1) == 0
     assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=3) == head + 32 * 3 * 64 * 128 * 4
     assert w4.workspace_size(300, 256, 4096, 128, path="tensor", parts=2) == head + 4 * 2 * 256 * 128 * 4
-    assert w4.workspace_size(1, 4096, 4096, 128, path="decode", parts=10) == head + 2 * 10 * 8 * 128 * 4
-    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", parts=10) == head + 2 * 10 * 16 * 128 * 4
-    # the CTA count is clamped to the work units: 32 blocks x 1 batch of 8 atoms
-    assert w4.workspace_size(1, 4096, 512, 128, path="decode", parts=1000) == head + 2 * 32 * 8 * 128 * 4
+    assert w4.workspace_size(1, 4096, 4096, 128, path="decode", parts=10) == head + 10 * 8 * 128 * 4
+    assert w4.workspace_size(16, 4096, 4096, 128, path="decode", parts=10) == head + 10 * 16 * 128 * 4
+    # the CTA count is clamped to the split granules (arguments: M, N, K,
+    # group): 32 blocks x 4 groups of 2 atoms
+    assert w4.workspace_size(1, 4096, 512, 128, path="decode", parts=1000) == head + 128 * 8 * 128 * 4
+    # groups of 8 atoms or more split every 8 atoms: 32 blocks x 1, 4 x 8
+    assert w4.workspace_size(1, 4096, 512, 512, path="decode", parts=1000) == head + 32 * 8 * 128 * 4
+    assert w4.workspace_size(1, 512, 4096, 1024, path="decode", parts=1000) == head + 32 * 8 * 128 * 4
+    # one group per column (K not a power-of-two number of atoms): any 64-k
+    # boundary, 4 blocks x 5 atoms
+    assert w4.workspace_size(1, 512, 320, 320, path="decode", parts=1000) == head + 20 * 8 * 128 * 4
+    # and never above 8192 CTAs
+    assert w4.workspace_size(1, 65536, 4096, 64, path="decode", parts=20000) == head + 8192 * 8 * 128 * 4

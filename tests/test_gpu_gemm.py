@@ -48,10 +48,11 @@ def test_outlier_activation_columns():
     run_and_check(4, 4096, 256, 128, seed=5, outliers=True)
 
 
-@pytest.mark.parametrize("parts", [1, 2, 3, 7, 11, 12, 13, 1000])
+@pytest.mark.parametrize("parts", [1, 2, 3, 7, 11, 12, 13, 25, 47, 48, 1000])
 def test_every_cta_count_meets_the_tolerance(parts):
-    """One CTA (every block whole), blocks shared unevenly, one unit per CTA,
-    clamping to the 3 x 4 = 12 units."""
+    """One CTA (every block whole), blocks shared unevenly between CTAs whose
+    runs start inside them, one group per CTA, clamping to the 3 x 16 = 48
+    split granules (groups of 2 atoms)."""
     run_and_check(8, 2048, 272, 128, seed=11, path="decode", parts=parts)
 
 
