@@ -232,6 +232,14 @@ def cpu_baseline(wl, target_s=15.0):
                        f"first {ncols} output columns of each layer; dequantize + fp64 matmul")}
 
 
+def workload_config(wl):
+    """The `config` object of the JSON line (both arms)."""
+    return {"workload": wl.name,
+            "layers": [f"{n} K={k} N={nn}" for (n, k, nn) in wl.layers],
+            "M": list(wl.ms), "group": list(wl.groups),
+            "gemms_per_step": len(wl.cases())}
+
+
 def run_reference(args, wl, dist, rank, world):
     """The CPU oracle as the reference arm, on the same metric and workload."""
     if rank != 0:
@@ -255,7 +263,7 @@ def run_reference(args, wl, dist, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name},
+            "config": workload_config(wl),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -452,10 +460,7 @@ def run_ours(args, wl, dist, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": wl.name,
-                   "layers": [f"{n} K={k} N={nn}" for (n, k, nn) in wl.layers],
-                   "M": list(wl.ms), "group": list(wl.groups),
-                   "gemms_per_step": len(cases),
+        "config": {**workload_config(wl),
                    "static_weights": True,
                    "l2": (f"inputs larger than L2: {len(rot)} rotating copies of the packed "
                           f"weights, {len(rot) * packed_bytes / 2**20:.0f} MiB")},
