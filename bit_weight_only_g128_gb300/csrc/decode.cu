@@ -17,8 +17,9 @@
 //     words of an atom with one 16-byte load (L1 bypassed); the next unit's
 //     atoms are loaded while the current one is computed, across block
 //     boundaries too. Activations and the units' scale and zero-point pairs
-//     go through a three-slot shared-memory ring (cp.async), two units ahead,
-//     with one CTA barrier per unit.
+//     go through a four-slot shared-memory ring (cp.async), three units
+//     ahead, with one CTA barrier per unit; a unit's copies have two units of
+//     compute to land.
 //   * Codes enter the tensor core as they are. A 4-bit code q masked into the
 //     low nibble of an fp16 half is the subnormal q * 2^-24, exact; masked
 //     one nibble higher it is 16 q * 2^-24. So one AND per pair of codes
@@ -60,7 +61,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRedStride = kDecodeBlockCols + 4;  // padded row of the partial tile
 constexpr int kBatch = 8;                         // atoms per unit
-constexpr int kSlots = 3;                         // activation ring slots
+constexpr int kSlots = 4;                         // activation ring slots
 constexpr int kDecodeWaitTimedOut = 32;           // device error bit
 // One staged activation row of a unit: 8 atoms x 64 k x 2 bytes, padded by
 // 64 bytes so that consecutive rows fall in opposite halves of the 32 banks
@@ -94,6 +95,8 @@ __device__ __forceinline__ void cp_async8(const void* dst_smem, const void* src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// all but the most recently committed group of this thread's copies landed
+__device__ __forceinline__ void cp_async_wait_prior() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Programmatic dependent launch: let the next grid on the stream be
 // scheduled, and wait until the previous grid has completed and its writes
@@ -276,19 +279,29 @@ __device__ __forceinline__ void atom_sums(const uint4* slot, float* sb, int atom
   }
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // One atom: the code pairs of the lane's four words (x, y: columns gq and
 // gq + 8 in the first 32 k; z, v: the same columns in the last 32 k) against
-// the staged activations. pe collects the q * 2^-24 pairs, po the
-// 16 q * 2^-24 ones; each MMA's B operand is one adjacent register pair of a
-// 16-byte fragment load.
+// the staged activations at shared address `frag` (row gq, k-octet t of the
+// atom). pe collects the q * 2^-24 pairs, po the 16 q * 2^-24 ones; each
+// MMA's B operand is one adjacent register pair of a 16-byte fragment load.
+// The fragment loads are volatile: they stay next to their MMAs instead of
+// being hoisted a whole unit ahead into registers.
 template <int MT, bool kFirst>
 __device__ __forceinline__ void atom_mma(float (&pe)[MT][4], float (&po)[MT][4],
                                          const uint32_t (&x)[4], const uint32_t (&y)[4],
                                          const uint32_t (&z)[4], const uint32_t (&v)[4],
-                                         const uint4* frag) {
+                                         uint32_t frag) {
 #pragma unroll
   for (int o = 0; o < MT; ++o) {
-    const uint4 b = frag[o * 8 * kActRowVec];
+    const uint4 b = lds128(frag + o * 8 * kActRow);
     if (kFirst) {
       mma_first(pe[o], x[0], y[0], x[1], y[1], b.x, b.y);
       mma_first(po[o], x[2], y[2], x[3], y[3], b.z, b.w);
@@ -299,7 +312,7 @@ __device__ __forceinline__ void atom_mma(float (&pe)[MT][4], float (&po)[MT][4],
   }
 #pragma unroll
   for (int o = 0; o < MT; ++o) {
-    const uint4 b = frag[o * 8 * kActRowVec + 4];
+    const uint4 b = lds128(frag + o * 8 * kActRow + 64);
     mma_acc(pe[o], z[0], v[0], z[1], v[1], b.x, b.y);
     mma_acc(po[o], z[2], v[2], z[3], v[3], b.z, b.w);
   }
@@ -349,7 +362,8 @@ __device__ __forceinline__ void unit_compute(float (&acc)[MT][4], uint4 (&w)[kBa
                                              int gq, int t) {
   constexpr int NG = kBatch / APG;
   using SM = Smem<MT, NG>;
-  const uint4* frag = slot + gq * kActRowVec + t;  // B fragments: row gq, k-octet t
+  // B fragments: row gq, k-octet t
+  const uint32_t frag = (uint32_t)__cvta_generic_to_shared(slot + gq * kActRowVec + t);
   const uint32_t* sps = reinterpret_cast<const uint32_t*>(slot + SM::kActVecs) + warp * NG * 8 + gq;
   const uint8_t* zps = reinterpret_cast<const uint8_t*>(slot + SM::kActVecs + SM::kSpVecs) + warp * NG * 8 + gq;
   float pe[MT][4], po[MT][4];
@@ -365,9 +379,9 @@ __device__ __forceinline__ void unit_compute(float (&acc)[MT][4], uint4 (&w)[kBa
     if (refill && (kFull || u < nu.n)) w[u] = ldg_stream(nu.wp + u * 32);
     if (compute && (kFull || u < cu.n)) {
       if (u % APG == 0)
-        atom_mma<MT, true>(pe, po, x, y, z, v, frag + u * 8);
+        atom_mma<MT, true>(pe, po, x, y, z, v, frag + u * 128);
       else
-        atom_mma<MT, false>(pe, po, x, y, z, v, frag + u * 8);
+        atom_mma<MT, false>(pe, po, x, y, z, v, frag + u * 128);
       if (APG < kBatch) {
         if (u % APG == APG - 1)
           apply_group<MT>(acc, pe, po, sps[(u / APG) * 8], zps[(u / APG) * 8], sb, u + 1 - APG, APG, t);
@@ -441,8 +455,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
   if (two) stage_act(ring + SM::kSlotVecs, p, nq.a0, n1);
   cp_async_commit();
   step(sq, cu.n, natoms);
-  if (two) step(sq, n1, natoms);  // sq: two units ahead of the current one
-  cp_async_wait_all();
+  if (two) step(sq, n1, natoms);
+  // the third unit in a group of its own, left in flight
+  if (sq.g < run_end) {
+    const int n2 = unit_len(sq, natoms, run_end);
+    stage_meta<MT, NG, APG>(ring + 2 * SM::kSlotVecs, p, sq.blk, sq.a0, n2, nstrips, groups);
+    stage_act(ring + 2 * SM::kSlotVecs, p, sq.a0, n2);
+    step(sq, n2, natoms);
+  }
+  cp_async_commit();  // sq: three units ahead of the current one
+  cp_async_wait_prior();
   __syncthreads();
   if (warp < cu.n) atom_sums<MT>(ring, sums, warp, gq, t);
 
@@ -457,15 +479,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
     const Unit nu = has_next ? make_unit(p, nq.blk, nq.a0, unit_len(nq, natoms, run_end), natoms,
                                          nstrips, warp, lane)
                              : cu;
-    const int slot1 = slot == kSlots - 1 ? 0 : slot + 1;
-    const int slot2 = slot1 == kSlots - 1 ? 0 : slot1 + 1;
-    cp_async_wait_all();
+    const int slot1 = (slot + 1) & (kSlots - 1);
+    const int slot3 = (slot + 3) & (kSlots - 1);
+    // the next unit's copies (committed two units ago) landed; the copies
+    // committed one unit ago may still be in flight
+    cp_async_wait_prior();
     __syncthreads();  // the next unit's slot and this unit's sums are visible; slot i-1 is free
     if (sq.g < run_end) {
-      const int n2 = unit_len(sq, natoms, run_end);
-      stage_meta<MT, NG, APG>(ring + slot2 * SM::kSlotVecs, p, sq.blk, sq.a0, n2, nstrips, groups);
-      stage_act(ring + slot2 * SM::kSlotVecs, p, sq.a0, n2);
-      step(sq, n2, natoms);
+      const int n3 = unit_len(sq, natoms, run_end);
+      stage_meta<MT, NG, APG>(ring + slot3 * SM::kSlotVecs, p, sq.blk, sq.a0, n3, nstrips, groups);
+      stage_act(ring + slot3 * SM::kSlotVecs, p, sq.a0, n3);
+      step(sq, n3, natoms);
     }
     cp_async_commit();
     if (has_next && warp < nu.n)
