@@ -318,10 +318,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint64_t bdesc0 = sw128_kmajor_desc(base);
       const uint64_t adesc0 = sw128_kmajor_desc(base + act_bytes);
       for (int kb = 0; kb < nk && ok; ++kb) {
-        // the dequant group arrives only after it saw the stage's TMA bytes land,
-        // so the second wait normally passes at the first test
-        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma) &&
-             mbar_wait(full_tma(s), ph, abort_flag, kErrMma);
+        // The dequant group arrives on full_dq only after its own wait on the
+        // stage's full_tma phase: acquiring full_dq orders these MMAs after the
+        // stage's TMA bytes (activations and codes) as well, so full_tma needs
+        // no wait of its own here.
+        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma);
         if (!ok) break;
         tc_fence_after();
         const uint64_t soff = (uint64_t)((uint32_t)s * (stage_bytes >> 4));
