@@ -24,7 +24,9 @@ import torch
 from .build import LIB as LIB_PATH
 
 PATH_AUTO, PATH_DECODE, PATH_TENSOR = 0, 1, 2
-_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR}
+PATH_DECODE_RESIDENT, PATH_DECODE_STREAMK = 3, 4
+_PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR,
+          "decode-resident": PATH_DECODE_RESIDENT, "decode-streamk": PATH_DECODE_STREAMK}
 STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
 
 ERRORS = {

@@ -77,6 +77,26 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 // Decode GEMV up to 16 rows; tensor-core GEMM above.
 int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
 
+bool is_decode(int path) {
+  return path == W4A16_PATH_DECODE || path == W4A16_PATH_DECODE_RESIDENT ||
+         path == W4A16_PATH_DECODE_STREAMK;
+}
+
+// The decode variant for one launch of `rows` rows: activations resident in
+// shared memory when they fit (with the CTA count `parts` asks for), else
+// stream-K. Returns the variant and its CTA count.
+int decode_variant(int path, int rows, int N, int K, int group, int parts, int* ctas) {
+  if (path != W4A16_PATH_DECODE_STREAMK) {
+    const int c = decode_resident_ctas(rows, N, K, group, parts, sm_count());
+    if (c > 0 || path == W4A16_PATH_DECODE_RESIDENT) {
+      *ctas = c;
+      return W4A16_PATH_DECODE_RESIDENT;
+    }
+  }
+  *ctas = decode_ctas(rows, N, K, group, parts);
+  return W4A16_PATH_DECODE_STREAMK;
+}
+
 // Scratch bytes of a (path, parts) choice: the decode path's counters and
 // partial tiles (16-row chunks share one workspace); none for tensor cores.
 // K split of the tensor-core path (requested, else chosen from the tiles).
@@ -87,10 +107,12 @@ int tc_split(int M, int N, int K, int requested) {
   return s < 1 ? 1 : s;
 }
 
+// The decode path's size covers either variant (the resident one uses none),
+// so that it does not depend on which one a device picks.
 size_t workspace_for(int M, int N, int K, int group, int path, int parts) {
   if (M == 0) return 0;
   if (path == W4A16_PATH_TENSOR) return tc_workspace_bytes(M, N, tc_split(M, N, K, parts));
-  if (path != W4A16_PATH_DECODE) return 0;
+  if (path == W4A16_PATH_DECODE_RESIDENT || !is_decode(path)) return 0;
   const int rows = M < 16 ? M : 16;
   const int c = decode_ctas(rows, N, K, group, parts);
   return c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
@@ -114,7 +136,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   const bool static_weights = (path & W4A16_STATIC_WEIGHTS) != 0;
   path &= ~W4A16_STATIC_WEIGHTS;
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
-  if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
+  if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (path == W4A16_PATH_TENSOR) {
@@ -134,17 +156,34 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (decode_units(N, K, group) <= 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
                 "decode path: group=%d must be K or 64 times a power of two", group);
-  const size_t need = workspace_for(M, N, K, group, path, parts);
-  if (!workspace || workspace_bytes < need)
-    return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
-                need, workspace ? workspace_bytes : (size_t)0);
-  if (!aligned(workspace, 256)) return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
   // 16 rows per launch; larger M re-streams the weights once per 16 rows
+  int ctas = 0;
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
-    cudaError_t e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, rows,
-                                  N, K, group, decode_ctas(rows, N, K, group, parts), workspace,
-                                  static_weights, stream);
+    if (decode_variant(path, rows, N, K, group, parts, &ctas) == W4A16_PATH_DECODE_RESIDENT &&
+        ctas == 0)
+      return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
+                  "resident decode variant: %d rows of K=%d (with the strips of N=%d over %d "
+                  "CTAs) do not fit a CTA's shared memory",
+                  rows, K, N, parts > 0 ? parts : 2 * sm_count());
+  }
+  const size_t need = workspace_for(M, N, K, group, path, parts);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
+                need, workspace ? workspace_bytes : (size_t)0);
+  if (need > 0 && !aligned(workspace, 256))
+    return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+  for (int r0 = 0; r0 < M; r0 += 16) {
+    const int rows = M - r0 < 16 ? M - r0 : 16;
+    const uint16_t* Ar = A + (size_t)r0 * K;
+    uint16_t* Yr = Y + (size_t)r0 * N;
+    cudaError_t e;
+    if (decode_variant(path, rows, N, K, group, parts, &ctas) == W4A16_PATH_DECODE_RESIDENT)
+      e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas,
+                                 static_weights, stream);
+    else
+      e = launch_decode(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, workspace,
+                        static_weights, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   return ok();
@@ -226,7 +265,7 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
-  if (path != W4A16_PATH_DECODE && path != W4A16_PATH_TENSOR)
+  if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   *bytes = workspace_for(M, N, K, group, path, parts);
   return ok();
@@ -252,7 +291,10 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   if (!path || !parts) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   *path = choose_path(M);
   const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
-  *parts = *path == W4A16_PATH_DECODE ? decode_ctas(rows, N, K, group, 0) : tc_split(M, N, K, 0);
+  if (*path == W4A16_PATH_DECODE)
+    *path = decode_variant(W4A16_PATH_DECODE, rows, N, K, group, 0, parts);
+  else
+    *parts = tc_split(M, N, K, 0);
   return ok();
 }
 

@@ -183,6 +183,8 @@ struct DecodeArgs {
   int gshift;         // group of atom a is a >> gshift (30: a single group per column)
   int granule;        // atoms per split granule (runs start at multiples of it)
   int early_weights;  // read the first units' weights before the grid-dependency wait
+  // strip variant: shared-memory layout (bytes)
+  int act_row, sums_off, meta_off, zp_off, red_off;
 };
 
 // Where one unit's data lives for this warp/lane.
@@ -604,6 +606,330 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Strip variant, for problems whose activations (M x K) fit in shared memory.
+// CTA c owns whole strips [c S / C, (c + 1) S / C) of the S strips, over all
+// of K, so no output column is shared between CTAs: no workspace, no flags,
+// no cross-CTA fix-up. The CTA's atoms, strip-major (a contiguous range of
+// Wq), are split among its 8 warps in equal ranges that start at group
+// boundaries; each warp streams its range through registers (one unit of up
+// to 8 atoms ahead) with no CTA barrier. A strip that a warp covers whole goes
+// to Y from registers; a strip shared by warps is summed after the CTA's one
+// final barrier, in warp order, from the warps' partials in shared memory.
+// A (with a zero row for tokens past M), the per-token sums of every atom and
+// the group pairs of the CTA's strips are staged once.
+
+// One atom against resident activations: as atom_mma, with the fragments of
+// token octet 0 at shared address fa and of octet 1 at fb.
+template <int MT, bool kFirst>
+__device__ __forceinline__ void atom_mma_rows(float (&pe)[MT][4], float (&po)[MT][4],
+                                              const uint32_t (&x)[4], const uint32_t (&y)[4],
+                                              const uint32_t (&z)[4], const uint32_t (&v)[4],
+                                              uint32_t fa, uint32_t fb) {
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const uint4 b = lds128(o == 0 ? fa : fb);
+    if (kFirst) {
+      mma_first(pe[o], x[0], y[0], x[1], y[1], b.x, b.y);
+      mma_first(po[o], x[2], y[2], x[3], y[3], b.z, b.w);
+    } else {
+      mma_acc(pe[o], x[0], y[0], x[1], y[1], b.x, b.y);
+      mma_acc(po[o], x[2], y[2], x[3], y[3], b.z, b.w);
+    }
+  }
+#pragma unroll
+  for (int o = 0; o < MT; ++o) {
+    const uint4 b = lds128((o == 0 ? fa : fb) + 64);
+    mma_acc(pe[o], z[0], v[0], z[1], v[1], b.x, b.y);
+    mma_acc(po[o], z[2], v[2], z[3], v[3], b.z, b.w);
+  }
+}
+
+// One unit of n atoms (a group boundary at its start) of the warp's strip,
+// activations resident: fa/fb address the unit's first atom, sps/zps its
+// first group's pairs, sb its first atom's sums. The next unit's nn atoms are
+// loaded from nwp into w as the codes leave it (when refill).
+template <int MT, int APG, bool kFull>
+__device__ __forceinline__ void resident_unit(float (&acc)[MT][4], uint4 (&w)[kBatch], int n, int nn,
+                                           const uint4* nwp, bool refill, uint32_t fa, uint32_t fb,
+                                           const uint32_t* sps, const uint8_t* zps, const float* sb,
+                                           int t) {
+  float pe[MT][4], po[MT][4];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    uint32_t x[4], y[4], z[4], v[4];
+    code_pairs(w[u].x, x);
+    code_pairs(w[u].y, y);
+    code_pairs(w[u].z, z);
+    code_pairs(w[u].w, v);
+    if (refill && (kFull || u < nn)) w[u] = ldg_stream(nwp + u * 32);
+    if (kFull || u < n) {
+      if (u % APG == 0)
+        atom_mma_rows<MT, true>(pe, po, x, y, z, v, fa + u * 128, fb + u * 128);
+      else
+        atom_mma_rows<MT, false>(pe, po, x, y, z, v, fa + u * 128, fb + u * 128);
+      if (APG < kBatch) {
+        if (u % APG == APG - 1)
+          apply_group<MT>(acc, pe, po, sps[(u / APG) * 8], zps[(u / APG) * 8], sb, u + 1 - APG, APG, t);
+      } else if (kFull ? u == kBatch - 1 : u == n - 1) {
+        apply_group<MT>(acc, pe, po, sps[0], zps[0], sb, 0, kFull ? kBatch : n, t);
+      }
+    }
+  }
+}
+
+template <int MT, int APG>
+__global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const DecodeArgs p) {
+  constexpr int kSeg = MT * 8 * kStripCols;  // floats of one partial strip
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* sums = reinterpret_cast<float*>(smem + p.sums_off);
+  const uint32_t* meta_sp = reinterpret_cast<const uint32_t*>(smem + p.meta_off);
+  const uint8_t* meta_zp = smem + p.zp_off;
+  float* red = reinterpret_cast<float*>(smem + p.red_off);  // [warp][2][kSeg]
+
+  allow_dependent_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, t = lane & 3;
+  const int M = p.M, K = p.K, N = p.N;
+  const int natoms = K / kAtomK;
+  const int nstrips = N / kStripCols;
+  const int G = (natoms + (1 << p.gshift) - 1) >> p.gshift;  // groups per strip
+  const int gr = p.granule;
+  // this CTA's strips [s0, s1): global atoms [s0 natoms, s1 natoms), split
+  // into 8 warp ranges of whole granules; warp w starts at wbeg(w)
+  const int C = gridDim.x;
+  const int s0 = (int)((long long)blockIdx.x * nstrips / C);
+  const int s1 = (int)((long long)(blockIdx.x + 1) * nstrips / C);
+  const int Lg = (s1 - s0) * (natoms / gr);
+  auto wbeg = [&](int w) { return s0 * natoms + gr * (int)((long long)w * Lg / kWarps); };
+  const int run_begin = wbeg(warp), run_end = wbeg(warp + 1);
+  const int rec0 = s0 * G;
+
+  int strip = run_begin / natoms, a = run_begin - strip * natoms, g = run_begin;
+  int n = g < run_end ? min(kBatch - (a & (kBatch - 1)), min(natoms - a, run_end - g)) : 0;
+  const uint4* wp = p.Wq + (size_t)g * 32 + lane;
+  uint4 w[kBatch];
+  auto prefetch = [&]() {
+    if (g < run_end) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (u < n) w[u] = ldg_stream(wp + u * 32);
+    }
+    // group pairs of the CTA's strips: records [rec0, rec0 + (s1 - s0) G)
+    const int nrec = (s1 - s0) * G;
+    const uint4* sp_src = reinterpret_cast<const uint4*>(p.Sp2) + (size_t)rec0 * 2;
+    const uint2* zp_src = reinterpret_cast<const uint2*>(p.Zp) + rec0;
+    for (int i = threadIdx.x; i < 3 * nrec; i += kThreads) {
+      if (i < 2 * nrec)
+        cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_src + i);
+      else
+        cp_async8(reinterpret_cast<uint2*>(smem + p.zp_off) + (i - 2 * nrec), zp_src + (i - 2 * nrec));
+    }
+  };
+  if (p.early_weights) prefetch();
+  grid_dependency_wait();
+  if (!p.early_weights) prefetch();
+
+  // activation rows 0..M-1, then the zero row M (token rows past M read it)
+  {
+    uint4* act = reinterpret_cast<uint4*>(smem);
+    const int row_vecs = p.act_row / 16, per_row = K / 8;
+    for (int i = threadIdx.x; i < M * per_row; i += kThreads) {
+      const int row = i / per_row, c = i - row * per_row;
+      cp_async16(act + row * row_vecs + c, p.A + (size_t)row * K + c * 8);
+    }
+    for (int c = threadIdx.x; c < row_vecs; c += kThreads) act[M * row_vecs + c] = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  const uint32_t act_s = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t fa0 = act_s + (uint32_t)((gq < M ? gq : M) * p.act_row + 16 * t);
+  const uint32_t fb0 = act_s + (uint32_t)((8 + gq < M ? 8 + gq : M) * p.act_row + 16 * t);
+  // per-token sums of every atom, sum_k 2^-24 a[k]: row sums of the staged
+  // rows against a ones B operand (fp16 2^-24). One MMA chain sums a block of
+  // 16 atoms of one token; lane (gq, t) loads atoms gq and gq + 8 of the
+  // block as A fragments (the order of k within a row does not matter to a
+  // sum). Atoms past K read the zero row.
+  {
+    constexpr uint32_t kOnes = 0x00010001u;
+    const int nab = (natoms + 15) >> 4;  // atom blocks per token
+    const uint32_t zero_row = act_s + (uint32_t)(M * p.act_row + 16 * t);
+    for (int b = warp; b < M * nab; b += kWarps) {
+      const int tok = b / nab, at = (b - tok * nab) * 16 + gq;
+      const uint32_t row = act_s + (uint32_t)(tok * p.act_row + 16 * t);
+      // lanes of odd gq read the atom's second 64 bytes first: the two rows of
+      // a quarter-warp then fall in opposite halves of the banks
+      const uint32_t first = (gq & 1) * 64, second = 64 - first;
+      const uint32_t lo = at < natoms ? row + at * 128 : zero_row;
+      const uint32_t hi = at + 8 < natoms ? row + (at + 8) * 128 : zero_row;
+      const uint4 l0 = lds128(lo + first), h0 = lds128(hi + first);
+      const uint4 l1 = lds128(lo + second), h1 = lds128(hi + second);
+      float d[4], e[4];
+      mma_first(d, l0.x, h0.x, l0.y, h0.y, kOnes, kOnes);
+      mma_first(e, l0.z, h0.z, l0.w, h0.w, kOnes, kOnes);
+      mma_acc(d, l1.x, h1.x, l1.y, h1.y, kOnes, kOnes);
+      mma_acc(e, l1.z, h1.z, l1.w, h1.w, kOnes, kOnes);
+      if (t == 0) {
+        if (at < natoms) sums[at * MT * 8 + tok] = d[0] + e[0];
+        if (at + 8 < natoms) sums[(at + 8) * MT * 8 + tok] = d[2] + e[2];
+      }
+    }
+  }
+  __syncthreads();
+  // the first unit's codes are not taken apart before this point, so the
+  // staging and sums above overlap its loads
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) asm volatile("" : "+r"(w[u].x), "+r"(w[u].y), "+r"(w[u].z), "+r"(w[u].w));
+
+  // element j of token octet o of this lane: token 8o + 2t + (j & 1), column gq + 8 (j >> 1)
+  auto elem = [&](int o, int j) { return (8 * o + 2 * t + (j & 1)) * kStripCols + gq + 8 * (j >> 1); };
+  auto store_y = [&](const float (&v)[MT][4], int s, float scale) {
+#pragma unroll
+    for (int o = 0; o < MT; ++o)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tok = 8 * o + 2 * t + (j & 1);
+        if (tok < M)
+          p.Y[(size_t)tok * N + s * kStripCols + gq + 8 * (j >> 1)] =
+              __half_as_ushort(__float2half_rn(v[o][j] * scale));
+      }
+  };
+  constexpr float kUnscale = 16777216.0f;  // 2^24: codes entered as q * 2^-24
+  float acc[MT][4];
+#pragma unroll
+  for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
+  const int first_strip = strip;
+  int seg_a0 = a;
+  bool first_seg = true;
+  int heads = 0;  // bit s: the segment in red slot s starts its strip
+  while (g < run_end) {
+    int s2 = strip, a2 = a + n;
+    if (a2 == natoms) {
+      a2 = 0;
+      ++s2;
+    }
+    const int g2 = g + n;
+    const bool has_next = g2 < run_end;
+    const int n2 = has_next ? min(kBatch - (a2 & (kBatch - 1)), min(natoms - a2, run_end - g2)) : 0;
+    const uint4* wp2 = wp + n * 32;
+    const int rec = strip * G + (a >> p.gshift) - rec0;
+    const uint32_t* sps = meta_sp + rec * 8 + gq;
+    const uint8_t* zps = meta_zp + rec * 8 + gq;
+    const float* sb = sums + a * MT * 8;
+    const uint32_t fa = fa0 + a * 128, fb = fb0 + a * 128;
+    if (n == kBatch && n2 == kBatch)
+      resident_unit<MT, APG, true>(acc, w, n, n2, wp2, true, fa, fb, sps, zps, sb, t);
+    else
+      resident_unit<MT, APG, false>(acc, w, n, n2, wp2, has_next, fa, fb, sps, zps, sb, t);
+    if (!has_next || s2 != strip) {
+      // ---- end of a segment: atoms [seg_a0, a + n) of `strip`
+      if (seg_a0 == 0 && a + n == natoms) {
+        store_y(acc, strip, kUnscale);  // the whole strip
+      } else {
+        const int rs = first_seg ? 0 : 1;
+        float* dst = red + (warp * 2 + rs) * kSeg;
+#pragma unroll
+        for (int o = 0; o < MT; ++o)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[elem(o, j)] = acc[o][j] * kUnscale;
+        if (seg_a0 == 0) heads |= 1 << rs;
+      }
+#pragma unroll
+      for (int o = 0; o < MT; ++o) acc[o][0] = acc[o][1] = acc[o][2] = acc[o][3] = 0.f;
+      seg_a0 = a2;
+      first_seg = false;
+    }
+    strip = s2;
+    a = a2;
+    g = g2;
+    n = n2;
+    wp = wp2;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int rs = 0; rs < 2; ++rs) {
+    if (!(heads >> rs & 1)) continue;
+    // this warp's segment in red slot rs starts strip s; the rest of the
+    // strip is the first segment of each following warp that starts inside it
+    const int s = rs == 0 ? first_strip : (run_end - 1) / natoms;
+    const int strip_end = (s + 1) * natoms;
+    float v[MT][4];
+    const float* own = red + (warp * 2 + rs) * kSeg;
+#pragma unroll
+    for (int o = 0; o < MT; ++o)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[o][j] = own[elem(o, j)];
+    for (int w2 = warp + 1; w2 < kWarps && wbeg(w2) < strip_end; ++w2) {
+      if (wbeg(w2) == wbeg(w2 + 1)) continue;  // an empty range
+      const float* part = red + (w2 * 2) * kSeg;
+#pragma unroll
+      for (int o = 0; o < MT; ++o)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[o][j] += part[elem(o, j)];
+    }
+    store_y(v, s, 1.f);
+  }
+}
+
+// Shared memory one CTA may use with two CTAs per SM (228 KiB per SM, 1 KiB
+// of it reserved per CTA).
+constexpr int kTwoCtaSmem = 113 * 1024;
+
+// Layout of the strip variant's shared memory for `ctas` CTAs: A (rows
+// 0..M), the atom sums, the scale and zero-point pairs of a CTA's strips and
+// the warps' partial strips. False if it does not fit two CTAs per SM.
+bool strip_layout(int M, int N, int K, int gshift, int ctas, DecodeArgs* a, int* bytes) {
+  const long mt = M <= 8 ? 1 : 2;
+  const long natoms = K / kAtomK;
+  const long nstrips = N / kStripCols;
+  const long G = (natoms + (1L << gshift) - 1) >> gshift;
+  const long strips_max = (nstrips + ctas - 1) / ctas;
+  const long act_row = 2L * K + 64;
+  const long sums_off = ((M + 1) * act_row + 15) & ~15L;
+  const long meta_off = sums_off + ((natoms * mt * 8 * 4 + 15) & ~15L);
+  const long zp_off = meta_off + strips_max * G * 32;
+  const long red_off = zp_off + ((strips_max * G * 8 + 15) & ~15L);
+  const long total = red_off + kWarps * 2 * mt * 8 * kStripCols * 4;
+  if (total > kTwoCtaSmem) return false;
+  a->act_row = (int)act_row;
+  a->sums_off = (int)sums_off;
+  a->meta_off = (int)meta_off;
+  a->zp_off = (int)zp_off;
+  a->red_off = (int)red_off;
+  *bytes = (int)total;
+  return true;
+}
+
+template <int MT, int APG>
+cudaError_t launch_strip(const DecodeArgs& args, int ctas, int bytes, cudaStream_t stream) {
+  auto kern = decode_resident_kernel<MT, APG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoCtaSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+template <int MT>
+cudaError_t launch_strip_mt(const DecodeArgs& args, int apg_t, int ctas, int bytes,
+                            cudaStream_t stream) {
+  switch (apg_t) {
+    case 1: return launch_strip<MT, 1>(args, ctas, bytes, stream);
+    case 2: return launch_strip<MT, 2>(args, ctas, bytes, stream);
+    case 4: return launch_strip<MT, 4>(args, ctas, bytes, stream);
+    default: return launch_strip<MT, 8>(args, ctas, bytes, stream);
+  }
+}
+
 template <int MT, int APG>
 cudaError_t launch_variant(const DecodeArgs& args, int ctas, cudaStream_t stream) {
   auto kern = decode_kernel<MT, APG>;
@@ -729,6 +1055,40 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
   args.early_weights = early_weights ? 1 : 0;
   if (M <= 8) return launch_mt<1>(args, apg_t, ctas, stream);
   return launch_mt<2>(args, apg_t, ctas, stream);
+}
+
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms) {
+  int apg_t = 0, gshift = 0;
+  if (M < 1 || M > 16 || !group_shape(K, group, &apg_t, &gshift)) return 0;
+  const int nstrips = N / kStripCols;
+  long c = requested > 0 ? requested : 2L * sms;
+  if (c > nstrips) c = nstrips;
+  if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
+  DecodeArgs args;
+  int bytes = 0;
+  return c >= 1 && strip_layout(M, N, K, gshift, (int)c, &args, &bytes) ? (int)c : 0;
+}
+
+cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
+                                   const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
+                                   int ctas, bool early_weights, cudaStream_t stream) {
+  DecodeArgs args = {};
+  int apg_t = 0, bytes = 0;
+  if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
+  if (ctas < 1 || ctas > N / kStripCols || !strip_layout(M, N, K, args.gshift, ctas, &args, &bytes))
+    return cudaErrorInvalidValue;
+  args.A = A;
+  args.Wq = reinterpret_cast<const uint4*>(Wq);
+  args.Sp2 = reinterpret_cast<const uint32_t*>(Sp);
+  args.Zp = reinterpret_cast<const uint8_t*>(Zp);
+  args.Y = Y;
+  args.granule = split_granule(apg_t, args.gshift);
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.early_weights = early_weights ? 1 : 0;
+  if (M <= 8) return launch_strip_mt<1>(args, apg_t, ctas, bytes, stream);
+  return launch_strip_mt<2>(args, apg_t, ctas, bytes, stream);
 }
 
 }  // namespace w4a16

@@ -28,6 +28,17 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int ctas, void* workspace, bool early_weights, cudaStream_t stream);
 size_t decode_workspace_bytes(int M, int N, int ctas);
+
+// Register-dequant GEMV with the activations resident in shared memory, for
+// M <= 16 rows: `ctas` CTAs (1 <= ctas <= N/16) each own whole 16-column
+// strips over all of K; no workspace.
+cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
+                                   const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
+                                   int ctas, bool early_weights, cudaStream_t stream);
+// CTAs of that kernel (`requested`, else two per SM, clamped to the strips
+// and to 8192), or 0 when the problem's activations, sums and group pairs do
+// not fit a CTA's shared memory at that count or the group is unsupported.
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
 // Split granules (128 columns x a group's atoms, at most 8) of a problem: the

@@ -77,8 +77,20 @@ extern "C" {
 
 /* Paths for w4a16_gemm_ex. */
 #define W4A16_PATH_AUTO 0
-#define W4A16_PATH_DECODE 1   /* stream-K register-dequant GEMV         */
+#define W4A16_PATH_DECODE 1   /* register-dequant GEMV, variant below chosen
+                                 per launch: resident when it fits    */
 #define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
+/* The two variants of the decode GEMV, forced. RESIDENT: each CTA owns whole
+ * 16-column strips over all of K and keeps the launch's activation rows in
+ * shared memory; it needs no workspace, and shapes whose rows (16 rows per
+ * launch at most) do not fit give W4A16_ERR_UNSUPPORTED_SHAPE (about M*K <=
+ * 48 Ki elements: K = 4096 up to 8 rows, K = 11008 up to 3). STREAMK: the
+ * weights of 128-column blocks are split across CTAs in equal runs of
+ * groups, the activations are streamed through shared memory with them, and
+ * blocks split between CTAs are combined through the workspace; any shape
+ * the decode path takes. */
+#define W4A16_PATH_DECODE_RESIDENT 3
+#define W4A16_PATH_DECODE_STREAMK 4
 /* Flag OR-ed into the path of w4a16_gemm_ex: the weights (Wq, scales, zeros)
  * are not written by the work queued just before this call on the stream, so
  * the kernel may read them while that work drains. Every kernel of the
@@ -126,8 +138,10 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 
 /* Scratch bytes w4a16_gemm needs for this problem on the current device
  * (0 when none). Work split across CTAs is combined through it: the decode
- * path (M <= 16 rows per launch) shares 128-column blocks between CTAs, and
- * the tensor-core path splits K when its output tiles cannot fill the SMs.
+ * path's stream-K variant (M <= 16 rows per launch) shares 128-column blocks
+ * between CTAs, and the tensor-core path splits K when its output tiles
+ * cannot fill the SMs. For W4A16_PATH_DECODE the size is that of the
+ * stream-K variant whichever variant the device then runs.
  * Layout: a 32 KiB flag/counter area followed by fp32 partial tiles. That
  * area must be zero-filled before the first use; every call leaves it
  * zero-filled again, so one buffer serves any number of calls, of any shape
@@ -153,9 +167,10 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
 
 /* As w4a16_gemm with the path forced (W4A16_PATH_AUTO = automatic) and the
  * work partition forced (`parts`, 0 = automatic): for the decode path the
- * number of persistent CTAs (clamped to 8192 and to the split granules:
- * 128-column blocks x groups of K, a group counted as at most 512 k and
- * K split anywhere on 64-k boundaries when group == K),
+ * number of CTAs. The resident variant clamps it to N/16 strips (and checks
+ * the fit at that count); the stream-K variant clamps it to 8192 and to the
+ * split granules: 128-column blocks x groups of K, a group counted as at most
+ * 512 k and K split anywhere on 64-k boundaries when group == K),
  * for the tensor-core path the number of K ranges per output tile (clamped to
  * K/64). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
@@ -166,12 +181,14 @@ int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,
                   int path, int parts, void* stream);
 
-/* The path and work partition w4a16_gemm would use on the current device
- * (parts: decode CTAs, or tensor-core K ranges). Host-only. */
+/* The path and work partition w4a16_gemm would use on the current device:
+ * for M <= 16 the decode variant (W4A16_PATH_DECODE_RESIDENT or
+ * W4A16_PATH_DECODE_STREAMK) of a 16-row launch and its CTAs, else
+ * W4A16_PATH_TENSOR and its K ranges. Host-only. */
 int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
 
 /* The decode-path GEMM (same kernel, same results as w4a16_gemm_ex with
- * W4A16_PATH_DECODE and the automatic CTA count) for callers that cannot
+ * W4A16_PATH_DECODE_STREAMK and the automatic CTA count) for callers that cannot
  * allocate device memory: code that must not allocate once running (a fixed
  * memory budget), plugins without access to their host's allocator, or loops
  * that cannot afford an allocation. The pages have no counterpart of it.

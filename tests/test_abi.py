@@ -93,6 +93,7 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Y=8) == -3
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
+    assert _gemm(lib, path=5) == -1
     assert _gemm(lib, path=0x200 | 1) == -1           # unknown flag bit
     assert _gemm(lib, parts=-1) == -1
     assert _gemm(lib, path=2, parts=4, ws=0) == -4      # a K-split tensor launch needs a workspace
@@ -100,6 +101,11 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, path=1, ws_bytes=16) == -4
     assert _gemm(lib, path=1, ws=8) == -3             # workspace not 256-byte aligned
     assert _gemm(lib, path=1, K=768, group=192) == -2  # decode: group 64 * 2^j or K
+    assert _gemm(lib, path=4, ws=0) == -4             # stream-K needs a workspace
+    # the resident variant needs none, and rejects rows that do not fit
+    # (16 rows of K = 16384 are 512 KiB of fp16)
+    assert _gemm(lib, path=3, M=16, K=16384, ws=0) == -2
+    assert _gemm(lib, path=3, M=16, K=16384, group=16384, ws=0) == -2
 
 
 def test_static_weights_flag_matches_the_header():
@@ -124,6 +130,12 @@ def test_workspace_sizes(lib):
     assert w4.workspace_size(300, 256, 4096, 128, path="tensor", parts=2) == head + 4 * 2 * 256 * 128 * 4
     assert w4.workspace_size(1, 4096, 4096, 128, path="decode", parts=10) == head + 10 * 8 * 128 * 4
     assert w4.workspace_size(16, 4096, 4096, 128, path="decode", parts=10) == head + 10 * 16 * 128 * 4
+    # the decode path's size is the stream-K variant's, whichever variant
+    # runs; the resident variant needs none
+    for M in (1, 8, 16):
+        assert (w4.workspace_size(M, 4096, 4096, 128, path="decode-streamk", parts=10)
+                == w4.workspace_size(M, 4096, 4096, 128, path="decode", parts=10))
+        assert w4.workspace_size(M, 4096, 4096, 128, path="decode-resident") == 0
     # the CTA count is clamped to the split granules (arguments: M, N, K,
     # group): 32 blocks x 4 groups of 2 atoms
     assert w4.workspace_size(1, 4096, 512, 128, path="decode", parts=1000) == head + 128 * 8 * 128 * 4
@@ -135,3 +147,12 @@ def test_workspace_sizes(lib):
     assert w4.workspace_size(1, 512, 320, 320, path="decode", parts=1000) == head + 20 * 8 * 128 * 4
     # and never above 8192 CTAs
     assert w4.workspace_size(1, 65536, 4096, 64, path="decode", parts=20000) == head + 8192 * 8 * 128 * 4
+
+
+def test_path_constants_match_the_header():
+    text = open(HEADER).read()
+    for name, value in (("W4A16_PATH_AUTO", 0), ("W4A16_PATH_DECODE", 1), ("W4A16_PATH_TENSOR", 2),
+                        ("W4A16_PATH_DECODE_RESIDENT", 3), ("W4A16_PATH_DECODE_STREAMK", 4)):
+        assert re.search(rf"#define {name} {value}\b", text), name
+    assert (w4.PATH_AUTO, w4.PATH_DECODE, w4.PATH_TENSOR, w4.PATH_DECODE_RESIDENT,
+            w4.PATH_DECODE_STREAMK) == (0, 1, 2, 3, 4)

@@ -3,7 +3,10 @@
 Tolerance (per element): |y - y_ref| <= 2^-9 * sum_k |a_k w_kn| + 1e-3, with
 y_ref the fp64 product of the same fp16 activations and the same
 fp16-dequantized weights. Shapes span several CTAs and ragged tails in N (at
-the 16-column granularity of the format), in M and in the K split.
+the 16-column granularity of the format), in M and in the K split. The decode
+path's two variants (activations resident in shared memory, whole strips per
+CTA; stream-K with streamed activations) are each forced on every case the
+variant takes.
 """
 import numpy as np
 import pytest
@@ -15,6 +18,18 @@ import synthetic
 from gpu_util import cuda, guarded_output, check_guard, half_bits, host, prepare, run_and_check
 
 pytestmark = pytest.mark.gpu
+
+VARIANTS = ["decode-resident", "decode-streamk"]
+
+
+def run_variant(M, K, N, group, seed, path, parts=0, **kw):
+    """run_and_check, skipping shapes the resident variant does not take."""
+    try:
+        return run_and_check(M, K, N, group, seed=seed, path=path, parts=parts, **kw)
+    except w4.W4A16Error as e:
+        if path == "decode-resident" and e.code == -2:
+            pytest.skip("activations do not fit the resident variant")
+        raise
 
 DECODE_CASES = [
     # M, K, N, group, persistent CTAs (0: automatic)
@@ -33,9 +48,20 @@ DECODE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("path", VARIANTS)
 @pytest.mark.parametrize("M,K,N,group,parts", DECODE_CASES)
-def test_decode_path(M, K, N, group, parts):
-    run_and_check(M, K, N, group, seed=M * 1000 + N, path="decode", parts=parts)
+def test_decode_path(M, K, N, group, parts, path):
+    run_variant(M, K, N, group, M * 1000 + N, path, parts)
+
+
+@pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (8, 4096, 512, 128),
+                                         (9, 2048, 256, 128), (16, 4096, 256, 128),
+                                         (3, 11008, 256, 128), (4, 11008, 256, 128)])
+def test_decode_path_picks_a_variant(M, K, N, group):
+    """The automatic choice runs whichever variant plan() reports."""
+    variant, _ = w4.plan(M, N, K, group)
+    assert variant in VARIANTS
+    run_and_check(M, K, N, group, seed=M + K, path="decode")
 
 
 @pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (16, 4096, 256, 128),
@@ -50,30 +76,41 @@ def test_outlier_activation_columns():
 
 @pytest.mark.parametrize("parts", [1, 2, 3, 7, 11, 12, 13, 25, 47, 48, 1000])
 def test_every_cta_count_meets_the_tolerance(parts):
-    """One CTA (every block whole), blocks shared unevenly between CTAs whose
-    runs start inside them, one group per CTA, clamping to the 3 x 16 = 48
-    split granules (groups of 2 atoms)."""
-    run_and_check(8, 2048, 272, 128, seed=11, path="decode", parts=parts)
+    """Stream-K: one CTA (every block whole), blocks shared unevenly between
+    CTAs whose runs start inside them, one group per CTA, clamping to the
+    3 x 16 = 48 split granules (groups of 2 atoms)."""
+    run_and_check(8, 2048, 272, 128, seed=11, path="decode-streamk", parts=parts)
 
 
+@pytest.mark.parametrize("M", [1, 8, 9])
+@pytest.mark.parametrize("parts", [1, 2, 3, 5, 8, 16, 17, 1000])
+def test_every_resident_cta_count_meets_the_tolerance(parts, M):
+    """Resident variant: all 17 strips in one CTA (warps sharing strips), 2..3
+    strips per CTA (strips split between warps at group boundaries), one
+    strip per CTA (every warp a part of one strip), clamping to the strips."""
+    run_variant(M, 2048, 272, 128, 11 + M, "decode-resident", parts)
+
+
+@pytest.mark.parametrize("path", VARIANTS)
 @pytest.mark.parametrize("M,K,N,group,parts", [(3, 512, 64, 64, 1), (5, 1024, 144, 256, 3),
                                               (9, 2048, 128, 512, 2), (2, 1536, 32, 1536, 2),
                                               (16, 4096, 160, 1024, 3), (1, 320, 48, 320, 1),
-                                              (4, 1600, 400, 1600, 5), (7, 704, 96, 64, 0)])
-def test_group_sizes(M, K, N, group, parts):
+                                              (4, 1600, 400, 1600, 5), (7, 704, 96, 64, 0),
+                                              (12, 2048, 96, 2048, 2)])
+def test_group_sizes(M, K, N, group, parts, path):
     """Groups of 1, 4, 8 and 16 atoms and per-channel groups of any length
     (short last batches of 1..7 atoms at 320, 704, 1600)."""
-    run_and_check(M, K, N, group, seed=M + K + group, path="decode", parts=parts)
+    run_variant(M, K, N, group, M + K + group, path, parts)
 
 
 def test_workspace_is_left_zeroed_and_reusable():
     K, N, group = 1024, 400, 128
     W = synthetic.small_weights(K, N, seed=4)
     (q, s, z), pw = prepare(W, group)
-    ws = w4.new_workspace(w4.workspace_size(16, N, K, group, path="decode", parts=9))
+    ws = w4.new_workspace(w4.workspace_size(16, N, K, group, path="decode-streamk", parts=9))
     for M in (1, 5, 16, 3):
         A = synthetic.small_activations(M, K, seed=M)
-        Y = w4.gemm(cuda(A), pw, path="decode", parts=9, workspace=ws)
+        Y = w4.gemm(cuda(A), pw, path="decode-streamk", parts=9, workspace=ws)
         w4.device_status()
         y, mag = oracle.reference(A, q, s, z, group)
         assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
@@ -108,9 +145,10 @@ def test_integer_product_is_exact():
     exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
     assert np.abs(exact).max() < 2048
     pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
-    for parts in (1, 4, 0):
-        Y = w4.gemm(cuda(A), pw, path="decode", parts=parts)
-        assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
+    for path in VARIANTS:
+        for parts in (1, 4, 0):
+            Y = w4.gemm(cuda(A), pw, path=path, parts=parts)
+            assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact), (path, parts)
 
 
 def test_zero_rows_is_a_noop():
@@ -135,7 +173,8 @@ def test_stream_ordering_on_a_side_stream():
     assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
 
 
-def test_static_weights_keeps_the_order_of_a_layer_chain():
+@pytest.mark.parametrize("path", VARIANTS)
+def test_static_weights_keeps_the_order_of_a_layer_chain(path):
     """With W4A16_STATIC_WEIGHTS the kernel reads its weights while the previous
     kernel drains, but its activations only after that kernel is done: a chain
     of layers fed by each other (and by a plain torch kernel in between) gives
@@ -153,7 +192,7 @@ def test_static_weights_keeps_the_order_of_a_layer_chain():
         x = A
         outs = []
         for i, pw in enumerate(pws):
-            x = w4.gemm(x, pw, path="decode", static_weights=static)
+            x = w4.gemm(x, pw, path=path, static_weights=static)
             outs.append(x)
             if i == 0:
                 x = x * 0.5      # a kernel of another library between two layers

@@ -47,7 +47,7 @@ def test_noalloc_matches_regular_entry_point_on_two_calls(M, K, N, group):
         Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
         rc = _noalloc(lib, Ad, pw, Y)
         assert rc == 0, lib.w4a16_last_error().decode()
-        ref = w4.gemm(Ad, pw, path="decode")
+        ref = w4.gemm(Ad, pw, path="decode-streamk")
         w4.device_status()
         diff = np.abs(oracle.from_half(half_bits(Y)) - oracle.from_half(half_bits(ref)))
         assert np.all(diff <= bound), f"call {call}: max diff/bound {np.max(diff / bound)}"
