@@ -87,7 +87,8 @@ bool is_decode(int path) {
 // stream-K. Returns the variant and its CTA count.
 int decode_variant(int path, int rows, int N, int K, int group, int parts, int* ctas) {
   if (path != W4A16_PATH_DECODE_STREAMK) {
-    const int c = decode_resident_ctas(rows, N, K, group, parts, sm_count());
+    const int c = decode_resident_ctas(rows, N, K, group, parts, sm_count(),
+                                       path == W4A16_PATH_DECODE);
     if (c > 0 || path == W4A16_PATH_DECODE_RESIDENT) {
       *ctas = c;
       return W4A16_PATH_DECODE_RESIDENT;
@@ -179,8 +180,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     uint16_t* Yr = Y + (size_t)r0 * N;
     cudaError_t e;
     if (decode_variant(path, rows, N, K, group, parts, &ctas) == W4A16_PATH_DECODE_RESIDENT)
-      e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas,
-                                 static_weights, stream);
+      e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, sm_count(),
+                                 path == W4A16_PATH_DECODE, static_weights, stream);
     else
       e = launch_decode(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, workspace,
                         static_weights, stream);

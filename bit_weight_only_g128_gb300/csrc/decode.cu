@@ -678,8 +678,8 @@ __device__ __forceinline__ void resident_unit(float (&acc)[MT][4], uint4 (&w)[kB
   }
 }
 
-template <int MT, int APG>
-__global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const DecodeArgs p) {
+template <int MT, int APG, int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const DecodeArgs p) {
   constexpr int kSeg = MT * 8 * kStripCols;  // floats of one partial strip
   extern __shared__ __align__(16) uint8_t smem[];
   float* sums = reinterpret_cast<float*>(smem + p.sums_off);
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
   const int s0 = (int)((long long)blockIdx.x * nstrips / C);
   const int s1 = (int)((long long)(blockIdx.x + 1) * nstrips / C);
   const int Lg = (s1 - s0) * (natoms / gr);
-  auto wbeg = [&](int w) { return s0 * natoms + gr * (int)((long long)w * Lg / kWarps); };
+  auto wbeg = [&](int w) { return s0 * natoms + gr * (int)((long long)w * Lg / NW); };
   const int run_begin = wbeg(warp), run_end = wbeg(warp + 1);
   const int rec0 = s0 * G;
 
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
     const int nrec = (s1 - s0) * G;
     const uint4* sp_src = reinterpret_cast<const uint4*>(p.Sp2) + (size_t)rec0 * 2;
     const uint2* zp_src = reinterpret_cast<const uint2*>(p.Zp) + rec0;
-    for (int i = threadIdx.x; i < 3 * nrec; i += kThreads) {
+    for (int i = threadIdx.x; i < 3 * nrec; i += (NW * 32)) {
       if (i < 2 * nrec)
         cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_src + i);
       else
@@ -734,11 +734,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
   {
     uint4* act = reinterpret_cast<uint4*>(smem);
     const int row_vecs = p.act_row / 16, per_row = K / 8;
-    for (int i = threadIdx.x; i < M * per_row; i += kThreads) {
+    for (int i = threadIdx.x; i < M * per_row; i += (NW * 32)) {
       const int row = i / per_row, c = i - row * per_row;
       cp_async16(act + row * row_vecs + c, p.A + (size_t)row * K + c * 8);
     }
-    for (int c = threadIdx.x; c < row_vecs; c += kThreads) act[M * row_vecs + c] = make_uint4(0, 0, 0, 0);
+    for (int c = threadIdx.x; c < row_vecs; c += (NW * 32)) act[M * row_vecs + c] = make_uint4(0, 0, 0, 0);
   }
   cp_async_commit();
   cp_async_wait_all();
@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
     constexpr uint32_t kOnes = 0x00010001u;
     const int nab = (natoms + 15) >> 4;  // atom blocks per token
     const uint32_t zero_row = act_s + (uint32_t)(M * p.act_row + 16 * t);
-    for (int b = warp; b < M * nab; b += kWarps) {
+    for (int b = warp; b < M * nab; b += NW) {
       const int tok = b / nab, at = (b - tok * nab) * 16 + gq;
       const uint32_t row = act_s + (uint32_t)(tok * p.act_row + 16 * t);
       // lanes of odd gq read the atom's second 64 bytes first: the two rows of
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
     for (int o = 0; o < MT; ++o)
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[o][j] = own[elem(o, j)];
-    for (int w2 = warp + 1; w2 < kWarps && wbeg(w2) < strip_end; ++w2) {
+    for (int w2 = warp + 1; w2 < NW && wbeg(w2) < strip_end; ++w2) {
       if (wbeg(w2) == wbeg(w2 + 1)) continue;  // an empty range
       const float* part = red + (w2 * 2) * kSeg;
 #pragma unroll
@@ -873,13 +873,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_resident_kernel(const Deco
 }
 
 // Shared memory one CTA may use with two CTAs per SM (228 KiB per SM, 1 KiB
-// of it reserved per CTA).
+// of it reserved per CTA), and the most one CTA may use.
 constexpr int kTwoCtaSmem = 113 * 1024;
+constexpr int kOneCtaSmem = 227 * 1024;
 
-// Layout of the strip variant's shared memory for `ctas` CTAs: A (rows
-// 0..M), the atom sums, the scale and zero-point pairs of a CTA's strips and
-// the warps' partial strips. False if it does not fit two CTAs per SM.
-bool strip_layout(int M, int N, int K, int gshift, int ctas, DecodeArgs* a, int* bytes) {
+// Layout of the strip variant's shared memory for `ctas` CTAs of `nw` warps:
+// A (rows 0..M), the atom sums, the scale and zero-point pairs of a CTA's
+// strips and the warps' partial strips. False if it exceeds `limit` bytes.
+bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, DecodeArgs* a,
+                  int* bytes) {
   const long mt = M <= 8 ? 1 : 2;
   const long natoms = K / kAtomK;
   const long nstrips = N / kStripCols;
@@ -890,8 +892,8 @@ bool strip_layout(int M, int N, int K, int gshift, int ctas, DecodeArgs* a, int*
   const long meta_off = sums_off + ((natoms * mt * 8 * 4 + 15) & ~15L);
   const long zp_off = meta_off + strips_max * G * 32;
   const long red_off = zp_off + ((strips_max * G * 8 + 15) & ~15L);
-  const long total = red_off + kWarps * 2 * mt * 8 * kStripCols * 4;
-  if (total > kTwoCtaSmem) return false;
+  const long total = red_off + (long)nw * 2 * mt * 8 * kStripCols * 4;
+  if (total > limit) return false;
   a->act_row = (int)act_row;
   a->sums_off = (int)sums_off;
   a->meta_off = (int)meta_off;
@@ -901,14 +903,15 @@ bool strip_layout(int M, int N, int K, int gshift, int ctas, DecodeArgs* a, int*
   return true;
 }
 
-template <int MT, int APG>
+template <int MT, int APG, int NW>
 cudaError_t launch_strip(const DecodeArgs& args, int ctas, int bytes, cudaStream_t stream) {
-  auto kern = decode_resident_kernel<MT, APG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTwoCtaSmem);
+  auto kern = decode_resident_kernel<MT, APG, NW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       NW == 8 ? kTwoCtaSmem : kOneCtaSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = (size_t)bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -919,14 +922,14 @@ cudaError_t launch_strip(const DecodeArgs& args, int ctas, int bytes, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
-template <int MT>
+template <int MT, int NW>
 cudaError_t launch_strip_mt(const DecodeArgs& args, int apg_t, int ctas, int bytes,
                             cudaStream_t stream) {
   switch (apg_t) {
-    case 1: return launch_strip<MT, 1>(args, ctas, bytes, stream);
-    case 2: return launch_strip<MT, 2>(args, ctas, bytes, stream);
-    case 4: return launch_strip<MT, 4>(args, ctas, bytes, stream);
-    default: return launch_strip<MT, 8>(args, ctas, bytes, stream);
+    case 1: return launch_strip<MT, 1, NW>(args, ctas, bytes, stream);
+    case 2: return launch_strip<MT, 2, NW>(args, ctas, bytes, stream);
+    case 4: return launch_strip<MT, 4, NW>(args, ctas, bytes, stream);
+    default: return launch_strip<MT, 8, NW>(args, ctas, bytes, stream);
   }
 }
 
@@ -1057,25 +1060,53 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
   return launch_mt<2>(args, apg_t, ctas, stream);
 }
 
-int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms) {
-  int apg_t = 0, gshift = 0;
-  if (M < 1 || M > 16 || !group_shape(K, group, &apg_t, &gshift)) return 0;
+namespace {
+
+// The resident variant's shape for a launch: 8 warps and two CTAs per SM
+// (113 KiB each) or 16 warps and one CTA per SM (227 KiB; the same warps per
+// SM, the activations staged once per SM). Measured on the Llama shapes, 16
+// warps are faster from 4 rows up and 8 warps below, so that order is tried
+// first. `requested` CTAs, else one per resident slot, clamped to the strips
+// and to 8192. With `automatic`, staged activations above 160 KiB count as
+// not fitting: there the stream-K variant was faster (8 rows of K = 11008).
+// Returns the CTA count (0: no fit) and sets the warps per CTA.
+int resident_shape(int M, int N, int K, int gshift, int requested, int sms, bool automatic,
+                   int* nw, DecodeArgs* args, int* bytes) {
   const int nstrips = N / kStripCols;
-  long c = requested > 0 ? requested : 2L * sms;
-  if (c > nstrips) c = nstrips;
-  if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
+  const long act_bytes = (M + 1L) * (2L * K + 64);
+  if (automatic && act_bytes > 160L * 1024) return 0;
+  for (int i = 0; i < 2; ++i) {
+    const int w = (M >= 4) == (i == 0) ? 16 : 8;
+    long c = requested > 0 ? requested : (w == 8 ? 2L : 1L) * sms;
+    if (c > nstrips) c = nstrips;
+    if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
+    if (c >= 1 && strip_layout(M, N, K, gshift, (int)c, w, w == 8 ? kTwoCtaSmem : kOneCtaSmem, args,
+                               bytes)) {
+      *nw = w;
+      return (int)c;
+    }
+  }
+  return 0;
+}
+
+}  // namespace
+
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic) {
+  int apg_t = 0, gshift = 0, nw = 0, bytes = 0;
+  if (M < 1 || M > 16 || !group_shape(K, group, &apg_t, &gshift)) return 0;
   DecodeArgs args;
-  int bytes = 0;
-  return c >= 1 && strip_layout(M, N, K, gshift, (int)c, &args, &bytes) ? (int)c : 0;
+  return resident_shape(M, N, K, gshift, requested, sms, automatic, &nw, &args, &bytes);
 }
 
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                                   int ctas, bool early_weights, cudaStream_t stream) {
+                                   int ctas, int sms, bool automatic, bool early_weights,
+                                   cudaStream_t stream) {
   DecodeArgs args = {};
-  int apg_t = 0, bytes = 0;
+  int apg_t = 0, bytes = 0, nw = 0;
   if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
-  if (ctas < 1 || ctas > N / kStripCols || !strip_layout(M, N, K, args.gshift, ctas, &args, &bytes))
+  if (ctas < 1 ||
+      resident_shape(M, N, K, args.gshift, ctas, sms, automatic, &nw, &args, &bytes) != ctas)
     return cudaErrorInvalidValue;
   args.A = A;
   args.Wq = reinterpret_cast<const uint4*>(Wq);
@@ -1087,8 +1118,11 @@ cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const 
   args.N = N;
   args.K = K;
   args.early_weights = early_weights ? 1 : 0;
-  if (M <= 8) return launch_strip_mt<1>(args, apg_t, ctas, bytes, stream);
-  return launch_strip_mt<2>(args, apg_t, ctas, bytes, stream);
+  if (nw == 8)
+    return M <= 8 ? launch_strip_mt<1, 8>(args, apg_t, ctas, bytes, stream)
+                  : launch_strip_mt<2, 8>(args, apg_t, ctas, bytes, stream);
+  return M <= 8 ? launch_strip_mt<1, 16>(args, apg_t, ctas, bytes, stream)
+                : launch_strip_mt<2, 16>(args, apg_t, ctas, bytes, stream);
 }
 
 }  // namespace w4a16

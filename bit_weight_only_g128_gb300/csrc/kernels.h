@@ -30,15 +30,19 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
 size_t decode_workspace_bytes(int M, int N, int ctas);
 
 // Register-dequant GEMV with the activations resident in shared memory, for
-// M <= 16 rows: `ctas` CTAs (1 <= ctas <= N/16) each own whole 16-column
-// strips over all of K; no workspace.
+// M <= 16 rows: `ctas` CTAs (as decode_resident_ctas returned for the same
+// `sms` and `automatic`) each own whole 16-column strips over all of K; no
+// workspace.
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                                   int ctas, bool early_weights, cudaStream_t stream);
-// CTAs of that kernel (`requested`, else two per SM, clamped to the strips
-// and to 8192), or 0 when the problem's activations, sums and group pairs do
-// not fit a CTA's shared memory at that count or the group is unsupported.
-int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms);
+                                   int ctas, int sms, bool automatic, bool early_weights,
+                                   cudaStream_t stream);
+// CTAs of that kernel (`requested`, else one per resident slot of `sms` SMs:
+// two 8-warp CTAs or one 16-warp CTA per SM; clamped to the strips and to
+// 8192), or 0 when the problem's activations, sums and group pairs do not fit
+// a CTA's shared memory at that count (with `automatic`, also when the
+// staged activations exceed 160 KiB) or the group is unsupported.
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
 // Split granules (128 columns x a group's atoms, at most 8) of a problem: the

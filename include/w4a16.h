@@ -82,9 +82,11 @@ extern "C" {
 #define W4A16_PATH_TENSOR 2   /* tcgen05/TMEM tensor-core GEMM          */
 /* The two variants of the decode GEMV, forced. RESIDENT: each CTA owns whole
  * 16-column strips over all of K and keeps the launch's activation rows in
- * shared memory; it needs no workspace, and shapes whose rows (16 rows per
- * launch at most) do not fit give W4A16_ERR_UNSUPPORTED_SHAPE (about M*K <=
- * 48 Ki elements: K = 4096 up to 8 rows, K = 11008 up to 3). STREAMK: the
+ * shared memory (two 8-warp CTAs per SM, or one 16-warp CTA for larger rows);
+ * it needs no workspace, and shapes whose rows (16 rows per launch at most)
+ * do not fit give W4A16_ERR_UNSUPPORTED_SHAPE (about (M+1)*K <= 110 Ki
+ * elements: K = 4096 up to 16 rows, K = 11008 up to 8). W4A16_PATH_DECODE
+ * takes it only up to 160 KiB of staged rows. STREAMK: the
  * weights of 128-column blocks are split across CTAs in equal runs of
  * groups, the activations are streamed through shared memory with them, and
  * blocks split between CTAs are combined through the workspace; any shape

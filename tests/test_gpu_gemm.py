@@ -45,6 +45,8 @@ DECODE_CASES = [
     (7, 1280, 400, 128, 5),
     (12, 2048, 1040, 2048, 2),
     (4, 11008, 256, 128, 0),
+    (8, 11008, 128, 128, 0),   # resident: 16 warps, about 224 KiB of shared memory
+    (16, 4096, 1040, 128, 0),  # resident: 16 warps, two token octets
 ]
 
 
@@ -56,7 +58,8 @@ def test_decode_path(M, K, N, group, parts, path):
 
 @pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (8, 4096, 512, 128),
                                          (9, 2048, 256, 128), (16, 4096, 256, 128),
-                                         (3, 11008, 256, 128), (4, 11008, 256, 128)])
+                                         (3, 11008, 256, 128), (4, 11008, 256, 128),
+                                         (8, 11008, 256, 128), (16, 11008, 256, 128)])
 def test_decode_path_picks_a_variant(M, K, N, group):
     """The automatic choice runs whichever variant plan() reports."""
     variant, _ = w4.plan(M, N, K, group)
