@@ -69,7 +69,8 @@ def peaks():
 # ncu summaries under profiles/: the dominant kernel of a workload, the sources
 # that build it, and the summary holding its DRAM bytes per launch
 PROFILED = {
-    1: ("decode_kernel", ["decode.cu", "common.cuh"], "decode_kernel_llama2-7b-decode.md"),
+    1: ("decode_resident_kernel", ["decode.cu", "common.cuh"],
+        "decode_resident_kernel_llama2-7b-decode.md"),
     3: ("tc_gemm_kernel", ["tc_gemm.cu", "common.cuh"], "tc_gemm_kernel_llama2-7b-prefill.md"),
 }
 
