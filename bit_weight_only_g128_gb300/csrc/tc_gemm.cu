@@ -267,7 +267,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_tma(s), 1);
-      mbar_init(full_dq(s), 32 * (kDqWarps / p.dq_groups));  // the stage's dequant group
+      mbar_init(full_dq(s), kDqWarps / p.dq_groups);  // one arrival per warp of the group
       mbar_init(empty(s), 1);
     }
     mbar_init(accum_bar, 1);
@@ -407,8 +407,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       }
-      fence_async_shared();  // generic-proxy stores -> visible to the tensor core
-      mbar_arrive(full_dq(s));
+      fence_async_shared();  // this thread's generic-proxy stores -> visible to the tensor core
+      __syncwarp();          // every lane of the warp has fenced its stores
+      if (lane == 0) mbar_arrive(full_dq(s));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         ms[i] = nms[i];
@@ -459,13 +460,44 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       epilogue_bar();
       if (*last_flag) {
-        const float* tb = p.tiles + (size_t)tile * p.split * bt * kTileN;
-        for (int e = dw * 32 + lane; e < bt * kTileN; e += kDqThreads) {
-          const int tok = m0 + e / kTileN, n = n0 + e % kTileN;
-          if (tok >= p.M || n >= p.N) continue;
-          float sum = 0.f;
-          for (int z = 0; z < p.split; ++z) sum += __ldcg(tb + (size_t)z * bt * kTileN + e);
-          p.Y[(size_t)tok * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+        // 4 columns per float4, 8 float4 per thread and round: the loads of
+        // one partial tile for the round are all in flight together, and the
+        // partial tiles are added in split order
+        const float4* tb = reinterpret_cast<const float4*>(p.tiles + (size_t)tile * p.split * bt * kTileN);
+        const int n4 = bt * kTileN / 4;
+        constexpr int kRound = 8;
+        for (int e0 = dw * 32 + lane; e0 < n4; e0 += kRound * kDqThreads) {
+          float4 acc[kRound];
+#pragma unroll
+          for (int u = 0; u < kRound; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int z = 0; z < p.split; ++z) {
+            float4 v[kRound];
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+              const int e = e0 + u * kDqThreads;
+              v[u] = e < n4 ? __ldcg(tb + (size_t)z * (n4) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+              acc[u].x += v[u].x;
+              acc[u].y += v[u].y;
+              acc[u].z += v[u].z;
+              acc[u].w += v[u].w;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kRound; ++u) {
+            const int e = e0 + u * kDqThreads;
+            const int tok = m0 + e / (kTileN / 4), n = n0 + (e % (kTileN / 4)) * 4;
+            if (e < n4 && tok < p.M && n < p.N) {
+              const __half2 lo = __floats2half2_rn(acc[u].x, acc[u].y);
+              const __half2 hi = __floats2half2_rn(acc[u].z, acc[u].w);
+              uint2 o;
+              o.x = *reinterpret_cast<const uint32_t*>(&lo);
+              o.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(p.Y + (size_t)tok * p.N + n) = o;
+            }
+          }
         }
         if (dw == 0 && lane == 0) p.counters[tile] = 0;
       }
