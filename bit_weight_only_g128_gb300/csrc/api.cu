@@ -101,9 +101,9 @@ int decode_variant(int path, int rows, int N, int K, int group, int parts, int* 
 // Scratch bytes of a (path, parts) choice: the decode path's counters and
 // partial tiles (16-row chunks share one workspace); none for tensor cores.
 // K split of the tensor-core path (requested, else chosen from the tiles).
-int tc_split(int M, int N, int K, int requested) {
-  const int nk = K / kAtomK;
-  int s = requested > 0 ? requested : tc_choose_split(M, N, K, sm_count());
+int tc_split(int M, int N, int K, int group, int requested) {
+  const int nk = K / (kAtomK * tc_stage_atoms(M, K, group));  // pipeline stages
+  int s = requested > 0 ? requested : tc_choose_split(M, N, K, group, sm_count());
   if (s > nk) s = nk;
   return s < 1 ? 1 : s;
 }
@@ -112,7 +112,7 @@ int tc_split(int M, int N, int K, int requested) {
 // so that it does not depend on which one a device picks.
 size_t workspace_for(int M, int N, int K, int group, int path, int parts) {
   if (M == 0) return 0;
-  if (path == W4A16_PATH_TENSOR) return tc_workspace_bytes(M, N, tc_split(M, N, K, parts));
+  if (path == W4A16_PATH_TENSOR) return tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
   if (path == W4A16_PATH_DECODE_RESIDENT || !is_decode(path)) return 0;
   const int rows = M < 16 ? M : 16;
   const int c = decode_ctas(rows, N, K, group, parts);
@@ -141,7 +141,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (path == W4A16_PATH_TENSOR) {
-    const int split = tc_split(M, N, K, parts);
+    const int split = tc_split(M, N, K, group, parts);
     const size_t need = tc_workspace_bytes(M, N, split);
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
@@ -295,7 +295,7 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   if (*path == W4A16_PATH_DECODE)
     *path = decode_variant(W4A16_PATH_DECODE, rows, N, K, group, 0, parts);
   else
-    *parts = tc_split(M, N, K, 0);
+    *parts = tc_split(M, N, K, group, 0);
   return ok();
 }
 

@@ -58,10 +58,13 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                            int split, void* workspace, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
-int tc_choose_split(int M, int N, int K, int sms);
+int tc_choose_split(int M, int N, int K, int group, int sms);
+// 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K
+// and the group are multiples of 128 and 4 such stages fit, else 1).
+int tc_stage_atoms(int M, int K, int group);
 // Token tile (MMA N) used for M rows, and the dynamic shared memory it needs.
 int tc_token_tile(int M);
-size_t tc_smem_bytes(int bt, int* stages);
+size_t tc_smem_bytes(int bt, int stage_atoms, int* stages);
 
 // Reads the device error word (bounded waits that gave up, self-checks) and
 // clears it if set.

@@ -38,7 +38,7 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int kTileN = 128;        // output columns per CTA (MMA M)
-constexpr int kStageK = 64;        // k per pipeline stage (one 128-byte swizzle row)
+constexpr int kStageK = 64;        // k per atom of a pipeline stage (one 128-byte swizzle row)
 constexpr int kDqWarps = 8;
 constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kThreads = 64 + kDqThreads;
@@ -236,6 +236,10 @@ struct TcParams {
 // named barrier of the 8 dequant/epilogue warps
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// SA: atoms (64 k) per pipeline stage, 1 or 2. A stage of two atoms halves
+// the barrier hand-offs per weight byte; it needs an even number of atoms
+// and groups of at least 128 (one scale and zero point per stage).
+template <int SA>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const TcParams p) {
@@ -243,9 +247,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const int bt = p.bt, stages = p.stages;
-  const uint32_t act_bytes = (uint32_t)bt * 128u;
-  const uint32_t stage_bytes = act_bytes + kWdqBytes + kPackedBytes;
-  // stage s: [activations | dequantized weights | packed codes], 1024-aligned
+  const uint32_t act_bytes = (uint32_t)bt * 128u;  // one atom of activations
+  const uint32_t stage_bytes = SA * (act_bytes + kWdqBytes + kPackedBytes);
+  // stage s: [activations of atom 0..SA-1 | dequantized weights of atom
+  // 0..SA-1 | packed codes of the SA atoms], each piece 1024-aligned
+  const uint32_t wdq_off = SA * act_bytes, packed_off = SA * (act_bytes + kWdqBytes);
   const uint32_t bars = base + (uint32_t)stages * stage_bytes;
   auto full_tma = [&](int s) { return bars + 8u * s; };
   auto full_dq = [&](int s) { return bars + 8u * (stages + s); };
@@ -260,7 +266,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int n0 = blockIdx.x * kTileN;
   const int m0 = blockIdx.y * bt;
   // this CTA's K range: stages [kb0, kb0 + nk)
-  const int nk_all = p.K / kStageK;
+  const int nk_all = p.K / (kStageK * SA);
   const int kb0 = (int)((long long)blockIdx.z * nk_all / p.split);
   const int nk = (int)((long long)(blockIdx.z + 1) * nk_all / p.split) - kb0;
 
@@ -292,9 +298,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
         const uint32_t st = base + (uint32_t)s * stage_bytes;
-        mbar_expect_tx(full_tma(s), act_bytes + kPackedBytes);
-        tma_load_2d(st, &tmA, (kb0 + kb) * kStageK, m0, full_tma(s));
-        tma_load_2d(st + act_bytes + kWdqBytes, &tmW, (kb0 + kb) * 128, n0 / kStripCols, full_tma(s));
+        mbar_expect_tx(full_tma(s), SA * (act_bytes + kPackedBytes));
+#pragma unroll
+        for (int u = 0; u < SA; ++u)
+          tma_load_2d(st + u * act_bytes, &tmA, ((kb0 + kb) * SA + u) * kStageK, m0, full_tma(s));
+        tma_load_2d(st + packed_off, &tmW, (kb0 + kb) * SA * kAtomWords, n0 / kStripCols,
+                    full_tma(s));
         ++issued;
         if (++s == stages) {
           s = 0;
@@ -314,9 +323,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool ok = true;
       int s = 0;
       uint32_t ph = 0;
-      // descriptors of stage 0; stage s adds s * stage_bytes >> 4
+      // descriptors of stage 0, atom 0; stage s adds s * stage_bytes >> 4,
+      // atom u adds u * act_bytes >> 4 (activations) or u * kWdqBytes >> 4
       const uint64_t bdesc0 = sw128_kmajor_desc(base);
-      const uint64_t adesc0 = sw128_kmajor_desc(base + act_bytes);
+      const uint64_t adesc0 = sw128_kmajor_desc(base + wdq_off);
       for (int kb = 0; kb < nk && ok; ++kb) {
         // The dequant group arrives on full_dq only after its own wait on the
         // stage's full_tma phase: acquiring full_dq orders these MMAs after the
@@ -327,9 +337,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         const uint64_t soff = (uint64_t)((uint32_t)s * (stage_bytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes of k per MMA
-          tc_mma_f16(tmem_base, adesc0 + soff + 2u * kk, bdesc0 + soff + 2u * kk, idesc,
-                     (kb | kk) != 0);
+        for (int u = 0; u < SA; ++u)
+#pragma unroll
+          for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes of k per MMA
+            tc_mma_f16(tmem_base, adesc0 + soff + (uint64_t)(u * (kWdqBytes >> 4)) + 2u * kk,
+                       bdesc0 + soff + (uint64_t)(u * (act_bytes >> 4)) + 2u * kk, idesc,
+                       (kb | u | kk) != 0);
         tc_commit(empty(s));
         if (++s == stages) {
           s = 0;
@@ -362,7 +375,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t flip = (uint32_t)(gq & 1);
     // (s[gq], s[gq+8]) and zero-point pairs of this warp's strips for a stage
     auto load_meta = [&](int kb, uint32_t (&ms)[4], uint32_t (&mz)[4]) {
-      const int grp = (int)((long long)(kb0 + kb) * kStageK / p.group);
+      const int grp = (int)((long long)(kb0 + kb) * SA * kStageK / p.group);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int strip = n0 / kStripCols + groups * sub + i;
@@ -384,14 +397,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (kb + groups < nk) load_meta(kb + groups, nms, nmz);  // this warp's next stage
       if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
-      const uint32_t wdq = st + act_bytes;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int ls = groups * sub + i;  // strip within the tile
         if (i < groups && n0 / kStripCols + ls < nstrips) {
           const DeqConst d0 = make_deq_const(mz[i] & 15u, (uint16_t)(ms[i] & 0xffffu));
           const DeqConst d1 = make_deq_const((mz[i] >> 4) & 15u, (uint16_t)(ms[i] >> 16));
-          const uint4 v = lds128(st + act_bytes + kWdqBytes + ls * 512 + lane * 16);
+#pragma unroll
+          for (int u = 0; u < SA; ++u) {
+          const uint32_t wdq = st + wdq_off + u * kWdqBytes;
+          const uint4 v = lds128(st + packed_off + ls * (SA * 512) + u * 512 + lane * 16);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
@@ -404,6 +419,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t kw = 4u * ks + t;
             sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4), o[0],
                    o[1], o[2], o[3]);
+          }
           }
         }
       }
@@ -547,14 +563,25 @@ int tc_token_tile(int M) {
 // pipeline that fits.
 int tc_ctas_per_sm(int bt) { return bt <= 48 ? 2 : 1; }
 
-size_t tc_smem_bytes(int bt, int* stages_out) {
-  const size_t stage = (size_t)bt * 128 + kWdqBytes + kPackedBytes;
+size_t tc_smem_bytes(int bt, int sa, int* stages_out) {
+  const size_t stage = (size_t)sa * ((size_t)bt * 128 + kWdqBytes + kPackedBytes);
   const size_t budget = (tc_ctas_per_sm(bt) == 2 ? 113 * 1024 : 227 * 1024) - 1024 - 256;
   int stages = (int)(budget / stage);
   if (stages > 8) stages = 8;
   if (stages >= 4) stages &= ~3;  // a multiple of the 4 dequant groups
+  else if (stages == 3) stages = 2;  // of 2 groups
   if (stages_out) *stages_out = stages;
   return (size_t)stages * stage + 1024 + 256;
+}
+
+// Two-atom stages halve the hand-offs per weight byte but need a ring of at
+// least 4 of them to pay: measured, 64-token tiles (4 stages) gained 15-22%
+// and 128- or 256-token tiles (2 stages) lost 5-10%.
+int tc_stage_atoms(int M, int K, int group) {
+  if (K % 128 != 0 || group % 128 != 0) return 1;
+  int stages = 0;
+  tc_smem_bytes(tc_token_tile(M), 2, &stages);
+  return stages >= 4 ? 2 : 1;
 }
 
 size_t tc_workspace_bytes(int M, int N, int split) {
@@ -575,18 +602,20 @@ size_t tc_workspace_bytes(int M, int N, int split) {
 // that keep >= 8 stages per CTA, the score is the wave efficiency times the
 // share of weight bytes in the traffic once the fp32 partial tiles (written
 // and read back) are counted.
-int tc_choose_split(int M, int N, int K, int sms) {
+int tc_choose_split(int M, int N, int K, int group, int sms) {
   const int bt = tc_token_tile(M);
   const long tiles = (long)((N + kTileN - 1) / kTileN) * ((M + bt - 1) / bt);
   const long slots = (long)sms * tc_ctas_per_sm(bt);
   if (tiles > (long)(kTcCounterBytes / sizeof(int))) return 1;
-  const long nk = K / kStageK;
+  const int sa = tc_stage_atoms(M, K, group);
+  const long stages = K / (kStageK * sa);  // pipeline stages of the whole K
+  const long nk = K / kStageK;             // atoms (costs are counted in atoms)
   if (bt >= 64 && bt <= 128) {
     int best = 1;
     long best_cost = -1;
-    for (int split = 1; split <= 16 && (split == 1 || nk / split >= 8); ++split) {
+    for (int split = 1; split <= 16 && split <= stages && (split == 1 || nk / split >= 8); ++split) {
       const long waves = (tiles * split + slots - 1) / slots;
-      const long cost = waves * ((nk + split - 1) / split + (split > 1 ? 2 + split : 0));
+      const long cost = waves * ((stages + split - 1) / split * sa + (split > 1 ? 2 + split : 0));
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         best = split;
@@ -598,7 +627,7 @@ int tc_choose_split(int M, int N, int K, int sms) {
   const double wbytes = (double)K * N / 2 + 2.0 * M * K;
   int best = 1;
   double best_score = -1.0;
-  for (int split = 1; split <= 16 && nk / split >= 8; ++split) {
+  for (int split = 1; split <= 16 && split <= stages && nk / split >= 8; ++split) {
     const long total = tiles * split;
     const long waves = (total + slots - 1) / slots;
     const double eff = (double)total / (double)(waves * slots);
@@ -618,6 +647,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const int bt = tc_token_tile(M);
+  const int sa = tc_stage_atoms(M, K, group);
   CUtensorMap tmA, tmW;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -633,7 +663,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
     // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
     const cuuint64_t dims[2] = {(cuuint64_t)(K / kAtomK) * kAtomWords, (cuuint64_t)(N / kStripCols)};
     const cuuint64_t strides[1] = {(cuuint64_t)(K / kAtomK) * kAtomWords * 4};
-    const cuuint32_t box[2] = {kAtomWords, kTileN / kStripCols};
+    const cuuint32_t box[2] = {(cuuint32_t)(kAtomWords * sa), kTileN / kStripCols};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(Wq), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -653,19 +683,25 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;
-  const size_t smem = tc_smem_bytes(bt, &prm.stages);
+  const size_t smem = tc_smem_bytes(bt, sa, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
   prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
-  static size_t attr_bytes = 0;
-  if (attr_bytes < smem) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(227 * 1024));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(227 * 1024));
     if (e != cudaSuccess) return e;
-    attr_bytes = 227 * 1024;
+    attr_set = true;
   }
   const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
                   (unsigned)prm.split);
-  tc_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  if (sa == 2)
+    tc_gemm_kernel<2><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  else
+    tc_gemm_kernel<1><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
   return cudaGetLastError();
 }
 

@@ -174,7 +174,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * split granules: 128-column blocks x groups of K, a group counted as at most
  * 512 k and K split anywhere on 64-k boundaries when group == K),
  * for the tensor-core path the number of K ranges per output tile (clamped to
- * K/64). The decode path handles any M in launches of 16 rows (it streams the
+ * the pipeline stages of K: K/64, or K/128 when K and the group are multiples
+ * of 128 and the token tile leaves room for four 128-k stages). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
  * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
  * W4A16_STATIC_WEIGHTS (see above); any other bit is W4A16_ERR_INVALID_ARG. */

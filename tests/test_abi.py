@@ -96,7 +96,8 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, path=5) == -1
     assert _gemm(lib, path=0x200 | 1) == -1           # unknown flag bit
     assert _gemm(lib, parts=-1) == -1
-    assert _gemm(lib, path=2, parts=4, ws=0) == -4      # a K-split tensor launch needs a workspace
+    # a K-split tensor launch needs a workspace (K = 512: four 128-k stages)
+    assert _gemm(lib, path=2, parts=4, K=512, ws=0) == -4
     assert _gemm(lib, path=1, ws=0) == -4             # decode needs a workspace
     assert _gemm(lib, path=1, ws_bytes=16) == -4
     assert _gemm(lib, path=1, ws=8) == -3             # workspace not 256-byte aligned

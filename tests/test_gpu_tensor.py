@@ -3,7 +3,8 @@
 Same tolerance as the decode path; shapes cover token tiles of 16..256,
 ragged M inside a token tile, several 128-column tiles with a ragged last
 tile (N a multiple of 16 only), K from one stage (64) to thousands, and
-groups 64, 128 and K (per-channel).
+groups 64, 128 and K (per-channel), and both pipeline stage sizes (64 k, and
+128 k for 64-token tiles when K and the group are multiples of 128).
 """
 import numpy as np
 import pytest
@@ -30,6 +31,10 @@ TENSOR_CASES = [
     (1024, 2048, 1280, 128),
     (8, 256, 16, 128),
     (1, 128, 32, 128),
+    # 64-token tiles run 128-k stages when K and the group allow it
+    (50, 1152, 144, 128),   # nine 128-k stages, ragged M and N tails
+    (60, 1024, 256, 64),    # groups of 64: 64-k stages
+    (64, 1088, 128, 1088),  # K not a multiple of 128: 64-k stages
 ]
 
 
