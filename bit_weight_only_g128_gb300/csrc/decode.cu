@@ -1068,13 +1068,15 @@ namespace {
 // warps are faster from 4 rows up and 8 warps below, so that order is tried
 // first. `requested` CTAs, else one per resident slot, clamped to the strips
 // and to 8192. With `automatic`, staged activations above 160 KiB count as
-// not fitting: there the stream-K variant was faster (8 rows of K = 11008).
+// not fitting unless the strips spread over the CTAs at least 90% evenly
+// (S / (C ceil(S / C))): measured, the stream-K variant was faster at 8 rows
+// of K = 11008 over 256 strips (84%) and 16 rows of K = 5120 over 320 strips
+// (70%), slower at 16 rows of K = 5120 over 960 and 1728 strips (90%, 95%).
 // Returns the CTA count (0: no fit) and sets the warps per CTA.
 int resident_shape(int M, int N, int K, int gshift, int requested, int sms, bool automatic,
                    int* nw, DecodeArgs* args, int* bytes) {
   const int nstrips = N / kStripCols;
   const long act_bytes = (M + 1L) * (2L * K + 64);
-  if (automatic && act_bytes > 160L * 1024) return 0;
   for (int i = 0; i < 2; ++i) {
     const int w = (M >= 4) == (i == 0) ? 16 : 8;
     long c = requested > 0 ? requested : (w == 8 ? 2L : 1L) * sms;
@@ -1082,6 +1084,10 @@ int resident_shape(int M, int N, int K, int gshift, int requested, int sms, bool
     if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
     if (c >= 1 && strip_layout(M, N, K, gshift, (int)c, w, w == 8 ? kTwoCtaSmem : kOneCtaSmem, args,
                                bytes)) {
+      if (automatic && act_bytes > 160L * 1024) {
+        const long most = (nstrips + c - 1) / c;  // strips of the busiest CTA
+        if (10L * nstrips < 9L * c * most) return 0;
+      }
       *nw = w;
       return (int)c;
     }

@@ -86,7 +86,8 @@ extern "C" {
  * it needs no workspace, and shapes whose rows (16 rows per launch at most)
  * do not fit give W4A16_ERR_UNSUPPORTED_SHAPE (about (M+1)*K <= 110 Ki
  * elements: K = 4096 up to 16 rows, K = 11008 up to 8). W4A16_PATH_DECODE
- * takes it only up to 160 KiB of staged rows. STREAMK: the
+ * takes it up to 160 KiB of staged rows, and beyond that only when the
+ * strips spread over the CTAs at least 90% evenly. STREAMK: the
  * weights of 128-column blocks are split across CTAs in equal runs of
  * groups, the activations are streamed through shared memory with them, and
  * blocks split between CTAs are combined through the workspace; any shape
