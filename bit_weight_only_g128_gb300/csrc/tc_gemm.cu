@@ -592,12 +592,14 @@ size_t tc_workspace_bytes(int M, int N, int split) {
 }
 
 // K split of the tensor-core GEMM.
-// Token tiles of 64..128 (one CTA per SM): a CTA streams its K range at a rate
+// Token tiles of 64..256 (one CTA per SM): a CTA streams its K range at a rate
 // per 64-k stage that does not depend on the split, so a launch takes about
 // waves x (stages per CTA + the fix-up of a split tile by its last CTA, about
-// 2 + split stages); the split minimizes that, keeping at least 8 stages per
-// CTA (measured on the Llama middle band: 13B gate_up at 64 rows 68.9 ->
-// 62.3 us with 2 ranges, 70B down at 64 rows 108 -> 95 us with 7).
+// 2 + split stages, 12 + split for 256-token tiles whose 128 KiB partial
+// tiles cost HBM time); the split minimizes that, keeping at least 8 stages
+// per CTA (measured on the Llama middle band: 13B gate_up at 64 rows 68.9 ->
+// 62.3 us with 2 ranges, 70B down at 64 rows 108 -> 95 us with 7; 70B qkv at
+// 512 rows, 160 tiles on 152 SMs, 126 -> 120 us with 3).
 // Other tiles: only when the output tiles cannot fill the SMs; among splits
 // that keep >= 8 stages per CTA, the score is the wave efficiency times the
 // share of weight bytes in the traffic once the fp32 partial tiles (written
@@ -610,12 +612,13 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
   const int sa = tc_stage_atoms(M, K, group);
   const long stages = K / (kStageK * sa);  // pipeline stages of the whole K
   const long nk = K / kStageK;             // atoms (costs are counted in atoms)
-  if (bt >= 64 && bt <= 128) {
+  if (bt >= 64) {
+    const long fixup = bt > 128 ? 12 : 2;
     int best = 1;
     long best_cost = -1;
     for (int split = 1; split <= 16 && split <= stages && (split == 1 || nk / split >= 8); ++split) {
       const long waves = (tiles * split + slots - 1) / slots;
-      const long cost = waves * ((stages + split - 1) / split * sa + (split > 1 ? 2 + split : 0));
+      const long cost = waves * ((stages + split - 1) / split * sa + (split > 1 ? fixup + split : 0));
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         best = split;
