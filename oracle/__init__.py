@@ -59,6 +59,9 @@ _SIGS = {
     "oracle_pack": (None, [_P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "oracle_unpack": (None, [_P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "oracle_threads": (_I, []),
+    "oracle_silu": (ctypes.c_double, [ctypes.c_double]),
+    "oracle_silu_mul": (None, [_P, _P, _I, _I, _P, _P]),
+    "oracle_check_bound": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
 }
 
 
@@ -197,3 +200,33 @@ def unpack(Wp, Sp, Zp, K: int, N: int, group: int):
     z = np.empty((G, N), np.uint8)
     lib().oracle_unpack(_ptr(Wp), _ptr(Sp), _ptr(Zp), K, N, group, _ptr(q), _ptr(s), _ptr(z))
     return q, s, z
+
+
+def silu(x: float) -> float:
+    """silu(x) = x / (1 + exp(-x)) in fp64."""
+    return float(lib().oracle_silu(float(x)))
+
+
+def silu_mul(y: np.ndarray, mag: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Fused gate/up epilogue of a product y [M, N] = [gate | up]:
+    (out [M, N/2] = silu(gate) * up, bound [M, N/2]) in fp64 (lmdeploy issue
+    #2274, "Modification": gate and up fused into one weight, SiLU fused)."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    mag = np.ascontiguousarray(mag, dtype=np.float64)
+    M, N = y.shape
+    assert N % 2 == 0 and mag.shape == y.shape
+    out = np.empty((M, N // 2), np.float64)
+    bound = np.empty((M, N // 2), np.float64)
+    lib().oracle_silu_mul(_ptr(y), _ptr(mag), M, N, _ptr(out), _ptr(bound))
+    return out, bound
+
+
+def check_bound(Y, ref: np.ndarray, bound: np.ndarray) -> Tuple[float, int]:
+    """max |Y - ref| / bound over all elements, and its index."""
+    Y = _as_half_bits(Y)
+    ref = np.ascontiguousarray(ref, dtype=np.float64)
+    bound = np.ascontiguousarray(bound, dtype=np.float64)
+    assert Y.shape == ref.shape == bound.shape
+    wi = _SZ(0)
+    r = lib().oracle_check_bound(_ptr(Y), _ptr(ref), _ptr(bound), Y.size, ctypes.byref(wi))
+    return float(r), int(wi.value)

@@ -316,6 +316,66 @@ void oracle_unpack(const uint32_t* Wp, const uint16_t* Sp, const uint32_t* Zp,
         }
 }
 
+/* ---------------------------------------------------------------------- */
+/* Fused gate/up epilogue.                                                  */
+/*                                                                          */
+/* lmdeploy issue #2274 "[Feature] support qqq(w4a8) for lmdeploy",         */
+/* section "Modification": the gate and up weights are fused into one       */
+/* weight, and element-wise operations such as SiLU are fused into the      */
+/* kernels around the GEMM.  Readings (the pages give no formula):          */
+/*   R-gu    the fused weight's N columns are [gate | up], N/2 each; the    */
+/*           output is out[m, j] = silu(y[m, j]) * y[m, N/2 + j];            */
+/*   R-silu  silu(x) = x * sigmoid(x) = x / (1 + exp(-x)), in fp64.          */
+/* bound[m, j] propagates the product's tolerance B = 2^-9 * mag + 1e-3 of  */
+/* the two inputs (|silu'| <= 1.1):                                         */
+/*   |silu(g)| * Bu + 1.1 * Bg * (|u| + Bu) + 2^-10 * |out| + 1e-3,          */
+/* the last two terms for the output's fp16 rounding and the evaluation of  */
+/* silu in fp32.                                                            */
+/* ---------------------------------------------------------------------- */
+
+double oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+void oracle_silu_mul(const double* y, const double* mag, int M, int N, double* out,
+                     double* bound)
+{
+    int H = N / 2;
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < H; ++j) {
+            double g = y[(size_t)m * N + j];
+            double u = y[(size_t)m * N + H + j];
+            double bg = ldexp(mag[(size_t)m * N + j], -9) + 1e-3;
+            double bu = ldexp(mag[(size_t)m * N + H + j], -9) + 1e-3;
+            double sg = oracle_silu(g);
+            double o = sg * u;
+            out[(size_t)m * H + j] = o;
+            bound[(size_t)m * H + j] =
+                fabs(sg) * bu + 1.1 * bg * (fabs(u) + bu) + ldexp(fabs(o), -10) + 1e-3;
+        }
+}
+
+/* max |Y - ref| / bound over all elements (NaN is the worst), and where. */
+double oracle_check_bound(const uint16_t* y_gpu, const double* ref, const double* bound,
+                          size_t count, size_t* worst_index)
+{
+    double worst = 0.0;
+    size_t wi = 0;
+    for (size_t i = 0; i < count; ++i) {
+        double r = fabs(oracle_half_to_double(y_gpu[i]) - ref[i]) / bound[i];
+        if (!(r <= worst)) {
+            worst = r;
+            wi = i;
+            if (isnan(r))
+                break;
+        }
+    }
+    if (worst_index)
+        *worst_index = wi;
+    return worst;
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

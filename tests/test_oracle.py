@@ -306,3 +306,65 @@ def test_pack_follows_layout_text_and_round_trips(K, N, group):
             assert (byte >> (4 * (c // 8))) & 15 == z[grp, n]
     q2, s2, z2 = oracle.unpack(Wp, Sp, Zp, K, N, group)
     assert np.array_equal(q2, q) and np.array_equal(s2, s) and np.array_equal(z2, z)
+
+
+# --- fused gate/up epilogue (lmdeploy issue #2274, "Modification": gate and up
+# fused into one weight; element-wise SiLU fused around the GEMM) ----------
+
+def test_silu_odd_even_identities():
+    """silu(x) - silu(-x) = x and silu(x) + silu(-x) = x tanh(x/2): the first
+    pins the sigmoid's symmetry, the second checks against numpy's tanh."""
+    for x in np.linspace(-30.0, 30.0, 241):
+        a, b = oracle.silu(x), oracle.silu(-x)
+        assert abs((a - b) - x) <= 1e-12 * max(1.0, abs(x))
+        assert abs((a + b) - x * np.tanh(x / 2)) <= 1e-12 * max(1.0, abs(x))
+
+
+def test_silu_limits_and_sign():
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12          # sigmoid(40) = 1 - 4e-18
+    assert abs(oracle.silu(-40.0)) < 1e-15
+    xs = np.linspace(-20, 20, 401)
+    vals = np.array([oracle.silu(x) for x in xs])
+    assert np.all(vals[xs > 0] > 0) and np.all(vals[xs < 0] < 0)
+    # the minimum lies between -1.29 and -1.27 (silu'(x) = 0 there) and is about -0.2785
+    xf = np.linspace(-2.0, -0.5, 1501)
+    vf = np.array([oracle.silu(x) for x in xf])
+    i = int(np.argmin(vf))
+    assert -1.29 <= xf[i] <= -1.27 and -0.279 < vf[i] < -0.278
+
+
+def test_silu_mul_pairs_gate_with_up_half():
+    rng = np.random.default_rng(3)
+    M, H = 3, 5
+    gate = rng.normal(size=(M, H))
+    up = rng.normal(size=(M, H))
+    y = np.concatenate([gate, up], axis=1)
+    out, _ = oracle.silu_mul(y, np.abs(y))
+    # zero up -> zero out; zero gate -> zero out; doubling up doubles out exactly
+    y0 = np.concatenate([gate, np.zeros_like(up)], axis=1)
+    assert np.all(oracle.silu_mul(y0, np.abs(y0))[0] == 0)
+    y1 = np.concatenate([np.zeros_like(gate), up], axis=1)
+    assert np.all(oracle.silu_mul(y1, np.abs(y1))[0] == 0)
+    y2 = np.concatenate([gate, 2 * up], axis=1)
+    assert np.array_equal(oracle.silu_mul(y2, np.abs(y2))[0], 2 * out)
+    # a large gate passes up through almost unscaled: out ~ gate * up
+    y3 = np.concatenate([np.full_like(gate, 40.0), up], axis=1)
+    assert np.allclose(oracle.silu_mul(y3, np.abs(y3))[0], 40.0 * up, rtol=1e-12, atol=0)
+    # column j of out depends on columns j and H + j only
+    for j in range(H):
+        yj = y.copy()
+        yj[:, j] += 1.0
+        d = oracle.silu_mul(yj, np.abs(yj))[0] - out
+        assert np.all(d[:, [c for c in range(H) if c != j]] == 0) and np.all(d[:, j] != 0)
+
+
+def test_silu_mul_bound_accepts_rounding_and_rejects_errors():
+    rng = np.random.default_rng(4)
+    y = rng.normal(size=(4, 64)) * 3
+    mag = np.abs(y) * 4
+    out, bound = oracle.silu_mul(y, mag)
+    h = oracle.to_half(out)
+    assert oracle.check_bound(h, out, bound)[0] <= 1.0
+    bad = oracle.to_half(out + 3 * bound)
+    assert oracle.check_bound(bad, out, bound)[0] > 1.0
