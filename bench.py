@@ -385,6 +385,26 @@ def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
     return out
 
 
+def silu_mul_times(torch, w4, cases, rot, a_views, stream, reps=20):
+    """Average launch time of each gate_up case with the fused gate/up
+    epilogue (output [M, N/2] = silu(gate) * up), timed like per_case_times."""
+    out = []
+    for c, A in zip(cases, a_views):
+        if c.layer != "gate_up":
+            continue
+        Y = torch.empty((c.M, c.N // 2), dtype=torch.float16, device=A.device)
+        ws = w4.new_workspace(w4.workspace_size(c.M, c.N, c.K, c.group, silu_mul=True), A.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=ws, static_weights=True,
+                        silu_mul=True)
+        time_graphs(torch, [g], 3, stream)
+        out.append((c, time_graphs(torch, [g], 5, stream) / (5 * reps)))
+        del g, ws
+    return out
+
+
 def roofline_entry(args, pk, cases, step_bytes, step_flops, secs):
     """Roofline of the step's kernel launches: bound by HBM if the step's
     algorithmic bytes take longer at the measured copy bandwidth than its
@@ -486,6 +506,13 @@ def run_ours(args, wl, dist, rank, world, local):
                     "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
                     "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
                     "bound": bound, "frac": roof / (1e6 * t)}) + "\n")
+            for c, t in silu_mul_times(torch, w4, cases, rot, a_views, stream):
+                # the fused layer writes half the columns
+                nbytes = alg_bytes(c.M, c.K, c.N, c.group) - c.M * c.N
+                f.write(json.dumps({
+                    "workload": wl.name, "layer": "gate_up+silu_mul", "M": c.M, "K": c.K,
+                    "N": c.N, "group": c.group, "us": 1e6 * t, "GBps": nbytes / t / 1e9,
+                    "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12}) + "\n")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:

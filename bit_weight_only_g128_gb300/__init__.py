@@ -28,6 +28,7 @@ PATH_DECODE_RESIDENT, PATH_DECODE_STREAMK = 3, 4
 _PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR,
           "decode-resident": PATH_DECODE_RESIDENT, "decode-streamk": PATH_DECODE_STREAMK}
 STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
+SILU_MUL = 0x200        # W4A16_SILU_MUL
 
 ERRORS = {
     -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
@@ -179,11 +180,13 @@ def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
     return deq
 
 
-def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0) -> int:
-    """Scratch bytes a gemm call needs (0 for the tensor-core path)."""
+def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0,
+                   silu_mul: bool = False) -> int:
+    """Scratch bytes a gemm call with these arguments needs."""
     b = ctypes.c_size_t()
-    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path], parts, ctypes.byref(b)),
-           "w4a16_workspace_size")
+    flags = SILU_MUL if silu_mul else 0
+    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path] | flags, parts,
+                                         ctypes.byref(b)), "w4a16_workspace_size")
     return b.value
 
 
@@ -201,22 +204,24 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
          path: str = "auto", parts: int = 0, workspace: Optional[torch.Tensor] = None,
-         stream=None, static_weights: bool = False) -> torch.Tensor:
+         stream=None, static_weights: bool = False, silu_mul: bool = False) -> torch.Tensor:
     """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
 
     `workspace` must be zero-filled before its first use (new_workspace);
     without one, a fresh zeroed buffer is allocated for this call.
     `static_weights` (W4A16_STATIC_WEIGHTS): the kernel may read pw while the
     work queued before it on the stream drains; pw must not be written by
-    that work.
+    that work. `silu_mul` (W4A16_SILU_MUL): pw's columns are [gate | up] and
+    Y [M, N/2] = silu(gate) * up.
     """
     M, K = A.shape
     if K != pw.K:
         raise ValueError(f"A has K={K}, weight has K={pw.K}")
     if out is None:
-        out = torch.empty((M, pw.N), dtype=torch.float16, device=A.device)
+        out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=torch.float16,
+                          device=A.device)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul)
     if need:
         if workspace is None:
             workspace = new_workspace(need, A.device)
@@ -224,7 +229,8 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
-                               _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0), parts,
+                               _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
+                               | (SILU_MUL if silu_mul else 0), parts,
                                _stream(stream)), "w4a16_gemm")
     return out
 

@@ -85,10 +85,10 @@ bool is_decode(int path) {
 // The decode variant for one launch of `rows` rows: activations resident in
 // shared memory when they fit (with the CTA count `parts` asks for), else
 // stream-K. Returns the variant and its CTA count.
-int decode_variant(int path, int rows, int N, int K, int group, int parts, int* ctas) {
+int decode_variant(int path, int rows, int N, int K, int group, int parts, bool silu, int* ctas) {
   if (path != W4A16_PATH_DECODE_STREAMK) {
     const int c = decode_resident_ctas(rows, N, K, group, parts, sm_count(),
-                                       path == W4A16_PATH_DECODE);
+                                       path == W4A16_PATH_DECODE, silu);
     if (c > 0 || path == W4A16_PATH_DECODE_RESIDENT) {
       *ctas = c;
       return W4A16_PATH_DECODE_RESIDENT;
@@ -109,14 +109,28 @@ int tc_split(int M, int N, int K, int group, int requested) {
 }
 
 // The decode path's size covers either variant (the resident one uses none),
-// so that it does not depend on which one a device picks.
-size_t workspace_for(int M, int N, int K, int group, int path, int parts) {
+// so that it does not depend on which one a device picks. With the fused
+// gate/up epilogue, a path that does not fuse it (stream-K, tensor cores)
+// also holds the fp16 product of the rows of one launch ([rows][N]; all M
+// rows for tensor cores, 16 for the decode path) at product_offset: after
+// the path's own scratch, and never inside the 32 KiB flag/counter area that
+// every call must leave zero-filled (a launch without a K split has no
+// scratch of its own, but a later call may use the area).
+constexpr size_t kFlagAreaBytes = 32768;
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+size_t product_offset(size_t base) { return align256(base > kFlagAreaBytes ? base : kFlagAreaBytes); }
+
+size_t workspace_for(int M, int N, int K, int group, int path, int parts, bool silu) {
   if (M == 0) return 0;
-  if (path == W4A16_PATH_TENSOR) return tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
+  if (path == W4A16_PATH_TENSOR) {
+    const size_t base = tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
+    return silu ? product_offset(base) + (size_t)M * N * 2 : base;
+  }
   if (path == W4A16_PATH_DECODE_RESIDENT || !is_decode(path)) return 0;
   const int rows = M < 16 ? M : 16;
   const int c = decode_ctas(rows, N, K, group, parts);
-  return c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
+  const size_t base = c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
+  return silu ? product_offset(base) + (size_t)rows * N * 2 : base;
 }
 
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
@@ -135,23 +149,35 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     return fail(W4A16_ERR_MISALIGNED,
                 "alignment: A, Wq, scales, Y need 16 bytes and zeros 8 bytes");
   const bool static_weights = (path & W4A16_STATIC_WEIGHTS) != 0;
-  path &= ~W4A16_STATIC_WEIGHTS;
+  const bool silu = (path & W4A16_SILU_MUL) != 0;
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
+  if (silu && N % 32 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
+                "fused gate/up epilogue: N=%d is not two halves of 16-column strips "
+                "(a multiple of 32)", N);
+  const int ycols = silu ? N / 2 : N;  // columns of Y
   if (path == W4A16_PATH_TENSOR) {
     const int split = tc_split(M, N, K, group, parts);
-    const size_t need = tc_workspace_bytes(M, N, split);
+    const size_t base = tc_workspace_bytes(M, N, split);
+    const size_t need = workspace_for(M, N, K, group, path, parts, silu);
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
                   "tensor-core path (K split %d) needs a workspace of %zu bytes (got %zu)", split,
                   need, workspace ? workspace_bytes : (size_t)0);
     if (need > 0 && !aligned(workspace, 256))
       return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
-    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, Y, M, N, K, group, split,
-                                   need > 0 ? workspace : nullptr, stream);
+    // with the fused epilogue the product goes to the workspace first
+    uint16_t* prod =
+        silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + product_offset(base)) : Y;
+    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
+                                   base > 0 ? workspace : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+    if (silu && (e = launch_silu_mul(prod, M, N, Y, stream)) != cudaSuccess)
+      return cuda_fail(e, "gate/up epilogue launch");
     return ok();
   }
   if (decode_units(N, K, group) <= 0)
@@ -161,30 +187,39 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   int ctas = 0;
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
-    if (decode_variant(path, rows, N, K, group, parts, &ctas) == W4A16_PATH_DECODE_RESIDENT &&
+    if (decode_variant(path, rows, N, K, group, parts, silu, &ctas) ==
+            W4A16_PATH_DECODE_RESIDENT &&
         ctas == 0)
       return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
                   "resident decode variant: %d rows of K=%d (with the strips of N=%d over %d "
                   "CTAs) do not fit a CTA's shared memory",
                   rows, K, N, parts > 0 ? parts : 2 * sm_count());
   }
-  const size_t need = workspace_for(M, N, K, group, path, parts);
+  const size_t need = workspace_for(M, N, K, group, path, parts, silu);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
                 need, workspace ? workspace_bytes : (size_t)0);
   if (need > 0 && !aligned(workspace, 256))
     return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+  // the stream-K variant's product, with the fused epilogue, before silu * up
+  uint16_t* prod =
+      silu && need > 0
+          ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) +
+                                        product_offset(workspace_for(M, N, K, group, path, parts, false)))
+          : nullptr;
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
     const uint16_t* Ar = A + (size_t)r0 * K;
-    uint16_t* Yr = Y + (size_t)r0 * N;
+    uint16_t* Yr = Y + (size_t)r0 * ycols;
     cudaError_t e;
-    if (decode_variant(path, rows, N, K, group, parts, &ctas) == W4A16_PATH_DECODE_RESIDENT)
+    if (decode_variant(path, rows, N, K, group, parts, silu, &ctas) == W4A16_PATH_DECODE_RESIDENT) {
       e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, sm_count(),
-                                 path == W4A16_PATH_DECODE, static_weights, stream);
-    else
-      e = launch_decode(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, workspace,
+                                 path == W4A16_PATH_DECODE, silu, static_weights, stream);
+    } else {
+      e = launch_decode(Ar, Wq, scales, zeros, silu ? prod : Yr, rows, N, K, group, ctas, workspace,
                         static_weights, stream);
+      if (e == cudaSuccess && silu) e = launch_silu_mul(prod, rows, N, Yr, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   return ok();
@@ -265,10 +300,14 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
+  const bool silu = (path & W4A16_SILU_MUL) != 0;
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
-  *bytes = workspace_for(M, N, K, group, path, parts);
+  if (silu && N % 32 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "fused gate/up epilogue: N=%d is not a multiple of 32", N);
+  *bytes = workspace_for(M, N, K, group, path, parts, silu);
   return ok();
 }
 
@@ -293,7 +332,7 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   *path = choose_path(M);
   const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
   if (*path == W4A16_PATH_DECODE)
-    *path = decode_variant(W4A16_PATH_DECODE, rows, N, K, group, 0, parts);
+    *path = decode_variant(W4A16_PATH_DECODE, rows, N, K, group, 0, false, parts);
   else
     *parts = tc_split(M, N, K, group, 0);
   return ok();

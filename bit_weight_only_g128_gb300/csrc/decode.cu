@@ -185,6 +185,9 @@ struct DecodeArgs {
   int early_weights;  // read the first units' weights before the grid-dependency wait
   // strip variant: shared-memory layout (bytes)
   int act_row, sums_off, meta_off, zp_off, red_off;
+  // resident variant, fused gate/up epilogue: the N columns are [gate | up]
+  // and Y (N/2 columns) = silu(gate) * up; ytile_off: the CTA's fp32 strips
+  int silu, ytile_off;
 };
 
 // Where one unit's data lives for this warp/lane.
@@ -678,7 +681,7 @@ __device__ __forceinline__ void resident_unit(float (&acc)[MT][4], uint4 (&w)[kB
   }
 }
 
-template <int MT, int APG, int NW>
+template <int MT, int APG, int NW, bool kSilu>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const DecodeArgs p) {
   constexpr int kSeg = MT * 8 * kStripCols;  // floats of one partial strip
   extern __shared__ __align__(16) uint8_t smem[];
@@ -695,19 +698,31 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
   const int nstrips = N / kStripCols;
   const int G = (natoms + (1 << p.gshift) - 1) >> p.gshift;  // groups per strip
   const int gr = p.granule;
-  // this CTA's strips [s0, s1): global atoms [s0 natoms, s1 natoms), split
-  // into 8 warp ranges of whole granules; warp w starts at wbeg(w)
+  // this CTA's strips: units [u0, u1) of the S strips, or with the fused
+  // gate/up epilogue of the S/2 strip pairs (pair q: gate strip q and up
+  // strip S/2 + q). Its nv "virtual" strips v (the unit strips in order; for
+  // pairs the gate strips, then the up strips) hold virtual atoms
+  // [0, nv natoms), split into NW warp ranges of whole granules; warp w
+  // starts at wbeg(w). Virtual strip v is strip gstrip(v) of Wq and Y.
   const int C = gridDim.x;
-  const int s0 = (int)((long long)blockIdx.x * nstrips / C);
-  const int s1 = (int)((long long)(blockIdx.x + 1) * nstrips / C);
-  const int Lg = (s1 - s0) * (natoms / gr);
-  auto wbeg = [&](int w) { return s0 * natoms + gr * (int)((long long)w * Lg / NW); };
+  const int units = kSilu ? nstrips / 2 : nstrips;
+  const int u0 = (int)((long long)blockIdx.x * units / C);
+  const int u1 = (int)((long long)(blockIdx.x + 1) * units / C);
+  const int nu = u1 - u0, nv = kSilu ? 2 * nu : nu;
+  auto gstrip = [&](int v) { return kSilu && v >= nu ? nstrips / 2 + u0 + (v - nu) : u0 + v; };
+  const int Lg = nv * (natoms / gr);
+  auto wbeg = [&](int w) { return gr * (int)((long long)w * Lg / NW); };
   const int run_begin = wbeg(warp), run_end = wbeg(warp + 1);
-  const int rec0 = s0 * G;
 
   int strip = run_begin / natoms, a = run_begin - strip * natoms, g = run_begin;
   int n = g < run_end ? min(kBatch - (a & (kBatch - 1)), min(natoms - a, run_end - g)) : 0;
-  const uint4* wp = p.Wq + (size_t)g * 32 + lane;
+  // the lane's word of virtual strip v, atom a
+  auto wptr = [&](int v, int a_) { return p.Wq + ((size_t)gstrip(v) * natoms + a_) * 32 + lane; };
+  const uint4* wp = wptr(strip, a);
+  // consecutive virtual strips are consecutive in Wq (strip-major, atoms in
+  // order), except from the last gate strip to the first up strip
+  const int jump_v = kSilu ? nu : -1;
+  const int jump = (nstrips / 2 - nu) * natoms * 32;
   uint4 w[kBatch];
   auto prefetch = [&]() {
     if (g < run_end) {
@@ -715,15 +730,19 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       for (int u = 0; u < kBatch; ++u)
         if (u < n) w[u] = ldg_stream(wp + u * 32);
     }
-    // group pairs of the CTA's strips: records [rec0, rec0 + (s1 - s0) G)
-    const int nrec = (s1 - s0) * G;
-    const uint4* sp_src = reinterpret_cast<const uint4*>(p.Sp2) + (size_t)rec0 * 2;
-    const uint2* zp_src = reinterpret_cast<const uint2*>(p.Zp) + rec0;
+    // group pairs of the CTA's strips, in virtual strip order: record
+    // v G + grp of the stage is record gstrip(v) G + grp of Sp/Zp
+    const int nrec = nv * G;
+    const uint4* sp_src = reinterpret_cast<const uint4*>(p.Sp2);
+    const uint2* zp_src = reinterpret_cast<const uint2*>(p.Zp);
     for (int i = threadIdx.x; i < 3 * nrec; i += (NW * 32)) {
+      const int r = i < 2 * nrec ? i >> 1 : i - 2 * nrec;  // staged record
+      const int v = r / G;
+      const size_t rg = (size_t)gstrip(v) * G + (r - v * G);  // its record in Sp/Zp
       if (i < 2 * nrec)
-        cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_src + i);
+        cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_src + rg * 2 + (i & 1));
       else
-        cp_async8(reinterpret_cast<uint2*>(smem + p.zp_off) + (i - 2 * nrec), zp_src + (i - 2 * nrec));
+        cp_async8(reinterpret_cast<uint2*>(smem + p.zp_off) + r, zp_src + rg);
     }
   };
   if (p.early_weights) prefetch();
@@ -784,14 +803,19 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
 
   // element j of token octet o of this lane: token 8o + 2t + (j & 1), column gq + 8 (j >> 1)
   auto elem = [&](int o, int j) { return (8 * o + 2 * t + (j & 1)) * kStripCols + gq + 8 * (j >> 1); };
+  // the finished virtual strip s: to Y, or with the fused epilogue to the
+  // CTA's fp32 tile ([virtual strip][token][column])
+  float* ytile = reinterpret_cast<float*>(smem + p.ytile_off);
   auto store_y = [&](const float (&v)[MT][4], int s, float scale) {
 #pragma unroll
     for (int o = 0; o < MT; ++o)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tok = 8 * o + 2 * t + (j & 1);
-        if (tok < M)
-          p.Y[(size_t)tok * N + s * kStripCols + gq + 8 * (j >> 1)] =
+        if (kSilu)
+          ytile[(s * MT * 8 + tok) * kStripCols + gq + 8 * (j >> 1)] = v[o][j] * scale;
+        else if (tok < M)
+          p.Y[(size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1)] =
               __half_as_ushort(__float2half_rn(v[o][j] * scale));
       }
   };
@@ -812,8 +836,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     const int g2 = g + n;
     const bool has_next = g2 < run_end;
     const int n2 = has_next ? min(kBatch - (a2 & (kBatch - 1)), min(natoms - a2, run_end - g2)) : 0;
-    const uint4* wp2 = wp + n * 32;
-    const int rec = strip * G + (a >> p.gshift) - rec0;
+    const uint4* wp2 = has_next ? wp + n * 32 + (s2 == jump_v && s2 != strip ? jump : 0) : wp;
+    const int rec = strip * G + (a >> p.gshift);
     const uint32_t* sps = meta_sp + rec * 8 + gq;
     const uint8_t* zps = meta_zp + rec * 8 + gq;
     const float* sb = sums + a * MT * 8;
@@ -870,6 +894,19 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     }
     store_y(v, s, 1.f);
   }
+  if (kSilu) {
+    // Y[tok][16 (u0 + q) + c] = silu(gate) * up for the CTA's pairs q
+    __syncthreads();
+    const int half = N / 2;
+    for (int e = threadIdx.x; e < nu * M * kStripCols; e += NW * 32) {
+      const int q = e / (M * kStripCols), r = e - q * (M * kStripCols);
+      const int tok = r / kStripCols, c = r - tok * kStripCols;
+      const float gv = ytile[(q * MT * 8 + tok) * kStripCols + c];
+      const float uv = ytile[((nu + q) * MT * 8 + tok) * kStripCols + c];
+      p.Y[(size_t)tok * half + (u0 + q) * kStripCols + c] =
+          __half_as_ushort(__float2half_rn(gv / (1.0f + expf(-gv)) * uv));
+    }
+  }
 }
 
 // Shared memory one CTA may use with two CTAs per SM (228 KiB per SM, 1 KiB
@@ -880,20 +917,25 @@ constexpr int kOneCtaSmem = 227 * 1024;
 // Layout of the strip variant's shared memory for `ctas` CTAs of `nw` warps:
 // A (rows 0..M), the atom sums, the scale and zero-point pairs of a CTA's
 // strips and the warps' partial strips. False if it exceeds `limit` bytes.
-bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, DecodeArgs* a,
-                  int* bytes) {
+bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, bool silu,
+                  DecodeArgs* a, int* bytes) {
   const long mt = M <= 8 ? 1 : 2;
   const long natoms = K / kAtomK;
   const long nstrips = N / kStripCols;
   const long G = (natoms + (1L << gshift) - 1) >> gshift;
-  const long strips_max = (nstrips + ctas - 1) / ctas;
+  // strips of the busiest CTA (with the fused gate/up epilogue: both strips
+  // of its pairs)
+  const long strips_max = silu ? 2 * ((nstrips / 2 + ctas - 1) / ctas) : (nstrips + ctas - 1) / ctas;
   const long act_row = 2L * K + 64;
   const long sums_off = ((M + 1) * act_row + 15) & ~15L;
   const long meta_off = sums_off + ((natoms * mt * 8 * 4 + 15) & ~15L);
   const long zp_off = meta_off + strips_max * G * 32;
   const long red_off = zp_off + ((strips_max * G * 8 + 15) & ~15L);
-  const long total = red_off + (long)nw * 2 * mt * 8 * kStripCols * 4;
+  const long ytile_off = red_off + (long)nw * 2 * mt * 8 * kStripCols * 4;
+  const long total = ytile_off + (silu ? strips_max * mt * 8 * kStripCols * 4 : 0);
   if (total > limit) return false;
+  a->silu = silu ? 1 : 0;
+  a->ytile_off = (int)ytile_off;
   a->act_row = (int)act_row;
   a->sums_off = (int)sums_off;
   a->meta_off = (int)meta_off;
@@ -905,7 +947,8 @@ bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, 
 
 template <int MT, int APG, int NW>
 cudaError_t launch_strip(const DecodeArgs& args, int ctas, int bytes, cudaStream_t stream) {
-  auto kern = decode_resident_kernel<MT, APG, NW>;
+  auto kern = args.silu ? decode_resident_kernel<MT, APG, NW, true>
+                        : decode_resident_kernel<MT, APG, NW, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        NW == 8 ? kTwoCtaSmem : kOneCtaSmem);
   if (e != cudaSuccess) return e;
@@ -1074,19 +1117,20 @@ namespace {
 // (70%), slower at 16 rows of K = 5120 over 960 and 1728 strips (90%, 95%).
 // Returns the CTA count (0: no fit) and sets the warps per CTA.
 int resident_shape(int M, int N, int K, int gshift, int requested, int sms, bool automatic,
-                   int* nw, DecodeArgs* args, int* bytes) {
-  const int nstrips = N / kStripCols;
+                   bool silu, int* nw, DecodeArgs* args, int* bytes) {
+  // units of work: strips, or with the fused gate/up epilogue strip pairs
+  const int units = silu ? N / kStripCols / 2 : N / kStripCols;
   const long act_bytes = (M + 1L) * (2L * K + 64);
   for (int i = 0; i < 2; ++i) {
     const int w = (M >= 4) == (i == 0) ? 16 : 8;
     long c = requested > 0 ? requested : (w == 8 ? 2L : 1L) * sms;
-    if (c > nstrips) c = nstrips;
+    if (c > units) c = units;
     if (c > kDecodeMaxCtas) c = kDecodeMaxCtas;
-    if (c >= 1 && strip_layout(M, N, K, gshift, (int)c, w, w == 8 ? kTwoCtaSmem : kOneCtaSmem, args,
-                               bytes)) {
+    if (c >= 1 && strip_layout(M, N, K, gshift, (int)c, w, w == 8 ? kTwoCtaSmem : kOneCtaSmem, silu,
+                               args, bytes)) {
       if (automatic && act_bytes > 160L * 1024) {
-        const long most = (nstrips + c - 1) / c;  // strips of the busiest CTA
-        if (10L * nstrips < 9L * c * most) return 0;
+        const long most = (units + c - 1) / c;  // units of the busiest CTA
+        if (10L * units < 9L * c * most) return 0;
       }
       *nw = w;
       return (int)c;
@@ -1097,22 +1141,25 @@ int resident_shape(int M, int N, int K, int gshift, int requested, int sms, bool
 
 }  // namespace
 
-int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic) {
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic,
+                         bool silu) {
   int apg_t = 0, gshift = 0, nw = 0, bytes = 0;
   if (M < 1 || M > 16 || !group_shape(K, group, &apg_t, &gshift)) return 0;
+  if (silu && (N / kStripCols) % 2 != 0) return 0;
   DecodeArgs args;
-  return resident_shape(M, N, K, gshift, requested, sms, automatic, &nw, &args, &bytes);
+  return resident_shape(M, N, K, gshift, requested, sms, automatic, silu, &nw, &args, &bytes);
 }
 
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                                   int ctas, int sms, bool automatic, bool early_weights,
-                                   cudaStream_t stream) {
+                                   int ctas, int sms, bool automatic, bool silu,
+                                   bool early_weights, cudaStream_t stream) {
   DecodeArgs args = {};
   int apg_t = 0, bytes = 0, nw = 0;
   if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
+  if (silu && (N / kStripCols) % 2 != 0) return cudaErrorInvalidValue;
   if (ctas < 1 ||
-      resident_shape(M, N, K, args.gshift, ctas, sms, automatic, &nw, &args, &bytes) != ctas)
+      resident_shape(M, N, K, args.gshift, ctas, sms, automatic, silu, &nw, &args, &bytes) != ctas)
     return cudaErrorInvalidValue;
   args.A = A;
   args.Wq = reinterpret_cast<const uint4*>(Wq);

@@ -31,18 +31,23 @@ size_t decode_workspace_bytes(int M, int N, int ctas);
 
 // Register-dequant GEMV with the activations resident in shared memory, for
 // M <= 16 rows: `ctas` CTAs (as decode_resident_ctas returned for the same
-// `sms` and `automatic`) each own whole 16-column strips over all of K; no
-// workspace.
+// `sms`, `automatic` and `silu`) each own whole 16-column strips over all of
+// K; no workspace. With `silu` the N columns are [gate | up], each CTA owns
+// pairs of strips (q, N/32 + q), and Y is M x N/2 = silu(gate) * up.
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                                   int ctas, int sms, bool automatic, bool early_weights,
-                                   cudaStream_t stream);
+                                   int ctas, int sms, bool automatic, bool silu,
+                                   bool early_weights, cudaStream_t stream);
 // CTAs of that kernel (`requested`, else one per resident slot of `sms` SMs:
 // two 8-warp CTAs or one 16-warp CTA per SM; clamped to the strips and to
 // 8192), or 0 when the problem's activations, sums and group pairs do not fit
 // a CTA's shared memory at that count (with `automatic`, also when the
 // staged activations exceed 160 KiB) or the group is unsupported.
-int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic);
+int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic,
+                         bool silu);
+// Y [M][N/2] = silu(Yfull[:, :N/2]) * Yfull[:, N/2:] for an fp16 product
+// Yfull [M][N] (row stride N): the fused gate/up epilogue as a separate pass.
+cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, cudaStream_t stream);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
 // Split granules (128 columns x a group's atoms, at most 8) of a problem: the

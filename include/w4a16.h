@@ -103,6 +103,22 @@ extern "C" {
  * which hides the gap between back-to-back layers. Without it the ordering is
  * that of a plain launch. */
 #define W4A16_STATIC_WEIGHTS 0x100
+/* Flag OR-ed into the path of w4a16_gemm_ex and w4a16_workspace_size_ex: the
+ * fused gate/up epilogue of a gated MLP (lmdeploy issue #2274 "[Feature]
+ * support qqq(w4a8) for lmdeploy", section "Modification": the gate and up
+ * projections fused into one weight, SiLU fused into the GEMM). The N
+ * columns of the weight are [gate | up], two halves of N/2 (N a multiple of
+ * 32, else W4A16_ERR_UNSUPPORTED_SHAPE), and the output is
+ * Y [M][N/2] = silu(A.W[:, :N/2]) * (A.W[:, N/2:]), silu(g) = g/(1+exp(-g)),
+ * formed in fp32 and rounded to fp16 once. The resident decode variant
+ * forms it from the fp32 accumulators inside the GEMM kernel (each CTA owns
+ * both strips of its column pairs; no workspace). The stream-K variant and
+ * the tensor-core path write the fp16 product [rows][N] to the workspace
+ * (after their own scratch and at least after its 32 KiB flag/counter area,
+ * at a 256-byte boundary; 16 rows per decode launch, all M rows for tensor
+ * cores) and a second kernel forms Y from it;
+ * w4a16_workspace_size_ex with this flag counts those bytes. */
+#define W4A16_SILU_MUL 0x200
 
 /* Message for the last error returned on the calling thread ("" if none). */
 const char* w4a16_last_error(void);
@@ -154,7 +170,8 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 int w4a16_workspace_size(int M, int N, int K, int group, size_t* bytes);
 
 /* As w4a16_workspace_size for a forced path and work partition (see
- * w4a16_gemm_ex). Host-only. */
+ * w4a16_gemm_ex); `path` may carry the flags w4a16_gemm_ex takes
+ * (W4A16_SILU_MUL adds the fp16 product's bytes). Host-only. */
 int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
                             size_t* bytes);
 
@@ -179,7 +196,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * of 128 and the token tile leaves room for four 128-k stages). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
  * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
- * W4A16_STATIC_WEIGHTS (see above); any other bit is W4A16_ERR_INVALID_ARG. */
+ * W4A16_STATIC_WEIGHTS and W4A16_SILU_MUL (see above; with the latter Y is
+ * [M][N/2]); any other bit is W4A16_ERR_INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,

@@ -94,7 +94,13 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
     assert _gemm(lib, path=5) == -1
-    assert _gemm(lib, path=0x200 | 1) == -1           # unknown flag bit
+    assert _gemm(lib, path=0x400 | 1) == -1           # unknown flag bit
+    # fused gate/up epilogue: N must be two halves of whole strips, and a
+    # path that does not fuse it keeps the product in the workspace
+    assert _gemm(lib, path=0x200 | 1, N=48) == -2
+    assert _gemm(lib, path=0x200 | 2, N=80) == -2
+    assert _gemm(lib, path=0x200 | 2, ws=0) == -4
+    assert _gemm(lib, path=0x200 | 4, ws=0) == -4
     assert _gemm(lib, parts=-1) == -1
     # a K-split tensor launch needs a workspace (K = 512: four 128-k stages)
     assert _gemm(lib, path=2, parts=4, K=512, ws=0) == -4
@@ -148,6 +154,28 @@ def test_workspace_sizes(lib):
     assert w4.workspace_size(1, 512, 320, 320, path="decode", parts=1000) == head + 20 * 8 * 128 * 4
     # and never above 8192 CTAs
     assert w4.workspace_size(1, 65536, 4096, 64, path="decode", parts=20000) == head + 8192 * 8 * 128 * 4
+
+
+def test_silu_mul_workspace_sizes(lib):
+    # the product [rows][N] fp16 after the path's own scratch, at a 256-byte
+    # boundary, and never inside the 32 KiB flag/counter area (which a later
+    # call may use); none for the resident variant, which fuses the epilogue
+    head = 32768
+    assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=1,
+                             silu_mul=True) == head + 64 * 4096 * 2
+    base = head + 32 * 3 * 64 * 128 * 4
+    assert w4.workspace_size(64, 4096, 4096, 128, path="tensor", parts=3,
+                             silu_mul=True) == (base + 255) // 256 * 256 + 64 * 4096 * 2
+    assert w4.workspace_size(300, 352, 4096, 128, path="tensor", parts=1,
+                             silu_mul=True) == head + 300 * 352 * 2
+    assert w4.workspace_size(16, 4096, 4096, 128, path="decode-resident", silu_mul=True) == 0
+    for M, rows in ((1, 1), (16, 16), (40, 16)):
+        base = w4.workspace_size(M, 4096, 4096, 128, path="decode-streamk", parts=10)
+        for path in ("decode", "decode-streamk"):
+            assert w4.workspace_size(M, 4096, 4096, 128, path=path, parts=10,
+                                     silu_mul=True) == (base + 255) // 256 * 256 + rows * 4096 * 2
+    assert w4.SILU_MUL == 0x200
+    assert re.search(r"#define W4A16_SILU_MUL 0x200\b", open(HEADER).read())
 
 
 def test_path_constants_match_the_header():
