@@ -186,8 +186,15 @@ struct DecodeArgs {
   // strip variant: shared-memory layout (bytes)
   int act_row, sums_off, meta_off, zp_off, red_off;
   // resident variant, fused gate/up epilogue: the N columns are [gate | up]
-  // and Y (N/2 columns) = silu(gate) * up; ytile_off: the CTA's fp32 strips
-  int silu, ytile_off;
+  // and Y (N/2 columns) = silu(gate) * up; the CTA's finished fp32 strips
+  // at ytile_off, ytile_stride floats apart. They overlay the scale records
+  // (each strip's own, which only the warp that finishes a whole strip
+  // reads, and nobody once every warp has left the main loop) when those
+  // are large enough; else the activation rows, dead after the main loop,
+  // when the CTA has no more strips than warps (whole_in_red: every warp
+  // then has at most two segments, and finished strips go through the
+  // warps' partial slots too); else a region of their own
+  int silu, ytile_off, ytile_stride, whole_in_red;
 };
 
 // Where one unit's data lives for this warp/lane.
@@ -813,7 +820,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       for (int j = 0; j < 4; ++j) {
         const int tok = 8 * o + 2 * t + (j & 1);
         if (kSilu)
-          ytile[(s * MT * 8 + tok) * kStripCols + gq + 8 * (j >> 1)] = v[o][j] * scale;
+          ytile[s * p.ytile_stride + tok * kStripCols + gq + 8 * (j >> 1)] = v[o][j] * scale;
         else if (tok < M)
           p.Y[(size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1)] =
               __half_as_ushort(__float2half_rn(v[o][j] * scale));
@@ -848,7 +855,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       resident_unit<MT, APG, false>(acc, w, n, n2, wp2, has_next, fa, fb, sps, zps, sb, t);
     if (!has_next || s2 != strip) {
       // ---- end of a segment: atoms [seg_a0, a + n) of `strip`
-      if (seg_a0 == 0 && a + n == natoms) {
+      if (seg_a0 == 0 && a + n == natoms && !(kSilu && p.whole_in_red)) {
         store_y(acc, strip, kUnscale);  // the whole strip
       } else {
         const int rs = first_seg ? 0 : 1;
@@ -901,8 +908,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     for (int e = threadIdx.x; e < nu * M * kStripCols; e += NW * 32) {
       const int q = e / (M * kStripCols), r = e - q * (M * kStripCols);
       const int tok = r / kStripCols, c = r - tok * kStripCols;
-      const float gv = ytile[(q * MT * 8 + tok) * kStripCols + c];
-      const float uv = ytile[((nu + q) * MT * 8 + tok) * kStripCols + c];
+      const float gv = ytile[q * p.ytile_stride + tok * kStripCols + c];
+      const float uv = ytile[(nu + q) * p.ytile_stride + tok * kStripCols + c];
       p.Y[(size_t)tok * half + (u0 + q) * kStripCols + c] =
           __half_as_ushort(__float2half_rn(gv / (1.0f + expf(-gv)) * uv));
     }
@@ -916,7 +923,9 @@ constexpr int kOneCtaSmem = 227 * 1024;
 
 // Layout of the strip variant's shared memory for `ctas` CTAs of `nw` warps:
 // A (rows 0..M), the atom sums, the scale and zero-point pairs of a CTA's
-// strips and the warps' partial strips. False if it exceeds `limit` bytes.
+// strips and the warps' partial strips; with the fused gate/up epilogue also
+// the CTA's finished strips (placed as DecodeArgs describes). False if it
+// exceeds `limit` bytes.
 bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, bool silu,
                   DecodeArgs* a, int* bytes) {
   const long mt = M <= 8 ? 1 : 2;
@@ -927,15 +936,25 @@ bool strip_layout(int M, int N, int K, int gshift, int ctas, int nw, int limit, 
   // of its pairs)
   const long strips_max = silu ? 2 * ((nstrips / 2 + ctas - 1) / ctas) : (nstrips + ctas - 1) / ctas;
   const long act_row = 2L * K + 64;
-  const long sums_off = ((M + 1) * act_row + 15) & ~15L;
+  // the fused epilogue's finished strips: over their own scale records, else
+  // over the activation rows, else apart
+  const long slot = mt * 8 * kStripCols * 4;
+  const bool on_meta = silu && G * 32 >= slot;
+  const bool on_rows = silu && !on_meta && strips_max <= nw;
+  const long ytile_bytes = silu ? strips_max * slot : 0;
+  const long act_bytes = (M + 1) * act_row;
+  const long sums_off = ((on_rows && ytile_bytes > act_bytes ? ytile_bytes : act_bytes) + 15) & ~15L;
   const long meta_off = sums_off + ((natoms * mt * 8 * 4 + 15) & ~15L);
   const long zp_off = meta_off + strips_max * G * 32;
   const long red_off = zp_off + ((strips_max * G * 8 + 15) & ~15L);
-  const long ytile_off = red_off + (long)nw * 2 * mt * 8 * kStripCols * 4;
-  const long total = ytile_off + (silu ? strips_max * mt * 8 * kStripCols * 4 : 0);
+  const long red_end = red_off + (long)nw * 2 * mt * 8 * kStripCols * 4;
+  const long ytile_off = on_meta ? meta_off : on_rows ? 0 : red_end;
+  const long total = silu && !on_meta && !on_rows ? red_end + ytile_bytes : red_end;
   if (total > limit) return false;
   a->silu = silu ? 1 : 0;
   a->ytile_off = (int)ytile_off;
+  a->ytile_stride = (int)((on_meta ? G * 32 : slot) / 4);
+  a->whole_in_red = on_rows ? 1 : 0;
   a->act_row = (int)act_row;
   a->sums_off = (int)sums_off;
   a->meta_off = (int)meta_off;

@@ -62,6 +62,15 @@ DECODE_CASES = [
     (16, 4096, 2048, 128, 0),
     (3, 11008, 256, 128, 0),    # 16 warps, about 90 KiB of staged rows
     (12, 2048, 1056, 2048, 7),
+    # more strips per CTA than warps, scale records too small to hold a
+    # finished strip: finished strips in a region of their own
+    (1, 512, 640, 128, 1),
+    (6, 1024, 1280, 128, 2),
+    # more strips per CTA than warps, finished strips over their scale records
+    (2, 2048, 1024, 128, 2),
+    (10, 4096, 2048, 128, 3),
+    # 16 rows of K = 5120 over 864 pairs: fits only with the strips over the rows
+    (16, 5120, 27648, 128, 0),
 ]
 
 
