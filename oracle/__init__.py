@@ -62,6 +62,15 @@ _SIGS = {
     "oracle_silu": (ctypes.c_double, [ctypes.c_double]),
     "oracle_silu_mul": (None, [_P, _P, _I, _I, _P, _P]),
     "oracle_check_bound": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "oracle_bf16_to_double": (ctypes.c_double, [ctypes.c_uint16]),
+    "oracle_double_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+    "oracle_doubles_to_bf16": (None, [_P, _SZ, _P]),
+    "oracle_bf16s_to_double": (None, [_P, _SZ, _P]),
+    "oracle_dequantize_bf16": (None, [_P, _P, _P, _I, _I, _I, _P]),
+    "oracle_matmul_bf16": (None, [_P, _P, _I, _I, _I, _P, _P]),
+    "oracle_check_bf16": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "oracle_silu_mul_bf16": (None, [_P, _P, _I, _I, _P, _P]),
+    "oracle_check_bound_bf16": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
 }
 
 
@@ -229,4 +238,102 @@ def check_bound(Y, ref: np.ndarray, bound: np.ndarray) -> Tuple[float, int]:
     assert Y.shape == ref.shape == bound.shape
     wi = _SZ(0)
     r = lib().oracle_check_bound(_ptr(Y), _ptr(ref), _ptr(bound), Y.size, ctypes.byref(wi))
+    return float(r), int(wi.value)
+
+
+# ---------------------------------------------------------------- bf16
+# compressed-tensors PR #269 "Some fixes for AWQ": W4A16 keeps the
+# activations as unquantized 16-bit floats, and a reply names an API taking
+# fp32, bf16 or fp16 activations. Readings (see w4a16_oracle.c): A and Y
+# bf16 with the same quantized weights; dequant = RNE_bf16((q - z) * s16);
+# tolerance 2^-6 * sum|a*w| + 1e-3 (four units of bf16 rounding).
+
+def _as_u16(a) -> np.ndarray:
+    a = np.asarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return np.ascontiguousarray(a)
+
+
+def to_bf16(x) -> np.ndarray:
+    """Round doubles to bfloat16 (ties to even); returns uint16 bit patterns."""
+    x = np.asarray(x, dtype=np.float64)
+    shape = x.shape
+    x = np.ascontiguousarray(x.reshape(-1))
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_doubles_to_bf16(_ptr(x), x.size, _ptr(out))
+    return out.reshape(shape)
+
+
+def from_bf16(h) -> np.ndarray:
+    """Exact value of bfloat16 bit patterns as doubles."""
+    h = np.asarray(h)
+    shape = h.shape
+    h = _as_u16(h.reshape(-1))
+    out = np.empty(h.shape, dtype=np.float64)
+    lib().oracle_bf16s_to_double(_ptr(h), h.size, _ptr(out))
+    return out.reshape(shape)
+
+
+def dequantize_bf16(q: np.ndarray, s: np.ndarray, z: np.ndarray, group: int) -> np.ndarray:
+    """(q, s, z) -> deq bf16 bits u16 [K, N] = RNE_bf16((q - z) * s)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _as_half_bits(s)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    K, N = q.shape
+    assert s.shape == (K // group, N) and z.shape == s.shape
+    deq = np.empty((K, N), np.uint16)
+    lib().oracle_dequantize_bf16(_ptr(q), _ptr(s), _ptr(z), K, N, group, _ptr(deq))
+    return deq
+
+
+def matmul_bf16(A, B) -> Tuple[np.ndarray, np.ndarray]:
+    """bf16 A [M,K] times bf16 B [K,N] in fp64 -> (y [M,N], sum|a*b| [M,N])."""
+    A = _as_u16(A)
+    B = _as_u16(B)
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    y = np.empty((M, N), np.float64)
+    mag = np.empty((M, N), np.float64)
+    lib().oracle_matmul_bf16(_ptr(A), _ptr(B), M, N, K, _ptr(y), _ptr(mag))
+    return y, mag
+
+
+def reference_bf16(A, q, s, z, group) -> Tuple[np.ndarray, np.ndarray]:
+    """The layer with bf16 activations: y = A . RNE_bf16(dequant), in fp64."""
+    return matmul_bf16(A, dequantize_bf16(q, s, z, group))
+
+
+def check_bf16(Y, y_ref: np.ndarray, mag: np.ndarray) -> Tuple[float, int]:
+    """max |Y - y_ref| / (2^-6 * mag + 1e-3) over bf16 results, and its index."""
+    Y = _as_u16(Y)
+    y_ref = np.ascontiguousarray(y_ref, dtype=np.float64)
+    mag = np.ascontiguousarray(mag, dtype=np.float64)
+    assert Y.shape == y_ref.shape == mag.shape
+    wi = _SZ(0)
+    r = lib().oracle_check_bf16(_ptr(Y), _ptr(y_ref), _ptr(mag), Y.size, ctypes.byref(wi))
+    return float(r), int(wi.value)
+
+
+def silu_mul_bf16(y: np.ndarray, mag: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """silu_mul of a bf16-activation product, with the bound propagated from
+    the bf16 tolerance."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    mag = np.ascontiguousarray(mag, dtype=np.float64)
+    M, N = y.shape
+    assert N % 2 == 0 and mag.shape == y.shape
+    out = np.empty((M, N // 2), np.float64)
+    bound = np.empty((M, N // 2), np.float64)
+    lib().oracle_silu_mul_bf16(_ptr(y), _ptr(mag), M, N, _ptr(out), _ptr(bound))
+    return out, bound
+
+
+def check_bound_bf16(Y, ref: np.ndarray, bound: np.ndarray) -> Tuple[float, int]:
+    """max |Y - ref| / bound over bf16 results, and its index."""
+    Y = _as_u16(Y)
+    ref = np.ascontiguousarray(ref, dtype=np.float64)
+    bound = np.ascontiguousarray(bound, dtype=np.float64)
+    assert Y.shape == ref.shape == bound.shape
+    wi = _SZ(0)
+    r = lib().oracle_check_bound_bf16(_ptr(Y), _ptr(ref), _ptr(bound), Y.size, ctypes.byref(wi))
     return float(r), int(wi.value)

@@ -376,6 +376,208 @@ double oracle_check_bound(const uint16_t* y_gpu, const double* ref, const double
     return worst;
 }
 
+/* ---------------------------------------------------------------------- */
+/* bf16 activations.                                                        */
+/*                                                                          */
+/* compressed-tensors PR #269 "Some fixes for AWQ": in the naming of the    */
+/* preset schemes, the number after "A" is the activations' width, and     */
+/* W4A16 keeps them as 16-bit floats, unquantized; a reply in the same      */
+/* thread names an API taking fp32, bf16 or fp16 activations.  Readings:    */
+/*   R-bf16    the A16 side may be bfloat16 as well as fp16: A and Y are    */
+/*             bf16, the quantized weights are the same (q, s16, z);       */
+/*   R-dq-bf16 dequant = RNE_bf16((q - z) * s16), one rounding of the exact */
+/*             product (both operands of the multiply-accumulate are bf16); */
+/*   R-tol-bf16 the fp16 tolerance is four units of fp16 rounding (2^-11)   */
+/*             of the magnitude sum; with bf16's unit (2^-8) it becomes     */
+/*             |y - y_ref| <= 2^-6 * sum|a*w| + 1e-3.                       */
+/* bfloat16 is the upper half of a binary32: 1 sign bit, 8 exponent bits    */
+/* with bias 127, 7 fraction bits.                                          */
+/* ---------------------------------------------------------------------- */
+
+double oracle_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);                /* zero or subnormal: f * 2^-126 / 128 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134);     /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest bfloat16, ties to even; overflow -> inf. */
+uint16_t oracle_double_to_bf16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return 0x7fc0;
+    if (isinf(a))
+        return sign | 0x7f80;
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);                  /* a in [2^(ex-1), 2^ex) */
+    int E = ex - 1;
+    if (E < -126)
+        E = -126;                   /* subnormal range: spacing 2^-133 */
+    double spacing = ldexp(1.0, E - 7);
+    double r = nearbyint(a / spacing);   /* ties to even */
+    double v = r * spacing;
+    if (v > ldexp(255.0, 120))      /* beyond the largest finite bf16, (2 - 2^-7) * 2^127 */
+        return sign | 0x7f80;
+    if (v < ldexp(1.0, -126))       /* subnormal (or zero) */
+        return sign | (uint16_t)(v / ldexp(1.0, -133));
+    frexp(v, &ex);
+    E = ex - 1;
+    uint16_t frac = (uint16_t)(v / ldexp(1.0, E - 7) - 128.0);
+    return sign | (uint16_t)((E + 127) << 7) | frac;
+}
+
+void oracle_doubles_to_bf16(const double* x, size_t n, uint16_t* out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = oracle_double_to_bf16(x[i]);
+}
+
+void oracle_bf16s_to_double(const uint16_t* h, size_t n, double* out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_to_double(h[i]);
+}
+
+/* deq[k][n] = RNE_bf16((q - z) * s16): the exact product, rounded once. */
+void oracle_dequantize_bf16(const uint8_t* q, const uint16_t* s16, const uint8_t* z,
+                            int K, int N, int group, uint16_t* deq)
+{
+    #pragma omp parallel for schedule(static)
+    for (int k = 0; k < K; ++k) {
+        int j = k / group;
+        for (int n = 0; n < N; ++n) {
+            int d = (int)q[(size_t)k * N + n] - (int)z[(size_t)j * N + n];
+            double s = oracle_half_to_double(s16[(size_t)j * N + n]);
+            deq[(size_t)k * N + n] = oracle_double_to_bf16((double)d * s);
+        }
+    }
+}
+
+static double bf16_table[65536];
+static int bf16_table_ready = 0;
+
+static void fill_bf16_table(void)
+{
+    if (bf16_table_ready)
+        return;
+    #pragma omp critical(oracle_bf16_table)
+    {
+        if (!bf16_table_ready) {
+            for (int h = 0; h < 65536; ++h)
+                bf16_table[h] = oracle_bf16_to_double((uint16_t)h);
+            bf16_table_ready = 1;
+        }
+    }
+}
+
+/* As oracle_matmul for bf16 A [M][K] and bf16 B [K][N]: y and the magnitude */
+/* sum in fp64, each (m, n) summed over k in order.                          */
+void oracle_matmul_bf16(const uint16_t* A, const uint16_t* B, int M, int N, int K,
+                        double* y, double* mag)
+{
+    enum { NC = 64 };
+    fill_bf16_table();
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int n0 = 0; n0 < N; n0 += NC) {
+        int n1 = n0 + NC < N ? n0 + NC : N;
+        double acc[NC], acc_abs[NC];
+        for (int m = 0; m < M; ++m) {
+            for (int n = n0; n < n1; ++n) {
+                acc[n - n0] = 0.0;
+                acc_abs[n - n0] = 0.0;
+            }
+            for (int k = 0; k < K; ++k) {
+                double a = bf16_table[A[(size_t)m * K + k]];
+                const uint16_t* brow = B + (size_t)k * N;
+                for (int n = n0; n < n1; ++n) {
+                    double p = a * bf16_table[brow[n]];
+                    acc[n - n0] += p;
+                    acc_abs[n - n0] += fabs(p);
+                }
+            }
+            for (int n = n0; n < n1; ++n) {
+                y[(size_t)m * N + n] = acc[n - n0];
+                mag[(size_t)m * N + n] = acc_abs[n - n0];
+            }
+        }
+    }
+}
+
+/* R-tol-bf16: ratio[i] = |y_gpu - y_ref| / (2^-6 * mag + 1e-3), y_gpu bf16. */
+double oracle_check_bf16(const uint16_t* y_gpu, const double* y_ref, const double* mag,
+                         size_t count, size_t* worst_index)
+{
+    double worst = 0.0;
+    size_t wi = 0;
+    for (size_t i = 0; i < count; ++i) {
+        double g = oracle_bf16_to_double(y_gpu[i]);
+        double bound = ldexp(mag[i], -6) + 1e-3;
+        double r = fabs(g - y_ref[i]) / bound;
+        if (!(r <= worst)) {
+            worst = r;
+            wi = i;
+            if (isnan(r))
+                break;
+        }
+    }
+    if (worst_index)
+        *worst_index = wi;
+    return worst;
+}
+
+/* The fused gate/up epilogue of a bf16 product: out as oracle_silu_mul,    */
+/* the bound propagated from R-tol-bf16 (B = 2^-6 * mag + 1e-3) with the    */
+/* output's bf16 rounding and fp32 evaluation as 2^-7 * |out| + 1e-3.       */
+void oracle_silu_mul_bf16(const double* y, const double* mag, int M, int N, double* out,
+                          double* bound)
+{
+    int H = N / 2;
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < H; ++j) {
+            double g = y[(size_t)m * N + j];
+            double u = y[(size_t)m * N + H + j];
+            double bg = ldexp(mag[(size_t)m * N + j], -6) + 1e-3;
+            double bu = ldexp(mag[(size_t)m * N + H + j], -6) + 1e-3;
+            double sg = oracle_silu(g);
+            double o = sg * u;
+            out[(size_t)m * H + j] = o;
+            bound[(size_t)m * H + j] =
+                fabs(sg) * bu + 1.1 * bg * (fabs(u) + bu) + ldexp(fabs(o), -7) + 1e-3;
+        }
+}
+
+/* max |Y - ref| / bound over bf16 results (NaN is the worst), and where. */
+double oracle_check_bound_bf16(const uint16_t* y_gpu, const double* ref, const double* bound,
+                               size_t count, size_t* worst_index)
+{
+    double worst = 0.0;
+    size_t wi = 0;
+    for (size_t i = 0; i < count; ++i) {
+        double r = fabs(oracle_bf16_to_double(y_gpu[i]) - ref[i]) / bound[i];
+        if (!(r <= worst)) {
+            worst = r;
+            wi = i;
+            if (isnan(r))
+                break;
+        }
+    }
+    if (worst_index)
+        *worst_index = wi;
+    return worst;
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

@@ -368,3 +368,111 @@ def test_silu_mul_bound_accepts_rounding_and_rejects_errors():
     assert oracle.check_bound(h, out, bound)[0] <= 1.0
     bad = oracle.to_half(out + 3 * bound)
     assert oracle.check_bound(bad, out, bound)[0] > 1.0
+
+
+# --------------------------------------------------------------- bf16 activations
+
+def _torch():
+    return pytest.importorskip("torch")
+
+
+def test_from_bf16_all_patterns_match_torch():
+    torch = _torch()
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.from_bf16(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_to_bf16_matches_torch_rounding():
+    """Float32 inputs (so no double rounding on torch's side): normal,
+    subnormal, huge and exact-tie values, both signs."""
+    torch = _torch()
+    rng = np.random.default_rng(21)
+    xs = [rng.standard_normal(20000).astype(np.float32),
+          (rng.standard_normal(2000) * 1e-39).astype(np.float32),     # bf16 subnormals
+          rng.uniform(-3.4e38, 3.4e38, 2000).astype(np.float32),       # near overflow
+          np.array([3.4028235e38, -3.4028235e38, 1e-45, 0.0, -0.0], np.float32)]
+    # exact ties: 1 + (2j + 1) 2^-8 lies halfway between bf16 neighbours
+    j = np.arange(128)
+    xs.append(((1.0 + (2 * j + 1) * 2.0 ** -8) * np.where(j % 2, 1.0, -4.0)).astype(np.float32))
+    x = np.concatenate(xs)
+    ours = oracle.to_bf16(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    # the ties went to the even neighbour
+    t = oracle.to_bf16(1.0 + 2.0 ** -8)
+    assert t == 0x3F80 and oracle.to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82
+
+
+def test_dequantize_bf16_matches_torch():
+    """RNE_bf16((q - z) * s16): the product is exact in float32 (4 x 11
+    significant bits), so torch's float32 -> bf16 rounding is the reference."""
+    torch = _torch()
+    K, N, group = 256, 48, 64
+    q, s, z = oracle.quantize(synthetic.small_weights(K, N, seed=22), group)
+    deq = oracle.dequantize_bf16(q, s, z, group)
+    sf = oracle.from_half(s).astype(np.float32)
+    d = (q.astype(np.int32) - np.repeat(z, group, axis=0).astype(np.int32)).astype(np.float32)
+    prod = d * np.repeat(sf, group, axis=0)
+    ref = torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(deq, ref)
+    # and it is the fp16 dequantization rounded again only where bf16 is coarser
+    d16 = oracle.from_half(oracle.dequantize(q, s, z, group))
+    assert np.all(np.abs(oracle.from_bf16(deq) - d16) <= 2.0 ** -8 * np.abs(d16) + 2.0 ** -11 * np.abs(d16))
+
+
+def test_matmul_bf16_brute_force_tiny():
+    rng = np.random.default_rng(23)
+    for (M, K, N) in [(1, 1, 1), (2, 3, 4), (4, 17, 3)]:
+        A = oracle.to_bf16(rng.standard_normal((M, K)))
+        B = oracle.to_bf16(rng.standard_normal((K, N)) * 0.1)
+        y, mag = oracle.matmul_bf16(A, B)
+        Av, Bv = oracle.from_bf16(A), oracle.from_bf16(B)
+        for m in range(M):
+            for n in range(N):
+                ex, exm = _exact_dot(Av[m], Bv[:, n])
+                assert abs(y[m, n] - float(ex)) <= 1e-13 * float(exm) + 1e-300
+                assert abs(mag[m, n] - float(exm)) <= 1e-13 * float(exm)
+
+
+def test_integer_closed_form_bf16():
+    """s = 1, z = 8 and small integer bf16 activations give an exact integer product."""
+    K, N, M, group = 256, 24, 3, 128
+    rng = np.random.default_rng(24)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 0x3C00, np.uint16)          # fp16 1.0
+    Ai = rng.integers(-4, 5, (M, K))
+    A = oracle.to_bf16(Ai)
+    y, _ = oracle.reference_bf16(A, q, s, z, group)
+    assert np.array_equal(y, (Ai @ (q.astype(np.int64) - 8)).astype(np.float64))
+
+
+def test_check_bf16_pins_its_bound():
+    K, N, group = 256, 32, 128
+    q, s, z = oracle.quantize(synthetic.small_weights(K, N, seed=25), group)
+    A = oracle.to_bf16(synthetic.small_activations(3, K, seed=25).astype(np.float64))
+    y, mag = oracle.reference_bf16(A, q, s, z, group)
+    Y = oracle.to_bf16(y)
+    assert oracle.check_bf16(Y, y, mag)[0] <= 0.25      # one bf16 rounding: at most 2^-9 |y|
+    # the bound is 2^-6 mag + 1e-3: a value just inside passes, just outside fails
+    b = 2.0 ** -6 * mag[2, 7] + 1e-3
+    for f, ok in ((0.98, True), (1.02, False)):
+        ref = y.copy()
+        ref[2, 7] = oracle.from_bf16(Y[2, 7]) - f * b
+        assert (oracle.check_bf16(Y, ref, mag)[0] <= 1.0) == ok
+
+
+def test_silu_mul_bf16_bound():
+    rng = np.random.default_rng(26)
+    y = rng.normal(size=(4, 64)) * 3
+    mag = np.abs(y) * 4
+    out, bound = oracle.silu_mul_bf16(y, mag)
+    out16, bound16 = oracle.silu_mul(y, mag)
+    assert np.array_equal(out, out16)                   # the same epilogue
+    assert np.all(bound > bound16)                      # under a looser product bound
+    assert oracle.check_bound_bf16(oracle.to_bf16(out), out, bound)[0] <= 1.0
+    assert oracle.check_bound_bf16(oracle.to_bf16(out + 3 * bound), out, bound)[0] > 1.0
