@@ -29,6 +29,7 @@ _PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR,
           "decode-resident": PATH_DECODE_RESIDENT, "decode-streamk": PATH_DECODE_STREAMK}
 STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
 SILU_MUL = 0x200        # W4A16_SILU_MUL
+BF16 = 0x400            # W4A16_BF16
 
 ERRORS = {
     -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
@@ -49,6 +50,7 @@ SIGNATURES = {
     "w4a16_pack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "w4a16_unpack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "w4a16_dequantize": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "w4a16_dequantize_bf16": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "w4a16_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
     "w4a16_workspace_size_ex": (_I, [_I, _I, _I, _I, _I, _I, _PSZ]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -172,11 +174,15 @@ def unpack(pw: PackedWeight, stream=None):
     return q, s, z
 
 
-def dequantize(pw: PackedWeight, stream=None) -> torch.Tensor:
-    deq = torch.empty((pw.K, pw.N), dtype=torch.float16, device=pw.Wq.device)
-    _check(lib().w4a16_dequantize(pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(), pw.K,
-                                  pw.N, pw.group, deq.data_ptr(), _stream(stream)),
-           "w4a16_dequantize")
+def dequantize(pw: PackedWeight, stream=None, dtype: torch.dtype = torch.float16) -> torch.Tensor:
+    """deq [K, N] = RNE((q - z) * s) in fp16, or in bf16 (the tensor-core
+    path's operand for bf16 activations)."""
+    if dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError(f"dtype must be float16 or bfloat16, got {dtype}")
+    deq = torch.empty((pw.K, pw.N), dtype=dtype, device=pw.Wq.device)
+    fn = lib().w4a16_dequantize_bf16 if dtype == torch.bfloat16 else lib().w4a16_dequantize
+    _check(fn(pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(), pw.K, pw.N, pw.group,
+              deq.data_ptr(), _stream(stream)), "w4a16_dequantize")
     return deq
 
 
@@ -205,7 +211,8 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
          path: str = "auto", parts: int = 0, workspace: Optional[torch.Tensor] = None,
          stream=None, static_weights: bool = False, silu_mul: bool = False) -> torch.Tensor:
-    """Y [M, N] fp16 = A [M, K] fp16 . dequant(pw), on the current stream.
+    """Y [M, N] = A [M, K] . dequant(pw), on the current stream; A and Y are
+    both fp16 or both bf16 (W4A16_BF16, chosen by A's dtype).
 
     `workspace` must be zero-filled before its first use (new_workspace);
     without one, a fresh zeroed buffer is allocated for this call.
@@ -217,20 +224,21 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     M, K = A.shape
     if K != pw.K:
         raise ValueError(f"A has K={K}, weight has K={pw.K}")
+    dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
     if out is None:
-        out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=torch.float16,
-                          device=A.device)
+        out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=dt, device=A.device)
     ws_ptr, ws_bytes = None, 0
     need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul)
     if need:
         if workspace is None:
             workspace = new_workspace(need, A.device)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check(lib().w4a16_gemm_ex(_dev(A, torch.float16, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
+    _check(lib().w4a16_gemm_ex(_dev(A, dt, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
-                               _dev(out, torch.float16, "out"), ws_ptr, ws_bytes,
+                               _dev(out, dt, "out"), ws_ptr, ws_bytes,
                                _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
-                               | (SILU_MUL if silu_mul else 0), parts,
+                               | (SILU_MUL if silu_mul else 0)
+                               | (BF16 if dt == torch.bfloat16 else 0), parts,
                                _stream(stream)), "w4a16_gemm")
     return out
 

@@ -150,7 +150,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                 "alignment: A, Wq, scales, Y need 16 bytes and zeros 8 bytes");
   const bool static_weights = (path & W4A16_STATIC_WEIGHTS) != 0;
   const bool silu = (path & W4A16_SILU_MUL) != 0;
-  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL);
+  const bool bf16 = (path & W4A16_BF16) != 0;
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
@@ -174,9 +175,9 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     uint16_t* prod =
         silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + product_offset(base)) : Y;
     cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
-                                   base > 0 ? workspace : nullptr, stream);
+                                   base > 0 ? workspace : nullptr, bf16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
-    if (silu && (e = launch_silu_mul(prod, M, N, Y, stream)) != cudaSuccess)
+    if (silu && (e = launch_silu_mul(prod, M, N, Y, bf16, stream)) != cudaSuccess)
       return cuda_fail(e, "gate/up epilogue launch");
     return ok();
   }
@@ -214,11 +215,11 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     cudaError_t e;
     if (decode_variant(path, rows, N, K, group, parts, silu, &ctas) == W4A16_PATH_DECODE_RESIDENT) {
       e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, sm_count(),
-                                 path == W4A16_PATH_DECODE, silu, static_weights, stream);
+                                 path == W4A16_PATH_DECODE, silu, static_weights, bf16, stream);
     } else {
       e = launch_decode(Ar, Wq, scales, zeros, silu ? prod : Yr, rows, N, K, group, ctas, workspace,
-                        static_weights, stream);
-      if (e == cudaSuccess && silu) e = launch_silu_mul(prod, rows, N, Yr, stream);
+                        static_weights, bf16, stream);
+      if (e == cudaSuccess && silu) e = launch_silu_mul(prod, rows, N, Yr, bf16, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
@@ -286,7 +287,16 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int group, uint16_t* deq, void* stream) {
   if (int rc = check_kn(K, N, group)) return rc;
   if (!Wq || !Sp || !Zp || !deq) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
-  cudaError_t e = launch_dequantize(Wq, Sp, Zp, K, N, group, deq, (cudaStream_t)stream);
+  cudaError_t e = launch_dequantize(Wq, Sp, Zp, K, N, group, deq, false, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel launch");
+  return ok();
+}
+
+int w4a16_dequantize_bf16(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K, int N,
+                          int group, uint16_t* deq, void* stream) {
+  if (int rc = check_kn(K, N, group)) return rc;
+  if (!Wq || !Sp || !Zp || !deq) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  cudaError_t e = launch_dequantize(Wq, Sp, Zp, K, N, group, deq, true, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel launch");
   return ok();
 }
@@ -301,7 +311,7 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   const bool silu = (path & W4A16_SILU_MUL) != 0;
-  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL);
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);

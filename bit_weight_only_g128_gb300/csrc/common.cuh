@@ -10,6 +10,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -72,6 +73,47 @@ __device__ __forceinline__ void dequant_word(uint32_t w, const DeqConst& c, uint
   out[1] = hmul2_rn(hsub2_rn(x1, c.zb), c.s2);
   out[2] = hmul2_rn(hfma2_rn(x2, kSixteenth, c.nzb4), c.s2);
   out[3] = hmul2_rn(hfma2_rn(x3, kSixteenth, c.nzb4), c.s2);
+}
+
+// Per (group, column) constants of the bf16 dequantization of one column.
+struct DeqConstBf16 {
+  float s;    // the fp16 scale, exact in fp32
+  float nzs;  // -(128 + z) * s, exact (8 x 11 significant bits)
+};
+
+__device__ __forceinline__ DeqConstBf16 make_deq_const_bf16(uint32_t z, uint16_t s_bits) {
+  DeqConstBf16 c;
+  c.s = __half2float(__ushort_as_half(s_bits));
+  c.nzs = -(float)(128u + z) * c.s;
+  return c;
+}
+
+// One packed word -> four bf16x2 values out[p] = (deq[2p], deq[2p+1]) with
+// deq = RNE_bf16((q - z) * s). Nibble p of the word lands in bits 16..19 of
+// an fp32 whose other bits are those of 128.0, which makes the fp32 value
+// 128 + q (the unit bit of 128's mantissa is bit 16). Then
+// (128 + q) s - (128 + z) s is one fma of exact operands whose exact result,
+// (q - z) s with at most 15 significant bits, is representable: the fma
+// returns it unrounded, and the conversion to bf16 is the only rounding.
+__device__ __forceinline__ float code_plus_128(uint32_t w, int p) {
+  const uint32_t nib = p <= 4 ? (w << (16 - 4 * p)) : (w >> (4 * p - 16));
+  return __uint_as_float((nib & 0x000F0000u) | 0x43000000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void dequant_word_bf16(uint32_t w, const DeqConstBf16& c, uint32_t out[4]) {
+  float v[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) v[p] = fmaf(code_plus_128(w, p), c.s, c.nzs);
+  // nibble p holds k-offset rev3(p): k 0..7 are nibbles 0 4 2 6 1 5 3 7
+  out[0] = bf16x2_rn(v[0], v[4]);
+  out[1] = bf16x2_rn(v[2], v[6]);
+  out[2] = bf16x2_rn(v[1], v[5]);
+  out[3] = bf16x2_rn(v[3], v[7]);
 }
 
 // ------------------------------------------------------------------ loads

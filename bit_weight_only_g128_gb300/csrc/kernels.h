@@ -1,5 +1,6 @@
 // Launchers of the W4A16 kernels (host side). Arguments are validated by the
-// C ABI layer (api.cu) before any of these is called.
+// C ABI layer (api.cu) before any of these is called. Activations and
+// results are 16-bit floats: fp16, or bf16 where a launcher takes `bf16`.
 #pragma once
 
 #include <cstddef>
@@ -15,8 +16,9 @@ cudaError_t launch_pack(const uint8_t* q, const uint16_t* s, const uint8_t* z, i
 cudaError_t launch_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
                           int N, int group, uint8_t* q, uint16_t* s, uint8_t* z,
                           cudaStream_t stream);
+// deq = RNE((q - z) * s) in fp16, or in bf16 with `bf16`.
 cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
-                              int N, int group, uint16_t* deq, cudaStream_t stream);
+                              int N, int group, uint16_t* deq, bool bf16, cudaStream_t stream);
 
 // Stream-K register-dequant GEMV for M <= 16 rows of A (one launch of `ctas`
 // persistent CTAs, 1 <= ctas <= min(decode_units, kDecodeMaxCtas)).
@@ -26,7 +28,8 @@ cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint
 // wait.
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                          int ctas, void* workspace, bool early_weights, cudaStream_t stream);
+                          int ctas, void* workspace, bool early_weights, bool bf16,
+                          cudaStream_t stream);
 size_t decode_workspace_bytes(int M, int N, int ctas);
 
 // Register-dequant GEMV with the activations resident in shared memory, for
@@ -37,7 +40,7 @@ size_t decode_workspace_bytes(int M, int N, int ctas);
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                                    int ctas, int sms, bool automatic, bool silu,
-                                   bool early_weights, cudaStream_t stream);
+                                   bool early_weights, bool bf16, cudaStream_t stream);
 // CTAs of that kernel (`requested`, else one per resident slot of `sms` SMs:
 // two 8-warp CTAs or one 16-warp CTA per SM; clamped to the strips and to
 // 8192), or 0 when the problem's activations, sums and group pairs do not fit
@@ -45,9 +48,10 @@ cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const 
 // staged activations exceed 160 KiB) or the group is unsupported.
 int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms, bool automatic,
                          bool silu);
-// Y [M][N/2] = silu(Yfull[:, :N/2]) * Yfull[:, N/2:] for an fp16 product
+// Y [M][N/2] = silu(Yfull[:, :N/2]) * Yfull[:, N/2:] for a 16-bit product
 // Yfull [M][N] (row stride N): the fused gate/up epilogue as a separate pass.
-cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, cudaStream_t stream);
+cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, bool bf16,
+                            cudaStream_t stream);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
 // Split granules (128 columns x a group's atoms, at most 8) of a problem: the
@@ -61,7 +65,7 @@ int decode_ctas_per_sm(int M);
 // counters, zero between calls, and the fp32 partial tiles).
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, cudaStream_t stream);
+                           int split, void* workspace, bool bf16, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
 int tc_choose_split(int M, int N, int K, int group, int sms);
 // 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K

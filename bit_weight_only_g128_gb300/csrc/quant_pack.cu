@@ -142,7 +142,9 @@ __global__ void unpack_meta_kernel(const uint16_t* __restrict__ Sp, const uint32
   }
 }
 
-// deq [K][N] from the packed buffers, through dequant_word (the GEMM routine).
+// deq [K][N] from the packed buffers, through dequant_word (kB: the bf16
+// routine dequant_word_bf16), the tensor-core GEMM's routines.
+template <bool kB>
 __global__ void dequantize_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __restrict__ Sp,
                                   const uint32_t* __restrict__ Zp, int K, int N, int group,
                                   uint16_t* __restrict__ deq) {
@@ -155,9 +157,13 @@ __global__ void dequantize_kernel(const uint32_t* __restrict__ Wq, const uint16_
   const int grp = k0 / group;
   const size_t jg = (size_t)j * G + grp;
   const uint32_t zbyte = reinterpret_cast<const uint8_t*>(Zp)[jg * 8 + (c & 7)];
-  const DeqConst dc = make_deq_const((zbyte >> (4 * (c >> 3))) & 15u, Sp[jg * 16 + 2 * (c & 7) + (c >> 3)]);
+  const uint32_t zc = (zbyte >> (4 * (c >> 3))) & 15u;
+  const uint16_t sc = Sp[jg * 16 + 2 * (c & 7) + (c >> 3)];
   uint32_t pairs[4];
-  dequant_word(Wq[widx], dc, pairs);
+  if (kB)
+    dequant_word_bf16(Wq[widx], make_deq_const_bf16(zc, sc), pairs);
+  else
+    dequant_word(Wq[widx], make_deq_const(zc, sc), pairs);
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     deq[(size_t)(k0 + 2 * p) * N + n] = (uint16_t)(pairs[p] & 0xffffu);
@@ -196,9 +202,12 @@ cudaError_t launch_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t
 }
 
 cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K,
-                              int N, int group, uint16_t* deq, cudaStream_t stream) {
+                              int N, int group, uint16_t* deq, bool bf16, cudaStream_t stream) {
   const size_t words = (size_t)K * N / 8;
-  dequantize_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(Wq, Sp, Zp, K, N, group, deq);
+  if (bf16)
+    dequantize_kernel<true><<<blocks_for(words, 256), 256, 0, stream>>>(Wq, Sp, Zp, K, N, group, deq);
+  else
+    dequantize_kernel<false><<<blocks_for(words, 256), 256, 0, stream>>>(Wq, Sp, Zp, K, N, group, deq);
   return cudaGetLastError();
 }
 

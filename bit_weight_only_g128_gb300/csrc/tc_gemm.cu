@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -210,11 +212,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 D [4,6) = 1, fp16 A
-// and B [7,10) = [10,13) = 0, both K-major [15] = [16] = 0, N >> 3 at
-// [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 D [4,6) = 1, A and
+// B types [7,10) and [10,13) (0 fp16, 1 bf16; both alike), both K-major
+// [15] = [16] = 0, N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n, bool bf16) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+// fp32 -> 16-bit result bits (fp16, or bf16 with kB), round to nearest even.
+template <bool kB>
+__device__ __forceinline__ uint16_t to_out(float v) {
+  if (kB) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+template <bool kB>
+__device__ __forceinline__ uint32_t to_out2(float lo, float hi) {
+  if (kB) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -239,7 +258,7 @@ __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;"
 // SA: atoms (64 k) per pipeline stage, 1 or 2. A stage of two atoms halves
 // the barrier hand-offs per weight byte; it needs an even number of atoms
 // and groups of at least 128 (one scale and zero point per stage).
-template <int SA>
+template <int SA, bool kB>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const TcParams p) {
@@ -319,7 +338,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = f16_idesc(kTileN, bt);
+      const uint32_t idesc = f16_idesc(kTileN, bt, kB);
       bool ok = true;
       int s = 0;
       uint32_t ph = 0;
@@ -401,8 +420,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int i = 0; i < 4; ++i) {
         const int ls = groups * sub + i;  // strip within the tile
         if (i < groups && n0 / kStripCols + ls < nstrips) {
-          const DeqConst d0 = make_deq_const(mz[i] & 15u, (uint16_t)(ms[i] & 0xffffu));
-          const DeqConst d1 = make_deq_const((mz[i] >> 4) & 15u, (uint16_t)(ms[i] >> 16));
+          const uint32_t z0 = mz[i] & 15u, z1 = (mz[i] >> 4) & 15u;
+          const uint16_t s0 = (uint16_t)(ms[i] & 0xffffu), s1 = (uint16_t)(ms[i] >> 16);
 #pragma unroll
           for (int u = 0; u < SA; ++u) {
           const uint32_t wdq = st + wdq_off + u * kWdqBytes;
@@ -413,7 +432,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
             const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
             uint32_t o[4];
-            dequant_word(word, r ? d1 : d0, o);
+            if (kB)
+              dequant_word_bf16(word, make_deq_const_bf16(r ? z1 : z0, r ? s1 : s0), o);
+            else
+              dequant_word(word, make_deq_const(r ? z1 : z0, r ? s1 : s0), o);
             // row n = 16 ls + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
             const uint32_t row = 16u * ls + gq + 8u * r;
             const uint32_t kw = 4u * ks + t;
@@ -455,7 +477,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int j = 0; j < 16; ++j) {
             const int tok = m0 + 16 * c + j;
             if (tok < p.M)
-              p.Y[(size_t)tok * p.N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
+              p.Y[(size_t)tok * p.N + n] = to_out<kB>(__uint_as_float(r[j]));
           }
         }
       }
@@ -506,11 +528,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int e = e0 + u * kDqThreads;
             const int tok = m0 + e / (kTileN / 4), n = n0 + (e % (kTileN / 4)) * 4;
             if (e < n4 && tok < p.M && n < p.N) {
-              const __half2 lo = __floats2half2_rn(acc[u].x, acc[u].y);
-              const __half2 hi = __floats2half2_rn(acc[u].z, acc[u].w);
               uint2 o;
-              o.x = *reinterpret_cast<const uint32_t*>(&lo);
-              o.y = *reinterpret_cast<const uint32_t*>(&hi);
+              o.x = to_out2<kB>(acc[u].x, acc[u].y);
+              o.y = to_out2<kB>(acc[u].z, acc[u].w);
               *reinterpret_cast<uint2*>(p.Y + (size_t)tok * p.N + n) = o;
             }
           }
@@ -646,7 +666,7 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
 
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, cudaStream_t stream) {
+                           int split, void* workspace, bool bf16, cudaStream_t stream) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const int bt = tc_token_tile(M);
@@ -657,7 +677,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)bt};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box,
+    if (encode(&tmA, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -691,20 +711,30 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(227 * 1024));
+    const int kMax = 227 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(227 * 1024));
+      e = cudaFuncSetAttribute(tc_gemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
                   (unsigned)prm.split);
-  if (sa == 2)
-    tc_gemm_kernel<2><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
-  else
-    tc_gemm_kernel<1><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  if (bf16) {
+    if (sa == 2)
+      tc_gemm_kernel<2, true><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+    else
+      tc_gemm_kernel<1, true><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  } else {
+    if (sa == 2)
+      tc_gemm_kernel<2, false><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+    else
+      tc_gemm_kernel<1, false><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
+  }
   return cudaGetLastError();
 }
 

@@ -119,6 +119,20 @@ extern "C" {
  * cores) and a second kernel forms Y from it;
  * w4a16_workspace_size_ex with this flag counts those bytes. */
 #define W4A16_SILU_MUL 0x200
+/* Flag OR-ed into the path of w4a16_gemm_ex (and accepted, with no effect on
+ * the sizes, by w4a16_workspace_size_ex): A and Y hold bfloat16 instead of
+ * fp16 (compressed-tensors PR #269 "Some fixes for AWQ": W4A16 keeps the
+ * activations as unquantized 16-bit floats, and a reply names an API taking
+ * fp32, bf16 or fp16 activations). The quantized weights are the same
+ * buffers (fp16 scales). The tensor-core path multiplies bf16 activations by
+ * RNE_bf16((q - z) * s) (w4a16_dequantize_bf16 gives the same values); the
+ * decode path takes the codes exactly and applies s and z per group in fp32;
+ * both accumulate in fp32 and round the result once to bf16. Accuracy
+ * contract: |y - y_ref| <= 2^-6 * sum_k |a_k w_kn| + 1e-3 against the fp64
+ * product of the same bf16 activations and bf16-dequantized weights (four
+ * units of bf16 rounding, as the fp16 bound is four of fp16). Combines with
+ * the other flags; w4a16_gemm_noalloc has no bf16 form. */
+#define W4A16_BF16 0x400
 
 /* Message for the last error returned on the calling thread ("" if none). */
 const char* w4a16_last_error(void);
@@ -154,6 +168,11 @@ int w4a16_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
  * with the same device routine the GEMM kernels use (for checks). */
 int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int K, int N, int group, uint16_t* deq, void* stream);
+
+/* As w4a16_dequantize with deq in bfloat16: RNE_bf16((q - z)*s), the
+ * operand the tensor-core path builds for bf16 activations (W4A16_BF16). */
+int w4a16_dequantize_bf16(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
+                          int K, int N, int group, uint16_t* deq, void* stream);
 
 /* Scratch bytes w4a16_gemm needs for this problem on the current device
  * (0 when none). Work split across CTAs is combined through it: the decode
@@ -196,8 +215,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * of 128 and the token tile leaves room for four 128-k stages). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
  * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
- * W4A16_STATIC_WEIGHTS and W4A16_SILU_MUL (see above; with the latter Y is
- * [M][N/2]); any other bit is W4A16_ERR_INVALID_ARG. */
+ * W4A16_STATIC_WEIGHTS, W4A16_SILU_MUL and W4A16_BF16 (see above; with
+ * W4A16_SILU_MUL Y is [M][N/2]); any other bit is W4A16_ERR_INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,

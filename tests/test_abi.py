@@ -94,7 +94,12 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
     assert _gemm(lib, path=5) == -1
-    assert _gemm(lib, path=0x400 | 1) == -1           # unknown flag bit
+    assert _gemm(lib, path=0x800 | 1) == -1           # unknown flag bit
+    # bf16 activations: the same host checks (the stream-K variant still
+    # needs its workspace)
+    assert _gemm(lib, path=0x400 | 4, ws=0) == -4
+    assert _gemm(lib, path=0x400 | 1, N=40) == -2
+    assert _gemm(lib, path=0x400 | 3, M=16, K=16384, ws=0) == -2
     # fused gate/up epilogue: N must be two halves of whole strips, and a
     # path that does not fuse it keeps the product in the workspace
     assert _gemm(lib, path=0x200 | 1, N=48) == -2
@@ -174,7 +179,18 @@ def test_silu_mul_workspace_sizes(lib):
         for path in ("decode", "decode-streamk"):
             assert w4.workspace_size(M, 4096, 4096, 128, path=path, parts=10,
                                      silu_mul=True) == (base + 255) // 256 * 256 + rows * 4096 * 2
-    assert w4.SILU_MUL == 0x200
+    assert w4.SILU_MUL == 0x200 and w4.BF16 == 0x400
+    assert re.search(r"#define W4A16_BF16 0x400\b", open(HEADER).read())
+    # bf16 activations change no size
+    for path, parts in (("tensor", 3), ("decode", 10), ("decode-streamk", 10)):
+        b = ctypes.c_size_t()
+        for flags in (0, 0x200):
+            assert lib.w4a16_workspace_size_ex(16, 4096, 4096, 128, w4._PATHS[path] | flags, parts,
+                                               ctypes.byref(b)) == 0
+            plain = b.value
+            assert lib.w4a16_workspace_size_ex(16, 4096, 4096, 128, w4._PATHS[path] | flags | 0x400,
+                                               parts, ctypes.byref(b)) == 0
+            assert b.value == plain
     assert re.search(r"#define W4A16_SILU_MUL 0x200\b", open(HEADER).read())
 
 
