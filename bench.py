@@ -69,7 +69,7 @@ def peaks():
 # ncu summaries under profiles/: the dominant kernel of a workload, the sources
 # that build it, and the summary holding its DRAM bytes per launch
 PROFILED = {
-    1: ("decode_resident_kernel", ["decode.cu", "common.cuh"],
+    1: ("decode_resident_kernel", ["decode_impl.cuh", "decode.cu", "common.cuh"],
         "decode_resident_kernel_llama2-7b-decode.md"),
     3: ("tc_gemm_kernel", ["tc_gemm.cu", "common.cuh"], "tc_gemm_kernel_llama2-7b-prefill.md"),
 }
@@ -298,7 +298,7 @@ def _aligned_views(torch, shapes, dtype, device):
     return flat, [flat[o:o + math.prod(s)].view(*s) for o, s in zip(offs, shapes)]
 
 
-def build_gpu_workload(wl, torch, w4, device, copies=None):
+def build_gpu_workload(wl, torch, w4, device, copies=None, act="f16"):
     cases = [Case(*c) for c in wl.cases()]
     layers = {}
     for c in cases:
@@ -313,8 +313,10 @@ def build_gpu_workload(wl, torch, w4, device, copies=None):
     for _ in range(copies - 1):
         rot.append({k: w4.PackedWeight(pw.Wq.clone(), pw.Sp.clone(), pw.Zp.clone(), pw.K, pw.N,
                                        pw.group) for k, pw in layers.items()})
-    a_flat, a_views = _aligned_views(torch, [(c.M, c.K) for c in cases], torch.float16, device)
-    y_flat, y_views = _aligned_views(torch, [(c.M, c.N) for c in cases], torch.float16, device)
+    # activations and results: fp16, or bf16 (the fp16 inputs rounded to bf16)
+    adt = torch.bfloat16 if act == "bf16" else torch.float16
+    a_flat, a_views = _aligned_views(torch, [(c.M, c.K) for c in cases], adt, device)
+    y_flat, y_views = _aligned_views(torch, [(c.M, c.N) for c in cases], adt, device)
     # one workspace serves every call: they run one after another on one stream
     ws = w4.new_workspace(max(w4.workspace_size(c.M, c.N, c.K, c.group) for c in cases), device)
     for r in rot:
@@ -338,9 +340,14 @@ def sanity_check(wl, cases, rot, a_views, y_views, torch, w4):
         cols = synthetic.sample_indices(c.N, 32, seed=0, salt=c.N)
         W = synthetic.weights(wl.cfg, c.K, c.N)[:, cols]
         q, s, z = oracle.quantize(np.ascontiguousarray(W), c.group)
-        y, mag = oracle.reference(A.cpu().numpy(), q, s, z, c.group)
-        got = Y.cpu().numpy().view(np.uint16)[:, cols]
-        ratio, _ = oracle.check(np.ascontiguousarray(got), y, mag)
+        got = np.ascontiguousarray(Y.cpu().view(torch.int16).numpy().view(np.uint16)[:, cols])
+        a_bits = A.cpu().view(torch.int16).numpy().view(np.uint16)
+        if A.dtype == torch.bfloat16:
+            y, mag = oracle.reference_bf16(a_bits, q, s, z, c.group)
+            ratio, _ = oracle.check_bf16(got, y, mag)
+        else:
+            y, mag = oracle.reference(a_bits, q, s, z, c.group)
+            ratio, _ = oracle.check(got, y, mag)
         if not ratio <= 1.0:
             raise SystemExit(f"parity check failed for {c.layer} M={c.M}: err/bound {ratio}")
 
@@ -392,7 +399,7 @@ def silu_mul_times(torch, w4, cases, rot, a_views, stream, reps=20):
     for c, A in zip(cases, a_views):
         if c.layer != "gate_up":
             continue
-        Y = torch.empty((c.M, c.N // 2), dtype=torch.float16, device=A.device)
+        Y = torch.empty((c.M, c.N // 2), dtype=A.dtype, device=A.device)
         ws = w4.new_workspace(w4.workspace_size(c.M, c.N, c.K, c.group, silu_mul=True), A.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -438,7 +445,7 @@ def run_ours(args, wl, dist, rank, world, local):
     torch.cuda.set_device(device)
     pk = peaks()
     cases, rot, (a_flat, a_views), (y_flat, y_views), packed_bytes = build_gpu_workload(
-        wl, torch, w4, device, args.copies)
+        wl, torch, w4, device, args.copies, args.act)
     sanity_check(wl, cases, rot, a_views, y_views, torch, w4)
 
     stream = torch.cuda.Stream(device)
@@ -479,9 +486,10 @@ def run_ours(args, wl, dist, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.act,
         "data": "synthetic",
         "config": {**workload_config(wl),
+                   "activations": args.act,
                    "static_weights": True,
                    "l2": (f"inputs larger than L2: {len(rot)} rotating copies of the packed "
                           f"weights, {len(rot) * packed_bytes / 2**20:.0f} MiB")},
@@ -501,8 +509,8 @@ def run_ours(args, wl, dist, rank, world, local):
                 roof, bound = roofline_us(c.M, c.K, c.N, c.group, pk)
                 path, parts = w4.plan(c.M, c.N, c.K, c.group)
                 f.write(json.dumps({
-                    "workload": wl.name, "layer": c.layer, "M": c.M, "K": c.K, "N": c.N,
-                    "group": c.group, "path": path, "parts": parts, "us": 1e6 * t,
+                    "workload": wl.name, "act": args.act, "layer": c.layer, "M": c.M, "K": c.K,
+                    "N": c.N, "group": c.group, "path": path, "parts": parts, "us": 1e6 * t,
                     "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
                     "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
                     "bound": bound, "frac": roof / (1e6 * t)}) + "\n")
@@ -510,7 +518,7 @@ def run_ours(args, wl, dist, rank, world, local):
                 # the fused layer writes half the columns
                 nbytes = alg_bytes(c.M, c.K, c.N, c.group) - c.M * c.N
                 f.write(json.dumps({
-                    "workload": wl.name, "layer": "gate_up+silu_mul", "M": c.M, "K": c.K,
+                    "workload": wl.name, "act": args.act, "layer": "gate_up+silu_mul", "M": c.M, "K": c.K,
                     "N": c.N, "group": c.group, "us": 1e6 * t, "GBps": nbytes / t / 1e9,
                     "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12}) + "\n")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -529,6 +537,8 @@ def main():
     ap.add_argument("--copies", type=int, default=None, help="weight copies for L2 rotation")
     ap.add_argument("--sweep", default=None, help="append per-case timings (JSONL) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--act", choices=("f16", "bf16"), default="f16",
+                    help="activation type (bf16: W4A16_BF16, the same weights)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     wl = synthetic.workload(args.workload)

@@ -89,31 +89,28 @@ __device__ __forceinline__ DeqConstBf16 make_deq_const_bf16(uint32_t z, uint16_t
 }
 
 // One packed word -> four bf16x2 values out[p] = (deq[2p], deq[2p+1]) with
-// deq = RNE_bf16((q - z) * s). Nibble p of the word lands in bits 16..19 of
-// an fp32 whose other bits are those of 128.0, which makes the fp32 value
-// 128 + q (the unit bit of 128's mantissa is bit 16). Then
-// (128 + q) s - (128 + z) s is one fma of exact operands whose exact result,
-// (q - z) s with at most 15 significant bits, is representable: the fma
-// returns it unrounded, and the conversion to bf16 is the only rounding.
-__device__ __forceinline__ float code_plus_128(uint32_t w, int p) {
-  const uint32_t nib = p <= 4 ? (w << (16 - 4 * p)) : (w >> (4 * p - 16));
-  return __uint_as_float((nib & 0x000F0000u) | 0x43000000u);
-}
-
+// deq = RNE_bf16((q - z) * s). Each code becomes the fp32 128 + q: byte
+// permutes put a byte 0x0q (the nibbles masked apart: even nibbles in place,
+// odd ones shifted down) under the bytes 0x43 and 0x00 of 128.0's bit
+// pattern, where its unit bit is bit 16. Then (128 + q) s - (128 + z) s is
+// one fma of exact operands whose exact result, (q - z) s with at most 15
+// significant bits, is representable: the fma returns it unrounded, and the
+// conversion to bf16 is the only rounding.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ void dequant_word_bf16(uint32_t w, const DeqConstBf16& c, uint32_t out[4]) {
-  float v[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) v[p] = fmaf(code_plus_128(w, p), c.s, c.nzs);
-  // nibble p holds k-offset rev3(p): k 0..7 are nibbles 0 4 2 6 1 5 3 7
-  out[0] = bf16x2_rn(v[0], v[4]);
-  out[1] = bf16x2_rn(v[2], v[6]);
-  out[2] = bf16x2_rn(v[1], v[5]);
-  out[3] = bf16x2_rn(v[3], v[7]);
+  const uint32_t t = w & 0x0F0F0F0Fu;         // bytes: nibbles 0 2 4 6 = k 0 2 1 3
+  const uint32_t u = (w >> 4) & 0x0F0F0F0Fu;  // bytes: nibbles 1 3 5 7 = k 4 6 5 7
+  constexpr uint32_t kHi = 0x00000043u;       // byte 4 = 0x43, bytes 5..7 = 0
+  auto f = [&](uint32_t x, uint32_t sel) { return fmaf(__uint_as_float(__byte_perm(x, kHi, sel)), c.s, c.nzs); };
+  // selector: result bytes (0, 0, byte b of x, 0x43) = 0x4b55
+  out[0] = bf16x2_rn(f(t, 0x4055), f(t, 0x4255));  // k 0, 1
+  out[1] = bf16x2_rn(f(t, 0x4155), f(t, 0x4355));  // k 2, 3
+  out[2] = bf16x2_rn(f(u, 0x4055), f(u, 0x4255));  // k 4, 5
+  out[3] = bf16x2_rn(f(u, 0x4155), f(u, 0x4355));  // k 6, 7
 }
 
 // ------------------------------------------------------------------ loads

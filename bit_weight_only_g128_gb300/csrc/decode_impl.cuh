@@ -206,19 +206,24 @@ __device__ __forceinline__ void mma_first(float (&d)[4], uint32_t a0, uint32_t a
 // The four code pairs of one packed word (nibble p holds k-offset rev3(p)).
 // fp16: as fp16x2 subnormals, c[0] = (k 0,1) and c[1] = (k 2,3) hold
 // q * 2^-24, c[2] = (k 4,5) and c[3] = (k 6,7) hold 16 q * 2^-24. bf16 (kB):
-// as bf16x2 normals 128 + q, every pair alike (the low 4 of a bf16's 7
-// fraction bits at exponent 2^7 count units, so the OR is exact); the
-// offset 128 is taken out with the group's sums.
+// as bf16x2 normals 128 + q, every pair alike: a byte 0x0q under a high
+// byte 0x43 is the bf16 128 + q (the low 4 of its 7 fraction bits count
+// units at exponent 2^7). The even nibbles (one mask) and the odd ones (a
+// shift and a mask) are paired with the 0x43 bytes by byte permutes; the
+// offset 128 is taken out with the group's sums. (Written as shifts, masks
+// and ORs, the same extraction measured 13-35% slower on the 7B decode
+// layers.)
 template <bool kB>
 __device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&c)[4]) {
-  const uint32_t w8 = w >> 8;
   if (kB) {
-    constexpr uint32_t k128 = 0x43004300u;  // bf16x2 (128, 128)
-    c[0] = (w & 0x000F000Fu) | k128;
-    c[1] = (w8 & 0x000F000Fu) | k128;
-    c[2] = ((w >> 4) & 0x000F000Fu) | k128;
-    c[3] = ((w8 >> 4) & 0x000F000Fu) | k128;
+    const uint32_t t = w & 0x0F0F0F0Fu;         // nibbles 0 2 4 6 (k 0 2 1 3)
+    const uint32_t u = (w >> 4) & 0x0F0F0F0Fu;  // nibbles 1 3 5 7 (k 4 6 5 7)
+    c[0] = __byte_perm(t, 0x43434343u, 0x4240);  // (k 0, k 1)
+    c[1] = __byte_perm(t, 0x43434343u, 0x4341);  // (k 2, k 3)
+    c[2] = __byte_perm(u, 0x43434343u, 0x4240);  // (k 4, k 5)
+    c[3] = __byte_perm(u, 0x43434343u, 0x4341);  // (k 6, k 7)
   } else {
+    const uint32_t w8 = w >> 8;
     c[0] = w & 0x000F000Fu;
     c[1] = w8 & 0x000F000Fu;
     c[2] = w & 0x00F000F0u;
