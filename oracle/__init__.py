@@ -71,6 +71,8 @@ _SIGS = {
     "oracle_check_bf16": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
     "oracle_silu_mul_bf16": (None, [_P, _P, _I, _I, _P, _P]),
     "oracle_check_bound_bf16": (ctypes.c_double, [_P, _P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "oracle_quantize_act": (None, [_P, _I, _I, _P, _P]),
+    "oracle_reference_a8": (None, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 
@@ -337,3 +339,38 @@ def check_bound_bf16(Y, ref: np.ndarray, bound: np.ndarray) -> Tuple[float, int]
     wi = _SZ(0)
     r = lib().oracle_check_bound_bf16(_ptr(Y), _ptr(ref), _ptr(bound), Y.size, ctypes.byref(wi))
     return float(r), int(wi.value)
+
+
+# ---------------------------------------------------------------- W4A8
+# compressed-tensors PR #269, the Arm example: fp16 in, activations quantized
+# to 8 bits inside the operation, 8-bit x 4-bit product, fp16 out (lmdeploy
+# issue #2274: W4A8 with online activation quantization). Readings (see
+# w4a16_oracle.c): dynamic symmetric per-token int8, s_a = amax/127 in fp32,
+# integer group dot products scaled per group and per row.
+
+def quantize_act(A_values: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Activation values [M, K] (exact fp16/bf16 values as doubles) ->
+    (a_q int8 [M, K], s_a float32 [M])."""
+    A = np.ascontiguousarray(A_values, dtype=np.float64)
+    M, K = A.shape
+    aq = np.empty((M, K), np.int8)
+    sa = np.empty((M,), np.float32)
+    lib().oracle_quantize_act(_ptr(A), M, K, _ptr(aq), _ptr(sa))
+    return aq, sa
+
+
+def reference_a8(aq, sa, q, s, z, group) -> Tuple[np.ndarray, np.ndarray]:
+    """y = s_a * sum_g s * sum_k a_q (q - z) and its magnitude sum, in fp64."""
+    aq = np.ascontiguousarray(aq, dtype=np.int8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _as_half_bits(s)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    M, K = aq.shape
+    N = q.shape[1]
+    assert q.shape == (K, N) and s.shape == (K // group, N) and z.shape == s.shape and sa.shape == (M,)
+    y = np.empty((M, N), np.float64)
+    mag = np.empty((M, N), np.float64)
+    lib().oracle_reference_a8(_ptr(aq), _ptr(sa), _ptr(q), _ptr(s), _ptr(z), M, N, K, group,
+                              _ptr(y), _ptr(mag))
+    return y, mag

@@ -578,6 +578,76 @@ double oracle_check_bound_bf16(const uint16_t* y_gpu, const double* ref, const d
     return worst;
 }
 
+/* ---------------------------------------------------------------------- */
+/* W4A8: activations quantized to 8 bits inside the operation.             */
+/*                                                                          */
+/* compressed-tensors PR #269 "Some fixes for AWQ", the Arm contributor's   */
+/* example: the operation takes fp16 activations, quantizes them to 8 bits  */
+/* internally, multiplies 8-bit activations by the 4-bit weights and        */
+/* returns fp16 (lmdeploy issue #2274: W4A8 with online activation          */
+/* quantization).  The pages give no formula.  Readings:                    */
+/*   R-a8      dynamic, symmetric, per token (row): amax = max_k |a[m,k]|,  */
+/*             s_a = amax / 127 and a_q = clamp(round(a / s_a), -127, 127), */
+/*             all in IEEE fp32 (the inputs are exact in fp32), round half  */
+/*             to even; a row of zeros has s_a = 1 and a_q = 0;             */
+/*   R-a8-dot  y[m,n] = s_a[m] * sum_groups s[g,n] * sum_k a_q (q - z): the  */
+/*             8-bit by 4-bit products and their group sums are integers,  */
+/*             scaled once per group and once per row; fp64 here;           */
+/*   R-a8-tol  the result is fp16 (or bf16), checked with the bound of the  */
+/*             16-bit product of the same type, with sum |a*w| taken as     */
+/*             s_a * sum |a_q (q - z) s|.                                   */
+/* ---------------------------------------------------------------------- */
+
+/* A: the activations' values [M][K] (fp16 or bf16, exact as doubles). */
+void oracle_quantize_act(const double* A, int M, int K, int8_t* aq, float* s_a)
+{
+    for (int m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float v = fabsf((float)A[(size_t)m * K + k]);
+            if (v > amax)
+                amax = v;
+        }
+        float s = amax > 0.0f ? amax / 127.0f : 1.0f;
+        s_a[m] = s;
+        for (int k = 0; k < K; ++k) {
+            float r = nearbyintf((float)A[(size_t)m * K + k] / s);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            aq[(size_t)m * K + k] = (int8_t)r;
+        }
+    }
+}
+
+/* y[m][n] = s_a[m] * sum_g s16[g][n] * sum_{k in g} aq[m][k] (q[k][n] - z[g][n]) */
+/* in fp64, and mag = s_a[m] * sum_k |aq (q - z) s16|.                       */
+void oracle_reference_a8(const int8_t* aq, const float* s_a, const uint8_t* q,
+                         const uint16_t* s16, const uint8_t* z, int M, int N, int K,
+                         int group, double* y, double* mag)
+{
+    const int G = K / group;
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int g = 0; g < G; ++g) {
+                long long dot = 0, dot_abs = 0;
+                int zz = z[(size_t)g * N + n];
+                for (int k = g * group; k < (g + 1) * group; ++k) {
+                    long long p = (long long)aq[(size_t)m * K + k] *
+                                  ((int)q[(size_t)k * N + n] - zz);
+                    dot += p;
+                    dot_abs += p < 0 ? -p : p;
+                }
+                double sg = oracle_half_to_double(s16[(size_t)g * N + n]);
+                acc += sg * (double)dot;
+                acc_abs += sg * (double)dot_abs;
+            }
+            y[(size_t)m * N + n] = (double)s_a[m] * acc;
+            mag[(size_t)m * N + n] = (double)s_a[m] * acc_abs;
+        }
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

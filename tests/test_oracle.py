@@ -476,3 +476,66 @@ def test_silu_mul_bf16_bound():
     assert np.all(bound > bound16)                      # under a looser product bound
     assert oracle.check_bound_bf16(oracle.to_bf16(out), out, bound)[0] <= 1.0
     assert oracle.check_bound_bf16(oracle.to_bf16(out + 3 * bound), out, bound)[0] > 1.0
+
+
+# --------------------------------------------------------------- W4A8
+
+def test_quantize_act_grid_rows_are_exact():
+    """Rows c * k with integer k in [-127, 127] reaching 127 and c a power of
+    two: amax / 127 = c exactly, so the codes are k and the scale is c."""
+    rng = np.random.default_rng(31)
+    k = rng.integers(-127, 128, (6, 200))
+    k[:, 17] = np.where(np.arange(6) % 2, 127, -127)
+    c = 2.0 ** np.array([-12, -6, -1, 0, 3, 5])[:, None]
+    aq, sa = oracle.quantize_act(k * c)
+    assert np.array_equal(aq, k) and np.array_equal(sa.astype(np.float64), c[:, 0])
+
+
+def test_quantize_act_error_bound_and_invariants():
+    A = oracle.from_half(oracle.to_half(synthetic.small_activations(9, 512, seed=32, outliers=True)
+                                        .astype(np.float64)))
+    aq, sa = oracle.quantize_act(A)
+    # each value within half a step (plus the fp32 rounding of the scale)
+    err = np.abs(A - sa[:, None].astype(np.float64) * aq)
+    assert np.all(err <= 0.5 * sa[:, None] * (1 + 2.0 ** -20))
+    # the largest magnitude of each row maps to +-127, and |a_q| <= 127
+    i = np.argmax(np.abs(A), axis=1)
+    assert np.all(np.abs(aq[np.arange(9), i]) == 127) and np.abs(aq.astype(int)).max() == 127
+    # odd in a, and a power-of-two factor scales s_a only
+    aq2, sa2 = oracle.quantize_act(-A)
+    assert np.array_equal(aq2, -aq) and np.array_equal(sa2, sa)
+    aq3, sa3 = oracle.quantize_act(A * 8.0)
+    assert np.array_equal(aq3, aq) and np.array_equal(sa3, sa * 8)
+    # a zero row: codes 0, scale 1
+    aq4, sa4 = oracle.quantize_act(np.zeros((2, 64)))
+    assert np.all(aq4 == 0) and np.all(sa4 == 1.0)
+
+
+def test_reference_a8_integer_closed_form():
+    K, N, M, group = 256, 24, 3, 128
+    rng = np.random.default_rng(33)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 0x3C00, np.uint16)          # 1.0
+    aq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    y, mag = oracle.reference_a8(aq, np.ones(M, np.float32), q, s, z, group)
+    exact = aq.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.array_equal(y, exact.astype(np.float64))
+    assert np.array_equal(mag, (np.abs(aq.astype(np.int64)) @ np.abs(q.astype(np.int64) - 8)).astype(np.float64))
+
+
+def test_reference_a8_against_the_16_bit_reference():
+    """s_a times the fp16 reference of the codes (exact in fp16) differs from
+    the W4A8 reference only by the fp16 rounding of each dequantized weight."""
+    K, N, M, group = 512, 40, 4, 128
+    q, s, z = oracle.quantize(synthetic.small_weights(K, N, seed=34), group)
+    A = synthetic.small_activations(M, K, seed=34).astype(np.float64)
+    aq, sa = oracle.quantize_act(A)
+    y8, m8 = oracle.reference_a8(aq, sa, q, s, z, group)
+    y16, m16 = oracle.reference(aq.astype(np.float16), q, s, z, group)
+    sa64 = sa[:, None].astype(np.float64)
+    assert np.all(np.abs(y8 - sa64 * y16) <= 2.0 ** -11 * m8 + 1e-12)
+    assert np.allclose(m8, sa64 * m16, rtol=2.0 ** -10)
+    # and the quantized product is close to the unquantized one
+    y, mag = oracle.reference(A.astype(np.float16), q, s, z, group)
+    assert np.all(np.abs(y8 - y) <= 0.02 * mag + 1e-3)
