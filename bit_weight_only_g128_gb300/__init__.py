@@ -30,6 +30,7 @@ _PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR,
 STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
 SILU_MUL = 0x200        # W4A16_SILU_MUL
 BF16 = 0x400            # W4A16_BF16
+ACT_A8 = 0x800          # W4A16_ACT_A8
 
 ERRORS = {
     -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
@@ -51,6 +52,7 @@ SIGNATURES = {
     "w4a16_unpack": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "w4a16_dequantize": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "w4a16_dequantize_bf16": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "w4a16_quantize_act": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "w4a16_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
     "w4a16_workspace_size_ex": (_I, [_I, _I, _I, _I, _I, _I, _PSZ]),
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -187,10 +189,10 @@ def dequantize(pw: PackedWeight, stream=None, dtype: torch.dtype = torch.float16
 
 
 def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0,
-                   silu_mul: bool = False) -> int:
+                   silu_mul: bool = False, a8: bool = False) -> int:
     """Scratch bytes a gemm call with these arguments needs."""
     b = ctypes.c_size_t()
-    flags = SILU_MUL if silu_mul else 0
+    flags = (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
     _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path] | flags, parts,
                                          ctypes.byref(b)), "w4a16_workspace_size")
     return b.value
@@ -210,7 +212,8 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
          path: str = "auto", parts: int = 0, workspace: Optional[torch.Tensor] = None,
-         stream=None, static_weights: bool = False, silu_mul: bool = False) -> torch.Tensor:
+         stream=None, static_weights: bool = False, silu_mul: bool = False,
+         a8: bool = False) -> torch.Tensor:
     """Y [M, N] = A [M, K] . dequant(pw), on the current stream; A and Y are
     both fp16 or both bf16 (W4A16_BF16, chosen by A's dtype).
 
@@ -219,7 +222,8 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     `static_weights` (W4A16_STATIC_WEIGHTS): the kernel may read pw while the
     work queued before it on the stream drains; pw must not be written by
     that work. `silu_mul` (W4A16_SILU_MUL): pw's columns are [gate | up] and
-    Y [M, N/2] = silu(gate) * up.
+    Y [M, N/2] = silu(gate) * up. `a8` (W4A16_ACT_A8): W4A8, the activations
+    are quantized per row to int8 inside the call.
     """
     M, K = A.shape
     if K != pw.K:
@@ -228,7 +232,7 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     if out is None:
         out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=dt, device=A.device)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul, a8)
     if need:
         if workspace is None:
             workspace = new_workspace(need, A.device)
@@ -237,10 +241,23 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
                                _dev(out, dt, "out"), ws_ptr, ws_bytes,
                                _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
-                               | (SILU_MUL if silu_mul else 0)
+                               | (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
                                | (BF16 if dt == torch.bfloat16 else 0), parts,
                                _stream(stream)), "w4a16_gemm")
     return out
+
+
+def quantize_act(A: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """W4A8 activation quantization: A [M, K] fp16/bf16 -> (a_q int8 [M, K],
+    s_a float32 [M]), the rule W4A16_ACT_A8 applies inside gemm."""
+    M, K = A.shape
+    dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
+    aq = torch.empty((M, K), dtype=torch.int8, device=A.device)
+    sa = torch.empty((M,), dtype=torch.float32, device=A.device)
+    _check(lib().w4a16_quantize_act(_dev(A, dt, "A"), M, K, BF16 if dt == torch.bfloat16 else 0,
+                                    aq.data_ptr(), sa.data_ptr(), _stream(stream)),
+           "w4a16_quantize_act")
+    return aq, sa
 
 
 def gemm_noalloc(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,

@@ -1,0 +1,110 @@
+// W4A8: the dynamic per-token quantization of the activations to 8 bits
+// (compressed-tensors PR #269, the Arm example: 16-bit activations in, 8-bit
+// activations inside the operation; lmdeploy issue #2274: W4A8 with online
+// activation quantization). Per row m: amax = max_k |a|, s_a = amax / 127
+// (1 for a row of zeros), a_q = clamp(round(a / s_a), -127, 127), in IEEE
+// fp32 with round-half-to-even: the divisions are __fdiv_rn, so the codes do
+// not depend on compiler flags.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kQThreads = 256;
+
+template <bool kIn>
+__device__ __forceinline__ float act_value(uint32_t bits16) {
+  return kIn ? __bfloat162float(__ushort_as_bfloat16((unsigned short)bits16))
+             : __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
+// One CTA per row; each thread reads 8 activations (16 bytes) at a time.
+// kIn: bf16 input; kCodes: the codes as bf16 (else fp16) integer values.
+template <bool kIn, bool kCodes>
+__global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t* __restrict__ A, int K,
+                                                                 int8_t* __restrict__ aq,
+                                                                 uint16_t* __restrict__ codes,
+                                                                 float* __restrict__ s_a) {
+  __shared__ float wmax[kQThreads / 32];
+  const int m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(A + (size_t)m * K);
+  const int nv = K / 8;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < nv; i += kQThreads) {
+    const uint4 v = row[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, fabsf(act_value<kIn>(w[j] & 0xffffu)));
+      amax = fmaxf(amax, fabsf(act_value<kIn>(w[j] >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = wmax[0];
+#pragma unroll
+  for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, wmax[i]);
+  const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+  if (threadIdx.x == 0) s_a[m] = s;
+  for (int i = threadIdx.x; i < nv; i += kQThreads) {
+    const uint4 v = row[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float r[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      r[2 * j] = act_value<kIn>(w[j] & 0xffffu);
+      r[2 * j + 1] = act_value<kIn>(w[j] >> 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = fminf(fmaxf(rintf(__fdiv_rn(r[j], s)), -127.f), 127.f);
+    if (aq) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= ((uint32_t)(int)r[j] & 0xffu) << (8 * j);
+        hi |= ((uint32_t)(int)r[4 + j] & 0xffu) << (8 * j);
+      }
+      reinterpret_cast<uint2*>(aq + (size_t)m * K)[i] = make_uint2(lo, hi);
+    }
+    if (codes) {
+      uint32_t c[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (kCodes) {
+          const __nv_bfloat162 b = __floats2bfloat162_rn(r[2 * j], r[2 * j + 1]);
+          c[j] = *reinterpret_cast<const uint32_t*>(&b);
+        } else {
+          const __half2 h = __floats2half2_rn(r[2 * j], r[2 * j + 1]);
+          c[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      reinterpret_cast<uint4*>(codes + (size_t)m * K)[i] = make_uint4(c[0], c[1], c[2], c[3]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const uint16_t* A, int M, int K, bool in_bf16, int8_t* aq,
+                                uint16_t* codes, bool codes_bf16, float* s_a, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  if (in_bf16) {
+    if (codes_bf16)
+      quantize_act_kernel<true, true><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
+    else
+      quantize_act_kernel<true, false><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
+  } else {
+    if (codes_bf16)
+      quantize_act_kernel<false, true><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
+    else
+      quantize_act_kernel<false, false><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

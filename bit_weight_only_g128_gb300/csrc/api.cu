@@ -108,29 +108,58 @@ int tc_split(int M, int N, int K, int group, int requested) {
   return s < 1 ? 1 : s;
 }
 
-// The decode path's size covers either variant (the resident one uses none),
-// so that it does not depend on which one a device picks. With the fused
-// gate/up epilogue, a path that does not fuse it (stream-K, tensor cores)
-// also holds the fp16 product of the rows of one launch ([rows][N]; all M
-// rows for tensor cores, 16 for the decode path) at product_offset: after
-// the path's own scratch, and never inside the 32 KiB flag/counter area that
-// every call must leave zero-filled (a launch without a K split has no
-// scratch of its own, but a later call may use the area).
+// Workspace of a call: the path's own scratch first (the decode path's size
+// covers either variant, so that it does not depend on which one a device
+// picks; the resident one uses none). Then, never inside the 32 KiB
+// flag/counter area that every call must leave zero-filled (a launch without
+// a K split has no scratch of its own, but a later call may use the area),
+// each at a 256-byte boundary:
+//   - with the fused gate/up epilogue on a path that does not fuse it
+//     (stream-K, tensor cores), the fp16 product of the rows of one launch
+//     ([rows][N]; all M rows for tensor cores, 16 for the decode path);
+//   - with W4A8, the activations' codes as 16-bit integer values [M][K] and
+//     their per-row scales [M] (fp32).
 constexpr size_t kFlagAreaBytes = 32768;
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 size_t product_offset(size_t base) { return align256(base > kFlagAreaBytes ? base : kFlagAreaBytes); }
 
-size_t workspace_for(int M, int N, int K, int group, int path, int parts, bool silu) {
-  if (M == 0) return 0;
+struct WsLayout {
+  size_t base;    // the path's own scratch
+  size_t prod;    // fused epilogue's product (0: none)
+  size_t codes;   // W4A8 codes (0: none)
+  size_t scales;  // W4A8 row scales
+  size_t total;
+};
+
+WsLayout ws_layout(int M, int N, int K, int group, int path, bool silu, bool a8, int parts) {
+  WsLayout l = {0, 0, 0, 0, 0};
+  if (M == 0) return l;
+  int prod_rows = 0;
   if (path == W4A16_PATH_TENSOR) {
-    const size_t base = tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
-    return silu ? product_offset(base) + (size_t)M * N * 2 : base;
+    l.base = tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
+    prod_rows = M;
+  } else if (is_decode(path) && path != W4A16_PATH_DECODE_RESIDENT) {
+    const int rows = M < 16 ? M : 16;
+    const int c = decode_ctas(rows, N, K, group, parts);
+    l.base = c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
+    prod_rows = rows;
   }
-  if (path == W4A16_PATH_DECODE_RESIDENT || !is_decode(path)) return 0;
-  const int rows = M < 16 ? M : 16;
-  const int c = decode_ctas(rows, N, K, group, parts);
-  const size_t base = c > 0 ? decode_workspace_bytes(rows, N, c) : 0;
-  return silu ? product_offset(base) + (size_t)rows * N * 2 : base;
+  size_t end = l.base;
+  if (silu && prod_rows > 0) {
+    l.prod = product_offset(end);
+    end = l.prod + (size_t)prod_rows * N * 2;
+  }
+  if (a8) {
+    l.codes = product_offset(end);
+    l.scales = align256(l.codes + (size_t)M * K * 2);
+    end = l.scales + (size_t)M * sizeof(float);
+  }
+  l.total = end;
+  return l;
+}
+
+size_t workspace_for(int M, int N, int K, int group, int path, int parts, bool silu, bool a8 = false) {
+  return ws_layout(M, N, K, group, path, silu, a8, parts).total;
 }
 
 int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
@@ -151,11 +180,24 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   const bool static_weights = (path & W4A16_STATIC_WEIGHTS) != 0;
   const bool silu = (path & W4A16_SILU_MUL) != 0;
   const bool bf16 = (path & W4A16_BF16) != 0;
-  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16);
+  const bool a8 = (path & W4A16_ACT_A8) != 0;
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16 | W4A16_ACT_A8);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
+  // W4A8: quantize the activations into the workspace, then multiply the
+  // codes and scale each row of the result (launched once the workspace is
+  // checked, below)
+  const float* row_scale = nullptr;
+  auto quantize_activations = [&](const WsLayout& l) -> cudaError_t {
+    uint16_t* codes = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + l.codes);
+    float* sc = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.scales);
+    cudaError_t e = launch_quantize_act(A, M, K, bf16, nullptr, codes, bf16, sc, stream);
+    A = codes;
+    row_scale = sc;
+    return e;
+  };
   if (silu && N % 32 != 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE,
                 "fused gate/up epilogue: N=%d is not two halves of 16-column strips "
@@ -163,19 +205,20 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   const int ycols = silu ? N / 2 : N;  // columns of Y
   if (path == W4A16_PATH_TENSOR) {
     const int split = tc_split(M, N, K, group, parts);
-    const size_t base = tc_workspace_bytes(M, N, split);
-    const size_t need = workspace_for(M, N, K, group, path, parts, silu);
+    const WsLayout l = ws_layout(M, N, K, group, path, silu, a8, parts);
+    const size_t need = l.total;
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
                   "tensor-core path (K split %d) needs a workspace of %zu bytes (got %zu)", split,
                   need, workspace ? workspace_bytes : (size_t)0);
     if (need > 0 && !aligned(workspace, 256))
       return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+    cudaError_t e = a8 ? quantize_activations(l) : cudaSuccess;
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
     // with the fused epilogue the product goes to the workspace first
-    uint16_t* prod =
-        silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + product_offset(base)) : Y;
-    cudaError_t e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
-                                   base > 0 ? workspace : nullptr, bf16, stream);
+    uint16_t* prod = silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + l.prod) : Y;
+    e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
+                       l.base > 0 ? workspace : nullptr, bf16, row_scale, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     if (silu && (e = launch_silu_mul(prod, M, N, Y, bf16, stream)) != cudaSuccess)
       return cuda_fail(e, "gate/up epilogue launch");
@@ -196,29 +239,31 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   "CTAs) do not fit a CTA's shared memory",
                   rows, K, N, parts > 0 ? parts : 2 * sm_count());
   }
-  const size_t need = workspace_for(M, N, K, group, path, parts, silu);
+  const WsLayout l = ws_layout(M, N, K, group, path, silu, a8, parts);
+  const size_t need = l.total;
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(W4A16_ERR_WORKSPACE_TOO_SMALL, "decode path needs a workspace of %zu bytes (got %zu)",
                 need, workspace ? workspace_bytes : (size_t)0);
   if (need > 0 && !aligned(workspace, 256))
     return fail(W4A16_ERR_MISALIGNED, "workspace needs 256-byte alignment");
+  if (a8) {
+    cudaError_t e = quantize_activations(l);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+  }
   // the stream-K variant's product, with the fused epilogue, before silu * up
-  uint16_t* prod =
-      silu && need > 0
-          ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) +
-                                        product_offset(workspace_for(M, N, K, group, path, parts, false)))
-          : nullptr;
+  uint16_t* prod = l.prod ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + l.prod) : nullptr;
   for (int r0 = 0; r0 < M; r0 += 16) {
     const int rows = M - r0 < 16 ? M - r0 : 16;
     const uint16_t* Ar = A + (size_t)r0 * K;
     uint16_t* Yr = Y + (size_t)r0 * ycols;
+    const float* rs = row_scale ? row_scale + r0 : nullptr;
     cudaError_t e;
     if (decode_variant(path, rows, N, K, group, parts, silu, &ctas) == W4A16_PATH_DECODE_RESIDENT) {
       e = launch_decode_resident(Ar, Wq, scales, zeros, Yr, rows, N, K, group, ctas, sm_count(),
-                                 path == W4A16_PATH_DECODE, silu, static_weights, bf16, stream);
+                                 path == W4A16_PATH_DECODE, silu, static_weights, bf16, rs, stream);
     } else {
       e = launch_decode(Ar, Wq, scales, zeros, silu ? prod : Yr, rows, N, K, group, ctas, workspace,
-                        static_weights, bf16, stream);
+                        static_weights, bf16, rs, stream);
       if (e == cudaSuccess && silu) e = launch_silu_mul(prod, rows, N, Yr, bf16, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
@@ -292,6 +337,21 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
   return ok();
 }
 
+int w4a16_quantize_act(const uint16_t* A, int M, int K, int flags, int8_t* aq, float* s_a,
+                       void* stream) {
+  if (M < 0 || K < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d, K=%d: negative", M, K);
+  if (flags & ~W4A16_BF16) return fail(W4A16_ERR_INVALID_ARG, "flags=0x%x: only W4A16_BF16", flags);
+  if (K % 8 != 0) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 8", K);
+  if (M == 0) return ok();
+  if (!A || !aq || !s_a) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(A, 16) || !aligned(aq, 16) || !aligned(s_a, 4))
+    return fail(W4A16_ERR_MISALIGNED, "alignment: A and aq need 16 bytes, s_a 4");
+  cudaError_t e = launch_quantize_act(A, M, K, (flags & W4A16_BF16) != 0, aq, nullptr, false, s_a,
+                                      (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+  return ok();
+}
+
 int w4a16_dequantize_bf16(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp, int K, int N,
                           int group, uint16_t* deq, void* stream) {
   if (int rc = check_kn(K, N, group)) return rc;
@@ -311,13 +371,14 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
   if (int rc = check_kn(K, N, group)) return rc;
   if (!bytes) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
   const bool silu = (path & W4A16_SILU_MUL) != 0;
-  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16);
+  const bool a8 = (path & W4A16_ACT_A8) != 0;
+  path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16 | W4A16_ACT_A8);
   if (path == W4A16_PATH_AUTO) path = choose_path(M);
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (silu && N % 32 != 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "fused gate/up epilogue: N=%d is not a multiple of 32", N);
-  *bytes = workspace_for(M, N, K, group, path, parts, silu);
+  *bytes = workspace_for(M, N, K, group, path, parts, silu, a8);
   return ok();
 }
 

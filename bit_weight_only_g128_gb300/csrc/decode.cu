@@ -83,8 +83,9 @@ size_t decode_workspace_bytes(int M, int N, int ctas) {
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int ctas, void* workspace, bool early_weights, bool bf16,
-                          cudaStream_t stream) {
-  DecodeArgs args;
+                          const float* row_scale, cudaStream_t stream) {
+  DecodeArgs args = {};
+  args.row_scale = row_scale;
   int apg_t = 0;
   if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
   args.A = A;
@@ -156,7 +157,8 @@ int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms,
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                                    int ctas, int sms, bool automatic, bool silu,
-                                   bool early_weights, bool bf16, cudaStream_t stream) {
+                                   bool early_weights, bool bf16, const float* row_scale,
+                                   cudaStream_t stream) {
   DecodeArgs args = {};
   int apg_t = 0, bytes = 0, nw = 0;
   if (!group_shape(K, group, &apg_t, &args.gshift)) return cudaErrorInvalidValue;
@@ -174,6 +176,7 @@ cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const 
   args.N = N;
   args.K = K;
   args.early_weights = early_weights ? 1 : 0;
+  args.row_scale = row_scale;
   const int mt = M <= 8 ? 1 : 2;
   return bf16 ? decode_dispatch_resident_bf16(args, mt, nw, apg_t, ctas, bytes, stream)
               : dispatch_resident<false>(args, mt, nw, apg_t, ctas, bytes, stream);

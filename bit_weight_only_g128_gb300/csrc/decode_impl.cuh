@@ -86,7 +86,12 @@ struct DecodeArgs {
   // then has at most two segments, and finished strips go through the
   // warps' partial slots too); else a region of their own
   int silu, ytile_off, ytile_stride, whole_in_red;
+  // W4A8: per-row factors of the result (the activations' scales), or null
+  const float* row_scale;
 };
+
+// The row factor of token `tok` (1 without one).
+__device__ __forceinline__ float row_factor(const float* rs, int tok) { return rs ? rs[tok] : 1.0f; }
 
 // The bf16-activation instantiations live in their own translation unit.
 cudaError_t decode_dispatch_resident_bf16(const DecodeArgs& args, int mt, int nw, int apg_t, int ctas,
@@ -608,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
           if (col0 + col < N)
-            p.Y[(size_t)tok * N + col0 + col] = to_act<kB>(red[tok * kRedStride + col]);
+            p.Y[(size_t)tok * N + col0 + col] =
+                to_act<kB>(red[tok * kRedStride + col] * row_factor(p.row_scale, tok));
         }
       } else if (head) {
         // finish the block: the later contributors' tiles, in CTA order
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
           const int e = threadIdx.x + k * kThreads;
           const int col = e & (kDecodeBlockCols - 1);
           if (e < total && col0 + col < N)
-            p.Y[(size_t)(e >> 7) * N + col0 + col] = to_act<kB>(v[k]);
+            p.Y[(size_t)(e >> 7) * N + col0 + col] = to_act<kB>(v[k] * row_factor(p.row_scale, e >> 7));
         }
       } else {
         // a run that starts inside block b: publish the partial tile, then
@@ -884,11 +890,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tok = 8 * o + 2 * t + (j & 1);
+        if (tok >= M) continue;  // rows past M hold nothing (the zero row)
+        const float val = v[o][j] * scale * row_factor(p.row_scale, tok);
         if (kSilu)
-          ytile[s * p.ytile_stride + tok * kStripCols + gq + 8 * (j >> 1)] = v[o][j] * scale;
-        else if (tok < M)
-          p.Y[(size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1)] =
-              to_act<kB>(v[o][j] * scale);
+          ytile[s * p.ytile_stride + tok * kStripCols + gq + 8 * (j >> 1)] = val;
+        else
+          p.Y[(size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1)] = to_act<kB>(val);
       }
   };
   constexpr float kUnscale = unscale<kB>();

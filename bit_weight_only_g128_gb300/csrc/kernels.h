@@ -1,6 +1,8 @@
 // Launchers of the W4A16 kernels (host side). Arguments are validated by the
 // C ABI layer (api.cu) before any of these is called. Activations and
 // results are 16-bit floats: fp16, or bf16 where a launcher takes `bf16`.
+// GEMM launchers take `row_scale`: per-row factors applied to the fp32
+// result before its rounding (W4A8: the activations' scales), or null.
 #pragma once
 
 #include <cstddef>
@@ -29,7 +31,7 @@ cudaError_t launch_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint
 cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                           int ctas, void* workspace, bool early_weights, bool bf16,
-                          cudaStream_t stream);
+                          const float* row_scale, cudaStream_t stream);
 size_t decode_workspace_bytes(int M, int N, int ctas);
 
 // Register-dequant GEMV with the activations resident in shared memory, for
@@ -40,7 +42,8 @@ size_t decode_workspace_bytes(int M, int N, int ctas);
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                                    int ctas, int sms, bool automatic, bool silu,
-                                   bool early_weights, bool bf16, cudaStream_t stream);
+                                   bool early_weights, bool bf16, const float* row_scale,
+                                   cudaStream_t stream);
 // CTAs of that kernel (`requested`, else one per resident slot of `sms` SMs:
 // two 8-warp CTAs or one 16-warp CTA per SM; clamped to the strips and to
 // 8192), or 0 when the problem's activations, sums and group pairs do not fit
@@ -52,6 +55,13 @@ int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms,
 // Yfull [M][N] (row stride N): the fused gate/up epilogue as a separate pass.
 cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, bool bf16,
                             cudaStream_t stream);
+// W4A8: per row, s_a = max|a| / 127 (1 for a zero row) and the codes
+// clamp(round(a / s_a), -127, 127), IEEE fp32. A [M][K] is fp16 (bf16 with
+// in_bf16); K a multiple of 8 and A 16-byte aligned. Writes the codes as int8
+// to aq and/or as 16-bit integer values (bf16 with codes_bf16) to `codes`,
+// either may be null; s_a [M].
+cudaError_t launch_quantize_act(const uint16_t* A, int M, int K, bool in_bf16, int8_t* aq,
+                                uint16_t* codes, bool codes_bf16, float* s_a, cudaStream_t stream);
 // Bytes of the counter area at the start of the decode workspace.
 size_t decode_counter_bytes(int N);
 // Split granules (128 columns x a group's atoms, at most 8) of a problem: the
@@ -65,7 +75,8 @@ int decode_ctas_per_sm(int M);
 // counters, zero between calls, and the fp32 partial tiles).
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, bool bf16, cudaStream_t stream);
+                           int split, void* workspace, bool bf16, const float* row_scale,
+                           cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
 int tc_choose_split(int M, int N, int K, int group, int sms);
 // 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K

@@ -104,7 +104,7 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const u
   for (int r0 = 0; e == cudaSuccess && r0 < M; r0 += 16) {
     const int r = M - r0 < 16 ? M - r0 : 16;
     e = launch_decode(A + (size_t)r0 * K, Wq, scales, zeros, Y + (size_t)r0 * N, r, N, K, group,
-                      (int)ctas, scratch, false, false, (cudaStream_t)stream);
+                      (int)ctas, scratch, false, false, nullptr, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) {
     char msg[256];

@@ -250,6 +250,7 @@ struct TcParams {
   int tmem_cols;
   int split;      // K ranges per output tile (grid z)
   int dq_groups;  // dequant warp groups (4, 2 or 1), dividing `stages`
+  const float* row_scale;  // W4A8: per-row factors of the result, or null
 };
 
 // named barrier of the 8 dequant/epilogue warps
@@ -477,7 +478,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int j = 0; j < 16; ++j) {
             const int tok = m0 + 16 * c + j;
             if (tok < p.M)
-              p.Y[(size_t)tok * p.N + n] = to_out<kB>(__uint_as_float(r[j]));
+              p.Y[(size_t)tok * p.N + n] =
+                  to_out<kB>(__uint_as_float(r[j]) * (p.row_scale ? p.row_scale[tok] : 1.0f));
           }
         }
       }
@@ -528,9 +530,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int e = e0 + u * kDqThreads;
             const int tok = m0 + e / (kTileN / 4), n = n0 + (e % (kTileN / 4)) * 4;
             if (e < n4 && tok < p.M && n < p.N) {
+              const float f = p.row_scale ? p.row_scale[tok] : 1.0f;
               uint2 o;
-              o.x = to_out2<kB>(acc[u].x, acc[u].y);
-              o.y = to_out2<kB>(acc[u].z, acc[u].w);
+              o.x = to_out2<kB>(acc[u].x * f, acc[u].y * f);
+              o.y = to_out2<kB>(acc[u].z * f, acc[u].w * f);
               *reinterpret_cast<uint2*>(p.Y + (size_t)tok * p.N + n) = o;
             }
           }
@@ -666,7 +669,8 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
 
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, bool bf16, cudaStream_t stream) {
+                           int split, void* workspace, bool bf16, const float* row_scale,
+                           cudaStream_t stream) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const int bt = tc_token_tile(M);
@@ -703,6 +707,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.group = group;
   prm.bt = bt;
   prm.split = split < 1 ? 1 : split;
+  prm.row_scale = row_scale;
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;

@@ -133,6 +133,22 @@ extern "C" {
  * units of bf16 rounding, as the fp16 bound is four of fp16). Combines with
  * the other flags; w4a16_gemm_noalloc has no bf16 form. */
 #define W4A16_BF16 0x400
+/* Flag OR-ed into the path of w4a16_gemm_ex and w4a16_workspace_size_ex:
+ * W4A8. The 16-bit activations A are quantized to 8 bits inside the call
+ * and the product is 8-bit activations by 4-bit weights (compressed-tensors
+ * PR #269, the Arm example: fp16 in, 8-bit activations inside the
+ * operation, fp16 out; lmdeploy issue #2274: W4A8 with online activation
+ * quantization). Per row m, in IEEE fp32: s_a = max_k |a| / 127 (1 for a row
+ * of zeros) and a_q = clamp(round(a / s_a), -127, 127), ties to even (what
+ * w4a16_quantize_act writes). Then y = s_a * sum_groups s * sum_k a_q (q - z):
+ * the codes enter the tensor cores as exact 16-bit integer values, and s_a
+ * scales the fp32 result before its one rounding. The workspace holds the
+ * codes ([M][K], 16-bit) and the scales after the path's own scratch (and
+ * after the fused epilogue's product), so w4a16_workspace_size_ex must be
+ * asked with the same flags. Accuracy contract: the 16-bit bound of the
+ * result's type with sum |a w| read as s_a * sum |a_q (q - z) s|. Combines
+ * with the other flags. */
+#define W4A16_ACT_A8 0x800
 
 /* Message for the last error returned on the calling thread ("" if none). */
 const char* w4a16_last_error(void);
@@ -168,6 +184,12 @@ int w4a16_unpack(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
  * with the same device routine the GEMM kernels use (for checks). */
 int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
                      int K, int N, int group, uint16_t* deq, void* stream);
+
+/* W4A8 activation quantization (the rule under W4A16_ACT_A8): A [M][K]
+ * 16-bit (fp16, or bf16 with flags = W4A16_BF16) -> aq [M][K] int8 and s_a
+ * [M] fp32. K a multiple of 8; A and aq 16-byte aligned. */
+int w4a16_quantize_act(const uint16_t* A, int M, int K, int flags, int8_t* aq, float* s_a,
+                       void* stream);
 
 /* As w4a16_dequantize with deq in bfloat16: RNE_bf16((q - z)*s), the
  * operand the tensor-core path builds for bf16 activations (W4A16_BF16). */
@@ -215,8 +237,9 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * of 128 and the token tile leaves room for four 128-k stages). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
  * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
- * W4A16_STATIC_WEIGHTS, W4A16_SILU_MUL and W4A16_BF16 (see above; with
- * W4A16_SILU_MUL Y is [M][N/2]); any other bit is W4A16_ERR_INVALID_ARG. */
+ * W4A16_STATIC_WEIGHTS, W4A16_SILU_MUL, W4A16_BF16 and W4A16_ACT_A8 (see
+ * above; with W4A16_SILU_MUL Y is [M][N/2]); any other bit is
+ * W4A16_ERR_INVALID_ARG. */
 int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   const uint32_t* zeros, int M, int N, int K, int group,
                   uint16_t* Y, void* workspace, size_t workspace_bytes,

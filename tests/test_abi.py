@@ -94,7 +94,10 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
     assert _gemm(lib, path=5) == -1
-    assert _gemm(lib, path=0x800 | 1) == -1           # unknown flag bit
+    assert _gemm(lib, path=0x1000 | 1) == -1          # unknown flag bit
+    # W4A8 keeps the activations' codes in the workspace: none given
+    assert _gemm(lib, path=0x800 | 3, ws=0) == -4
+    assert _gemm(lib, path=0x800 | 2, ws=0) == -4
     # bf16 activations: the same host checks (the stream-K variant still
     # needs its workspace)
     assert _gemm(lib, path=0x400 | 4, ws=0) == -4
@@ -192,6 +195,32 @@ def test_silu_mul_workspace_sizes(lib):
                                                parts, ctypes.byref(b)) == 0
             assert b.value == plain
     assert re.search(r"#define W4A16_SILU_MUL 0x200\b", open(HEADER).read())
+
+
+def test_w4a8_workspace_and_quantize_act_errors(lib):
+    head = 32768
+    # codes [M][K] 16-bit then scales [M], after the path's scratch (and at
+    # least after the flag area), at 256-byte boundaries
+    def up(b):
+        return (b + 255) // 256 * 256
+    M, N, K = 16, 4096, 4096
+    assert w4.workspace_size(M, N, K, 128, path="decode-resident", a8=True) == up(head + M * K * 2) + M * 4
+    base = w4.workspace_size(M, N, K, 128, path="tensor", parts=3)
+    assert w4.workspace_size(M, N, K, 128, path="tensor", parts=3, a8=True) == up(up(base) + M * K * 2) + M * 4
+    both = w4.workspace_size(M, N, K, 128, path="decode-streamk", parts=10, silu_mul=True)
+    assert w4.workspace_size(M, N, K, 128, path="decode-streamk", parts=10, silu_mul=True,
+                             a8=True) == up(up(both) + M * K * 2) + M * 4
+    assert w4.workspace_size(40, N, K, 128, path="decode", parts=10, a8=True) == \
+        up(up(w4.workspace_size(40, N, K, 128, path="decode", parts=10)) + 40 * K * 2) + 40 * 4
+    A, Q, S = 0x10000, 0x20000, 0x30000
+    assert lib.w4a16_quantize_act(A, -1, 64, 0, Q, S, None) == -1
+    assert lib.w4a16_quantize_act(A, 4, 60, 0, Q, S, None) == -2
+    assert lib.w4a16_quantize_act(A, 4, 64, 0x200, Q, S, None) == -1
+    assert lib.w4a16_quantize_act(A + 8, 4, 64, 0, Q, S, None) == -3
+    assert lib.w4a16_quantize_act(A, 4, 64, 0, Q + 4, S, None) == -3
+    assert lib.w4a16_quantize_act(None, 4, 64, 0, Q, S, None) == -1
+    assert lib.w4a16_quantize_act(None, 0, 64, 0, None, None, None) == 0
+    assert w4.ACT_A8 == 0x800 and re.search(r"#define W4A16_ACT_A8 0x800\b", open(HEADER).read())
 
 
 def test_path_constants_match_the_header():
