@@ -277,6 +277,10 @@ def run_reference(args, wl, dist, rank, world):
 METRIC = "W4A16-g128 GEMM HBM GB/s (algorithmic bytes / time), % of roofline, 1 GB300"
 
 
+# extra keyword arguments of every timed gemm call (W4A8: {"a8": True})
+GEMM_KW = {}
+
+
 class Case:
     def __init__(self, layer, M, K, N, group):
         self.layer, self.M, self.K, self.N, self.group = layer, M, K, N, group
@@ -318,7 +322,8 @@ def build_gpu_workload(wl, torch, w4, device, copies=None, act="f16"):
     a_flat, a_views = _aligned_views(torch, [(c.M, c.K) for c in cases], adt, device)
     y_flat, y_views = _aligned_views(torch, [(c.M, c.N) for c in cases], adt, device)
     # one workspace serves every call: they run one after another on one stream
-    ws = w4.new_workspace(max(w4.workspace_size(c.M, c.N, c.K, c.group) for c in cases), device)
+    ws = w4.new_workspace(max(w4.workspace_size(c.M, c.N, c.K, c.group, **GEMM_KW) for c in cases),
+                          device)
     for r in rot:
         r["workspace"] = ws
     for c, av in zip(cases, a_views):
@@ -335,14 +340,19 @@ def sanity_check(wl, cases, rot, a_views, y_views, torch, w4):
         if c.key in seen:
             continue
         seen.add(c.key)
-        w4.gemm(A, rot[0][c.key], out=Y, workspace=rot[0]["workspace"])
+        w4.gemm(A, rot[0][c.key], out=Y, workspace=rot[0]["workspace"], **GEMM_KW)
         torch.cuda.synchronize()
         cols = synthetic.sample_indices(c.N, 32, seed=0, salt=c.N)
         W = synthetic.weights(wl.cfg, c.K, c.N)[:, cols]
         q, s, z = oracle.quantize(np.ascontiguousarray(W), c.group)
         got = np.ascontiguousarray(Y.cpu().view(torch.int16).numpy().view(np.uint16)[:, cols])
         a_bits = A.cpu().view(torch.int16).numpy().view(np.uint16)
-        if A.dtype == torch.bfloat16:
+        if GEMM_KW.get("a8"):
+            vals = (oracle.from_bf16 if A.dtype == torch.bfloat16 else oracle.from_half)(a_bits)
+            aq, sa = oracle.quantize_act(vals)
+            y, mag = oracle.reference_a8(aq, sa, q, s, z, c.group)
+            ratio, _ = (oracle.check_bf16 if A.dtype == torch.bfloat16 else oracle.check)(got, y, mag)
+        elif A.dtype == torch.bfloat16:
             y, mag = oracle.reference_bf16(a_bits, q, s, z, c.group)
             ratio, _ = oracle.check_bf16(got, y, mag)
         else:
@@ -356,7 +366,8 @@ def capture_step(torch, w4, cases, weights, a_views, y_views, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for c, A, Y in zip(cases, a_views, y_views):
-            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"], static_weights=True)
+            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"], static_weights=True,
+                    **GEMM_KW)
     return g
 
 
@@ -384,7 +395,7 @@ def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
                 w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=rot[0]["workspace"],
-                        static_weights=True)
+                        static_weights=True, **GEMM_KW)
         time_graphs(torch, [g], 3, stream)
         secs = time_graphs(torch, [g], 5, stream) / (5 * reps)
         out.append(secs)
@@ -400,12 +411,13 @@ def silu_mul_times(torch, w4, cases, rot, a_views, stream, reps=20):
         if c.layer != "gate_up":
             continue
         Y = torch.empty((c.M, c.N // 2), dtype=A.dtype, device=A.device)
-        ws = w4.new_workspace(w4.workspace_size(c.M, c.N, c.K, c.group, silu_mul=True), A.device)
+        ws = w4.new_workspace(w4.workspace_size(c.M, c.N, c.K, c.group, silu_mul=True, **GEMM_KW),
+                              A.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(reps):
                 w4.gemm(A, rot[r % len(rot)][c.key], out=Y, workspace=ws, static_weights=True,
-                        silu_mul=True)
+                        silu_mul=True, **GEMM_KW)
         time_graphs(torch, [g], 3, stream)
         out.append((c, time_graphs(torch, [g], 5, stream) / (5 * reps)))
         del g, ws
@@ -443,9 +455,11 @@ def run_ours(args, wl, dist, rank, world, local):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.act == "a8":
+        GEMM_KW["a8"] = True
     pk = peaks()
     cases, rot, (a_flat, a_views), (y_flat, y_views), packed_bytes = build_gpu_workload(
-        wl, torch, w4, device, args.copies, args.act)
+        wl, torch, w4, device, args.copies, "bf16" if args.act == "bf16" else "f16")
     sanity_check(wl, cases, rot, a_views, y_views, torch, w4)
 
     stream = torch.cuda.Stream(device)
@@ -474,7 +488,7 @@ def run_ours(args, wl, dist, rank, world, local):
         with torch.cuda.graph(g, stream=stream):
             a_flat.copy_(a_host, non_blocking=True)
             for c, A, Y in zip(cases, a_views, y_views):
-                w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"], static_weights=True)
+                w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"], static_weights=True, **GEMM_KW)
             y_host.copy_(y_flat, non_blocking=True)
         e2e_graphs.append(g)
     time_graphs(torch, e2e_graphs, args.warmup, stream)
@@ -499,7 +513,8 @@ def run_ours(args, wl, dist, rank, world, local):
         "e2e": {"value": e2e_value, "unit": "GB/s",
                 "h2d_bytes_per_step": sum(2 * c.M * c.K for c in cases),
                 "d2h_bytes_per_step": sum(2 * c.M * c.N for c in cases)},
-        "gpu_launches": len(cases) * args.steps,
+        # one kernel per GEMM (W4A8: the activation quantization too)
+        "gpu_launches": len(cases) * args.steps * (2 if GEMM_KW.get("a8") else 1),
         "clocks": clocks,
     }
     if args.sweep:
@@ -537,8 +552,9 @@ def main():
     ap.add_argument("--copies", type=int, default=None, help="weight copies for L2 rotation")
     ap.add_argument("--sweep", default=None, help="append per-case timings (JSONL) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--act", choices=("f16", "bf16"), default="f16",
-                    help="activation type (bf16: W4A16_BF16, the same weights)")
+    ap.add_argument("--act", choices=("f16", "bf16", "a8"), default="f16",
+                    help="activations: fp16, bf16 (W4A16_BF16) or fp16 quantized to int8 per "
+                         "row inside each call (W4A8, W4A16_ACT_A8); the same weights")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     wl = synthetic.workload(args.workload)

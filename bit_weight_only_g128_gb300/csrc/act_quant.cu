@@ -21,20 +21,34 @@ __device__ __forceinline__ float act_value(uint32_t bits16) {
              : __half2float(__ushort_as_half((unsigned short)bits16));
 }
 
-// One CTA per row; each thread reads 8 activations (16 bytes) at a time.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_for_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One CTA per row. The row is read once from global memory, 16 bytes per
+// thread at a time, into shared memory (K * 2 bytes) while its largest
+// magnitude is found; the codes are then formed from shared memory. Launched
+// as a plain launch (fully after the previous kernel, fully before the GEMM):
+// measured on the 7B decode step, letting the GEMM start early (programmatic
+// serialization) helped at one row but delayed the GEMM's CTAs on the SMs
+// this kernel holds at 8 and 16 rows, and the step lost 3%. (The grid-
+// dependency instructions below are then no-ops.)
 // kIn: bf16 input; kCodes: the codes as bf16 (else fp16) integer values.
 template <bool kIn, bool kCodes>
 __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t* __restrict__ A, int K,
                                                                  int8_t* __restrict__ aq,
                                                                  uint16_t* __restrict__ codes,
                                                                  float* __restrict__ s_a) {
+  extern __shared__ uint4 srow[];
   __shared__ float wmax[kQThreads / 32];
+  allow_dependents();
+  wait_for_previous_grid();
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(A + (size_t)m * K);
   const int nv = K / 8;
   float amax = 0.f;
   for (int i = threadIdx.x; i < nv; i += kQThreads) {
     const uint4 v = row[i];
+    srow[i] = v;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -52,7 +66,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
   const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
   if (threadIdx.x == 0) s_a[m] = s;
   for (int i = threadIdx.x; i < nv; i += kQThreads) {
-    const uint4 v = row[i];
+    const uint4 v = srow[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float r[8];
 #pragma unroll
@@ -88,23 +102,35 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
   }
 }
 
+template <bool kIn, bool kCodes>
+cudaError_t launch_q(const uint16_t* A, int M, int K, int8_t* aq, uint16_t* codes, float* s_a,
+                     cudaStream_t stream) {
+  auto kern = quantize_act_kernel<kIn, kCodes>;
+  const size_t smem = (size_t)K * 2;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, A, K, aq, codes, s_a);
+}
+
 }  // namespace
 
+// K up to 2^16 (128 KiB of shared memory for the row).
 cudaError_t launch_quantize_act(const uint16_t* A, int M, int K, bool in_bf16, int8_t* aq,
                                 uint16_t* codes, bool codes_bf16, float* s_a, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
-  if (in_bf16) {
-    if (codes_bf16)
-      quantize_act_kernel<true, true><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
-    else
-      quantize_act_kernel<true, false><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
-  } else {
-    if (codes_bf16)
-      quantize_act_kernel<false, true><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
-    else
-      quantize_act_kernel<false, false><<<M, kQThreads, 0, stream>>>(A, K, aq, codes, s_a);
-  }
-  return cudaGetLastError();
+  if (K > 65536) return cudaErrorInvalidValue;
+  if (in_bf16)
+    return codes_bf16 ? launch_q<true, true>(A, M, K, aq, codes, s_a, stream)
+                      : launch_q<true, false>(A, M, K, aq, codes, s_a, stream);
+  return codes_bf16 ? launch_q<false, true>(A, M, K, aq, codes, s_a, stream)
+                    : launch_q<false, false>(A, M, K, aq, codes, s_a, stream);
 }
 
 }  // namespace w4a16

@@ -186,6 +186,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   if (!is_decode(path) && path != W4A16_PATH_TENSOR)
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
+  if (a8 && K > 65536)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "W4A8: K=%d above 65536 (a row must fit shared memory)", K);
   // W4A8: quantize the activations into the workspace, then multiply the
   // codes and scale each row of the result (launched once the workspace is
   // checked, below)
@@ -341,7 +343,8 @@ int w4a16_quantize_act(const uint16_t* A, int M, int K, int flags, int8_t* aq, f
                        void* stream) {
   if (M < 0 || K < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d, K=%d: negative", M, K);
   if (flags & ~W4A16_BF16) return fail(W4A16_ERR_INVALID_ARG, "flags=0x%x: only W4A16_BF16", flags);
-  if (K % 8 != 0) return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 8", K);
+  if (K % 8 != 0 || K > 65536)
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 8 up to 65536", K);
   if (M == 0) return ok();
   if (!A || !aq || !s_a) return fail(W4A16_ERR_INVALID_ARG, "null pointer");
   if (!aligned(A, 16) || !aligned(aq, 16) || !aligned(s_a, 4))

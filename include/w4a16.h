@@ -187,7 +187,8 @@ int w4a16_dequantize(const uint32_t* Wq, const uint16_t* Sp, const uint32_t* Zp,
 
 /* W4A8 activation quantization (the rule under W4A16_ACT_A8): A [M][K]
  * 16-bit (fp16, or bf16 with flags = W4A16_BF16) -> aq [M][K] int8 and s_a
- * [M] fp32. K a multiple of 8; A and aq 16-byte aligned. */
+ * [M] fp32. K a multiple of 8, at most 65536 (the same limit applies to
+ * W4A16_ACT_A8); A and aq 16-byte aligned. */
 int w4a16_quantize_act(const uint16_t* A, int M, int K, int flags, int8_t* aq, float* s_a,
                        void* stream);
 

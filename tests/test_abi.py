@@ -215,6 +215,8 @@ def test_w4a8_workspace_and_quantize_act_errors(lib):
     A, Q, S = 0x10000, 0x20000, 0x30000
     assert lib.w4a16_quantize_act(A, -1, 64, 0, Q, S, None) == -1
     assert lib.w4a16_quantize_act(A, 4, 60, 0, Q, S, None) == -2
+    assert lib.w4a16_quantize_act(A, 4, 65536 + 64, 0, Q, S, None) == -2
+    assert _gemm(lib, path=0x800 | 2, K=65536 + 64, group=64) == -2
     assert lib.w4a16_quantize_act(A, 4, 64, 0x200, Q, S, None) == -1
     assert lib.w4a16_quantize_act(A + 8, 4, 64, 0, Q, S, None) == -3
     assert lib.w4a16_quantize_act(A, 4, 64, 0, Q + 4, S, None) == -3
