@@ -3,8 +3,15 @@
 // activations inside the operation; lmdeploy issue #2274: W4A8 with online
 // activation quantization). Per row m: amax = max_k |a|, s_a = amax / 127
 // (1 for a row of zeros), a_q = clamp(round(a / s_a), -127, 127), in IEEE
-// fp32 with round-half-to-even: the divisions are __fdiv_rn, so the codes do
-// not depend on compiler flags.
+// fp32 with round-half-to-even, so the codes do not depend on compiler
+// flags (the scale's division is __fdiv_rn).
+//
+// The codes need round(RN(a / s_a)), not the quotient itself. t = a * RN(1/s_a)
+// differs from the exact quotient a / s_a by under 2 ulps of t (two
+// roundings), and so does RN(a / s_a); where the exact quotient is farther
+// than that from a midpoint k + 1/2, both round to the same integer. So t
+// decides unless it lies within 2^-14 (at least 4 ulps, |t| < 128) of a
+// midpoint, and there the code is taken from the correctly rounded quotient.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -64,7 +71,15 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
 #pragma unroll
   for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, wmax[i]);
   const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+  const float inv = __frcp_rn(s);
   if (threadIdx.x == 0) s_a[m] = s;
+  auto code = [&](float a) {
+    const float t = a * inv;
+    float r = rintf(t);
+    if (fabsf(fabsf(t - r) - 0.5f) < 6.103515625e-05f)  // within 2^-14 of a midpoint
+      r = rintf(__fdiv_rn(a, s));
+    return fminf(fmaxf(r, -127.f), 127.f);
+  };
   for (int i = threadIdx.x; i < nv; i += kQThreads) {
     const uint4 v = srow[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -75,7 +90,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
       r[2 * j + 1] = act_value<kIn>(w[j] >> 16);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) r[j] = fminf(fmaxf(rintf(__fdiv_rn(r[j], s)), -127.f), 127.f);
+    for (int j = 0; j < 8; ++j) r[j] = code(r[j]);
     if (aq) {
       uint32_t lo = 0, hi = 0;
 #pragma unroll

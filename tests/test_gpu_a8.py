@@ -54,6 +54,28 @@ def test_quantize_act_special_rows():
     assert np.all(raq[0] == 0) and rsa[0] == 1.0 and raq[1, 7] == -127
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+def test_quantize_act_near_midpoints(bf16):
+    """Values whose quotient a / s_a lies on or next to k + 1/2 (where a fast
+    reciprocal product and the correctly rounded quotient could round apart):
+    the codes must still be the oracle's."""
+    rng = np.random.default_rng(12)
+    rows = []
+    for amax in (127.0, 100.0, 3.0, 0.37, 1e-3, 6e4 if not bf16 else 3e38):
+        k = rng.integers(-127, 127, 4096)
+        a = (k + 0.5) * (amax / 127.0) * (1 + rng.choice([0, 1, -1, 2, -2], 4096) * 2.0 ** -20)
+        a[0] = amax
+        rows.append(a)
+    A = np.array(rows)
+    bits = oracle.to_bf16(A) if bf16 else oracle.to_half(A)
+    vals = oracle.from_bf16(bits) if bf16 else oracle.from_half(bits)
+    Ad = cuda(bits.view(np.int16)).view(torch.bfloat16 if bf16 else torch.float16)
+    aq, sa = w4.quantize_act(Ad)
+    raq, rsa = oracle.quantize_act(vals)
+    assert np.array_equal(host(sa).view(np.uint32), rsa.view(np.uint32))
+    assert np.array_equal(host(aq), raq), int((host(aq) != raq).sum())
+
+
 def run_a8(M, K, N, group, seed, path, parts=0, bf16=False, silu=False):
     W = synthetic.small_weights(K, N, seed)
     Ad, Av = activations(M, K, seed, bf16)
