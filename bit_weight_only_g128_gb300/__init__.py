@@ -60,6 +60,7 @@ SIGNATURES = {
     "w4a16_plan": (_I, [_I, _I, _I, _I, _PI, _PI]),
     "w4a16_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "w4a16_device_status": (_I, [_P]),
+    "w4a16_selftest_wait": (_I, [_I, _P]),
 }
 
 _lock = threading.Lock()
@@ -274,6 +275,12 @@ def gemm_noalloc(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] 
                                     _dev(out, torch.float16, "out"), _stream(stream)),
            "w4a16_gemm_noalloc")
     return out
+
+
+def selftest_wait(which: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (0: flag wait, 1: mbarrier wait); the
+    next device_status() raises W4A16Error with DEVICE_CHECK."""
+    _check(lib().w4a16_selftest_wait(which, _stream(stream)), "w4a16_selftest_wait")
 
 
 def device_status(stream=None) -> None:

@@ -412,6 +412,18 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   return ok();
 }
 
+int w4a16_selftest_wait(int which, void* stream) {
+  cudaError_t e;
+  if (which == 0)
+    e = launch_selftest_flag_wait((cudaStream_t)stream);
+  else if (which == 1)
+    e = launch_selftest_mbar_wait((cudaStream_t)stream);
+  else
+    return fail(W4A16_ERR_INVALID_ARG, "which=%d: 0 (flag wait) or 1 (mbarrier wait)", which);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ok();
+}
+
 int w4a16_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

@@ -154,6 +154,28 @@ int decode_resident_ctas(int M, int N, int K, int group, int requested, int sms,
   return resident_shape(M, N, K, gshift, requested, sms, automatic, silu, &nw, &args, &bytes);
 }
 
+namespace {
+
+__device__ int g_selftest_flag;  // never set: the self-test waits on it
+
+// Self-test of the stream-K fix-up's bounded wait: one thread waits, with
+// the kernel's own routine and limit, for a flag that nothing sets; the wait
+// gives up, the thread records kDecodeWaitTimedOut in the error word and the
+// kernel returns.
+__global__ void selftest_flag_kernel(int* err) {
+  if (threadIdx.x == 0 && !wait_flag(&g_selftest_flag)) atomicOr(err, kDecodeWaitTimedOut);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_flag_wait(cudaStream_t stream) {
+  int* err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  selftest_flag_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_resident(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                                    const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                                    int ctas, int sms, bool automatic, bool silu,

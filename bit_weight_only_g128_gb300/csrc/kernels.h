@@ -86,6 +86,13 @@ int tc_stage_atoms(int M, int K, int group);
 int tc_token_tile(int M);
 size_t tc_smem_bytes(int bt, int stage_atoms, int* stages);
 
+// Self-tests of the bounded waits (a flag wait of the stream-K decode
+// kernel's kind, an mbarrier wait of the tensor-core pipeline's kind): each
+// waits about a second for something that never happens, then records its
+// error bit and returns.
+cudaError_t launch_selftest_flag_wait(cudaStream_t stream);
+cudaError_t launch_selftest_mbar_wait(cudaStream_t stream);
+
 // Reads the device error word (bounded waits that gave up, self-checks) and
 // clears it if set.
 cudaError_t read_and_clear_device_error(int* flag);

@@ -743,6 +743,30 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   return cudaGetLastError();
 }
 
+namespace {
+
+// Self-test of the pipeline's bounded wait: one thread initializes an
+// mbarrier that nothing ever arrives on and waits for its first phase with
+// the kernel's own wait routine and limit. The wait gives up, records
+// kErrMma in the error word, and the kernel returns.
+__global__ void selftest_mbar_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+  mbar_init(b, 1);
+  abort_flag = 0;
+  fence_barrier_init();
+  mbar_wait(b, 0, &abort_flag, kErrMma);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_mbar_wait(cudaStream_t stream) {
+  selftest_mbar_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t device_error_word(int** ptr) {
   static int* cache[64] = {};
   int dev = 0;

@@ -277,6 +277,17 @@ int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const uint16_t* sc
  * Returns W4A16_OK or W4A16_ERR_DEVICE_CHECK (message: which check, where). */
 int w4a16_device_status(void* stream);
 
+/* Self-test of the failure path of the kernels' bounded waits, for tests:
+ * launches on `stream` one kernel whose wait can never be satisfied, with
+ * the kernels' own wait routine and limit (about a second): which = 0, a
+ * flag that nothing sets (the stream-K decode fix-up's kind of wait; error
+ * bit 32); which = 1, an mbarrier that nothing arrives on (the tensor-core
+ * pipeline's kind; error bit 2). The wait gives up, records its bit in the
+ * device error word and the kernel returns: nothing faults, and the next
+ * w4a16_device_status returns W4A16_ERR_DEVICE_CHECK (and clears the word).
+ * Other `which`: W4A16_ERR_INVALID_ARG. */
+int w4a16_selftest_wait(int which, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -123,6 +123,12 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, path=3, M=16, K=16384, group=16384, ws=0) == -2
 
 
+def test_selftest_rejects_unknown_kinds(lib):
+    # decided on the host, before any launch
+    assert lib.w4a16_selftest_wait(2, None) == -1
+    assert lib.w4a16_selftest_wait(-1, None) == -1
+
+
 def test_static_weights_flag_matches_the_header():
     text = open(HEADER).read()
     assert re.search(r"#define W4A16_STATIC_WEIGHTS 0x100\b", text)
