@@ -714,8 +714,12 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   const size_t smem = tc_smem_bytes(bt, sa, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
   prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory limit is a per-device attribute of each kernel: set it
+  // once on every device this process launches on
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
     const int kMax = 227 * 1024;
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
     if (e == cudaSuccess)
@@ -725,7 +729,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_gemm_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
                   (unsigned)prm.split);
