@@ -11,6 +11,10 @@
  *     s = (max - min)/15,  z = round(-min/s),  q = clamp(round(w/s) + z, 0, 15),
  * and are dequantized inside the kernels as (q - z)*s, rounded once to fp16.
  * Products accumulate in fp32; Y is rounded to fp16 (ties to even).
+ * Variants, chosen per call by flags of w4a16_gemm_ex (below): bf16
+ * activations and results (W4A16_BF16), the fused gate/up epilogue
+ * silu(gate)*up (W4A16_SILU_MUL), and W4A8, the activations quantized to
+ * 8 bits inside the call (W4A16_ACT_A8). All use the same packed weights.
  *
  * Conventions for every entry point:
  *   - Every pointer argument is a DEVICE pointer on the current CUDA device,
