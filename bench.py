@@ -13,7 +13,13 @@ Algorithmic bytes of one GEMM = K*N/2 (int4 codes) + 2*G*N (fp16 scales)
 Roofline time = max(bytes / HBM peak, 2*M*N*K / fp16 tensor peak).
 
   python bench.py [--steps K] [--warmup W] [--workload 1] [--sweep out.jsonl]
+  python bench.py --act bf16|a8 ...      # bf16 activations, or W4A8
   python bench.py --impl reference ...   # the CPU oracle on the same metric
+
+The end-to-end figure (`e2e`) runs the same step through the public API with
+every step's input copied in from pinned host memory and its result copied
+back, double-buffered on a second stream as a serving loop would (step i
+overlaps step i+1's input copy and step i-1's result copy).
 
 Under torchrun (WORLD_SIZE > 1) every rank runs its own replica of the
 workload on its own GPU (independent problems, no collective on the data
