@@ -539,3 +539,20 @@ def test_reference_a8_against_the_16_bit_reference():
     # and the quantized product is close to the unquantized one
     y, mag = oracle.reference(A.astype(np.float16), q, s, z, group)
     assert np.all(np.abs(y8 - y) <= 0.02 * mag + 1e-3)
+
+
+def test_worked_example_bf16_and_w4a8():
+    """tests/golden/a8_bf16_worked.txt: RNE_bf16 dequantization and the W4A8
+    codes and product of the golden group, derived by hand in the file."""
+    g = {k: [float(v) for v in vals] for k, vals in _read_golden("a8_bf16_worked.txt").items()}
+    q = np.array([0, 4, 6, 10, 15, 9, 5, 8], np.uint8).reshape(8, 1)
+    z = np.array([[6]], np.uint8)
+    s = np.array([[0x2A66]], np.uint16)
+    deq = oracle.from_bf16(oracle.dequantize_bf16(q, s, z, 8)).ravel()
+    assert np.array_equal(deq, np.array(g["deq_bf16"]))
+    A = np.array([g["a"]])
+    aq, sa = oracle.quantize_act(A)
+    assert np.array_equal(aq.ravel(), np.array(g["a_q"], dtype=np.int64))
+    assert float(sa[0]) == g["s_a"][0]
+    y, mag = oracle.reference_a8(aq, sa, q, s, z, 8)
+    assert float(y[0, 0]) == g["y"][0] and float(mag[0, 0]) == g["mag"][0]
