@@ -1,18 +1,25 @@
 #!/usr/bin/env python3
 """Benchmark of the W4A16 group-quantized linear layer on one GB300.
 
-Metric: achieved HBM GB/s (algorithmic bytes / time) of the W4A16-g128 GEMM,
-with TFLOP/s and the fraction of the roofline beside it. A step is one pass
-over every linear layer of the workload at every batch size M of it (the
-Llama-2-7B decode workload by default: qkv, o_proj, gate_up, down at
-M = 1, 4, 8, 16), with the packed weights resident in HBM and rotated over
-enough copies that the working set exceeds L2 between repeats.
+Metric: W4A16 GEMM TFLOP/s and HBM GB/s against M, and the fraction of the
+roofline. A step is one pass over every linear layer of the workload at every
+batch size M of it, with the packed weights resident in HBM and rotated over
+enough copies that the working set exceeds L2 between repeats. The default
+workload is the Llama-2-70B sweep: qkv, o_proj, gate_up, down at
+M = 1, 8, 64, 512, 4096, with groups of 128 and per-channel groups (group = K),
+40 GEMMs per step.
 
 Algorithmic bytes of one GEMM = K*N/2 (int4 codes) + 2*G*N (fp16 scales)
-+ G*N/2 (int4 zero points) + 2*M*K (A) + 2*M*N (Y), G = K/group.
-Roofline time = max(bytes / HBM peak, 2*M*N*K / fp16 tensor peak).
++ G*N/2 (int4 zero points) + 2*M*K (A) + 2*M*N (Y), G = K/group; FLOPs =
+2*M*N*K. Roofline time = max(bytes / HBM peak, FLOPs / 16-bit tensor peak).
 
-  python bench.py [--steps K] [--warmup W] [--workload 1] [--sweep out.jsonl]
+The step runs as two CUDA graphs, timed separately with events on the stream
+they replay on: the GEMMs whose roofline is HBM-bound, then those that are
+tensor-bound. `value` is the step's TFLOP/s (GB/s when the step's roofline
+time is mostly HBM-bound); `roofline` describes the dominant group's kernel,
+and `roofline_by_bound` both groups.
+
+  python bench.py [--steps K] [--warmup W] [--workload 4] [--sweep out.jsonl]
   python bench.py --act bf16|a8 ...      # bf16 activations, or W4A8
   python bench.py --impl reference ...   # the CPU oracle on the same metric
 
@@ -225,16 +232,32 @@ def oracle_sample_pass(wl, ncols, group_cache):
     return secs, nbytes, nflops
 
 
-def cpu_baseline(wl, target_s=15.0):
+def headline_unit(wl, pk):
+    """TFLOP/s when the step's roofline time is mostly tensor-bound, else GB/s."""
+    t_mem = t_tc = 0.0
+    for (_, M, K, N, g) in wl.cases():
+        t, bound = roofline_us(M, K, N, g, pk)
+        if bound == "hbm":
+            t_mem += t
+        else:
+            t_tc += t
+    return "TFLOP/s" if t_tc > t_mem else "GB/s"
+
+
+def rate(unit, nbytes, nflops, secs):
+    return nflops / secs / 1e12 if unit == "TFLOP/s" else nbytes / secs / 1e9
+
+
+def cpu_baseline(wl, unit, target_s=15.0):
     import oracle
     cache = {}
-    probe_cols = 64
+    probe_cols = 16
     t, _, _ = oracle_sample_pass(wl, probe_cols, cache)
     ncols = max(16, int(probe_cols * target_s / max(t, 1e-3)) // 16 * 16)
     ncols = min(ncols, max(N for (_, _, _, N, _) in wl.cases()))
     t, b, f = oracle_sample_pass(wl, ncols, cache)
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-            "tflops": f / t / 1e12, "seconds": t,
+    return {"value": rate(unit, b, f, t), "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+            "gbs": b / t / 1e9, "tflops": f / t / 1e12, "seconds": t,
             "sample": (f"every GEMM of one step ({len(wl.cases())} cases) restricted to the "
                        f"first {ncols} output columns of each layer; dequantize + fp64 matmul")}
 
@@ -252,36 +275,41 @@ def run_reference(args, wl, dist, rank, world):
     if rank != 0:
         return
     import oracle
+    unit = headline_unit(wl, peaks())
     budget = 150.0 / max(1, args.steps + args.warmup)
     cache = {}
-    t, _, _ = oracle_sample_pass(wl, 32, cache)
-    ncols = max(16, int(32 * budget / max(t, 1e-3)) // 16 * 16)
+    t, _, _ = oracle_sample_pass(wl, 16, cache)
+    ncols = max(16, int(16 * budget / max(t, 1e-3)) // 16 * 16)
     for _ in range(args.warmup):
         oracle_sample_pass(wl, ncols, cache)
-    tot_s, tot_b = 0.0, 0
+    tot_s, tot_b, tot_f = 0.0, 0, 0
     for _ in range(args.steps):
-        s, b, _ = oracle_sample_pass(wl, ncols, cache)
+        s, b, f = oracle_sample_pass(wl, ncols, cache)
         tot_s += s
         tot_b += b
-    value = tot_b / tot_s / 1e9
+        tot_f += f
+    value = rate(unit, tot_b, tot_f, tot_s)
     sample = (f"each step: every GEMM of the workload restricted to the first {ncols} output "
               f"columns of each layer (dequantize + fp64 matmul)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.threads(),
                              "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------- GPU arm
 
-METRIC = "W4A16-g128 GEMM HBM GB/s (algorithmic bytes / time), % of roofline, 1 GB300"
+METRIC = "W4A16-g128 GEMM TFLOP/s and HBM GB/s vs M (1-4096), % of roofline, 1 GB300"
 
+# kernel of each path that w4a16_plan reports
+KERNEL_OF_PATH = {"decode-resident": "decode_resident_kernel", "decode-streamk": "decode_kernel",
+                  "tensor": "tc_gemm_kernel", "tensor-pair": "tc_pair_kernel"}
 
 # extra keyword arguments of every timed gemm call (W4A8: {"a8": True})
 GEMM_KW = {}
@@ -294,6 +322,14 @@ class Case:
     @property
     def key(self):
         return (self.layer, self.K, self.N, self.group)
+
+
+def split_by_bound(cases, pk):
+    """Indices of the cases whose roofline is HBM-bound, then tensor-bound."""
+    hbm, tc = [], []
+    for i, c in enumerate(cases):
+        (hbm if roofline_us(c.M, c.K, c.N, c.group, pk)[1] == "hbm" else tc).append(i)
+    return hbm, tc
 
 
 def _aligned_views(torch, shapes, dtype, device):
@@ -368,12 +404,16 @@ def sanity_check(wl, cases, rot, a_views, y_views, torch, w4):
             raise SystemExit(f"parity check failed for {c.layer} M={c.M}: err/bound {ratio}")
 
 
-def capture_step(torch, w4, cases, weights, a_views, y_views, stream):
+def capture(torch, w4, cases, idx, weights, a_views, y_views, stream):
+    """A CUDA graph of the GEMMs `idx` of one step (None if there are none)."""
+    if not idx:
+        return None
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for c, A, Y in zip(cases, a_views, y_views):
-            w4.gemm(A, weights[c.key], out=Y, workspace=weights["workspace"], static_weights=True,
-                    **GEMM_KW)
+        for i in idx:
+            c = cases[i]
+            w4.gemm(a_views[i], weights[c.key], out=y_views[i], workspace=weights["workspace"],
+                    static_weights=True, **GEMM_KW)
     return g
 
 
@@ -390,6 +430,26 @@ def time_graphs(torch, graphs, steps, stream):
         end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / 1e3
+
+
+def time_split_steps(torch, parts, steps, stream):
+    """Run `steps` steps, each the replay of its part graphs in order (parts[r]
+    is a list of graphs for rotation copy r, None for an empty part). Events
+    on the replay stream bracket every part of every step; returns per-step
+    lists of part durations in seconds."""
+    nparts = len(parts[0])
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nparts + 1)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            gs = parts[i % len(parts)]
+            ev[i][0].record(stream)
+            for j, g in enumerate(gs):
+                if g is not None:
+                    g.replay()
+                ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    return [[ev[i][j].elapsed_time(ev[i][j + 1]) / 1e3 for j in range(nparts)] for i in range(steps)]
 
 
 def per_case_times(torch, w4, cases, rot, a_views, y_views, stream, reps=20):
@@ -430,29 +490,79 @@ def silu_mul_times(torch, w4, cases, rot, a_views, stream, reps=20):
     return out
 
 
-def roofline_entry(args, pk, cases, step_bytes, step_flops, secs):
-    """Roofline of the step's kernel launches: bound by HBM if the step's
-    algorithmic bytes take longer at the measured copy bandwidth than its
-    flops at the measured dense tensor rate (fp16 runs at the bf16 rate),
-    else by the tensor cores. achieved = algorithmic bytes (or flops) per
-    launch / mean launch time; traffic = ncu DRAM bytes per launch."""
-    t_mem = step_bytes / (pk["hbm_gbs"] * 1e9)
-    t_tc = step_flops / (pk["tflops"] * 1e12)
-    per_launch_s = secs / args.steps / len(cases)
-    kernel = PROFILED.get(args.workload, ("decode_kernel" if t_mem >= t_tc else "tc_gemm_kernel",))[0]
-    entry = {"traffic": profiled_traffic(args.workload),
-             "traffic_unit": "DRAM bytes per launch (ncu summary in profiles/)",
-             "algorithmic_bytes_per_launch": step_bytes / len(cases),
-             "peak_source": pk["source"], "kernel": kernel}
-    if t_mem >= t_tc:
-        achieved = step_bytes / len(cases) / per_launch_s / 1e9
+def group_roofline(pk, cases, idx, secs, steps, bound, kernels):
+    """Roofline entry of the launches `idx` of a step that took `secs` in
+    total over `steps` steps: achieved = algorithmic bytes (or flops) per
+    launch / mean launch time of the group. Tensor-bound launches run back to
+    back for the whole timed region, so their peak is the sustained dense
+    rate (the burst fraction is given beside it)."""
+    n = len(idx) * steps
+    per_launch_s = secs / n
+    nbytes = sum(alg_bytes(cases[i].M, cases[i].K, cases[i].N, cases[i].group) for i in idx)
+    nflops = sum(flops(cases[i].M, cases[i].K, cases[i].N) for i in idx)
+    roof_s = sum(roofline_us(cases[i].M, cases[i].K, cases[i].N, cases[i].group, pk)[0]
+                 for i in idx) * 1e-6
+    entry = {"launches_per_step": len(idx), "kernels": kernels,
+             "ms_per_step": 1e3 * secs / steps,
+             "algorithmic_bytes_per_launch": nbytes / len(idx),
+             "flops_per_launch": nflops / len(idx),
+             "roofline_frac": roof_s * steps / secs}
+    if bound == "hbm":
+        achieved = nbytes / len(idx) / per_launch_s / 1e9
         entry.update({"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                      "frac": achieved / pk["hbm_gbs"]})
+                      "frac": achieved / pk["hbm_gbs"], "peak_kind": "copy bandwidth"})
     else:
-        achieved = step_flops / len(cases) / per_launch_s / 1e12
-        entry.update({"bound": "tensor", "achieved": achieved, "peak": pk["tflops"],
-                      "unit": "TFLOP/s", "frac": achieved / pk["tflops"]})
+        achieved = nflops / len(idx) / per_launch_s / 1e12
+        entry.update({"bound": "tensor", "achieved": achieved, "peak": pk["tflops_sustained"],
+                      "unit": "TFLOP/s", "frac": achieved / pk["tflops_sustained"],
+                      "peak_kind": "sustained dense bf16 (16-bit) rate",
+                      "frac_of_burst": achieved / pk["tflops"]})
     return entry
+
+
+def kernels_of(w4, cases, idx):
+    """Kernel names (with launch counts) that the automatic plan uses for the
+    cases `idx`."""
+    out = {}
+    for i in idx:
+        c = cases[i]
+        path, _ = w4.plan(c.M, c.N, c.K, c.group)
+        name = KERNEL_OF_PATH.get(path, path)
+        out[name] = out.get(name, 0) + 1
+    return out
+
+
+def host_call_us(torch, w4, case, weights, A, Y, stream, calls=200):
+    """Host time per eager call (enqueue only: no synchronization inside the
+    loop) through the Python API and through the C ABI directly."""
+    import ctypes
+    lib = w4.lib()
+    pw = weights[case.key]
+    ws = weights["workspace"]
+    flags = w4.STATIC_WEIGHTS | (w4.ACT_A8 if GEMM_KW.get("a8") else 0) | \
+        (w4.BF16 if A.dtype == torch.bfloat16 else 0)
+    s = ctypes.c_void_p(stream.cuda_stream)
+    out = {}
+    with torch.cuda.stream(stream):
+        for name in ("python", "c_abi"):
+            for rep in range(2):          # the first pass warms caches
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                if name == "python":
+                    for _ in range(calls):
+                        w4.gemm(A, pw, out=Y, workspace=ws, static_weights=True, **GEMM_KW)
+                else:
+                    args = (A.data_ptr(), pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(),
+                            case.M, case.N, case.K, case.group, Y.data_ptr(), ws.data_ptr(),
+                            ws.numel(), flags, 0, s)
+                    for _ in range(calls):
+                        rc = lib.w4a16_gemm_ex(*args)
+                        if rc != 0:
+                            raise RuntimeError(lib.w4a16_last_error().decode())
+                t1 = time.perf_counter()
+                torch.cuda.synchronize()
+            out[name] = 1e6 * (t1 - t0) / calls
+    return out
 
 
 def run_ours(args, wl, dist, rank, world, local):
@@ -464,24 +574,41 @@ def run_ours(args, wl, dist, rank, world, local):
     if args.act == "a8":
         GEMM_KW["a8"] = True
     pk = peaks()
+    unit = headline_unit(wl, pk)
     cases, rot, (a_flat, a_views), (y_flat, y_views), packed_bytes = build_gpu_workload(
         wl, torch, w4, device, args.copies, "bf16" if args.act == "bf16" else "f16")
     sanity_check(wl, cases, rot, a_views, y_views, torch, w4)
 
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
-    graphs = [capture_step(torch, w4, cases, r, a_views, y_views, stream) for r in rot]
+    hbm_idx, tc_idx = split_by_bound(cases, pk)
+    parts = [[capture(torch, w4, cases, hbm_idx, r, a_views, y_views, stream),
+              capture(torch, w4, cases, tc_idx, r, a_views, y_views, stream)] for r in rot]
     step_bytes = sum(alg_bytes(c.M, c.K, c.N, c.group) for c in cases)
     step_flops = sum(flops(c.M, c.K, c.N) for c in cases)
     step_roof_us = sum(roofline_us(c.M, c.K, c.N, c.group, pk)[0] for c in cases)
 
-    time_graphs(torch, graphs, args.warmup, stream)
+    time_split_steps(torch, parts, args.warmup, stream)
     barrier(dist)
     with ClockSampler(local) as clk:
-        secs = time_graphs(torch, graphs, args.steps, stream)
+        per_step = time_split_steps(torch, parts, args.steps, stream)
     barrier(dist)
-    secs = max_over_ranks(dist, secs)
+    secs_parts = [sum(s[j] for s in per_step) for j in range(2)]
+    secs = max_over_ranks(dist, sum(secs_parts))
     clocks = clk.summary()
+    step_ms = sorted(1e3 * sum(s) for s in per_step)
+
+    groups = {}
+    for name, idx, j in (("hbm", hbm_idx, 0), ("tensor", tc_idx, 1)):
+        if idx:
+            groups[name] = group_roofline(pk, cases, idx, secs_parts[j], args.steps, name,
+                                          kernels_of(w4, cases, idx))
+    dominant = max(groups, key=lambda k: groups[k]["ms_per_step"])
+    roofline = dict(groups[dominant])
+    roofline["kernel"] = max(roofline["kernels"], key=roofline["kernels"].get)
+    roofline.update({"traffic": profiled_traffic(args.workload),
+                     "traffic_unit": "DRAM bytes per launch (ncu summary in profiles/)",
+                     "peak_source": pk["source"]})
 
     # end to end through the public API: every step's activations copied in
     # from pinned host memory and every step's results read back (weights are
@@ -534,11 +661,14 @@ def run_ours(args, wl, dist, rank, world, local):
     time_e2e(args.warmup)
     barrier(dist)
     e2e_secs = max_over_ranks(dist, time_e2e(args.steps))
+    del e2e_graphs
 
-    value = world * step_bytes * args.steps / secs / 1e9
-    e2e_value = world * step_bytes * args.steps / e2e_secs / 1e9
+    value = world * rate(unit, step_bytes, step_flops, secs / args.steps)
+    e2e_value = world * rate(unit, step_bytes, step_flops, e2e_secs / args.steps)
+    # one kernel per GEMM (W4A8: the activation quantization too)
+    launches = len(cases) * args.steps * (2 if GEMM_KW.get("a8") else 1)
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.act,
         "data": "synthetic",
@@ -548,38 +678,62 @@ def run_ours(args, wl, dist, rank, world, local):
                    "l2": (f"inputs larger than L2: {len(rot)} rotating copies of the packed "
                           f"weights, {len(rot) * packed_bytes / 2**20:.0f} MiB")},
         "tflops": world * step_flops * args.steps / secs / 1e12,
+        "hbm_gbs": world * step_bytes * args.steps / secs / 1e9,
+        "step_ms_quantiles": {"p10": step_ms[len(step_ms) // 10], "p50": step_ms[len(step_ms) // 2],
+                              "p90": step_ms[(9 * len(step_ms)) // 10]},
         "roofline_frac_step": step_roof_us * 1e-6 * args.steps / secs,
-        "roofline": roofline_entry(args, pk, cases, step_bytes, step_flops, secs),
-        "e2e": {"value": e2e_value, "unit": "GB/s",
+        "roofline": roofline,
+        "roofline_by_bound": groups,
+        "e2e": {"value": e2e_value, "unit": unit,
                 "copies": "double-buffered on a second stream: step i overlaps the input copy "
                           "of step i+1 and the result copy of step i-1",
                 "h2d_bytes_per_step": sum(2 * c.M * c.K for c in cases),
                 "d2h_bytes_per_step": sum(2 * c.M * c.N for c in cases)},
-        # one kernel per GEMM (W4A8: the activation quantization too)
-        "gpu_launches": len(cases) * args.steps * (2 if GEMM_KW.get("a8") else 1),
+        "gpu_launches": launches,
         "clocks": clocks,
     }
-    if args.sweep:
+    if not args.no_by_m:
+        # per M (outside the timed region): a graph of 20 launches per case
         times = per_case_times(torch, w4, cases, rot, a_views, y_views, stream)
-        with open(args.sweep, "a") as f:
-            for c, t in zip(cases, times):
-                roof, bound = roofline_us(c.M, c.K, c.N, c.group, pk)
-                path, parts = w4.plan(c.M, c.N, c.K, c.group)
-                f.write(json.dumps({
-                    "workload": wl.name, "act": args.act, "layer": c.layer, "M": c.M, "K": c.K,
-                    "N": c.N, "group": c.group, "path": path, "parts": parts, "us": 1e6 * t,
-                    "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
-                    "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
-                    "bound": bound, "frac": roof / (1e6 * t)}) + "\n")
-            for c, t in silu_mul_times(torch, w4, cases, rot, a_views, stream):
-                # the fused layer writes half the columns
-                nbytes = alg_bytes(c.M, c.K, c.N, c.group) - c.M * c.N
-                f.write(json.dumps({
-                    "workload": wl.name, "act": args.act, "layer": "gate_up+silu_mul", "M": c.M, "K": c.K,
-                    "N": c.N, "group": c.group, "us": 1e6 * t, "GBps": nbytes / t / 1e9,
-                    "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12}) + "\n")
+        by_m = {}
+        for c, t in zip(cases, times):
+            d = by_m.setdefault(c.M, {"bytes": 0, "flops": 0, "s": 0.0, "roof_us": 0.0})
+            d["bytes"] += alg_bytes(c.M, c.K, c.N, c.group)
+            d["flops"] += flops(c.M, c.K, c.N)
+            d["s"] += t
+            d["roof_us"] += roofline_us(c.M, c.K, c.N, c.group, pk)[0]
+        line["by_m"] = {str(m): {"TFLOP/s": d["flops"] / d["s"] / 1e12, "GB/s": d["bytes"] / d["s"] / 1e9,
+                                 "us": 1e6 * d["s"], "roofline_frac": d["roof_us"] * 1e-6 / d["s"]}
+                        for m, d in sorted(by_m.items())}
+        line["by_m_how"] = ("per case: a CUDA graph of 20 launches over the rotating weight "
+                            "copies, outside the timed region; summed over the layers and groups")
+        if args.sweep:
+            with open(args.sweep, "a") as f:
+                for c, t in zip(cases, times):
+                    roof, bound = roofline_us(c.M, c.K, c.N, c.group, pk)
+                    path, parts_n = w4.plan(c.M, c.N, c.K, c.group)
+                    f.write(json.dumps({
+                        "workload": wl.name, "act": args.act, "layer": c.layer, "M": c.M,
+                        "K": c.K, "N": c.N, "group": c.group, "path": path, "parts": parts_n,
+                        "us": 1e6 * t, "GBps": alg_bytes(c.M, c.K, c.N, c.group) / t / 1e9,
+                        "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12, "roofline_us": roof,
+                        "bound": bound, "frac": roof / (1e6 * t)}) + "\n")
+                for c, t in silu_mul_times(torch, w4, cases, rot, a_views, stream):
+                    # the fused layer writes half the columns
+                    nbytes = alg_bytes(c.M, c.K, c.N, c.group) - c.M * c.N
+                    f.write(json.dumps({
+                        "workload": wl.name, "act": args.act, "layer": "gate_up+silu_mul",
+                        "M": c.M, "K": c.K, "N": c.N, "group": c.group, "us": 1e6 * t,
+                        "GBps": nbytes / t / 1e9, "TFLOPs": flops(c.M, c.K, c.N) / t / 1e12}) + "\n")
+    # host cost of one eager call of the smallest GEMM (outside graphs)
+    small = min(range(len(cases)), key=lambda i: (cases[i].M, cases[i].N * cases[i].K))
+    line["host_us_per_call"] = {
+        **host_call_us(torch, w4, cases[small], rot[0], a_views[small], y_views[small], stream),
+        "case": f"{cases[small].layer} M={cases[small].M} K={cases[small].K} N={cases[small].N} "
+                f"group={cases[small].group}",
+        "how": "200 eager calls, host time to enqueue (no synchronization inside the loop)"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, unit)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -587,13 +741,14 @@ def run_ours(args, wl, dist, rank, world, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", type=int, default=1, help="workload index (0..4)")
+    ap.add_argument("--workload", type=int, default=4, help="workload index (0..4)")
     ap.add_argument("--copies", type=int, default=None, help="weight copies for L2 rotation")
     ap.add_argument("--sweep", default=None, help="append per-case timings (JSONL) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-by-m", action="store_true", help="skip the per-M table")
     ap.add_argument("--act", choices=("f16", "bf16", "a8"), default="f16",
                     help="activations: fp16, bf16 (W4A16_BF16) or fp16 quantized to int8 per "
                          "row inside each call (W4A8, W4A16_ACT_A8); the same weights")

@@ -189,19 +189,44 @@ def dequantize(pw: PackedWeight, stream=None, dtype: torch.dtype = torch.float16
     return deq
 
 
+_ws_sizes = {}
+
+
 def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0,
                    silu_mul: bool = False, a8: bool = False) -> int:
-    """Scratch bytes a gemm call with these arguments needs."""
-    b = ctypes.c_size_t()
-    flags = (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
-    _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path] | flags, parts,
-                                         ctypes.byref(b)), "w4a16_workspace_size")
-    return b.value
+    """Scratch bytes a gemm call with these arguments needs on the current
+    device (cached per device and arguments: the size depends on nothing else)."""
+    dev = torch.cuda.current_device() if torch.cuda.is_available() else -1
+    key = (dev, M, N, K, group, path, parts, silu_mul, a8)
+    size = _ws_sizes.get(key)
+    if size is None:
+        b = ctypes.c_size_t()
+        flags = (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
+        _check(lib().w4a16_workspace_size_ex(M, N, K, group, _PATHS[path] | flags, parts,
+                                             ctypes.byref(b)), "w4a16_workspace_size")
+        size = _ws_sizes[key] = b.value
+    return size
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     """A zero-filled, 256-byte aligned workspace (every call leaves it zeroed)."""
     return torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+# workspaces of gemm calls that pass none: one per (device, stream), grown on
+# demand. Calls on one stream run one after another, so they can share one;
+# calls on different streams get different ones.
+_stream_ws = {}
+
+
+def stream_workspace(nbytes: int, device, stream) -> torch.Tensor:
+    """The cached workspace of `stream` on `device`, at least `nbytes` long
+    (a larger zero-filled one replaces it when it is too small)."""
+    key = (torch.device(device).index, stream.cuda_stream)
+    ws = _stream_ws.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = _stream_ws[key] = new_workspace(nbytes, device)
+    return ws
 
 
 def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
@@ -219,7 +244,9 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     both fp16 or both bf16 (W4A16_BF16, chosen by A's dtype).
 
     `workspace` must be zero-filled before its first use (new_workspace);
-    without one, a fresh zeroed buffer is allocated for this call.
+    without one, the call uses the cached workspace of its stream
+    (stream_workspace), allocated on the first call that needs it and grown
+    when a call needs more.
     `static_weights` (W4A16_STATIC_WEIGHTS): the kernel may read pw while the
     work queued before it on the stream drains; pw must not be written by
     that work. `silu_mul` (W4A16_SILU_MUL): pw's columns are [gate | up] and
@@ -230,17 +257,20 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
     if K != pw.K:
         raise ValueError(f"A has K={K}, weight has K={pw.K}")
     dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
+    a_ptr = _dev(A, dt, "A")
     if out is None:
         out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=dt, device=A.device)
+    y_ptr = _dev(out, dt, "out")
     ws_ptr, ws_bytes = None, 0
     need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul, a8)
     if need:
         if workspace is None:
-            workspace = new_workspace(need, A.device)
+            s = stream if stream is not None else torch.cuda.current_stream(A.device)
+            workspace = stream_workspace(need, A.device, s)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check(lib().w4a16_gemm_ex(_dev(A, dt, "A"), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
+    _check(lib().w4a16_gemm_ex(a_ptr, pw.Wq.data_ptr(), pw.Sp.data_ptr(),
                                pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
-                               _dev(out, dt, "out"), ws_ptr, ws_bytes,
+                               y_ptr, ws_ptr, ws_bytes,
                                _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
                                | (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
                                | (BF16 if dt == torch.bfloat16 else 0), parts,

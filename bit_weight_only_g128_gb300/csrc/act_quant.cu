@@ -123,7 +123,7 @@ cudaError_t launch_q(const uint16_t* A, int M, int K, int8_t* aq, uint16_t* code
   auto kern = quantize_act_kernel<kIn, kCodes>;
   const size_t smem = (size_t)K * 2;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(kern), (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};

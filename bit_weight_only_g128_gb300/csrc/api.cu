@@ -2,7 +2,9 @@
 // Declarations and the contract of every entry point: include/w4a16.h.
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -220,7 +222,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     // with the fused epilogue the product goes to the workspace first
     uint16_t* prod = silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + l.prod) : Y;
     e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
-                       l.base > 0 ? workspace : nullptr, bf16, row_scale, stream);
+                       l.base > 0 ? workspace : nullptr, static_weights, bf16, row_scale, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     if (silu && (e = launch_silu_mul(prod, M, N, Y, bf16, stream)) != cudaSuccess)
       return cuda_fail(e, "gate/up epilogue launch");
@@ -274,6 +276,24 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
 }
 
 }  // namespace
+
+cudaError_t set_max_smem_once(const void* kernel, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& d : done)
+    if (d.kernel == kernel && d.device == dev && d.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
+  return e;
+}
 
 // Record an error (or success) for w4a16_last_error from other translation
 // units of the library.

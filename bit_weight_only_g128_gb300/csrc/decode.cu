@@ -1,6 +1,8 @@
 // Decode path of the W4A16 linear layer: host side (shapes, layouts,
 // launches) and the fp16-activation instantiations of the kernels in
 // decode_impl.cuh.
+#include <atomic>
+
 #include "decode_impl.cuh"
 
 namespace w4a16 {
@@ -30,26 +32,33 @@ bool group_shape(int K, int group, int* apg_t, int* gshift) {
 }  // namespace
 
 // CTAs of the decode kernel that fit on one SM (occupancy query, M <= 8 or
-// 9..16 rows, for the variant with the most shared memory: groups of 64).
+// 9..16 rows, for the variant with the most shared memory: groups of 64),
+// cached per device; concurrent first calls may both run the query, and
+// store the same value.
 int decode_ctas_per_sm(int M) {
-  static int cache[2] = {0, 0};
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices][2];
   const int v = M <= 8 ? 0 : 1;
-  if (cache[v] == 0) {
-    int n = 0;
-    cudaError_t e;
-    if (v == 0) {
-      e = cudaFuncSetAttribute(decode_kernel<1, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<1, 8>::kTotal);
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<1, 1, false>, kThreads, Smem<1, 8>::kTotal);
-    } else {
-      e = cudaFuncSetAttribute(decode_kernel<2, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<2, 8>::kTotal);
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<2, 1, false>, kThreads, Smem<2, 8>::kTotal);
-    }
-    if (e != cudaSuccess || n <= 0) return 1;
-    cache[v] = n;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+  if (dev >= 0) {
+    const int c = cache[dev][v].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
-  return cache[v];
+  int n = 0;
+  cudaError_t e;
+  if (v == 0) {
+    e = set_max_smem_once(reinterpret_cast<const void*>(decode_kernel<1, 1, false>), Smem<1, 8>::kTotal);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<1, 1, false>, kThreads, Smem<1, 8>::kTotal);
+  } else {
+    e = set_max_smem_once(reinterpret_cast<const void*>(decode_kernel<2, 1, false>), Smem<2, 8>::kTotal);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<2, 1, false>, kThreads, Smem<2, 8>::kTotal);
+  }
+  if (e != cudaSuccess || n <= 0) return 1;
+  if (dev >= 0) cache[dev][v].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // Atoms per split granule: runs start at group boundaries (a group's atoms,

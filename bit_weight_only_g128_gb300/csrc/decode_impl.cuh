@@ -1040,8 +1040,8 @@ template <int MT, int APG, int NW, bool kB>
 cudaError_t launch_strip(const DecodeArgs& args, int ctas, int bytes, cudaStream_t stream) {
   auto kern = args.silu ? decode_resident_kernel<MT, APG, NW, true, kB>
                         : decode_resident_kernel<MT, APG, NW, false, kB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       NW == 8 ? kTwoCtaSmem : kOneCtaSmem);
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(kern),
+                                    NW == 8 ? kTwoCtaSmem : kOneCtaSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
@@ -1082,7 +1082,7 @@ template <int MT, int APG, bool kB>
 cudaError_t launch_variant(const DecodeArgs& args, int ctas, cudaStream_t stream) {
   auto kern = decode_kernel<MT, APG, kB>;
   constexpr int kSmem = Smem<MT, kBatch / APG>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(kern), kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);

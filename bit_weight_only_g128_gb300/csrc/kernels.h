@@ -73,10 +73,12 @@ int decode_ctas_per_sm(int M);
 // tcgen05/TMEM tensor-core GEMM: one CTA per 128 output columns x token tile
 // x K range (`split` ranges; with split > 1 the workspace holds the tile
 // counters, zero between calls, and the fp32 partial tiles).
+// With early_weights (static weights) the first stages' codes, scales and
+// zero points are read before the wait for the previous grid.
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, bool bf16, const float* row_scale,
-                           cudaStream_t stream);
+                           int split, void* workspace, bool early_weights, bool bf16,
+                           const float* row_scale, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
 int tc_choose_split(int M, int N, int K, int group, int sms);
 // 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K
@@ -96,6 +98,11 @@ cudaError_t launch_selftest_mbar_wait(cudaStream_t stream);
 // Reads the device error word (bounded waits that gave up, self-checks) and
 // clears it if set.
 cudaError_t read_and_clear_device_error(int* flag);
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device): the attribute is per device, and setting
+// it on every launch costs a driver call.
+cudaError_t set_max_smem_once(const void* kernel, int bytes);
 
 // Set (or clear) the calling thread's w4a16_last_error message; returns code.
 int report_error(int code, const char* message);

@@ -11,7 +11,9 @@
 // loads the library reserves it (32 KiB of flags plus 8 MiB of partial
 // tiles) until the process exits. Host code cannot pass the array's name to
 // a kernel (on the host it only stands for the symbol); its device address is
-// looked up once per device, on the first call made with that device current.
+// looked up once per device, on the first call made with that device current,
+// and kept for the life of the process (a device reset would make it stale:
+// no call may follow one).
 #include <cstdio>
 #include <mutex>
 
@@ -82,6 +84,16 @@ extern "C" int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const u
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // the kernels run on the stream's device with this device's scratch address:
+  // the two must be the same device
+  int stream_dev = dev;
+  if (e == cudaSuccess) e = cudaStreamGetDevice((cudaStream_t)stream, &stream_dev);
+  if (e == cudaSuccess && stream_dev != dev) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "the stream belongs to device %d, the current device is %d",
+             stream_dev, dev);
+    return report_error(W4A16_ERR_INVALID_ARG, msg);
+  }
   void* scratch = nullptr;
   if (e == cudaSuccess) e = scratch_address(dev, &scratch);
   if (e != cudaSuccess) {

@@ -36,6 +36,9 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 template <bool kB>
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ yfull, int M, int N,
                                                        uint4* __restrict__ y) {
+  // launched with programmatic serialization: scheduled while the GEMM that
+  // writes the product drains, it waits for that grid before reading it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int hv = N / 16;  // 16-byte vectors of one half of a row
   const long total = (long)M * hv;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
@@ -64,11 +67,17 @@ cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, bo
   if (blocks > 152 * 16) blocks = 152 * 16;
   const uint4* in = reinterpret_cast<const uint4*>(Yfull);
   uint4* out = reinterpret_cast<uint4*>(Y);
-  if (bf16)
-    silu_mul_kernel<true><<<blocks, 256, 0, stream>>>(in, M, N, out);
-  else
-    silu_mul_kernel<false><<<blocks, 256, 0, stream>>>(in, M, N, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return bf16 ? cudaLaunchKernelEx(&cfg, silu_mul_kernel<true>, in, M, N, out)
+              : cudaLaunchKernelEx(&cfg, silu_mul_kernel<false>, in, M, N, out);
 }
 
 }  // namespace w4a16

@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -250,8 +252,18 @@ struct TcParams {
   int tmem_cols;
   int split;      // K ranges per output tile (grid z)
   int dq_groups;  // dequant warp groups (4, 2 or 1), dividing `stages`
+  int early_weights;  // weights are static: read the first stages' codes and
+                      // scales before the grid-dependency wait
   const float* row_scale;  // W4A8: per-row factors of the result, or null
 };
+
+// Programmatic dependent launch: let the next grid on the stream be
+// scheduled, and wait until the previous grid has completed and its writes
+// are visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // named barrier of the 8 dequant/epilogue warps
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -308,27 +320,41 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gen_base + (tmem_slot - base));
+  // the next grid may be scheduled now: its CTAs land on SMs as this grid's
+  // CTAs leave them, and it waits for this grid before it touches memory
+  allow_dependent_launch();
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      int issued = 0;
-      int s = 0;
-      uint32_t ph = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
-        const uint32_t st = base + (uint32_t)s * stage_bytes;
-        mbar_expect_tx(full_tma(s), SA * (act_bytes + kPackedBytes));
+      auto load_codes = [&](int kb, uint32_t st, int s) {
+        tma_load_2d(st + packed_off, &tmW, (kb0 + kb) * SA * kAtomWords, n0 / kStripCols,
+                    full_tma(s));
+      };
+      auto load_act = [&](int kb, uint32_t st, int s) {
 #pragma unroll
         for (int u = 0; u < SA; ++u)
           tma_load_2d(st + u * act_bytes, &tmA, ((kb0 + kb) * SA + u) * kStageK, m0, full_tma(s));
-        tma_load_2d(st + packed_off, &tmW, (kb0 + kb) * SA * kAtomWords, n0 / kStripCols,
-                    full_tma(s));
+      };
+      // static weights: the first ring's codes go out before the wait for the
+      // previous grid (the slots are free: nothing has used them yet)
+      const int pre = p.early_weights ? (nk < stages ? nk : stages) : 0;
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_expect_tx(full_tma(kb), SA * (act_bytes + kPackedBytes));
+        load_codes(kb, base + (uint32_t)kb * stage_bytes, kb);
+      }
+      grid_dependency_wait();
+      for (int kb = 0; kb < pre; ++kb) load_act(kb, base + (uint32_t)kb * stage_bytes, kb);
+      int issued = pre;
+      for (int kb = pre; kb < nk; ++kb) {
+        const int s = kb % stages;
+        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
+        const uint32_t st = base + (uint32_t)s * stage_bytes;
+        mbar_expect_tx(full_tma(s), SA * (act_bytes + kPackedBytes));
+        load_act(kb, st, s);
+        load_codes(kb, st, s);
         ++issued;
-        if (++s == stages) {
-          s = 0;
-          ph ^= 1u;
-        }
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA exits
@@ -409,7 +435,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     };
     uint32_t ms[4], mz[4];
-    if (dg < nk) load_meta(dg, ms, mz);
+    // scales and zero points are weights: with static weights read before the
+    // wait for the previous grid (which orders this warp's stores of Y)
+    if (p.early_weights && dg < nk) load_meta(dg, ms, mz);
+    grid_dependency_wait();
+    if (!p.early_weights && dg < nk) load_meta(dg, ms, mz);
     for (int kb = dg; kb < nk; kb += groups) {
       const int s = kb % stages;
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
@@ -555,15 +585,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -667,36 +697,93 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
   return best;
 }
 
+namespace {
+
+// Encoded tensor maps of recent calls, keyed by what they encode: encoding
+// one costs a driver call, and a layer calls with the same pointers and
+// shapes every step. A small table per process, replaced round-robin.
+struct MapKey {
+  const void* ptr;
+  uint64_t dims0, dims1;
+  uint32_t box0, box1;
+  int dtype;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && dims0 == o.dims0 && dims1 == o.dims1 && box0 == o.box0 &&
+           box1 == o.box1 && dtype == o.dtype;
+  }
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mutex;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+// 2-D tensor map of a row-major [dims1][dims0] array (row pitch dims0
+// elements), box [box1][box0], 128B swizzle for the activations.
+bool tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
+                uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
+                CUtensorMapSwizzle swizzle) {
+  const MapKey key = {ptr, dims0, dims1, box0, box1, (int)dt};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_keys[i] == key) {
+        *out = g_maps[i];
+        return true;
+      }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)dims0, (cuuint64_t)dims1};
+  const cuuint64_t strides[1] = {(cuuint64_t)dims0 * esize};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  const int slot = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+  g_map_keys[slot] = key;
+  g_maps[slot] = *out;
+  return true;
+}
+
+template <int SA, bool kB>
+cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const TcParams& prm,
+                          dim3 grid, size_t smem, cudaStream_t stream) {
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(tc_gemm_kernel<SA, kB>), 227 * 1024);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<SA, kB>, tmA, tmW, prm);
+}
+
+}  // namespace
+
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
-                           int split, void* workspace, bool bf16, const float* row_scale,
-                           cudaStream_t stream) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
-  if (!encode) return cudaErrorNotSupported;
+                           int split, void* workspace, bool early_weights, bool bf16,
+                           const float* row_scale, cudaStream_t stream) {
   const int bt = tc_token_tile(M);
   const int sa = tc_stage_atoms(M, K, group);
   CUtensorMap tmA, tmW;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)bt};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tmA, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
-    const cuuint64_t dims[2] = {(cuuint64_t)(K / kAtomK) * kAtomWords, (cuuint64_t)(N / kStripCols)};
-    const cuuint64_t strides[1] = {(cuuint64_t)(K / kAtomK) * kAtomWords * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)(kAtomWords * sa), kTileN / kStripCols};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(Wq), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!tensor_map(&tmA, A, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, (uint64_t)K, (uint64_t)M, 64, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
+  if (!tensor_map(&tmW, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(K / kAtomK) * kAtomWords,
+                  (uint64_t)(N / kStripCols), (uint32_t)(kAtomWords * sa), kTileN / kStripCols,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   TcParams prm;
   prm.Sp = Sp;
   prm.Zp = Zp;
@@ -708,43 +795,20 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.bt = bt;
   prm.split = split < 1 ? 1 : split;
   prm.row_scale = row_scale;
+  prm.early_weights = early_weights ? 1 : 0;
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;
   const size_t smem = tc_smem_bytes(bt, sa, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
   prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
-  // the shared-memory limit is a per-device attribute of each kernel: set it
-  // once on every device this process launches on
-  static bool attr_set[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    const int kMax = 227 * 1024;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
                   (unsigned)prm.split);
-  if (bf16) {
-    if (sa == 2)
-      tc_gemm_kernel<2, true><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
-    else
-      tc_gemm_kernel<1, true><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
-  } else {
-    if (sa == 2)
-      tc_gemm_kernel<2, false><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
-    else
-      tc_gemm_kernel<1, false><<<grid, kThreads, smem, stream>>>(tmA, tmW, prm);
-  }
-  return cudaGetLastError();
+  if (bf16)
+    return sa == 2 ? launch_kernel<2, true>(tmA, tmW, prm, grid, smem, stream)
+                   : launch_kernel<1, true>(tmA, tmW, prm, grid, smem, stream);
+  return sa == 2 ? launch_kernel<2, false>(tmA, tmW, prm, grid, smem, stream)
+                 : launch_kernel<1, false>(tmA, tmW, prm, grid, smem, stream);
 }
 
 namespace {

@@ -19,8 +19,15 @@
  * Conventions for every entry point:
  *   - Every pointer argument is a DEVICE pointer on the current CUDA device,
  *     owned by the caller. The library never allocates, frees or keeps device
- *     memory, and never synchronizes: work is enqueued on `stream` (a
- *     cudaStream_t passed as void*; NULL is the legacy default stream).
+ *     memory (apart from its static device arrays: a 4-byte error word, and
+ *     the scratch of w4a16_gemm_noalloc), and never synchronizes (apart from
+ *     w4a16_device_status): work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream), which must belong
+ *     to the current device.
+ *   - The library keeps per-device state for the life of the process (the
+ *     error word's address, kernel attributes, encoded tensor maps keyed by
+ *     pointer and shape): make no call after a reset of the device
+ *     (cudaDeviceReset) in the same process.
  *   - fp16 values are passed as uint16_t bit patterns (IEEE binary16).
  *   - Return value: W4A16_OK (0) or a negative W4A16_ERR_* code. On error no
  *     kernel has been launched (except W4A16_ERR_CUDA, which reports a failed
@@ -100,12 +107,16 @@ extern "C" {
 #define W4A16_PATH_DECODE_STREAMK 4
 /* Flag OR-ed into the path of w4a16_gemm_ex: the weights (Wq, scales, zeros)
  * are not written by the work queued just before this call on the stream, so
- * the kernel may read them while that work drains. Every kernel of the
- * library is launched with programmatic stream serialization and touches A,
- * Y and the workspace only after the previous grid has completed; with this
- * flag the decode kernel also loads its first weights before that point,
- * which hides the gap between back-to-back layers. Without it the ordering is
- * that of a plain launch. */
+ * the kernel may read them while that work drains. The GEMM kernels (both
+ * decode variants and the tensor-core GEMM) and the fused epilogue's
+ * separate pass are launched with programmatic stream serialization: a grid
+ * may be scheduled while the previous one drains, and touches A, Y and the
+ * workspace only after the previous grid has completed. (The W4A8
+ * activation-quantization kernel is a plain launch.) With this flag the
+ * decode kernels also load their first weights before that point, and the
+ * tensor-core kernel its first ring of packed codes and its first scales and
+ * zero points, which hides the gap between back-to-back layers. Without it
+ * every read of the weights also waits for the previous grid. */
 #define W4A16_STATIC_WEIGHTS 0x100
 /* Flag OR-ed into the path of w4a16_gemm_ex and w4a16_workspace_size_ex: the
  * fused gate/up epilogue of a gated MLP (lmdeploy issue #2274 "[Feature]
@@ -144,9 +155,14 @@ extern "C" {
  * operation, fp16 out; lmdeploy issue #2274: W4A8 with online activation
  * quantization). Per row m, in IEEE fp32: s_a = max_k |a| / 127 (1 for a row
  * of zeros) and a_q = clamp(round(a / s_a), -127, 127), ties to even (what
- * w4a16_quantize_act writes). Then y = s_a * sum_groups s * sum_k a_q (q - z):
- * the codes enter the tensor cores as exact 16-bit integer values, and s_a
- * scales the fp32 result before its one rounding. The workspace holds the
+ * w4a16_quantize_act writes). Then y = s_a * sum_k a_q (q - z) s, with s_a
+ * scaling the fp32 result before its one rounding; the codes enter the
+ * tensor cores as exact 16-bit integer values. On the decode path each
+ * integer product a_q (q - z) and each group's sum is exact in fp32 and the
+ * group's sum is multiplied by s; on the tensor-core path the codes multiply
+ * the same dequantized operand RNE_fp16((q - z) s) (RNE_bf16 with
+ * W4A16_BF16) that 16-bit activations use, so each product carries that
+ * weight's one rounding. The workspace holds the
  * codes ([M][K], 16-bit) and the scales after the path's own scratch (and
  * after the fused epilogue's product), so w4a16_workspace_size_ex must be
  * asked with the same flags. Accuracy contract: the 16-bit bound of the
@@ -267,7 +283,11 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
  * not fit (more than 1024 CTAs for 9..16 rows, 2048 for up to 8) are rejected
  * with W4A16_ERR_UNSUPPORTED_SHAPE; the decode path's group rule applies.
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * that device current) and keeps it for the life of the process; make that
+ * first call before any stream capture, and make no call after a reset of
+ * the device (cudaDeviceReset), which would leave the kept address stale.
+ * `stream` must belong to the current device (W4A16_ERR_INVALID_ARG
+ * otherwise).
  * Every call on a device shares the one array: calls that overlap on the GPU
  * (other streams, other host threads) race and give wrong results. Each call
  * clears the flags it uses before its kernels run. Any M is taken, in

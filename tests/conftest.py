@@ -24,3 +24,33 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+# worst err/bound ratio of each GPU parity case, gathered by the tests (see
+# gpu_util.MARGINS) and reported at the end of the session
+@pytest.fixture(scope="session")
+def margins():
+    import gpu_util
+    return gpu_util.MARGINS
+
+
+def pytest_terminal_summary(terminalreporter):
+    gpu_util = sys.modules.get("gpu_util")
+    rows = getattr(gpu_util, "MARGINS", None)
+    if not rows:
+        return
+    worst = {}
+    for r in rows:
+        key = (r["test"], r["path"])
+        if key not in worst or r["max_err_over_bound"] > worst[key]["max_err_over_bound"]:
+            worst[key] = r
+    terminalreporter.write_sep("-", "worst err/bound per test kind and path")
+    for (test, path), r in sorted(worst.items()):
+        terminalreporter.write_line(
+            f"{test:12s} {path:16s} {r['max_err_over_bound']:.4f}  "
+            f"({', '.join(f'{k}={v}' for k, v in r.items() if k not in ('test', 'path', 'max_err_over_bound'))})")
+    out = os.path.join(ROOT, "gpurun_out")
+    if os.path.isdir(out):
+        import json
+        with open(os.path.join(out, "parity_margins.json"), "w") as f:
+            json.dump(rows, f)

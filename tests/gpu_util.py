@@ -6,6 +6,10 @@ import bit_weight_only_g128_gb300 as w4
 import oracle
 import synthetic
 
+# worst err/bound ratio of each parity case: dicts with "test", "path" and
+# "max_err_over_bound" (and the case's shape), reported by conftest.py
+MARGINS = []
+
 
 def cuda(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -58,6 +62,9 @@ def run_and_check(M, K, N, group, seed, path="auto", parts=0, outliers=False, re
         assert np.array_equal(o, outs[0]), "repeated call is not bitwise identical"
     y, mag = oracle.reference(A, q, s, z, group)
     ratio, idx = oracle.check(outs[0], y, mag)
+    MARGINS.append({"test": "small", "path": path if path != "auto" else w4.plan(M, N, K, group)[0],
+                    "M": M, "K": K, "N": N, "group": group, "parts": parts,
+                    "max_err_over_bound": float(ratio)})
     assert ratio <= 1.0, (f"max err/bound {ratio:.3f} at (m={idx // N}, n={idx % N}): "
                           f"got {oracle.from_half(outs[0].reshape(-1)[idx])}, want {y.reshape(-1)[idx]}")
     return ratio

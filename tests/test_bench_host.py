@@ -20,25 +20,41 @@ def test_algorithmic_bytes_and_flops():
     assert bench.flops(2, 64, 16) == 2 * 2 * 16 * 64
 
 
-def test_roofline_entry_picks_the_binding_resource():
-    class A:
-        steps = 2
-    pk = {"hbm_gbs": 1000.0, "tflops": 100.0, "source": "measured"}
-    dec = [bench.Case(*c) for c in synthetic.workload(1).cases()]
-    step_bytes = sum(bench.alg_bytes(c.M, c.K, c.N, c.group) for c in dec)
-    step_flops = sum(bench.flops(c.M, c.K, c.N) for c in dec)
-    A.workload = 1
-    e = bench.roofline_entry(A, pk, dec, step_bytes, step_flops, secs=2e-3)
+def test_cases_split_by_roofline_bound():
+    pk = {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "measured"}
+    cases = [bench.Case(*c) for c in synthetic.workload(4).cases()]
+    hbm, tc = bench.split_by_bound(cases, pk)
+    assert sorted(hbm + tc) == list(range(len(cases)))
+    # the 70B sweep: M <= 64 is below the ridge, M >= 512 above it
+    assert {cases[i].M for i in hbm} == {1, 8, 64}
+    assert {cases[i].M for i in tc} == {512, 4096}
+    # the headline unit follows the bound that holds most of the roofline time
+    assert bench.headline_unit(synthetic.workload(4), pk) == "TFLOP/s"
+    assert bench.headline_unit(synthetic.workload(1), pk) == "GB/s"
+
+
+def test_group_roofline_per_bound():
+    pk = {"hbm_gbs": 1000.0, "tflops": 100.0, "tflops_sustained": 80.0, "source": "measured"}
+    cases = [bench.Case(*c) for c in synthetic.workload(4).cases()]
+    hbm, tc = bench.split_by_bound(cases, pk)
+    steps = 4
+    hb = sum(bench.alg_bytes(cases[i].M, cases[i].K, cases[i].N, cases[i].group) for i in hbm)
+    e = bench.group_roofline(pk, cases, hbm, secs=2e-3, steps=steps, bound="hbm", kernels={})
+    # achieved = algorithmic bytes per launch / mean launch time = bytes per step / step time
     assert e["bound"] == "hbm" and e["unit"] == "GB/s"
-    assert e["achieved"] == pytest.approx(step_bytes / 1e-3 / 1e9)   # per launch = per step here
+    assert e["achieved"] == pytest.approx(hb * steps / 2e-3 / 1e9)
     assert e["frac"] == pytest.approx(e["achieved"] / 1000.0)
-    pre = [bench.Case(*c) for c in synthetic.workload(3).cases()]
-    sb = sum(bench.alg_bytes(c.M, c.K, c.N, c.group) for c in pre)
-    sf = sum(bench.flops(c.M, c.K, c.N) for c in pre)
-    A.workload = 3
-    e = bench.roofline_entry(A, pk, pre, sb, sf, secs=1.0)
+    assert e["launches_per_step"] == len(hbm)
+    tf = sum(bench.flops(cases[i].M, cases[i].K, cases[i].N) for i in tc)
+    e = bench.group_roofline(pk, cases, tc, secs=1.0, steps=steps, bound="tensor", kernels={})
     assert e["bound"] == "tensor" and e["unit"] == "TFLOP/s"
-    assert e["achieved"] == pytest.approx(sf / 0.5 / 1e12)
+    assert e["achieved"] == pytest.approx(tf * steps / 1.0 / 1e12)
+    # tensor-bound launches are timed back to back: sustained peak, burst beside it
+    assert e["peak"] == 80.0 and e["frac"] == pytest.approx(e["achieved"] / 80.0)
+    assert e["frac_of_burst"] == pytest.approx(e["achieved"] / 100.0)
+    roof = sum(bench.roofline_us(cases[i].M, cases[i].K, cases[i].N, cases[i].group, pk)[0]
+               for i in tc) * 1e-6
+    assert e["roofline_frac"] == pytest.approx(roof * steps / 1.0)
 
 
 def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
@@ -74,6 +90,7 @@ def test_reference_arm_line(monkeypatch, capsys):
     bench.run_reference(A, wl, None, 0, 2)
     line = json.loads(capsys.readouterr().out)
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s"                          # the decode workload is HBM-bound
     assert line["value"] == pytest.approx(2e-3)            # 1 MB / 0.5 s in GB/s
     assert line["config"] == bench.workload_config(wl)
     assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0

@@ -212,3 +212,44 @@ def test_static_weights_keeps_the_order_of_a_layer_chain(path):
     # and the first layer against the oracle
     y, mag = oracle.reference(host(A), *refs[0], 128)
     assert oracle.check(plain[0], y, mag)[0] <= 1.0
+
+
+def _cancelling_weights(K, N, group, c, seed):
+    """Every group of every column holds one weight -c and zeros elsewhere:
+    max = 0, min = -c, so s = c/15, z = 15 and every zero weight gets the code
+    q = z = 15. The result is one product per group, while the decode path's
+    group terms s*(sum q a - z sum a) subtract two sums that are each about
+    15 * sum|a| over the group."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 31, K, N, group]))
+    W = np.zeros((K, N), np.float32)
+    for j in range(K // group):
+        rows = j * group + rng.integers(0, group, size=N)
+        W[rows, np.arange(N)] = -c
+    return W
+
+
+@pytest.mark.parametrize("path", VARIANTS + ["tensor"])
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_cancellation_in_the_group_terms(M, path, margins):
+    # activations with a large common offset and x20 outlier channels, so that
+    # sum a over a group is large and of one sign
+    K, N, group = 4096, 256, 128
+    W = _cancelling_weights(K, N, group, c=2.0, seed=M)
+    (q, s, z), pw = prepare(W, group)
+    assert np.all(z == 15) and np.mean(q == 15) > 0.99
+    rng = np.random.default_rng(np.random.SeedSequence([M, 32, K]))
+    A = rng.standard_normal((M, K)) + 3.0
+    A[:, synthetic.outlier_columns(K, rng)] *= 20.0
+    A = A.astype(np.float16)
+    try:
+        Y = w4.gemm(cuda(A), pw, path=path)
+    except w4.W4A16Error as e:
+        if path == "decode-resident" and e.code == -2:
+            pytest.skip("activations do not fit the resident variant")
+        raise
+    w4.device_status()
+    y, mag = oracle.reference(A, q, s, z, group)
+    ratio, idx = oracle.check(half_bits(Y), y, mag)
+    margins.append({"test": "cancellation", "path": path, "M": M, "K": K, "N": N,
+                    "group": group, "max_err_over_bound": float(ratio)})
+    assert ratio <= 1.0, f"max err/bound {ratio:.3f} at (m={idx // N}, n={idx % N})"

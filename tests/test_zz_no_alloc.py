@@ -4,8 +4,9 @@ Some callers may not allocate device memory once they run (a fixed memory
 budget, a plugin without access to its host's allocator). For them the
 library offers a decode-path GEMM that takes no workspace and uses a device
 array inside the library instead. This file checks, through the C ABI, that
-two calls in a row give the same results as the regular entry point, within
-the parity tolerance 2^-9 * sum|a*w| + 1e-3 per element. It is collected
+two calls in a row give the same results as the regular entry point: within
+the parity tolerance 2^-9 * sum|a*w| + 1e-3 per element, and bit for bit
+(both run the same kernel with the same CTA count and summation order). It is collected
 last so that a failure here never hides the other tests.
 """
 import ctypes
@@ -51,6 +52,21 @@ def test_noalloc_matches_regular_entry_point_on_two_calls(M, K, N, group):
         w4.device_status()
         diff = np.abs(oracle.from_half(half_bits(Y)) - oracle.from_half(half_bits(ref)))
         assert np.all(diff <= bound), f"call {call}: max diff/bound {np.max(diff / bound)}"
+        # same kernel, same CTA count, same fixed summation order: the same bits
+        assert np.array_equal(half_bits(Y), half_bits(ref)), f"call {call}: not bitwise equal"
+
+
+def test_noalloc_rejects_a_stream_of_another_device():
+    if torch.cuda.device_count() < 2:
+        pytest.skip("one device: no stream of another device to pass")
+    lib = w4.lib()
+    pw = prepare(synthetic.small_weights(128, 32, seed=1), 128)[1]
+    A = torch.zeros((1, 128), dtype=torch.float16, device="cuda")
+    Y = torch.empty((1, 32), dtype=torch.float16, device="cuda")
+    other = torch.cuda.Stream(device=1)
+    assert lib.w4a16_gemm_noalloc(A.data_ptr(), pw.Wq.data_ptr(), pw.Sp.data_ptr(),
+                                  pw.Zp.data_ptr(), 1, 32, 128, 128, Y.data_ptr(),
+                                  ctypes.c_void_p(other.cuda_stream)) == -1
 
 
 def test_noalloc_rejects_bad_arguments():
