@@ -24,9 +24,10 @@ import torch
 from .build import LIB as LIB_PATH
 
 PATH_AUTO, PATH_DECODE, PATH_TENSOR = 0, 1, 2
-PATH_DECODE_RESIDENT, PATH_DECODE_STREAMK = 3, 4
+PATH_DECODE_RESIDENT, PATH_DECODE_STREAMK, PATH_TENSOR_PAIR = 3, 4, 5
 _PATHS = {"auto": PATH_AUTO, "decode": PATH_DECODE, "tensor": PATH_TENSOR,
-          "decode-resident": PATH_DECODE_RESIDENT, "decode-streamk": PATH_DECODE_STREAMK}
+          "decode-resident": PATH_DECODE_RESIDENT, "decode-streamk": PATH_DECODE_STREAMK,
+          "tensor-pair": PATH_TENSOR_PAIR}
 STATIC_WEIGHTS = 0x100  # W4A16_STATIC_WEIGHTS
 SILU_MUL = 0x200        # W4A16_SILU_MUL
 BF16 = 0x400            # W4A16_BF16

@@ -76,8 +76,17 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
   return (int)c;
 }
 
-// Decode GEMV up to 16 rows; tensor-core GEMM above.
-int choose_path(int M) { return M <= 16 ? W4A16_PATH_DECODE : W4A16_PATH_TENSOR; }
+// Decode GEMV up to 16 rows; above, the one-SM tensor-core GEMM, and from
+// 256 rows the two-SM one.
+int choose_path(int M, int N, int K, int group) {
+  (void)N;
+  (void)K;
+  (void)group;
+  if (M <= 16) return W4A16_PATH_DECODE;
+  return M >= 256 ? W4A16_PATH_TENSOR_PAIR : W4A16_PATH_TENSOR;
+}
+
+bool is_tensor(int path) { return path == W4A16_PATH_TENSOR || path == W4A16_PATH_TENSOR_PAIR; }
 
 bool is_decode(int path) {
   return path == W4A16_PATH_DECODE || path == W4A16_PATH_DECODE_RESIDENT ||
@@ -140,6 +149,8 @@ WsLayout ws_layout(int M, int N, int K, int group, int path, bool silu, bool a8,
   if (path == W4A16_PATH_TENSOR) {
     l.base = tc_workspace_bytes(M, N, tc_split(M, N, K, group, parts));
     prod_rows = M;
+  } else if (path == W4A16_PATH_TENSOR_PAIR) {
+    prod_rows = M;  // no K split: no scratch of its own
   } else if (is_decode(path) && path != W4A16_PATH_DECODE_RESIDENT) {
     const int rows = M < 16 ? M : 16;
     const int c = decode_ctas(rows, N, K, group, parts);
@@ -184,8 +195,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
   const bool bf16 = (path & W4A16_BF16) != 0;
   const bool a8 = (path & W4A16_ACT_A8) != 0;
   path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16 | W4A16_ACT_A8);
-  if (path == W4A16_PATH_AUTO) path = choose_path(M);
-  if (!is_decode(path) && path != W4A16_PATH_TENSOR)
+  if (path == W4A16_PATH_AUTO) path = choose_path(M, N, K, group);
+  if (!is_decode(path) && !is_tensor(path))
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (parts < 0) return fail(W4A16_ERR_INVALID_ARG, "parts=%d is negative", parts);
   if (a8 && K > 65536)
@@ -207,8 +218,9 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                 "fused gate/up epilogue: N=%d is not two halves of 16-column strips "
                 "(a multiple of 32)", N);
   const int ycols = silu ? N / 2 : N;  // columns of Y
-  if (path == W4A16_PATH_TENSOR) {
-    const int split = tc_split(M, N, K, group, parts);
+  if (is_tensor(path)) {
+    const bool pair = path == W4A16_PATH_TENSOR_PAIR;
+    const int split = pair ? 1 : tc_split(M, N, K, group, parts);
     const WsLayout l = ws_layout(M, N, K, group, path, silu, a8, parts);
     const size_t need = l.total;
     if (need > 0 && (!workspace || workspace_bytes < need))
@@ -221,8 +233,11 @@ int gemm_impl(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
     if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
     // with the fused epilogue the product goes to the workspace first
     uint16_t* prod = silu ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + l.prod) : Y;
-    e = launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
-                       l.base > 0 ? workspace : nullptr, static_weights, bf16, row_scale, stream);
+    e = pair ? launch_tc_pair(A, Wq, scales, zeros, prod, M, N, K, group, static_weights, bf16,
+                              row_scale, stream)
+             : launch_tc_gemm(A, Wq, scales, zeros, prod, M, N, K, group, split,
+                              l.base > 0 ? workspace : nullptr, static_weights, bf16, row_scale,
+                              stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     if (silu && (e = launch_silu_mul(prod, M, N, Y, bf16, stream)) != cudaSuccess)
       return cuda_fail(e, "gate/up epilogue launch");
@@ -396,8 +411,8 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
   const bool silu = (path & W4A16_SILU_MUL) != 0;
   const bool a8 = (path & W4A16_ACT_A8) != 0;
   path &= ~(W4A16_STATIC_WEIGHTS | W4A16_SILU_MUL | W4A16_BF16 | W4A16_ACT_A8);
-  if (path == W4A16_PATH_AUTO) path = choose_path(M);
-  if (!is_decode(path) && path != W4A16_PATH_TENSOR)
+  if (path == W4A16_PATH_AUTO) path = choose_path(M, N, K, group);
+  if (!is_decode(path) && !is_tensor(path))
     return fail(W4A16_ERR_INVALID_ARG, "unknown path %d", path);
   if (silu && N % 32 != 0)
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "fused gate/up epilogue: N=%d is not a multiple of 32", N);
@@ -423,10 +438,12 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts) {
   if (M < 0) return fail(W4A16_ERR_INVALID_ARG, "M=%d is negative", M);
   if (int rc = check_kn(K, N, group)) return rc;
   if (!path || !parts) return fail(W4A16_ERR_INVALID_ARG, "null output pointer");
-  *path = choose_path(M);
+  *path = choose_path(M, N, K, group);
   const int rows = M < 16 ? (M > 0 ? M : 1) : 16;
   if (*path == W4A16_PATH_DECODE)
     *path = decode_variant(W4A16_PATH_DECODE, rows, N, K, group, 0, false, parts);
+  else if (*path == W4A16_PATH_TENSOR_PAIR)
+    *parts = 1;
   else
     *parts = tc_split(M, N, K, group, 0);
   return ok();

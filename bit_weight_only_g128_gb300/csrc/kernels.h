@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace w4a16 {
@@ -80,6 +81,23 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
                            int split, void* workspace, bool early_weights, bool bf16,
                            const float* row_scale, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
+// Two-SM tensor-core GEMM for large M: clusters of two CTAs, each pair one
+// output tile of 256 columns x tc_pair_token_tile(M) tokens over all of K
+// (tcgen05.mma.cta_group::2); no workspace.
+cudaError_t launch_tc_pair(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
+                           const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
+                           bool early_weights, bool bf16, const float* row_scale,
+                           cudaStream_t stream);
+int tc_pair_token_tile(int M);
+int tc_pair_stage_atoms(int K, int group);
+size_t tc_pair_smem_bytes(int bt, int sa, int* act_slots, int* dq_slots, int* code_slots);
+// 2-D tensor map of a row-major [dims1][dims0] array of `esize`-byte elements
+// with box [box1][box0], from a per-process cache keyed by pointer, shape,
+// box and type (encoding one costs a driver call); false if it cannot be
+// encoded.
+bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
+                       uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle);
 int tc_choose_split(int M, int N, int K, int group, int sms);
 // 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K
 // and the group are multiples of 128 and 4 such stages fit, else 1).

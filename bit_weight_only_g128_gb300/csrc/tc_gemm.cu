@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace w4a16 {
 
@@ -48,195 +49,9 @@ constexpr int kDqThreads = kDqWarps * 32;
 constexpr int kThreads = 64 + kDqThreads;
 constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
 constexpr int kPackedBytes = kTileN * kStageK / 2;  // 4 KiB packed codes
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr size_t kTcCounterBytes = 32768;          // tile counters of a K-split launch
 
-// error codes written to g_device_error (one bit per role)
-constexpr int kErrProducer = 1, kErrMma = 2, kErrDequant = 4, kErrEpilogue = 8, kErrDrain = 16;
-
-// ------------------------------------------------------------------ PTX
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Non-blocking test of the phase of parity `parity`.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of parity `parity`. Returns false if the CTA is
-// aborting (another role gave up) or if this wait exceeded the limit, in
-// which case it raises the abort flag and records `code` in the error word.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int code) {
-  if (mbar_test(bar, parity)) return true;  // already complete: no suspend
-  for (int i = 0; i < 256; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicOr(&g_device_error, code);
-      return false;
-    }
-  }
-}
-
-// Wait used only while aborting: for this CTA's own asynchronous work (copies
-// or MMAs already issued) to finish, ignoring the abort flag, bounded by a
-// shorter limit.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs / 10) {
-      atomicOr(&g_device_error, kErrDrain);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-// Shared-memory matrix descriptor of a K-major operand in the canonical
-// 128-byte-swizzle layout: rows of 128 bytes (64 fp16 of k), 8-row groups
-// 1024 bytes apart (stride byte offset), tile base 1024-byte aligned.
-// Fields: start address >> 4 [0,14), leading byte offset >> 4 [16,30)
-// (unused for this layout, set to 1), stride byte offset >> 4 [32,46),
-// descriptor version 1 [46,48), swizzle mode 2 = 128B [61,64).
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 D [4,6) = 1, A and
-// B types [7,10) and [10,13) (0 fp16, 1 bf16; both alike), both K-major
-// [15] = [16] = 0, N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t f16_idesc(int m, int n, bool bf16) {
-  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
-
-// fp32 -> 16-bit result bits (fp16, or bf16 with kB), round to nearest even.
-template <bool kB>
-__device__ __forceinline__ uint16_t to_out(float v) {
-  if (kB) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return __half_as_ushort(__float2half_rn(v));
-}
-template <bool kB>
-__device__ __forceinline__ uint32_t to_out2(float lo, float hi) {
-  if (kB) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-  }
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
+using namespace tc;
 
 // ------------------------------------------------------------------ kernel
 
@@ -255,15 +70,9 @@ struct TcParams {
   int early_weights;  // weights are static: read the first stages' codes and
                       // scales before the grid-dependency wait
   const float* row_scale;  // W4A8: per-row factors of the result, or null
+  int* err;                // the library's error word
 };
 
-// Programmatic dependent launch: let the next grid on the stream be
-// scheduled, and wait until the previous grid has completed and its writes
-// are visible (a no-op when the launch had no programmatic dependency).
-__device__ __forceinline__ void allow_dependent_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // named barrier of the 8 dequant/epilogue warps
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -349,7 +158,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int kb = pre; kb < nk; ++kb) {
         const int s = kb % stages;
         const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer)) break;
+        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer, p.err)) break;
         const uint32_t st = base + (uint32_t)s * stage_bytes;
         mbar_expect_tx(full_tma(s), SA * (act_bytes + kPackedBytes));
         load_act(kb, st, s);
@@ -359,7 +168,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (*abort_flag) {
         // let the copies already issued land before the CTA exits
         for (int kb = (issued > stages ? issued - stages : 0); kb < issued; ++kb)
-          mbar_drain(full_tma(kb % stages), (uint32_t)(kb / stages) & 1u);
+          mbar_drain(full_tma(kb % stages), (uint32_t)(kb / stages) & 1u, p.err);
       }
     }
   } else if (warp == 1) {
@@ -378,7 +187,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // stage's full_tma phase: acquiring full_dq orders these MMAs after the
         // stage's TMA bytes (activations and codes) as well, so full_tma needs
         // no wait of its own here.
-        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma);
+        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma, p.err);
         if (!ok) break;
         tc_fence_after();
         const uint64_t soff = (uint64_t)((uint32_t)s * (stage_bytes >> 4));
@@ -396,7 +205,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       tc_commit(accum_bar);  // fires once every MMA issued above has completed
-      if (!ok) mbar_drain(accum_bar, 0);  // no MMA may run past the TMEM release
+      if (!ok) mbar_drain(accum_bar, 0, p.err);  // no MMA may run past the TMEM release
     }
   } else {
     // ---------------------------------------------------------- dequant + epilogue
@@ -434,18 +243,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     };
-    uint32_t ms[4], mz[4];
-    // scales and zero points are weights: with static weights read before the
-    // wait for the previous grid (which orders this warp's stores of Y)
-    if (p.early_weights && dg < nk) load_meta(dg, ms, mz);
-    grid_dependency_wait();
-    if (!p.early_weights && dg < nk) load_meta(dg, ms, mz);
-    for (int kb = dg; kb < nk; kb += groups) {
+    // one stage of this group: wait for its copies, dequantize this warp's
+    // strips with the stage's scales and zero points (ms, mz), arrive
+    auto stage = [&](int kb, const uint32_t (&ms)[4], const uint32_t (&mz)[4]) -> bool {
       const int s = kb % stages;
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-      uint32_t nms[4] = {0, 0, 0, 0}, nmz[4] = {0, 0, 0, 0};
-      if (kb + groups < nk) load_meta(kb + groups, nms, nmz);  // this warp's next stage
-      if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant)) break;
+      if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant, p.err)) return false;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -455,39 +258,51 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint16_t s0 = (uint16_t)(ms[i] & 0xffffu), s1 = (uint16_t)(ms[i] >> 16);
 #pragma unroll
           for (int u = 0; u < SA; ++u) {
-          const uint32_t wdq = st + wdq_off + u * kWdqBytes;
-          const uint4 v = lds128(st + packed_off + ls * (SA * 512) + u * 512 + lane * 16);
+            const uint32_t wdq = st + wdq_off + u * kWdqBytes;
+            const uint4 v = lds128(st + packed_off + ls * (SA * 512) + u * 512 + lane * 16);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
-            const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
-            const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
-            uint32_t o[4];
-            if (kB)
-              dequant_word_bf16(word, make_deq_const_bf16(r ? z1 : z0, r ? s1 : s0), o);
-            else
-              dequant_word(word, make_deq_const(r ? z1 : z0, r ? s1 : s0), o);
-            // row n = 16 ls + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
-            const uint32_t row = 16u * ls + gq + 8u * r;
-            const uint32_t kw = 4u * ks + t;
-            sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4), o[0],
-                   o[1], o[2], o[3]);
-          }
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
+              const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
+              const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
+              uint32_t o[4];
+              if (kB)
+                dequant_word_bf16(word, make_deq_const_bf16(r ? z1 : z0, r ? s1 : s0), o);
+              else
+                dequant_word(word, make_deq_const(r ? z1 : z0, r ? s1 : s0), o);
+              // row n = 16 ls + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
+              const uint32_t row = 16u * ls + gq + 8u * r;
+              const uint32_t kw = 4u * ks + t;
+              sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4),
+                     o[0], o[1], o[2], o[3]);
+            }
           }
         }
       }
       fence_async_shared();  // this thread's generic-proxy stores -> visible to the tensor core
       __syncwarp();          // every lane of the warp has fenced its stores
       if (lane == 0) mbar_arrive(full_dq(s));
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ms[i] = nms[i];
-        mz[i] = nmz[i];
-      }
+      return true;
+    };
+    // two register sets of scales and zero points, alternating between this
+    // group's stages: each set is loaded one stage ahead and read only by its
+    // own stage, so no stage waits for the next stage's loads. Scales and
+    // zero points are weights: with static weights the first set is read
+    // before the wait for the previous grid (which orders this warp's stores
+    // of Y)
+    uint32_t ma[4], za[4], mb[4], zb[4];
+    if (p.early_weights && dg < nk) load_meta(dg, ma, za);
+    grid_dependency_wait();
+    if (!p.early_weights && dg < nk) load_meta(dg, ma, za);
+    for (int kb = dg; kb < nk; kb += 2 * groups) {
+      if (kb + groups < nk) load_meta(kb + groups, mb, zb);
+      if (!stage(kb, ma, za) || kb + groups >= nk) break;
+      if (kb + 2 * groups < nk) load_meta(kb + 2 * groups, ma, za);
+      if (!stage(kb + groups, mb, zb)) break;
     }
 
     // epilogue: TMEM lanes 32q..32q+31 are output columns, TMEM columns are tokens
-    const bool have_accum = mbar_wait(accum_bar, 0, abort_flag, kErrEpilogue);
+    const bool have_accum = mbar_wait(accum_bar, 0, abort_flag, kErrEpilogue, p.err);
     __syncwarp();
     if (__all_sync(0xffffffffu, have_accum)) {  // warp-uniform: tcgen05.ld is .aligned
       tc_fence_after();
@@ -699,9 +514,31 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
 
 namespace {
 
+template <int SA, bool kB>
+cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const TcParams& prm,
+                          dim3 grid, size_t smem, cudaStream_t stream) {
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(tc_gemm_kernel<SA, kB>), 227 * 1024);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<SA, kB>, tmA, tmW, prm);
+}
+
+}  // namespace
+
 // Encoded tensor maps of recent calls, keyed by what they encode: encoding
 // one costs a driver call, and a layer calls with the same pointers and
 // shapes every step. A small table per process, replaced round-robin.
+namespace {
+
 struct MapKey {
   const void* ptr;
   uint64_t dims0, dims1;
@@ -718,11 +555,11 @@ MapKey g_map_keys[kMapCache];
 CUtensorMap g_maps[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-// 2-D tensor map of a row-major [dims1][dims0] array (row pitch dims0
-// elements), box [box1][box0], 128B swizzle for the activations.
-bool tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
-                uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
-                CUtensorMapSwizzle swizzle) {
+}  // namespace
+
+bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
+                       uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle) {
   const MapKey key = {ptr, dims0, dims1, box0, box1, (int)dt};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
@@ -749,26 +586,6 @@ bool tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int e
   return true;
 }
 
-template <int SA, bool kB>
-cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const TcParams& prm,
-                          dim3 grid, size_t smem, cudaStream_t stream) {
-  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(tc_gemm_kernel<SA, kB>), 227 * 1024);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<SA, kB>, tmA, tmW, prm);
-}
-
-}  // namespace
-
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                            int split, void* workspace, bool early_weights, bool bf16,
@@ -776,11 +593,11 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   const int bt = tc_token_tile(M);
   const int sa = tc_stage_atoms(M, K, group);
   CUtensorMap tmA, tmW;
-  if (!tensor_map(&tmA, A, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  if (!cached_tensor_map(&tmA, A, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   2, (uint64_t)K, (uint64_t)M, 64, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
-  if (!tensor_map(&tmW, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(K / kAtomK) * kAtomWords,
+  if (!cached_tensor_map(&tmW, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(K / kAtomK) * kAtomWords,
                   (uint64_t)(N / kStripCols), (uint32_t)(kAtomWords * sa), kTileN / kStripCols,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
@@ -796,6 +613,8 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.split = split < 1 ? 1 : split;
   prm.row_scale = row_scale;
   prm.early_weights = early_weights ? 1 : 0;
+  cudaError_t e = device_error_word(&prm.err);
+  if (e != cudaSuccess) return e;
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;
@@ -817,7 +636,7 @@ namespace {
 // mbarrier that nothing ever arrives on and waits for its first phase with
 // the kernel's own wait routine and limit. The wait gives up, records
 // kErrMma in the error word, and the kernel returns.
-__global__ void selftest_mbar_kernel() {
+__global__ void selftest_mbar_kernel(int* err) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x != 0) return;
@@ -825,13 +644,16 @@ __global__ void selftest_mbar_kernel() {
   mbar_init(b, 1);
   abort_flag = 0;
   fence_barrier_init();
-  mbar_wait(b, 0, &abort_flag, kErrMma);
+  mbar_wait(b, 0, &abort_flag, kErrMma, err);
 }
 
 }  // namespace
 
 cudaError_t launch_selftest_mbar_wait(cudaStream_t stream) {
-  selftest_mbar_kernel<<<1, 32, 0, stream>>>();
+  int* err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  selftest_mbar_kernel<<<1, 32, 0, stream>>>(err);
   return cudaGetLastError();
 }
 

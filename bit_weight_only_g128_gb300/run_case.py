@@ -6,9 +6,11 @@
 Each case is MxKxN with an optional group suffix (gK is the per-channel
 group; default g128). Its weight is drawn on the device from a seeded
 generator (N(0, 0.02)), quantized and packed by the library, and multiplied
-by a seeded N(0, 1) activation matrix `warmup + iters` times; each timed
-launch is bracketed by CUDA events on the launching stream and its time is
-printed with the achieved TFLOP/s and HBM GB/s (algorithmic bytes). The
+by a seeded N(0, 1) activation matrix `warmup + iters` times, launched back
+to back with a CUDA event between consecutive launches on the launching
+stream; each timed launch's interval is printed with the achieved TFLOP/s and
+HBM GB/s (algorithmic bytes; weights in L2 after the first launch when they
+fit there). The
 cases run one after another and each frees its buffers before the next, so
 that a profiler can be pointed at a few launches of one shape (for example
 `ncu -k regex:tc_ -s <warm-up launches> -c 1 ...`) without the memory of a
@@ -49,16 +51,15 @@ def run(M, K, N, group, path="auto", parts=0, warmup=1, iters=3, bf16=False, see
     Y = torch.empty((M, N), dtype=dt, device=dev)
     ws = w4.new_workspace(w4.workspace_size(M, N, K, group, path, parts), dev)
     stream = torch.cuda.current_stream()
-    times = []
+    # every launch queued back to back, an event between consecutive launches:
+    # each interval is one launch's device time (the host never idles the GPU)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(warmup + iters + 1)]
+    events[0].record(stream)
     for i in range(warmup + iters):
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
         w4.gemm(A, pw, out=Y, path=path, parts=parts, workspace=ws, static_weights=True)
-        end.record(stream)
-        end.synchronize()
-        if i >= warmup:
-            times.append(start.elapsed_time(end) * 1e3)
+        events[i + 1].record(stream)
+    events[-1].synchronize()
+    times = [events[i].elapsed_time(events[i + 1]) * 1e3 for i in range(warmup, warmup + iters)]
     w4.device_status()
     used_path, used_parts = w4.plan(M, N, K, group)
     us = min(times) if times else float("nan")

@@ -105,6 +105,13 @@ extern "C" {
  * the decode path takes. */
 #define W4A16_PATH_DECODE_RESIDENT 3
 #define W4A16_PATH_DECODE_STREAMK 4
+/* The tensor-core GEMM on pairs of SMs (tcgen05.mma.cta_group::2): clusters
+ * of two CTAs, each pair one output tile of 256 columns x 256 tokens (128
+ * when M <= 128) over all of K; each CTA dequantizes its 128 columns and
+ * stages half of the tokens, and the pair's MMAs read both halves. The same
+ * arithmetic as W4A16_PATH_TENSOR (RNE_fp16((q - z) s) operands, fp32
+ * accumulation); no K split and no workspace of its own. */
+#define W4A16_PATH_TENSOR_PAIR 5
 /* Flag OR-ed into the path of w4a16_gemm_ex: the weights (Wq, scales, zeros)
  * are not written by the work queued just before this call on the stream, so
  * the kernel may read them while that work drains. The GEMM kernels (both

@@ -93,7 +93,7 @@ def test_gemm_argument_errors(lib):
     assert _gemm(lib, Y=8) == -3
     assert _gemm(lib, Z=4) == -3
     assert _gemm(lib, path=7) == -1
-    assert _gemm(lib, path=5) == -1
+    assert _gemm(lib, path=6) == -1
     assert _gemm(lib, path=0x1000 | 1) == -1          # unknown flag bit
     # W4A8 keeps the activations' codes in the workspace: none given
     assert _gemm(lib, path=0x800 | 3, ws=0) == -4

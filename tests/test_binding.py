@@ -48,4 +48,5 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def test_flag_values():
     assert (w4.STATIC_WEIGHTS, w4.SILU_MUL, w4.BF16, w4.ACT_A8) == (0x100, 0x200, 0x400, 0x800)
-    assert set(w4._PATHS) == {"auto", "decode", "tensor", "decode-resident", "decode-streamk"}
+    assert set(w4._PATHS) == {"auto", "decode", "tensor", "decode-resident", "decode-streamk",
+                              "tensor-pair"}

@@ -15,7 +15,7 @@ from gpu_util import cuda, host, prepare
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["decode-resident", "decode-streamk", "tensor"]
+PATHS = ["decode-resident", "decode-streamk", "tensor", "tensor-pair"]
 
 
 def bits16(t):

@@ -98,3 +98,67 @@ def test_tensor_split_workspace_is_left_zeroed():
         y, mag = oracle.reference(A, q, s, z, group)
         assert oracle.check(half_bits(Y), y, mag)[0] <= 1.0
         assert int(ws[:32768].view(torch.int32).abs().sum()) == 0
+
+
+# the two-SM kernel (cta_group::2): pairs of 128-column halves, 128- or
+# 256-token tiles split between the two CTAs; ragged pairs (N not a multiple
+# of 256, a second CTA with few or no columns), ragged and partly empty token
+# halves (M inside the first half of a tile), every ring depth in use
+PAIR_CASES = [
+    # M, K, N, group
+    (1, 64, 16, 64),
+    (17, 128, 256, 128),
+    (128, 256, 256, 128),
+    (129, 512, 512, 128),
+    (256, 1024, 384, 128),   # second pair: one CTA with 128 columns, one with none
+    (300, 768, 400, 256),    # second token tile: the second CTA's half is empty
+    (512, 4096, 1024, 128),
+    (700, 2048, 272, 2048),
+    (1024, 1088, 512, 64),   # K not a multiple of 128
+    (4096, 512, 768, 128),
+]
+
+
+@pytest.mark.parametrize("M,K,N,group", PAIR_CASES)
+def test_tensor_pair_path(M, K, N, group):
+    run_and_check(M, K, N, group, seed=M * 11 + N, path="tensor-pair")
+
+
+def test_tensor_pair_outliers_and_auto_choice():
+    run_and_check(512, 4096, 512, 128, seed=4, path="tensor-pair", outliers=True)
+    assert w4.plan(512, 512, 4096, 128)[0] in ("tensor", "tensor-pair")
+    run_and_check(512, 4096, 512, 128, seed=5, path="auto", outliers=True)
+
+
+def test_integer_product_is_exact_on_the_pair():
+    K, N, M, group = 512, 256, 300, 128
+    rng = np.random.default_rng(18)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = np.full((K // group, N), 8, np.uint8)
+    s = np.full((K // group, N), 1.0, np.float16)
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    exact = A.astype(np.int64) @ (q.astype(np.int64) - 8)
+    pw = w4.pack(cuda(q), cuda(s), cuda(z), group)
+    Y = w4.gemm(cuda(A), pw, path="tensor-pair")
+    w4.device_status()
+    assert np.array_equal(Y.cpu().numpy().astype(np.int64), exact)
+
+
+@pytest.mark.parametrize("M", [256, 512])
+def test_one_and_two_sm_kernels_agree(M):
+    """Both tensor-core kernels within tolerance of the oracle; with the same
+    operands and fp32 accumulation over the same K order they should agree to
+    the last bit or within one unit of the result's rounding."""
+    K, N, group = 2048, 512, 128
+    W = synthetic.small_weights(K, N, seed=M + 1)
+    A = synthetic.small_activations(M, K, seed=M + 1)
+    (q, s, z), pw = prepare(W, group)
+    y, mag = oracle.reference(A, q, s, z, group)
+    Ad = cuda(A)
+    Y1 = half_bits(w4.gemm(Ad, pw, path="tensor"))
+    Y2 = half_bits(w4.gemm(Ad, pw, path="tensor-pair"))
+    w4.device_status()
+    assert oracle.check(Y1, y, mag)[0] <= 1.0
+    assert oracle.check(Y2, y, mag)[0] <= 1.0
+    diff = np.abs(oracle.from_half(Y1) - oracle.from_half(Y2))
+    assert np.all(diff <= 2 * (2.0 ** -9 * mag + 1e-3))
