@@ -76,14 +76,25 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
   return (int)c;
 }
 
-// Decode GEMV up to 16 rows; above, the one-SM tensor-core GEMM, and from
-// 256 rows the two-SM one.
+// Decode GEMV up to 16 rows; above, the tensor-core GEMM: on SM pairs
+// (tcgen05.mma.cta_group::2) where it measured faster than on single SMs, else
+// one SM per tile. Measured on GB300 with the Llama shapes (TFLOP/s, one SM /
+// pair):
+//   4096 rows: 70B gate_up 1234 / 1276, down 1285 / 1333, qkv 1167 / 1198,
+//              o_proj 1190 / 1223; 7B o_proj (K = N = 4096) 973 / 945
+//   2048 rows: 7B qkv 968 / 959, gate_up 1046 / 1049
+//    512 rows: 70B gate_up 1166 / 1240, down 1068 / 1129, qkv 677 / 665,
+//              o_proj 992 / 992
+//    256, 128 rows: 13B qkv 862 / 855, 522 / 451
+// so the pair takes M >= 4096 with N*K >= 2^26 and M >= 512 with
+// N*K >= 2^27.
 int choose_path(int M, int N, int K, int group) {
-  (void)N;
-  (void)K;
   (void)group;
   if (M <= 16) return W4A16_PATH_DECODE;
-  return M >= 256 ? W4A16_PATH_TENSOR_PAIR : W4A16_PATH_TENSOR;
+  const long long nk = (long long)N * K;
+  if ((M >= 4096 && nk >= (1LL << 26)) || (M >= 512 && nk >= (1LL << 27)))
+    return W4A16_PATH_TENSOR_PAIR;
+  return W4A16_PATH_TENSOR;
 }
 
 bool is_tensor(int path) { return path == W4A16_PATH_TENSOR || path == W4A16_PATH_TENSOR_PAIR; }

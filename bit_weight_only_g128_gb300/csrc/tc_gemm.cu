@@ -104,8 +104,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   volatile int* last_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 8u - base));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTileN;
-  const int m0 = blockIdx.y * bt;
+  // grid: x = token tiles (fastest, so the token tiles of one column tile run
+  // together and its weights are read from DRAM once), y = column tiles, z = K
+  // ranges
+  const int n0 = blockIdx.y * kTileN;
+  const int m0 = blockIdx.x * bt;
   // this CTA's K range: stages [kb0, kb0 + nk)
   const int nk_all = p.K / (kStageK * SA);
   const int kb0 = (int)((long long)blockIdx.z * nk_all / p.split);
@@ -621,7 +624,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   const size_t smem = tc_smem_bytes(bt, sa, &prm.stages);
   prm.tmem_cols = pow2_at_least(bt);
   prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
-  const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + bt - 1) / bt),
+  const dim3 grid((unsigned)((M + bt - 1) / bt), (unsigned)((N + kTileN - 1) / kTileN),
                   (unsigned)prm.split);
   if (bf16)
     return sa == 2 ? launch_kernel<2, true>(tmA, tmW, prm, grid, smem, stream)

@@ -204,8 +204,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   const uint32_t rank = cluster_rank();  // 0: the CTA that issues the MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kCols;     // this CTA's 128 weight columns
-  const int m0 = blockIdx.y * bt;        // the pair's tokens
+  // grid: x = 2 * token tile + column half (the pair: two consecutive x; token
+  // tiles fastest, so the token tiles of one column pair run together and its
+  // weights are read from DRAM once), y = column pair
+  const int n0 = (2 * blockIdx.y + (blockIdx.x & 1)) * kCols;  // this CTA's 128 weight columns
+  const int m0 = (blockIdx.x >> 1) * bt;                        // the pair's tokens
   const int nk = p.K / (kStageK * SA);   // stages
   const int groups = p.dq_groups;
   const int wpg = kDqWarps / groups;     // dequant warps per group
@@ -560,7 +563,7 @@ cudaError_t launch_tc_pair(const uint16_t* A, const uint32_t* Wq, const uint16_t
   if (e != cudaSuccess) return e;
   const size_t smem = tc_pair_smem_bytes(bt, sa, &prm.act_slots, &prm.dq_slots, &prm.code_slots);
   prm.dq_groups = 2;
-  const dim3 grid((unsigned)(2 * ((N + 2 * kCols - 1) / (2 * kCols))), (unsigned)((M + bt - 1) / bt), 1);
+  const dim3 grid((unsigned)(2 * ((M + bt - 1) / bt)), (unsigned)((N + 2 * kCols - 1) / (2 * kCols)), 1);
   if (bf16)
     return sa == 2 ? launch_pair_kernel<2, true>(tmA, tmW, prm, grid, smem, stream)
                    : launch_pair_kernel<1, true>(tmA, tmW, prm, grid, smem, stream);
