@@ -253,8 +253,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t ph = (uint32_t)(kb / stages) & 1u;
       if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant, p.err)) return false;
       const uint32_t st = base + (uint32_t)s * stage_bytes;
+      // the next strip's codes are loaded while this strip is converted (the
+      // loop is unrolled: no register copies)
+      uint4 v[2][SA];
+      auto load_codes = [&](int i, uint4 (&d)[SA]) {
+#pragma unroll
+        for (int u = 0; u < SA; ++u)
+          d[u] = lds128(st + packed_off + (groups * sub + i) * (SA * 512) + u * 512 + lane * 16);
+      };
+      load_codes(0, v[0]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
+        if (i + 1 < 4 && i + 1 < groups) load_codes(i + 1, v[(i + 1) & 1]);
         const int ls = groups * sub + i;  // strip within the tile
         if (i < groups && n0 / kStripCols + ls < nstrips) {
           const uint32_t z0 = mz[i] & 15u, z1 = (mz[i] >> 4) & 15u;
@@ -262,12 +272,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int u = 0; u < SA; ++u) {
             const uint32_t wdq = st + wdq_off + u * kWdqBytes;
-            const uint4 v = lds128(st + packed_off + ls * (SA * 512) + u * 512 + lane * 16);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
               const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
-              const uint32_t word = ks ? (r ? v.w : v.z) : (r ? v.y : v.x);
+              const uint4 vv = v[i & 1][u];
+              const uint32_t word = ks ? (r ? vv.w : vv.z) : (r ? vv.y : vv.x);
               uint32_t o[4];
               if (kB)
                 dequant_word_bf16(word, make_deq_const_bf16(r ? z1 : z0, r ? s1 : s0), o);
