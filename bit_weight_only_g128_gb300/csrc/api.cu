@@ -76,10 +76,19 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
   return (int)c;
 }
 
-// Decode GEMV up to 16 rows; above, the tensor-core GEMM: on SM pairs
-// (tcgen05.mma.cta_group::2) where it measured faster than on single SMs, else
-// one SM per tile. Measured on GB300 with the Llama shapes (TFLOP/s, one SM /
-// pair):
+// The path for M rows, from measurements on GB300 (CUDA graphs of 20 launches
+// over weight copies larger than L2; the full table is kept with the design
+// notes).
+// Decode GEMV up to 16 rows, and up to 32 rows (two 16-row passes over the
+// weights) for wide layers of up to 2^28 weights, where one pass costs less
+// than half a tensor-core pass (us, decode / tensor):
+//   7B gate_up (4096 x 22016):  16 rows 16.4 / 31.8, 32 rows 32.0 / 32.5
+//   13B gate_up (5120 x 27648): 16 rows 22.6 / 46.1, 32 rows 44.5 / 44.8
+//   13B qkv (5120 x 15360):     16 rows 16.4 / 27.3, 20 rows 26.6 / 26.3
+//   70B gate_up (8192 x 57344): 20 rows 116.3 / 120.4, 24 rows 133.2 / 120.6
+// Above, the tensor-core GEMM: on SM pairs (tcgen05.mma.cta_group::2) where
+// it measured faster than on single SMs, else one SM per tile (TFLOP/s, one
+// SM / pair):
 //   4096 rows: 70B gate_up 1234 / 1276, down 1285 / 1333, qkv 1167 / 1198,
 //              o_proj 1190 / 1223; 7B o_proj (K = N = 4096) 973 / 945
 //   2048 rows: 7B qkv 968 / 959, gate_up 1046 / 1049
@@ -89,9 +98,10 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 // so the pair takes M >= 4096 with N*K >= 2^26 and M >= 512 with
 // N*K >= 2^27.
 int choose_path(int M, int N, int K, int group) {
-  (void)group;
-  if (M <= 16) return W4A16_PATH_DECODE;
   const long long nk = (long long)N * K;
+  // (group sizes the decode kernel does not take go to the tensor cores)
+  if ((M <= 16 || (M <= 32 && N >= 16384 && nk <= (1LL << 28))) && decode_units(N, K, group) > 0)
+    return W4A16_PATH_DECODE;
   if ((M >= 4096 && nk >= (1LL << 26)) || (M >= 512 && nk >= (1LL << 27)))
     return W4A16_PATH_TENSOR_PAIR;
   return W4A16_PATH_TENSOR;

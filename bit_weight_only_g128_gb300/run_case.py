@@ -14,7 +14,9 @@ fit there). The
 cases run one after another and each frees its buffers before the next, so
 that a profiler can be pointed at a few launches of one shape (for example
 `ncu -k regex:tc_ -s <warm-up launches> -c 1 ...`) without the memory of a
-whole workload.
+whole workload. With --graph L the case is instead timed as a CUDA graph of
+L launches over copies of the weight that together exceed L2, as the bench
+times its steps.
 """
 from __future__ import annotations
 
@@ -38,7 +40,10 @@ def alg_bytes(M, K, N, group):
     return K * N // 2 + 2 * G * N + G * N // 2 + 2 * M * K + 2 * M * N
 
 
-def run(M, K, N, group, path="auto", parts=0, warmup=1, iters=3, bf16=False, seed=0):
+L2_BYTES = 129 * 1024 * 1024
+
+
+def run(M, K, N, group, path="auto", parts=0, warmup=1, iters=3, bf16=False, seed=0, graph=0):
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
@@ -51,6 +56,8 @@ def run(M, K, N, group, path="auto", parts=0, warmup=1, iters=3, bf16=False, see
     Y = torch.empty((M, N), dtype=dt, device=dev)
     ws = w4.new_workspace(w4.workspace_size(M, N, K, group, path, parts), dev)
     stream = torch.cuda.current_stream()
+    if graph:
+        return run_graph(M, K, N, group, path, parts, pw, A, Y, ws, graph)
     # every launch queued back to back, an event between consecutive launches:
     # each interval is one launch's device time (the host never idles the GPU)
     events = [torch.cuda.Event(enable_timing=True) for _ in range(warmup + iters + 1)]
@@ -69,6 +76,41 @@ def run(M, K, N, group, path="auto", parts=0, warmup=1, iters=3, bf16=False, see
             "GBps": alg_bytes(M, K, N, group) / us / 1e3}
 
 
+def run_graph(M, K, N, group, path, parts, pw, A, Y, ws, launches):
+    """Mean time of one launch in a CUDA graph of `launches` back-to-back
+    launches (static weights, as a model's layers run), rotating over enough
+    copies of the packed weight that they do not stay in L2 between uses."""
+    copies = max(1, -(-3 * L2_BYTES // pw.nbytes))
+    ws_copies = [pw] + [w4.PackedWeight(pw.Wq.clone(), pw.Sp.clone(), pw.Zp.clone(), pw.K, pw.N,
+                                        pw.group) for _ in range(copies - 1)]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(launches):
+            w4.gemm(A, ws_copies[i % copies], out=Y, path=path, parts=parts, workspace=ws,
+                    static_weights=True)
+    times = []
+    with torch.cuda.stream(stream):
+        for rep in range(4):
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            g.replay()
+            end.record(stream)
+            end.synchronize()
+            if rep > 0:  # the first replay warms up
+                times.append(start.elapsed_time(end) * 1e3 / launches)
+    w4.device_status()
+    used_path, used_parts = w4.plan(M, N, K, group)
+    us = min(times)
+    return {"M": M, "K": K, "N": N, "group": group, "path": path,
+            "plan": used_path if path == "auto" else path, "parts": parts or used_parts,
+            "us": times, "best_us": us, "TFLOPs": 2.0 * M * N * K / us / 1e6,
+            "GBps": alg_bytes(M, K, N, group) / us / 1e3, "graph_launches": launches,
+            "weight_copies": copies}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--case", action="append", required=True, help="MxKxN[gG|gK]")
@@ -77,10 +119,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--bf16", action="store_true")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="time a CUDA graph of this many launches over L2-rotated weight copies")
     args = ap.parse_args()
     for text in args.case:
         M, K, N, group = parse_case(text)
-        res = run(M, K, N, group, args.path, args.parts, args.warmup, args.iters, args.bf16)
+        res = run(M, K, N, group, args.path, args.parts, args.warmup, args.iters, args.bf16,
+                  graph=args.graph)
         print(json.dumps(res), flush=True)
         torch.cuda.empty_cache()
 

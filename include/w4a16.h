@@ -245,8 +245,13 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
                             size_t* bytes);
 
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
- * The path (decode GEMV for M <= 16, tensor-core GEMM above) and its grid
- * are chosen from M, N, K and the device's SM count. `workspace` (256-byte
+ * The path and its grid are chosen from M, N, K, the group and the device's
+ * SM count, by rules measured on GB300: the decode GEMV for M <= 16 (and up
+ * to 32 rows, in two passes over the weights, for layers with N >= 16384
+ * and N*K <= 2^28), else the tensor-core GEMM, on SM pairs
+ * (W4A16_PATH_TENSOR_PAIR) for M >= 4096 with N*K >= 2^26 and for M >= 512
+ * with N*K >= 2^27, on single SMs otherwise; group sizes the decode kernel
+ * does not take always go to the tensor cores. `workspace` (256-byte
  * aligned, zero-filled before first use) may be NULL when
  * w4a16_workspace_size reports 0; W4A16_ERR_WORKSPACE_TOO_SMALL otherwise.
  * Y must not overlap the inputs. */
@@ -274,9 +279,10 @@ int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
                   int path, int parts, void* stream);
 
 /* The path and work partition w4a16_gemm would use on the current device:
- * for M <= 16 the decode variant (W4A16_PATH_DECODE_RESIDENT or
- * W4A16_PATH_DECODE_STREAMK) of a 16-row launch and its CTAs, else
- * W4A16_PATH_TENSOR and its K ranges. Host-only. */
+ * for the decode path the variant (W4A16_PATH_DECODE_RESIDENT or
+ * W4A16_PATH_DECODE_STREAMK) of a launch of min(M, 16) rows and its CTAs;
+ * for the tensor-core paths W4A16_PATH_TENSOR and its K ranges, or
+ * W4A16_PATH_TENSOR_PAIR and 1. Host-only. */
 int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
 
 /* The decode-path GEMM (same kernel, same results as w4a16_gemm_ex with

@@ -68,8 +68,11 @@ def test_decode_path_picks_a_variant(M, K, N, group):
 
 
 @pytest.mark.parametrize("M,K,N,group", [(1, 4096, 1024, 128), (16, 4096, 256, 128),
-                                         (17, 256, 64, 128), (33, 384, 80, 128)])
+                                         (17, 256, 64, 128), (33, 384, 80, 128),
+                                         (24, 1024, 16384, 128), (32, 512, 16400, 128),
+                                         (9, 768, 256, 192)])
 def test_auto_path(M, K, N, group):
+    # (24 and 32 rows of a wide layer: two decode passes; group 192: tensor cores)
     run_and_check(M, K, N, group, seed=M + K + N)
 
 
