@@ -77,6 +77,8 @@ class W4A16Error(RuntimeError):
 def lib() -> ctypes.CDLL:
     """Load libw4a16.so (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -98,9 +100,14 @@ def _check(rc: int, where: str) -> None:
         raise W4A16Error(rc, where, msg)
 
 
-def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream(stream: Optional[torch.cuda.Stream], device: Optional[int] = None) -> int:
+    """The cudaStream_t of `stream`, or of the current stream of `device`
+    (default: the current device)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if device is None:
+        device = torch.cuda.current_device()
+    return torch._C._cuda_getCurrentRawStream(device)
 
 
 def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
@@ -194,10 +201,11 @@ _ws_sizes = {}
 
 
 def workspace_size(M: int, N: int, K: int, group: int, path: str = "auto", parts: int = 0,
-                   silu_mul: bool = False, a8: bool = False) -> int:
+                   silu_mul: bool = False, a8: bool = False, device: Optional[int] = None) -> int:
     """Scratch bytes a gemm call with these arguments needs on the current
     device (cached per device and arguments: the size depends on nothing else)."""
-    dev = torch.cuda.current_device() if torch.cuda.is_available() else -1
+    dev = device if device is not None else (
+        torch.cuda.current_device() if torch.cuda.is_available() else -1)
     key = (dev, M, N, K, group, path, parts, silu_mul, a8)
     size = _ws_sizes.get(key)
     if size is None:
@@ -220,13 +228,14 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
 _stream_ws = {}
 
 
-def stream_workspace(nbytes: int, device, stream) -> torch.Tensor:
-    """The cached workspace of `stream` on `device`, at least `nbytes` long
-    (a larger zero-filled one replaces it when it is too small)."""
-    key = (torch.device(device).index, stream.cuda_stream)
+def stream_workspace(nbytes: int, device: int, stream: int) -> torch.Tensor:
+    """The cached workspace of the stream `stream` (a cudaStream_t) on device
+    index `device`, at least `nbytes` long (a larger zero-filled one replaces
+    it when it is too small)."""
+    key = (device, stream)
     ws = _stream_ws.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = _stream_ws[key] = new_workspace(nbytes, device)
+        ws = _stream_ws[key] = new_workspace(nbytes, torch.device("cuda", device))
     return ws
 
 
@@ -259,23 +268,24 @@ def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,
         raise ValueError(f"A has K={K}, weight has K={pw.K}")
     dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
     a_ptr = _dev(A, dt, "A")
+    dev = A.device.index
     if out is None:
         out = torch.empty((M, pw.N // 2 if silu_mul else pw.N), dtype=dt, device=A.device)
     y_ptr = _dev(out, dt, "out")
+    st = _stream(stream, dev)
     ws_ptr, ws_bytes = None, 0
-    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul, a8)
+    need = workspace_size(M, pw.N, pw.K, pw.group, path, parts, silu_mul, a8, dev)
     if need:
         if workspace is None:
-            s = stream if stream is not None else torch.cuda.current_stream(A.device)
-            workspace = stream_workspace(need, A.device, s)
+            workspace = stream_workspace(need, dev, st)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check(lib().w4a16_gemm_ex(a_ptr, pw.Wq.data_ptr(), pw.Sp.data_ptr(),
-                               pw.Zp.data_ptr(), M, pw.N, pw.K, pw.group,
-                               y_ptr, ws_ptr, ws_bytes,
-                               _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
-                               | (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
-                               | (BF16 if dt == torch.bfloat16 else 0), parts,
-                               _stream(stream)), "w4a16_gemm")
+    rc = lib().w4a16_gemm_ex(a_ptr, pw.Wq.data_ptr(), pw.Sp.data_ptr(), pw.Zp.data_ptr(), M,
+                             pw.N, pw.K, pw.group, y_ptr, ws_ptr, ws_bytes,
+                             _PATHS[path] | (STATIC_WEIGHTS if static_weights else 0)
+                             | (SILU_MUL if silu_mul else 0) | (ACT_A8 if a8 else 0)
+                             | (BF16 if dt == torch.bfloat16 else 0), parts, st)
+    if rc:
+        _check(rc, "w4a16_gemm")
     return out
 
 
