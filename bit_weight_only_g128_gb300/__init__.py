@@ -59,6 +59,7 @@ SIGNATURES = {
     "w4a16_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "w4a16_gemm_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _I, _I, _P]),
     "w4a16_plan": (_I, [_I, _I, _I, _I, _PI, _PI]),
+    "w4a16_tc_config": (_I, [_I, _I, _I, _PI, _I]),
     "w4a16_gemm_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "w4a16_device_status": (_I, [_P]),
     "w4a16_selftest_wait": (_I, [_I, _P]),
@@ -244,6 +245,17 @@ def plan(M: int, N: int, K: int, group: int) -> Tuple[str, int]:
     p, c = ctypes.c_int(), ctypes.c_int()
     _check(lib().w4a16_plan(M, N, K, group, ctypes.byref(p), ctypes.byref(c)), "w4a16_plan")
     return {v: k for k, v in _PATHS.items()}[p.value], c.value
+
+
+TC_CONFIG_KEYS = ("token_tile", "stage_atoms", "act_slots", "code_slots", "dq_slots",
+                  "dequant_groups", "smem_bytes", "ctas_per_sm")
+
+
+def tc_config(M: int, K: int, group: int) -> dict:
+    """The one-SM tensor-core kernel's configuration for M rows (host-only)."""
+    out = (ctypes.c_int * 8)()
+    _check(lib().w4a16_tc_config(M, K, group, out, 8), "w4a16_tc_config")
+    return dict(zip(TC_CONFIG_KEYS, list(out)))
 
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,

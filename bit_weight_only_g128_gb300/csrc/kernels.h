@@ -99,12 +99,14 @@ bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt
                        uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
                        CUtensorMapSwizzle swizzle);
 int tc_choose_split(int M, int N, int K, int group, int sms);
-// 64-k atoms per pipeline stage of the tensor-core GEMM for M rows (2 when K
-// and the group are multiples of 128 and 4 such stages fit, else 1).
+// 64-k atoms per pipeline stage of the tensor-core GEMM (2 when K and the
+// group are multiples of 128, else 1).
 int tc_stage_atoms(int M, int K, int group);
-// Token tile (MMA N) used for M rows, and the dynamic shared memory it needs.
+// Token tile (MMA N) used for M rows.
 int tc_token_tile(int M);
-size_t tc_smem_bytes(int bt, int stage_atoms, int* stages);
+// The one-SM kernel's configuration for M rows (w4a16_tc_config's out[0..7]);
+// false if its rings would break the kernel's barrier invariants.
+bool tc_config(int M, int K, int group, int out[8]);
 
 // Self-tests of the bounded waits (a flag wait of the stream-K decode
 // kernel's kind, an mbarrier wait of the tensor-core pipeline's kind): each

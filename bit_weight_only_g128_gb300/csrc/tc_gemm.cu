@@ -2,29 +2,42 @@
 //
 // At large M the layer is a dense contraction: once the weights are
 // dequantized, what remains is an ordinary fp16 matrix product (the point made
-// in the vLLM PR #1032 thread). So the int4 weights are dequantized into
-// shared memory and fed to tcgen05.mma kind::f16 with fp32 accumulation in
-// tensor memory.
+// in the vLLM PR #1032 thread). Here CUDA cores dequantize the int4 weights
+// straight into tensor memory, which tcgen05.mma kind::f16 reads as its A
+// operand; the activations are the B operand, in shared memory; the fp32
+// accumulators are in tensor memory too.
 //
-// Orientation: D[n][m] = sum_k Wdeq[n][k] * A[m][k] (the weight tile is the
-// 128-row MMA operand, the tokens are the MMA's N dimension). Each
-// dequantized weight then serves up to 256 tokens, which halves the dequant
-// work per FLOP compared with putting the tokens on the 128-row side, and
-// token tiles of 16..256 cover the middle band of M as well.
+// Orientation: D[n][m] = sum_k Wdeq[n][k] * A[m][k]: weight column n is
+// tensor-memory lane n of the 128-row A operand and of the accumulator, the
+// tokens are the MMA's N dimension (16..256). Each dequantized weight serves
+// up to 256 tokens.
 //
-// CTA (one output tile: 128 columns x BT tokens, full K):
-//   warp 0      TMA producer: activations tile [BT x 64] (128B swizzle) and
-//               the packed int4 atoms of 8 strips [8 x 512 B] per k-stage;
-//   warp 1      TMEM allocation; one thread issues 4 MMAs (K=16) per stage;
-//   warps 2..9  dequantize the packed atoms into the 128B-swizzled K-major
-//               operand tile (usually 4 pairs of warps, each pair on every
-//               4th stage, so 4 stages are converted concurrently), then run
-//               the epilogue (TMEM -> fp16 Y).
-// Stages form a ring guarded by mbarriers: full_tma (TMA bytes landed),
-// full_dq (the stage's dequant group done), empty (MMAs of the stage
-// completed).
-// Every wait is bounded; a wait that gives up sets the library's device
-// error word and the CTA drains and exits.
+// Shared memory per SM carries only the copies of the packed codes and of the
+// activations and their reads; the dequantized operand (16 KiB per 64 k of a
+// 128-column tile) never passes through it, which leaves room for rings deep
+// enough to cover a DRAM round trip.
+//
+// CTA (one output tile of 128 columns x BT tokens over one K range):
+//   warp 0      TMA producer (one thread, polling): the packed codes of the
+//               tile's 8 strips (a 3-D map with the 128-byte swizzle, so that
+//               the dequantizing threads' 16-byte reads of one column each
+//               fall on distinct banks) up to the code ring's depth ahead,
+//               and the activations [BT x 64 k] per atom (128-byte swizzle)
+//               up to the activation ring's depth ahead;
+//   warp 1      tensor-memory allocation; one thread issues 4 MMAs per 64 k
+//               of a stage, A from tensor memory;
+//   warps 2..9  two groups of four warps, one warp per lane quarter; group g
+//               converts the stages g, g + 2, ...: each thread dequantizes
+//               one weight column's k of the stage into 32-bit tensor-memory
+//               cells of its own lane (tcgen05.st 32x32b); then the epilogue
+//               (tensor memory -> Y).
+// Rings and their barriers: activations (act_full; stage_done when the
+// stage's MMAs completed, which also frees the stage's dequantized slot),
+// packed codes (code_full, code_empty once the converting warps hold them in
+// registers), dequantized operand in tensor memory (dq_full, after the
+// converting warps' stores and the stage's activations landed).
+// Every wait is bounded; a wait that gives up sets the library's device error
+// word and the CTA drains and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,13 +56,18 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int kTileN = 128;        // output columns per CTA (MMA M)
-constexpr int kStageK = 64;        // k per atom of a pipeline stage (one 128-byte swizzle row)
-constexpr int kDqWarps = 8;
-constexpr int kDqThreads = kDqWarps * 32;
-constexpr int kThreads = 64 + kDqThreads;
-constexpr int kWdqBytes = kTileN * kStageK * 2;   // 16 KiB dequantized operand
-constexpr int kPackedBytes = kTileN * kStageK / 2;  // 4 KiB packed codes
-constexpr size_t kTcCounterBytes = 32768;          // tile counters of a K-split launch
+constexpr int kStageK = 64;        // k per atom (one 128-byte swizzle row of activations)
+// NG groups of four dequantizing warps (one warp per tensor-memory lane
+// quarter): 2 at two CTAs per SM, 4 at one
+template <int NG>
+struct Warps {
+  static constexpr int kDqThreads = 128 * NG;
+  static constexpr int kThreads = 64 + kDqThreads;
+};
+constexpr int kCodeAtomBytes = kTileN * kStageK / 2;  // 4 KiB: 8 strips x 512 B
+constexpr int kAtomCols = kStageK / 2;  // tensor-memory columns of one atom's A operand
+constexpr size_t kTcCounterBytes = 32768;  // tile counters of a K-split launch
+constexpr int kBarBytes = 1024;            // barriers and flags after the rings
 
 using namespace tc;
 
@@ -62,42 +80,48 @@ struct TcParams {
   int* counters;  // split > 1: one per output tile, zero between calls
   float* tiles;   // split > 1: fp32 partial tiles [tile][split][bt][128]
   int M, N, K, group;
-  int bt;         // token tile (MMA N): multiple of 16, 16..256
-  int stages;     // pipeline depth
+  int bt;          // token tile (MMA N): multiple of 16, 16..256
+  int act_slots;   // activation ring depth (stages)
+  int code_slots;  // packed-code ring depth (stages)
+  int dq_slots;    // dequantized-operand ring depth (stages), at most act_slots
+  int dq_col0;     // first tensor-memory column of the dequantized-operand ring
   int tmem_cols;
-  int split;      // K ranges per output tile (grid z)
-  int dq_groups;  // dequant warp groups (4, 2 or 1), dividing `stages`
+  int split;       // K ranges per output tile (grid z)
   int early_weights;  // weights are static: read the first stages' codes and
                       // scales before the grid-dependency wait
   const float* row_scale;  // W4A8: per-row factors of the result, or null
   int* err;                // the library's error word
 };
 
+// named barrier of the dequant/epilogue warps
+template <int NT>
+__device__ __forceinline__ void epilogue_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
-// named barrier of the 8 dequant/epilogue warps
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// SA: atoms (64 k) per pipeline stage, 1 or 2. A stage of two atoms halves
-// the barrier hand-offs per weight byte; it needs an even number of atoms
-// and groups of at least 128 (one scale and zero point per stage).
-template <int SA, bool kB>
-__global__ void __launch_bounds__(kThreads, 2)
+// SA: atoms (64 k) per pipeline stage, 1, 2 or 4. Larger stages cut the
+// barrier hand-offs per weight byte; SA >= 2 needs K and the group to be
+// multiples of 128 (one scale and zero point per 128 k). NG: dequant groups.
+template <int SA, bool kB, int NG>
+__global__ void __launch_bounds__(Warps<NG>::kThreads, NG == 2 ? 2 : 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const int bt = p.bt, stages = p.stages;
-  const uint32_t act_bytes = (uint32_t)bt * 128u;  // one atom of activations
-  const uint32_t stage_bytes = SA * (act_bytes + kWdqBytes + kPackedBytes);
-  // stage s: [activations of atom 0..SA-1 | dequantized weights of atom
-  // 0..SA-1 | packed codes of the SA atoms], each piece 1024-aligned
-  const uint32_t wdq_off = SA * act_bytes, packed_off = SA * (act_bytes + kWdqBytes);
-  const uint32_t bars = base + (uint32_t)stages * stage_bytes;
-  auto full_tma = [&](int s) { return bars + 8u * s; };
-  auto full_dq = [&](int s) { return bars + 8u * (stages + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * stages + s); };
-  const uint32_t accum_bar = bars + 8u * (3 * stages);
+  const int bt = p.bt, nact = p.act_slots, ncode = p.code_slots, ndq = p.dq_slots;
+  const uint32_t atom_act = (uint32_t)bt * 128u;  // one atom of activations
+  const uint32_t act_bytes = SA * atom_act;
+  const uint32_t code_bytes = SA * kCodeAtomBytes;
+  // [activation ring | code ring | barriers], slots 1024-aligned
+  const uint32_t code_base = base + (uint32_t)nact * act_bytes;
+  const uint32_t bars = code_base + (uint32_t)ncode * code_bytes;
+  auto act_full = [&](int a) { return bars + 8u * a; };
+  auto stage_done = [&](int a) { return bars + 8u * (nact + a); };
+  auto dq_full = [&](int w) { return bars + 8u * (2 * nact + w); };
+  auto code_full = [&](int c) { return bars + 8u * (2 * nact + ndq + c); };
+  auto code_empty = [&](int c) { return bars + 8u * (2 * nact + ndq + ncode + c); };
+  const uint32_t accum_bar = bars + 8u * (2 * nact + ndq + 2 * ncode);
   const uint32_t tmem_slot = accum_bar + 8u;
   uint8_t* gen_base = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 4u - base));
@@ -115,10 +139,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int nk = (int)((long long)(blockIdx.z + 1) * nk_all / p.split) - kb0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(full_tma(s), 1);
-      mbar_init(full_dq(s), kDqWarps / p.dq_groups);  // one arrival per warp of the group
-      mbar_init(empty(s), 1);
+    for (int a = 0; a < nact; ++a) {
+      mbar_init(act_full(a), 1);
+      mbar_init(stage_done(a), 1);
+    }
+    for (int w = 0; w < ndq; ++w) mbar_init(dq_full(w), 4);  // the group's four warps
+    for (int c = 0; c < ncode; ++c) {
+      mbar_init(code_full(c), 1);
+      mbar_init(code_empty(c), 4);
     }
     mbar_init(accum_bar, 1);
     *abort_flag = 0;
@@ -138,180 +166,238 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
+    // One thread keeps both rings full: it polls the slot of the next copy of
+    // each ring and issues whichever is free, so that neither ring waits for
+    // the other's slots.
     if (lane == 0) {
-      auto load_codes = [&](int kb, uint32_t st, int s) {
-        tma_load_2d(st + packed_off, &tmW, (kb0 + kb) * SA * kAtomWords, n0 / kStripCols,
-                    full_tma(s));
+      auto codes = [&](int kb) {
+        const int c = kb % ncode;
+        mbar_expect_tx(code_full(c), code_bytes);
+        tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, (kb0 + kb) * SA * 4,
+                    n0 / kStripCols, code_full(c));
       };
-      auto load_act = [&](int kb, uint32_t st, int s) {
+      auto acts = [&](int kb) {
+        const int a = kb % nact;
+        const uint32_t st = base + (uint32_t)a * act_bytes;
+        mbar_expect_tx(act_full(a), act_bytes);
 #pragma unroll
         for (int u = 0; u < SA; ++u)
-          tma_load_2d(st + u * act_bytes, &tmA, ((kb0 + kb) * SA + u) * kStageK, m0, full_tma(s));
+          tma_load_2d(st + u * atom_act, &tmA, ((kb0 + kb) * SA + u) * kStageK, m0, act_full(a));
       };
-      // static weights: the first ring's codes go out before the wait for the
-      // previous grid (the slots are free: nothing has used them yet)
-      const int pre = p.early_weights ? (nk < stages ? nk : stages) : 0;
-      for (int kb = 0; kb < pre; ++kb) {
-        mbar_expect_tx(full_tma(kb), SA * (act_bytes + kPackedBytes));
-        load_codes(kb, base + (uint32_t)kb * stage_bytes, kb);
-      }
+      int ci = 0, ai = 0;
+      // static weights: the first ring of codes goes out before the wait for
+      // the previous grid (the slots are free: nothing has used them yet)
+      if (p.early_weights)
+        for (; ci < nk && ci < ncode; ++ci) codes(ci);
       grid_dependency_wait();
-      for (int kb = 0; kb < pre; ++kb) load_act(kb, base + (uint32_t)kb * stage_bytes, kb);
-      int issued = pre;
-      for (int kb = pre; kb < nk; ++kb) {
-        const int s = kb % stages;
-        const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, kErrProducer, p.err)) break;
-        const uint32_t st = base + (uint32_t)s * stage_bytes;
-        mbar_expect_tx(full_tma(s), SA * (act_bytes + kPackedBytes));
-        load_act(kb, st, s);
-        load_codes(kb, st, s);
-        ++issued;
+      uint64_t t0 = globaltimer();
+      uint32_t idle = 0;
+      while (ci < nk || ai < nk) {
+        bool progress = false;
+        if (ci < nk && mbar_test(code_empty(ci % ncode), ((uint32_t)(ci / ncode) & 1u) ^ 1u)) {
+          codes(ci++);
+          progress = true;
+        }
+        if (ai < nk && mbar_test(stage_done(ai % nact), ((uint32_t)(ai / nact) & 1u) ^ 1u)) {
+          acts(ai++);
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          if (*abort_flag) break;
+          const uint64_t t = globaltimer();
+          if (idle == 64) t0 = t;  // first check of this idle spell
+          else if (t - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(p.err, kErrProducer);
+            break;
+          }
+        }
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA exits
-        for (int kb = (issued > stages ? issued - stages : 0); kb < issued; ++kb)
-          mbar_drain(full_tma(kb % stages), (uint32_t)(kb / stages) & 1u, p.err);
+        for (int kb = (ai > nact ? ai - nact : 0); kb < ai; ++kb)
+          mbar_drain(act_full(kb % nact), (uint32_t)(kb / nact) & 1u, p.err);
+        for (int kb = (ci > ncode ? ci - ncode : 0); kb < ci; ++kb)
+          mbar_drain(code_full(kb % ncode), (uint32_t)(kb / ncode) & 1u, p.err);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // dq_full completes when the stage's four converting warps have arrived,
+    // each after its tensor-memory stores completed and the stage's
+    // activations landed: one test covers both operands. The next stage's
+    // barrier is tested between this stage's MMAs, while the tensor core
+    // works through the queued ones.
     if (lane == 0) {
       const uint32_t idesc = f16_idesc(kTileN, bt, kB);
-      bool ok = true;
-      int s = 0;
-      uint32_t ph = 0;
-      // descriptors of stage 0, atom 0; stage s adds s * stage_bytes >> 4,
-      // atom u adds u * act_bytes >> 4 (activations) or u * kWdqBytes >> 4
-      const uint64_t bdesc0 = sw128_kmajor_desc(base);
-      const uint64_t adesc0 = sw128_kmajor_desc(base + wdq_off);
+      int a = 0, w = 0;
+      uint32_t pw = 0;
+      bool ok = nk > 0 && mbar_wait(dq_full(0), 0, abort_flag, kErrMma, p.err);
       for (int kb = 0; kb < nk && ok; ++kb) {
-        // The dequant group arrives on full_dq only after its own wait on the
-        // stage's full_tma phase: acquiring full_dq orders these MMAs after the
-        // stage's TMA bytes (activations and codes) as well, so full_tma needs
-        // no wait of its own here.
-        ok = mbar_wait(full_dq(s), ph, abort_flag, kErrMma, p.err);
-        if (!ok) break;
         tc_fence_after();
-        const uint64_t soff = (uint64_t)((uint32_t)s * (stage_bytes >> 4));
+        const uint32_t bst = base + (uint32_t)a * act_bytes;
+        const uint32_t acol = tmem_base + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
+        const int w2 = w + 1 == ndq ? 0 : w + 1;
+        const uint32_t pw2 = w2 == 0 ? pw ^ 1u : pw;
+        bool ready = true;
 #pragma unroll
-        for (int u = 0; u < SA; ++u)
+        for (int u = 0; u < SA; ++u) {
+          const uint64_t bdesc = sw128_kmajor_desc(bst + u * atom_act);
 #pragma unroll
-          for (int kk = 0; kk < kStageK / 16; ++kk)  // +32 bytes of k per MMA
-            tc_mma_f16(tmem_base, adesc0 + soff + (uint64_t)(u * (kWdqBytes >> 4)) + 2u * kk,
-                       bdesc0 + soff + (uint64_t)(u * (act_bytes >> 4)) + 2u * kk, idesc,
-                       (kb | u | kk) != 0);
-        tc_commit(empty(s));
-        if (++s == stages) {
-          s = 0;
-          ph ^= 1u;
+          for (int kk = 0; kk < kStageK / 16; ++kk) {  // 16 k per MMA: 8 columns of A, 32 bytes of B
+            tc_mma_f16_ts(tmem_base, acol + (uint32_t)(u * kAtomCols + 8 * kk), bdesc + 2u * kk, idesc,
+                          (kb | u | kk) != 0);
+            if (u == 0 && kk == 1 && kb + 1 < nk) ready = mbar_test(dq_full(w2), pw2);
+          }
         }
+        tc_commit(stage_done(a));
+        a = a + 1 == nact ? 0 : a + 1;
+        w = w2;
+        pw = pw2;
+        if (kb + 1 < nk && !ready) ok = mbar_wait(dq_full(w), pw, abort_flag, kErrMma, p.err);
       }
       tc_commit(accum_bar);  // fires once every MMA issued above has completed
       if (!ok) mbar_drain(accum_bar, 0, p.err);  // no MMA may run past the TMEM release
     }
   } else {
     // ---------------------------------------------------------- dequant + epilogue
-    // The 8 warps form `groups` groups (4, 2 or 1); group g dequantizes the
-    // stages kb = g, g + groups, ... so several stages are converted at once;
-    // within a stage each of the group's warps converts `groups` strips.
-    // `stages` is a multiple of `groups`, so a ring slot is always converted
-    // by the same group, which has waited for the slot's previous round: a
-    // parity wait can then never run more than one phase ahead of its
-    // barrier (where it would take an older phase for the awaited one).
-    const int groups = p.dq_groups;
-    const int wpg = kDqWarps / groups;  // warps per group
+    // NG groups of four warps; group g converts the stages g, g + NG, ...
+    // Thread (lane quarter q, lane) owns weight column 32 q + lane of the
+    // tile: tensor-memory lane 32 q + lane, strip 2 q + lane / 16, column c =
+    // lane % 16 of the strip. In the packed format the 16 bytes at 64 (c % 8)
+    // + 16 l (l = 0..3) of a strip's atom hold the words of k-octets l and
+    // 4 + l of columns c % 8 (words 0, 2) and c % 8 + 8 (words 1, 3).
     const int dw = warp - 2;
-    const int dg = dw / wpg, sub = dw % wpg;
-    const int gq = lane >> 2, t = lane & 3;
-    const int nstrips = p.N / kStripCols;
+    const int grp_id = dw >> 2;  // this warp's group
+    const int q = warp & 3;      // lane quarter
+    const int ls = 2 * q + (lane >> 4);
+    const int c = lane & 15, cp = c & 7;
+    const bool hi = c >= 8;
+    const int strip = n0 / kStripCols + ls;
+    const bool live = strip < p.N / kStripCols;
     const int G = p.K / p.group;
-    const uint32_t* sp2 = reinterpret_cast<const uint32_t*>(p.Sp);
-    const uint8_t* zpb = reinterpret_cast<const uint8_t*>(p.Zp);
-    // process the lane's words in an order that keeps the 16-byte stores of
-    // each quarter-warp on distinct banks (odd rows take the other k-half first)
-    const uint32_t flip = (uint32_t)(gq & 1);
-    // (s[gq], s[gq+8]) and zero-point pairs of this warp's strips for a stage
-    auto load_meta = [&](int kb, uint32_t (&ms)[4], uint32_t (&mz)[4]) {
-      const int grp = (int)((long long)(kb0 + kb) * SA * kStageK / p.group);
+    const uint32_t tlane = (uint32_t)(32 * q) << 16;
+    // scale bits (low half) and zero point (bits 16..19) of this column for
+    // each 128 k of a stage (one group: SA >= 2 needs groups of 128 or more)
+    constexpr int MH = SA >= 2 ? SA / 2 : 1;
+    struct Meta {
+      uint32_t v[MH];
+    };
+    auto load_meta = [&](int kb, Meta& m) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int strip = n0 / kStripCols + groups * sub + i;
-        ms[i] = 0;
-        mz[i] = 0;
-        if (i < groups && strip < nstrips) {
-          const size_t off = ((size_t)strip * G + grp) * 8 + gq;
-          ms[i] = sp2[off];
-          mz[i] = zpb[off];
+      for (int h = 0; h < MH; ++h) {
+        m.v[h] = 0u;
+        if (kb < nk && live) {
+          const int grp = (int)(((long long)(kb0 + kb) * SA * kStageK + h * 128) / p.group);
+          const size_t pg = (size_t)strip * G + grp;
+          const uint32_t sb = p.Sp[pg * 16 + 2 * cp + (hi ? 1 : 0)];
+          const uint32_t zb = reinterpret_cast<const uint8_t*>(p.Zp)[pg * 8 + cp];
+          m.v[h] = sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
         }
       }
     };
-    // one stage of this group: wait for its copies, dequantize this warp's
-    // strips with the stage's scales and zero points (ms, mz), arrive
-    auto stage = [&](int kb, const uint32_t (&ms)[4], const uint32_t (&mz)[4]) -> bool {
-      const int s = kb % stages;
-      const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-      if (!mbar_wait(full_tma(s), ph, abort_flag, kErrDequant, p.err)) return false;
-      const uint32_t st = base + (uint32_t)s * stage_bytes;
-      // the next strip's codes are loaded while this strip is converted (the
-      // loop is unrolled: no register copies)
-      uint4 v[2][SA];
-      auto load_codes = [&](int i, uint4 (&d)[SA]) {
-#pragma unroll
-        for (int u = 0; u < SA; ++u)
-          d[u] = lds128(st + packed_off + (groups * sub + i) * (SA * 512) + u * 512 + lane * 16);
+    // one stage: wait for its codes, read this column's words, release the
+    // codes; wait for the tensor-memory slot; dequantize and store; wait for
+    // the stage's activations; arrive
+    auto stage = [&](int kb, const Meta& meta) -> bool {
+      const int cs = kb % ncode, a = kb % nact, w = kb % ndq;
+      if (!mbar_wait(code_full(cs), (uint32_t)(kb / ncode) & 1u, abort_flag, kErrDequant, p.err))
+        return false;
+      const uint32_t cb = code_base + (uint32_t)cs * code_bytes;
+      // the slot's previous stage (kb - dq_slots) has completed its MMAs
+      auto wait_slot = [&]() -> bool {
+        if (kb < ndq) return true;
+        const int prev = kb - ndq;
+        if (!mbar_wait(stage_done(prev % nact), (uint32_t)(prev / nact) & 1u, abort_flag, kErrDequant,
+                       p.err))
+          return false;
+        tc_fence_after();
+        return true;
       };
-      load_codes(0, v[0]);
+      // atoms are read and converted CA at a time (four atoms of words would
+      // not fit the registers of 18 warps); the codes are released once the
+      // last ones are in registers
+      constexpr int CA = SA > 2 ? 2 : SA;
+      if (SA > CA && !wait_slot()) return false;
+      const uint32_t tcol = tmem_base + tlane + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i + 1 < 4 && i + 1 < groups) load_codes(i + 1, v[(i + 1) & 1]);
-        const int ls = groups * sub + i;  // strip within the tile
-        if (i < groups && n0 / kStripCols + ls < nstrips) {
-          const uint32_t z0 = mz[i] & 15u, z1 = (mz[i] >> 4) & 15u;
-          const uint16_t s0 = (uint16_t)(ms[i] & 0xffffu), s1 = (uint16_t)(ms[i] >> 16);
+      for (int u0 = 0; u0 < SA; u0 += CA) {
+        uint32_t wl[CA][4], wh[CA][4];  // k-octets l and 4 + l of each atom
 #pragma unroll
-          for (int u = 0; u < SA; ++u) {
-            const uint32_t wdq = st + wdq_off + u * kWdqBytes;
+        for (int u = 0; u < CA; ++u) {
+          const uint32_t row = (uint32_t)(ls * 4 * SA + 4 * (u0 + u) + (cp >> 1));  // 128-byte row of the tile
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t ks = (uint32_t)(j >> 1) ^ flip;  // k-half of this word
-              const uint32_t r = (uint32_t)(j & 1);           // column gq or gq + 8
-              const uint4 vv = v[i & 1][u];
-              const uint32_t word = ks ? (r ? vv.w : vv.z) : (r ? vv.y : vv.x);
-              uint32_t o[4];
-              if (kB)
-                dequant_word_bf16(word, make_deq_const_bf16(r ? z1 : z0, r ? s1 : s0), o);
-              else
-                dequant_word(word, make_deq_const(r ? z1 : z0, r ? s1 : s0), o);
-              // row n = 16 ls + gq + 8 r of the operand, 16-byte chunk kw = 4 ks + t
-              const uint32_t row = 16u * ls + gq + 8u * r;
-              const uint32_t kw = 4u * ks + t;
-              sts128(wdq + (row >> 3) * 1024u + (row & 7u) * 128u + ((kw ^ (row & 7u)) << 4),
-                     o[0], o[1], o[2], o[3]);
-            }
+          for (int l = 0; l < 4; ++l) {
+            const uint32_t chunk = ((uint32_t)(4 * (cp & 1) + l)) ^ (row & 7u);  // 128-byte swizzle
+            const uint4 v = lds128(cb + row * 128u + (chunk << 4));
+            wl[u][l] = hi ? v.y : v.x;
+            wh[u][l] = hi ? v.w : v.z;
           }
         }
+        if (u0 + CA == SA) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(code_empty(cs));  // the codes are in registers
+          if (SA == CA && !wait_slot()) return false;
+        }
+#pragma unroll
+        for (int u = 0; u < CA; ++u) {
+          const uint32_t mv = meta.v[(u0 + u) / 2 < MH ? (u0 + u) / 2 : 0];
+          const uint32_t z = (mv >> 16) & 15u;
+          const uint16_t s = (uint16_t)(mv & 0xffffu);
+          uint32_t r[32];  // cell j = (deq[2j], deq[2j + 1]): k-octet o fills cells 4o..4o+3
+#pragma unroll
+          for (int l = 0; l < 4; ++l) {
+            uint32_t o0[4], o1[4];
+            if (kB) {
+              const DeqConstBf16 dc = make_deq_const_bf16(z, s);
+              dequant_word_bf16(wl[u][l], dc, o0);
+              dequant_word_bf16(wh[u][l], dc, o1);
+            } else {
+              const DeqConst dc = make_deq_const(z, s);
+              dequant_word(wl[u][l], dc, o0);
+              dequant_word(wh[u][l], dc, o1);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              r[4 * l + j] = o0[j];
+              r[16 + 4 * l + j] = o1[j];
+            }
+          }
+          tmem_st32(tcol + (uint32_t)((u0 + u) * kAtomCols), r);
+        }
       }
-      fence_async_shared();  // this thread's generic-proxy stores -> visible to the tensor core
-      __syncwarp();          // every lane of the warp has fenced its stores
-      if (lane == 0) mbar_arrive(full_dq(s));
+      tmem_wait_st();
+      // the stage's activations have landed (the MMAs read them too)
+      if (!mbar_wait(act_full(a), (uint32_t)(kb / nact) & 1u, abort_flag, kErrDequant, p.err))
+        return false;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_full(w));
       return true;
     };
-    // two register sets of scales and zero points, alternating between this
-    // group's stages: each set is loaded one stage ahead and read only by its
-    // own stage, so no stage waits for the next stage's loads. Scales and
-    // zero points are weights: with static weights the first set is read
-    // before the wait for the previous grid (which orders this warp's stores
-    // of Y)
-    uint32_t ma[4], za[4], mb[4], zb[4];
-    if (p.early_weights && dg < nk) load_meta(dg, ma, za);
+    // scales and zero points: three register sets in rotation, each loaded two
+    // of this group's stages before its own (no stage waits for its loads).
+    // They are weights: with static weights the first sets are read before the
+    // wait for the previous grid (which orders this warp's stores of Y)
+    Meta m0s, m1s, m2s;
+    if (p.early_weights) {
+      load_meta(grp_id, m0s);
+      load_meta(grp_id + NG, m1s);
+    }
     grid_dependency_wait();
-    if (!p.early_weights && dg < nk) load_meta(dg, ma, za);
-    for (int kb = dg; kb < nk; kb += 2 * groups) {
-      if (kb + groups < nk) load_meta(kb + groups, mb, zb);
-      if (!stage(kb, ma, za) || kb + groups >= nk) break;
-      if (kb + 2 * groups < nk) load_meta(kb + 2 * groups, ma, za);
-      if (!stage(kb + groups, mb, zb)) break;
+    if (!p.early_weights) {
+      load_meta(grp_id, m0s);
+      load_meta(grp_id + NG, m1s);
+    }
+    for (int kb = grp_id; kb < nk; kb += 3 * NG) {
+      load_meta(kb + 2 * NG, m2s);
+      if (!stage(kb, m0s) || kb + NG >= nk) break;
+      load_meta(kb + 3 * NG, m0s);
+      if (!stage(kb + NG, m1s) || kb + 2 * NG >= nk) break;
+      load_meta(kb + 4 * NG, m1s);
+      if (!stage(kb + 2 * NG, m2s)) break;
     }
 
     // epilogue: TMEM lanes 32q..32q+31 are output columns, TMEM columns are tokens
@@ -319,22 +405,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncwarp();
     if (__all_sync(0xffffffffu, have_accum)) {  // warp-uniform: tcgen05.ld is .aligned
       tc_fence_after();
-      const int q = warp & 3;
-      const int half = dw >> 2;  // two warpgroups split the token chunks
+      const int half = dw >> 2;  // the NG warpgroups split the token chunks
       const int n = n0 + 32 * q + lane;
       float* part = p.tiles + (((size_t)blockIdx.y * gridDim.x + blockIdx.x) * p.split + blockIdx.z) *
                                   (size_t)bt * kTileN;
-      for (int c = half; c < bt / 16; c += 2) {
+      for (int ch = half; ch < bt / 16; ch += NG) {
         uint32_t r[16];
-        tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * c), r);
+        tmem_ld16(tmem_base + tlane + (uint32_t)(16 * ch), r);
         tmem_wait_ld();
         if (p.split > 1) {  // fp32 partial tile [token][column]
 #pragma unroll
-          for (int j = 0; j < 16; ++j) part[(16 * c + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
+          for (int j = 0; j < 16; ++j) part[(16 * ch + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
         } else if (n < p.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int tok = m0 + 16 * c + j;
+            const int tok = m0 + 16 * ch + j;
             if (tok < p.M)
               p.Y[(size_t)tok * p.N + n] =
                   to_out<kB>(__uint_as_float(r[j]) * (p.row_scale ? p.row_scale[tok] : 1.0f));
@@ -346,7 +431,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // K split: the last of the tile's CTAs to arrive sums the partial tiles in
       // split order (deterministic), writes Y and resets the tile's counter
       const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-      epilogue_bar();  // every partial store issued; one release atomic covers them
+      epilogue_bar<Warps<NG>::kDqThreads>();  // every partial store issued; one release atomic covers them
       if (dw == 0 && lane == 0) {
         int old = 0;
         if (*abort_flag == 0)
@@ -356,7 +441,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                        : "memory");
         *last_flag = (*abort_flag == 0) && old == p.split - 1;
       }
-      epilogue_bar();
+      epilogue_bar<Warps<NG>::kDqThreads>();
       if (*last_flag) {
         // 4 columns per float4, 8 float4 per thread and round: the loads of
         // one partial tile for the round are all in flight together, and the
@@ -364,7 +449,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const float4* tb = reinterpret_cast<const float4*>(p.tiles + (size_t)tile * p.split * bt * kTileN);
         const int n4 = bt * kTileN / 4;
         constexpr int kRound = 8;
-        for (int e0 = dw * 32 + lane; e0 < n4; e0 += kRound * kDqThreads) {
+        for (int e0 = dw * 32 + lane; e0 < n4; e0 += kRound * Warps<NG>::kDqThreads) {
           float4 acc[kRound];
 #pragma unroll
           for (int u = 0; u < kRound; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -372,7 +457,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             float4 v[kRound];
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
-              const int e = e0 + u * kDqThreads;
+              const int e = e0 + u * Warps<NG>::kDqThreads;
               v[u] = e < n4 ? __ldcg(tb + (size_t)z * (n4) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
@@ -385,7 +470,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
 #pragma unroll
           for (int u = 0; u < kRound; ++u) {
-            const int e = e0 + u * kDqThreads;
+            const int e = e0 + u * Warps<NG>::kDqThreads;
             const int tok = m0 + e / (kTileN / 4), n = n0 + (e % (kTileN / 4)) * 4;
             if (e < n4 && tok < p.M && n < p.N) {
               const float f = p.row_scale ? p.row_scale[tok] : 1.0f;
@@ -425,11 +510,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int pow2_at_least(int v) {
-  int p = 32;
-  while (p < v) p <<= 1;
-  return p;
-}
 
 }  // namespace
 
@@ -439,30 +519,83 @@ int tc_token_tile(int M) {
 }
 
 // CTAs per SM the tensor-core kernel is sized for: two when the token tile is
-// at most 48 (four stages still fit in half the shared memory; more CTAs for
-// the small tile counts of the middle band of M), else one with the deepest
-// pipeline that fits.
+// at most 48 (more CTAs for the small tile counts of the middle band of M),
+// else one.
 int tc_ctas_per_sm(int bt) { return bt <= 48 ? 2 : 1; }
 
-size_t tc_smem_bytes(int bt, int sa, int* stages_out) {
-  const size_t stage = (size_t)sa * ((size_t)bt * 128 + kWdqBytes + kPackedBytes);
-  const size_t budget = (tc_ctas_per_sm(bt) == 2 ? 113 * 1024 : 227 * 1024) - 1024 - 256;
-  int stages = (int)(budget / stage);
-  if (stages > 8) stages = 8;
-  if (stages >= 4) stages &= ~3;  // a multiple of the 4 dequant groups
-  else if (stages == 3) stages = 2;  // of 2 groups
-  if (stages_out) *stages_out = stages;
-  return (size_t)stages * stage + 1024 + 256;
+namespace {
+
+struct TcRings {
+  int act, code, dq;  // ring depths in stages
+  int groups;         // dequant groups (2 or 4)
+  int dq_col0, tmem_cols;
+  size_t smem;
+};
+
+// Ring depths of a token tile. Codes: 16 atoms (64 KiB), 8 at two CTAs per
+// SM or for tiles of 192 tokens and more (whose activation slots are large).
+// Activations: as deep as the rest of the shared memory allows, at most 16
+// atoms. Dequantized operand: in the tensor memory the accumulator leaves, at
+// most 16 atoms and no deeper than the activation ring. Dequant groups: four
+// where one CTA per SM has at least four activation slots, else two.
+//
+// A parity wait is unambiguous only while its barrier is at most one phase
+// away from the awaited one. Group g waits for stage kb's codes, for the MMAs
+// of stage kb - dq (its slot) and for stage kb's activations; it has already
+// seen its own previous stage kb - groups through the same three waits. So:
+//   - code slots are a multiple of the groups: the previous stage in stage
+//     kb's code slot is one of this group's own, whose codes have landed;
+//   - activation slots (which index stage_done) are at least the groups and
+//     at least the dequantized slots: the previous phase of the awaited
+//     stage_done, stage kb - dq - act, is no later than kb - groups - dq,
+//     whose MMAs the group saw complete (MMAs complete in order), and the
+//     previous phase of stage kb's act_full, stage kb - act, is no later than
+//     kb - dq, whose MMAs read those activations.
+TcRings tc_rings(int bt, int sa) {
+  TcRings r;
+  const bool two = tc_ctas_per_sm(bt) == 2;
+  const size_t budget = (size_t)(two ? 113 : 227) * 1024 - 1024 - kBarBytes;
+  r.code = ((two || bt >= 192) ? 8 : 16) / sa;
+  const size_t act_slot = (size_t)sa * bt * 128;
+  const size_t code_slot = (size_t)sa * kCodeAtomBytes;
+  int act = (int)((budget - (size_t)r.code * code_slot) / act_slot);
+  r.act = act > 16 / sa ? 16 / sa : act;
+  r.groups = !two && r.act >= 4 ? 4 : 2;
+  r.tmem_cols = two ? 256 : 512;
+  r.dq_col0 = (bt + 31) / 32 * 32;
+  int dq = (r.tmem_cols - r.dq_col0) / (sa * kAtomCols);
+  if (dq > 16 / sa) dq = 16 / sa;
+  r.dq = dq > r.act ? r.act : dq;
+  r.smem = (size_t)r.act * act_slot + (size_t)r.code * code_slot + 1024 + kBarBytes;
+  return r;
 }
 
-// Two-atom stages halve the hand-offs per weight byte but need a ring of at
-// least 4 of them to pay: measured, 64-token tiles (4 stages) gained 15-22%
-// and 128- or 256-token tiles (2 stages) lost 5-10%.
+bool tc_rings_valid(const TcRings& r) {
+  return r.dq >= 1 && r.dq <= r.act && r.act >= r.groups && r.code % r.groups == 0;
+}
+
+}  // namespace
+
+// Atoms per stage: two when K and the group are multiples of 128 (one scale
+// and zero point per stage), else one.
 int tc_stage_atoms(int M, int K, int group) {
-  if (K % 128 != 0 || group % 128 != 0) return 1;
-  int stages = 0;
-  tc_smem_bytes(tc_token_tile(M), 2, &stages);
-  return stages >= 4 ? 2 : 1;
+  (void)M;
+  return K % 128 == 0 && group % 128 == 0 ? 2 : 1;
+}
+
+bool tc_config(int M, int K, int group, int out[8]) {
+  const int bt = tc_token_tile(M);
+  const int sa = tc_stage_atoms(M, K, group);
+  const TcRings r = tc_rings(bt, sa);
+  out[0] = bt;
+  out[1] = sa;
+  out[2] = r.act;
+  out[3] = r.code;
+  out[4] = r.dq;
+  out[5] = r.groups;
+  out[6] = (int)r.smem;
+  out[7] = tc_ctas_per_sm(bt);
+  return tc_rings_valid(r) && !(sa == 4 && r.groups != 4);
 }
 
 size_t tc_workspace_bytes(int M, int N, int split) {
@@ -527,14 +660,14 @@ int tc_choose_split(int M, int N, int K, int group, int sms) {
 
 namespace {
 
-template <int SA, bool kB>
+template <int SA, bool kB, int NG>
 cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const TcParams& prm,
                           dim3 grid, size_t smem, cudaStream_t stream) {
-  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(tc_gemm_kernel<SA, kB>), 227 * 1024);
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(tc_gemm_kernel<SA, kB, NG>), 227 * 1024);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Warps<NG>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -542,7 +675,18 @@ cudaError_t launch_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<SA, kB>, tmA, tmW, prm);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<SA, kB, NG>, tmA, tmW, prm);
+}
+
+template <bool kB>
+cudaError_t launch_sa(int sa, int ng, const CUtensorMap& tmA, const CUtensorMap& tmW, const TcParams& prm,
+                      dim3 grid, size_t smem, cudaStream_t stream) {
+  if (ng == 2)
+    return sa == 2 ? launch_kernel<2, kB, 2>(tmA, tmW, prm, grid, smem, stream)
+                   : launch_kernel<1, kB, 2>(tmA, tmW, prm, grid, smem, stream);
+  if (sa == 4) return launch_kernel<4, kB, 4>(tmA, tmW, prm, grid, smem, stream);
+  return sa == 2 ? launch_kernel<2, kB, 4>(tmA, tmW, prm, grid, smem, stream)
+                 : launch_kernel<1, kB, 4>(tmA, tmW, prm, grid, smem, stream);
 }
 
 }  // namespace
@@ -554,12 +698,13 @@ namespace {
 
 struct MapKey {
   const void* ptr;
-  uint64_t dims0, dims1;
-  uint32_t box0, box1;
-  int dtype;
+  uint64_t dims[3];
+  uint32_t box[3];
+  int dtype, rank, swizzle;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && dims0 == o.dims0 && dims1 == o.dims1 && box0 == o.box0 &&
-           box1 == o.box1 && dtype == o.dtype;
+    return ptr == o.ptr && dims[0] == o.dims[0] && dims[1] == o.dims[1] && dims[2] == o.dims[2] &&
+           box[0] == o.box[0] && box[1] == o.box[1] && box[2] == o.box[2] && dtype == o.dtype &&
+           rank == o.rank && swizzle == o.swizzle;
   }
 };
 constexpr int kMapCache = 64;
@@ -568,12 +713,11 @@ MapKey g_map_keys[kMapCache];
 CUtensorMap g_maps[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-}  // namespace
-
-bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
-                       uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
-                       CUtensorMapSwizzle swizzle) {
-  const MapKey key = {ptr, dims0, dims1, box0, box1, (int)dt};
+// A densely packed row-major array of rank 2 or 3 (dims[0] innermost).
+bool cached_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize, int rank,
+                const uint64_t (&dims)[3], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+  const MapKey key = {ptr, {dims[0], dims[1], dims[2]}, {box[0], box[1], box[2]}, (int)dt, rank,
+                      (int)swizzle};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_map_used; ++i)
@@ -584,11 +728,11 @@ bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt
   }
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)dims0, (cuuint64_t)dims1};
-  const cuuint64_t strides[1] = {(cuuint64_t)dims0 * esize};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  if (encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  const cuuint64_t gdims[3] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2]};
+  const cuuint64_t strides[2] = {(cuuint64_t)dims[0] * esize, (cuuint64_t)dims[0] * dims[1] * esize};
+  const cuuint32_t gbox[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (encode(out, dt, (cuuint32_t)rank, const_cast<void*>(ptr), gdims, strides, gbox, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -597,6 +741,14 @@ bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt
   g_map_keys[slot] = key;
   g_maps[slot] = *out;
   return true;
+}
+
+}  // namespace
+
+bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
+                       uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
+                       CUtensorMapSwizzle swizzle) {
+  return cached_map(out, ptr, dt, esize, 2, {dims0, dims1, 1}, {box0, box1, 1}, swizzle);
 }
 
 cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
@@ -609,10 +761,12 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   if (!cached_tensor_map(&tmA, A, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   2, (uint64_t)K, (uint64_t)M, 64, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // packed weights viewed as [N/16 strips][K/64 atoms * 128 words] of uint32
-  if (!cached_tensor_map(&tmW, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(K / kAtomK) * kAtomWords,
-                  (uint64_t)(N / kStripCols), (uint32_t)(kAtomWords * sa), kTileN / kStripCols,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+  // packed weights viewed as [N/16 strips][K/64 atoms * 4 rows][32 words] of
+  // uint32: a box is the stage's SA atoms of the tile's 8 strips, 128-byte rows
+  // swizzled
+  if (!cached_map(&tmW, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 3,
+                  {32, (uint64_t)(K / kAtomK) * 4, (uint64_t)(N / kStripCols)},
+                  {32, (uint32_t)(4 * sa), (uint32_t)(kTileN / kStripCols)}, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams prm;
   prm.Sp = Sp;
@@ -631,16 +785,19 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;
-  const size_t smem = tc_smem_bytes(bt, sa, &prm.stages);
-  prm.tmem_cols = pow2_at_least(bt);
-  prm.dq_groups = prm.stages % 4 == 0 ? 4 : (prm.stages % 2 == 0 ? 2 : 1);
+  const TcRings rings = tc_rings(bt, sa);
+  prm.act_slots = rings.act;
+  prm.code_slots = rings.code;
+  prm.dq_slots = rings.dq;
+  prm.dq_col0 = rings.dq_col0;
+  prm.tmem_cols = rings.tmem_cols;
+  const size_t smem = rings.smem;
   const dim3 grid((unsigned)((M + bt - 1) / bt), (unsigned)((N + kTileN - 1) / kTileN),
                   (unsigned)prm.split);
-  if (bf16)
-    return sa == 2 ? launch_kernel<2, true>(tmA, tmW, prm, grid, smem, stream)
-                   : launch_kernel<1, true>(tmA, tmW, prm, grid, smem, stream);
-  return sa == 2 ? launch_kernel<2, false>(tmA, tmW, prm, grid, smem, stream)
-                 : launch_kernel<1, false>(tmA, tmW, prm, grid, smem, stream);
+  const int ng = rings.groups;
+  if (!tc_rings_valid(rings) || (sa == 4 && ng != 4)) return cudaErrorInvalidValue;
+  return bf16 ? launch_sa<true>(sa, ng, tmA, tmW, prm, grid, smem, stream)
+              : launch_sa<false>(sa, ng, tmA, tmW, prm, grid, smem, stream);
 }
 
 namespace {

@@ -267,7 +267,7 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * 512 k and K split anywhere on 64-k boundaries when group == K),
  * for the tensor-core path the number of K ranges per output tile (clamped to
  * the pipeline stages of K: K/64, or K/128 when K and the group are multiples
- * of 128 and the token tile leaves room for four 128-k stages). The decode path handles any M in launches of 16 rows (it streams the
+ * of 128). The decode path handles any M in launches of 16 rows (it streams the
  * weights once per launch) and needs group == K or group = 64 * 2^j
  * (W4A16_ERR_UNSUPPORTED_SHAPE otherwise). `path` may carry
  * W4A16_STATIC_WEIGHTS, W4A16_SILU_MUL, W4A16_BF16 and W4A16_ACT_A8 (see
@@ -284,6 +284,16 @@ int w4a16_gemm_ex(const uint16_t* A, const uint32_t* Wq, const uint16_t* scales,
  * for the tensor-core paths W4A16_PATH_TENSOR and its K ranges, or
  * W4A16_PATH_TENSOR_PAIR and 1. Host-only. */
 int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
+
+/* The configuration of the one-SM tensor-core kernel (W4A16_PATH_TENSOR) for
+ * M rows of a K x N layer with the given group: out[0] token tile (the MMA's
+ * N), out[1] 64-k atoms per pipeline stage, out[2] activation ring slots,
+ * out[3] packed-code ring slots, out[4] dequantized-operand ring slots (in
+ * tensor memory), out[5] dequantizing warp groups, out[6] dynamic shared
+ * memory bytes, out[7] CTAs per SM. `n` is the length of `out` (at least 8).
+ * Host-only (no device is touched); W4A16_ERR_INVALID_ARG for M < 1, a null
+ * `out` or n < 8, and the shape errors of w4a16_gemm. */
+int w4a16_tc_config(int M, int K, int group, int* out, int n);
 
 /* The decode-path GEMM (same kernel, same results as w4a16_gemm_ex with
  * W4A16_PATH_DECODE_STREAMK and the automatic CTA count) for callers that cannot
