@@ -77,33 +77,31 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 }
 
 // The path for M rows, from measurements on GB300 (CUDA graphs of 20 launches
-// over weight copies larger than L2; the full table is kept with the design
+// over weight copies larger than L2; the full tables are kept with the design
 // notes).
-// Decode GEMV up to 16 rows, and up to 32 rows (two 16-row passes over the
-// weights) for wide layers of up to 2^28 weights, where one pass costs less
-// than half a tensor-core pass (us, decode / tensor):
-//   7B gate_up (4096 x 22016):  16 rows 16.4 / 31.8, 32 rows 32.0 / 32.5
-//   13B gate_up (5120 x 27648): 16 rows 22.6 / 46.1, 32 rows 44.5 / 44.8
-//   13B qkv (5120 x 15360):     16 rows 16.4 / 27.3, 20 rows 26.6 / 26.3
-//   70B gate_up (8192 x 57344): 20 rows 116.3 / 120.4, 24 rows 133.2 / 120.6
-// Above, the tensor-core GEMM: on SM pairs (tcgen05.mma.cta_group::2) where
-// it measured faster than on single SMs, else one SM per tile (TFLOP/s, one
-// SM / pair):
-//   4096 rows: 70B gate_up 1234 / 1276, down 1285 / 1333, qkv 1167 / 1198,
-//              o_proj 1190 / 1223; 7B o_proj (K = N = 4096) 973 / 945
-//   2048 rows: 7B qkv 968 / 959, gate_up 1046 / 1049
-//    512 rows: 70B gate_up 1166 / 1240, down 1068 / 1129, qkv 677 / 665,
-//              o_proj 992 / 992
-//    256, 128 rows: 13B qkv 862 / 855, 522 / 451
-// so the pair takes M >= 4096 with N*K >= 2^26 and M >= 512 with
-// N*K >= 2^27.
+// Decode GEMV up to 16 rows; on wide layers (N >= 16384) up to 24 rows, and
+// up to 32 rows (two 16-row passes over the weights) where the layer has at
+// most 2^28 weights (us, decode / one-SM tensor cores):
+//   7B gate_up (4096 x 22016):  16 rows 16.2 / 31.2, 24 rows 26.9 / 31.8, 32 rows 32.0 / 31.7
+//   13B gate_up (5120 x 27648): 16 rows 22.7 / 44.9, 32 rows 44.3 / 51.6, 48 rows 66.0 / 51.6
+//   70B gate_up (8192 x 57344): 24 rows 133.2 / 144.4, 32 rows 154.2 / 145.7
+//   13B qkv (5120 x 15360):     16 rows 16.3 / 27.1, 20 rows 26.5 / 27.5, 32 rows 31.4 / 27.5
+// Above, the tensor cores: a CTA pair per 256-column tile (tcgen05.mma
+// cta_group::2) from 256 rows where the pairs' CTAs make at least 80 (they
+// have no K split), else one SM per tile (TFLOP/s, one SM / pair):
+//   256 rows: 70B gate_up 1374 / 1633, 70B qkv 829 / 982, 70B o_proj 951 / 804
+//   512 rows: 70B down 1323 / 1674, 13B o_proj 757 / 886, 7B o_proj 751 / 697
+//   4096 rows: 70B gate_up 1344 / 1457, 7B o_proj 1176 / 1277, 7B qkv 1317 / 1275
+//   128 rows: 13B qkv 701 / 686, 70B qkv 550 / 513, 7B qkv 472 / 535
 int choose_path(int M, int N, int K, int group) {
   const long long nk = (long long)N * K;
   // (group sizes the decode kernel does not take go to the tensor cores)
-  if ((M <= 16 || (M <= 32 && N >= 16384 && nk <= (1LL << 28))) && decode_units(N, K, group) > 0)
+  const bool wide = N >= 16384;
+  if ((M <= 16 || (wide && (M <= 24 || (M <= 32 && nk <= (1LL << 28))))) &&
+      decode_units(N, K, group) > 0)
     return W4A16_PATH_DECODE;
-  if ((M >= 4096 && nk >= (1LL << 26)) || (M >= 512 && nk >= (1LL << 27)))
-    return W4A16_PATH_TENSOR_PAIR;
+  const long long pair_ctas = 2LL * ((N + 255) / 256) * ((M + 255) / 256);
+  if (M >= 256 && pair_ctas >= 80) return W4A16_PATH_TENSOR_PAIR;
   return W4A16_PATH_TENSOR;
 }
 

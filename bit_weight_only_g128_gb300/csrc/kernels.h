@@ -98,6 +98,10 @@ size_t tc_pair_smem_bytes(int bt, int sa, int* act_slots, int* dq_slots, int* co
 bool cached_tensor_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dt, int esize,
                        uint64_t dims0, uint64_t dims1, uint32_t box0, uint32_t box1,
                        CUtensorMapSwizzle swizzle);
+// 3-D tensor map of the packed weights as [N/16 strips][K/64 atoms x 4 rows]
+// [32 words] with the 128-byte swizzle; a box is `sa` atoms of 8 strips (128
+// columns). From the same cache.
+bool cached_code_map(CUtensorMap* out, const uint32_t* Wq, int N, int K, int sa);
 int tc_choose_split(int M, int N, int K, int group, int sms);
 // 64-k atoms per pipeline stage of the tensor-core GEMM (2 when K and the
 // group are multiples of 128, else 1).

@@ -107,8 +107,9 @@ extern "C" {
 #define W4A16_PATH_DECODE_STREAMK 4
 /* The tensor-core GEMM on pairs of SMs (tcgen05.mma.cta_group::2): clusters
  * of two CTAs, each pair one output tile of 256 columns x 256 tokens (128
- * when M <= 128) over all of K; each CTA dequantizes its 128 columns and
- * stages half of the tokens, and the pair's MMAs read both halves. The same
+ * when M <= 128) over all of K; each CTA dequantizes its 128 columns into
+ * its tensor memory (the MMA's A operand) and stages half of the tokens, and
+ * the pair's MMAs read both halves. The same
  * arithmetic as W4A16_PATH_TENSOR (RNE_fp16((q - z) s) operands, fp32
  * accumulation); no K split and no workspace of its own. */
 #define W4A16_PATH_TENSOR_PAIR 5
@@ -246,12 +247,12 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
 
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
  * The path and its grid are chosen from M, N, K, the group and the device's
- * SM count, by rules measured on GB300: the decode GEMV for M <= 16 (and up
- * to 32 rows, in two passes over the weights, for layers with N >= 16384
- * and N*K <= 2^28), else the tensor-core GEMM, on SM pairs
- * (W4A16_PATH_TENSOR_PAIR) for M >= 4096 with N*K >= 2^26 and for M >= 512
- * with N*K >= 2^27, on single SMs otherwise; group sizes the decode kernel
- * does not take always go to the tensor cores. `workspace` (256-byte
+ * SM count, by rules measured on GB300: the decode GEMV for M <= 16 (for
+ * layers with N >= 16384 up to 24 rows, and up to 32 rows when N*K <= 2^28,
+ * in two passes over the weights), else the tensor-core GEMM, on SM pairs
+ * (W4A16_PATH_TENSOR_PAIR) for M >= 256 when the pairs make at least 80
+ * CTAs (2 x ceil(N/256) x ceil(M/256)), on single SMs otherwise; group sizes
+ * the decode kernel does not take always go to the tensor cores. `workspace` (256-byte
  * aligned, zero-filled before first use) may be NULL when
  * w4a16_workspace_size reports 0; W4A16_ERR_WORKSPACE_TOO_SMALL otherwise.
  * Y must not overlap the inputs. */

@@ -126,11 +126,11 @@ def test_tensor_pair_path(M, K, N, group):
 
 def test_tensor_pair_outliers_and_auto_choice():
     run_and_check(512, 4096, 512, 128, seed=4, path="tensor-pair", outliers=True)
-    # the automatic choice: pairs for large layers at 512 rows and more
+    # the automatic choice: pairs from 256 rows where they make 80 CTAs
     assert w4.plan(512, 512, 4096, 128)[0] == "tensor"
     assert w4.plan(512, 57344, 8192, 128)[0] == "tensor-pair"
     assert w4.plan(4096, 8192, 8192, 128)[0] == "tensor-pair"
-    assert w4.plan(4096, 4096, 4096, 128)[0] == "tensor"
+    assert w4.plan(256, 8192, 8192, 128)[0] == "tensor"
     run_and_check(4096, 8192, 8192, 128, seed=5, path="auto", outliers=True)
 
 
