@@ -21,7 +21,11 @@ from typing import Optional, Tuple
 
 import torch
 
-from .build import LIB as LIB_PATH
+from .build import LIB as _BUILT_LIB
+
+# the library to load: W4A16_LIBRARY (for example the bounds-checked build),
+# else the in-tree build
+LIB_PATH = os.environ.get("W4A16_LIBRARY") or _BUILT_LIB
 
 PATH_AUTO, PATH_DECODE, PATH_TENSOR = 0, 1, 2
 PATH_DECODE_RESIDENT, PATH_DECODE_STREAMK, PATH_TENSOR_PAIR = 3, 4, 5

@@ -2,7 +2,13 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into one
 shared library against the shared CUDA runtime (the one PyTorch loads).
-Running ``python -m bit_weight_only_g128_gb300.build`` builds it by hand.
+``build(checked=True)`` builds the bounds-checked variant instead
+(-DW4A16_CHECKED, _build/checked/libw4a16_checked.so): every global and
+shared-memory access of its kernels is tested against its buffer first, and
+an access outside sets a bit of the device error word instead of running.
+Load it by setting W4A16_LIBRARY to its path before the binding loads the
+library. Running ``python -m bit_weight_only_g128_gb300.build [--checked]``
+builds by hand.
 """
 from __future__ import annotations
 
@@ -17,6 +23,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libw4a16.so")
+BUILD_CHECKED = os.path.join(BUILD, "checked")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libw4a16_checked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -44,29 +52,31 @@ def _compile(src: str, obj: str, extra) -> str:
     return res.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libw4a16.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libw4a16.so (with
+    `checked`, the bounds-checked libw4a16_checked.so); returns its path."""
+    out_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    os.makedirs(out_dir, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources]
-    extra = list(extra_flags) + (["-Xptxas", "-v"] if verbose else [])
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in sources]
+    extra = list(extra_flags) + (["-DW4A16_CHECKED"] if checked else []) + (["-Xptxas", "-v"] if verbose else [])
     with cf.ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
         logs = list(ex.map(lambda so: _compile(so[0], so[1], extra), zip(sources, objs)))
     if verbose:
         for src, log in zip(sources, logs):
             if log.strip():
                 print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -44,7 +44,8 @@ template <bool kIn, bool kCodes>
 __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t* __restrict__ A, int K,
                                                                  int8_t* __restrict__ aq,
                                                                  uint16_t* __restrict__ codes,
-                                                                 float* __restrict__ s_a) {
+                                                                 float* __restrict__ s_a, int M,
+                                                                 int* err) {
   extern __shared__ uint4 srow[];
   __shared__ float wmax[kQThreads / 32];
   allow_dependents();
@@ -53,9 +54,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
   const uint4* row = reinterpret_cast<const uint4*>(A + (size_t)m * K);
   const int nv = K / 8;
   float amax = 0.f;
+  const uint4* Av = reinterpret_cast<const uint4*>(A);
+  uint32_t dyn;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
   for (int i = threadIdx.x; i < nv; i += kQThreads) {
-    const uint4 v = row[i];
-    srow[i] = v;
+    const uint4 v = *ld_at(row + i, Av, (size_t)M * nv, err);
+    if (!kCheckedBuild || in_buf(srow + i, srow, dyn / 16, err)) srow[i] = v;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -72,7 +76,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
   for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, wmax[i]);
   const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
   const float inv = __frcp_rn(s);
-  if (threadIdx.x == 0) s_a[m] = s;
+  if (threadIdx.x == 0 && in_buf(s_a + m, s_a, (size_t)M, err)) s_a[m] = s;
   auto code = [&](float a) {
     const float t = a * inv;
     float r = rintf(t);
@@ -81,7 +85,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
     return fminf(fmaxf(r, -127.f), 127.f);
   };
   for (int i = threadIdx.x; i < nv; i += kQThreads) {
-    const uint4 v = srow[i];
+    const uint4 v = *ld_at(srow + i, srow, kCheckedBuild ? dyn / 16 : (size_t)nv, err);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float r[8];
 #pragma unroll
@@ -98,7 +102,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
         lo |= ((uint32_t)(int)r[j] & 0xffu) << (8 * j);
         hi |= ((uint32_t)(int)r[4 + j] & 0xffu) << (8 * j);
       }
-      reinterpret_cast<uint2*>(aq + (size_t)m * K)[i] = make_uint2(lo, hi);
+      uint2* d = reinterpret_cast<uint2*>(aq + (size_t)m * K) + i;
+      if (in_buf(d, reinterpret_cast<uint2*>(aq), (size_t)M * nv, err)) *d = make_uint2(lo, hi);
     }
     if (codes) {
       uint32_t c[4];
@@ -112,7 +117,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(const uint16_t*
           c[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
       }
-      reinterpret_cast<uint4*>(codes + (size_t)m * K)[i] = make_uint4(c[0], c[1], c[2], c[3]);
+      uint4* d = reinterpret_cast<uint4*>(codes + (size_t)m * K) + i;
+      if (in_buf(d, reinterpret_cast<uint4*>(codes), (size_t)M * nv, err)) *d = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
 }
@@ -126,12 +132,15 @@ cudaError_t launch_q(const uint16_t* A, int M, int K, int8_t* aq, uint16_t* code
     cudaError_t e = set_max_smem_once(reinterpret_cast<const void*>(kern), (int)smem);
     if (e != cudaSuccess) return e;
   }
+  int* err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M);
   cfg.blockDim = dim3(kQThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, A, K, aq, codes, s_a);
+  return cudaLaunchKernelEx(&cfg, kern, A, K, aq, codes, s_a, M, err);
 }
 
 }  // namespace

@@ -500,7 +500,8 @@ int w4a16_device_status(void* stream) {
   if (flag != 0)
     return fail(W4A16_ERR_DEVICE_CHECK,
                 "device error word = 0x%x (bits: 1 producer, 2 MMA, 4 dequant, 8 epilogue waits "
-                "timed out; 16 drain timed out; 32 decode fix-up wait timed out)",
+                "timed out; 16 drain timed out; 32 decode fix-up wait timed out; 64 access out of "
+                "bounds, bounds-checked build)",
                 flag);
   return ok();
 }

@@ -22,6 +22,56 @@ constexpr int kStripCols = 16;   // columns per strip
 constexpr int kAtomK = 64;       // k per atom
 constexpr int kAtomWords = 128;  // 32-bit words per atom (16 * 64 / 8)
 
+// ------------------------------------------------------------------ checked build
+// Compiled with -DW4A16_CHECKED (build(checked=True)), every global and
+// shared-memory access of the kernels is tested against its buffer's extent
+// first; an access outside sets kErrBounds in the library's device error
+// word and is skipped (a load reads the buffer's first element instead), so
+// nothing faults and w4a16_device_status reports it. In the normal build the
+// tests compile away.
+constexpr int kErrBounds = 64;
+
+#ifdef W4A16_CHECKED
+constexpr bool kCheckedBuild = true;
+#else
+constexpr bool kCheckedBuild = false;
+#endif
+
+// p lies in [base, base + n): true; else (checked build) records kErrBounds.
+template <class T>
+__device__ __forceinline__ bool in_buf(const T* p, const T* base, size_t n, int* err) {
+  if (!kCheckedBuild) return true;
+  if (p >= base && p < base + n) return true;
+  atomicOr(err, kErrBounds);
+  return false;
+}
+
+// The address to load element p from: p if it lies in [base, base + n), else
+// base (and kErrBounds).
+template <class T>
+__device__ __forceinline__ const T* ld_at(const T* p, const T* base, size_t n, int* err) {
+  return in_buf(p, base, n, err) ? p : base;
+}
+
+// [addr, addr + bytes) lies in this CTA's dynamic shared memory, which starts
+// at shared address `dyn_base`: true; else (checked build) records kErrBounds.
+__device__ __forceinline__ bool in_smem(uint32_t addr, uint32_t bytes, uint32_t dyn_base, int* err) {
+  if (!kCheckedBuild) return true;
+  uint32_t dyn;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+  if (addr >= dyn_base && addr + bytes <= dyn_base + dyn) return true;
+  atomicOr(err, kErrBounds);
+  return false;
+}
+
+// Tensor-memory columns [col, col + ncols) lie in an allocation of `cols`.
+__device__ __forceinline__ bool in_tmem(uint32_t col, uint32_t ncols, uint32_t cols, int* err) {
+  if (!kCheckedBuild) return true;
+  if (col + ncols <= cols) return true;
+  atomicOr(err, kErrBounds);
+  return false;
+}
+
 // ------------------------------------------------------------------ fp16x2
 
 __device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {

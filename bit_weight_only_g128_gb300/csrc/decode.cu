@@ -104,6 +104,7 @@ cudaError_t launch_decode(const uint16_t* A, const uint32_t* Wq, const uint16_t*
   args.Y = Y;
   args.flags = static_cast<int*>(workspace);
   args.tiles = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + decode_counter_bytes(N));
+  args.tile_floats = (decode_workspace_bytes(M, N, ctas) - decode_counter_bytes(N)) / sizeof(float);
   args.granule = split_granule(apg_t, args.gshift);
   cudaError_t e = device_error_word(&args.err);
   if (e != cudaSuccess) return e;

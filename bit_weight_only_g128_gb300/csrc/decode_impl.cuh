@@ -88,10 +88,39 @@ struct DecodeArgs {
   int silu, ytile_off, ytile_stride, whole_in_red;
   // W4A8: per-row factors of the result (the activations' scales), or null
   const float* row_scale;
+  size_t tile_floats;  // extent of `tiles` (for the checked build)
 };
 
 // The row factor of token `tok` (1 without one).
 __device__ __forceinline__ float row_factor(const float* rs, int tok) { return rs ? rs[tok] : 1.0f; }
+
+// The decode kernels' global accesses, tested against the buffers' extents
+// in the checked build (see common.cuh): packed weights, activation rows,
+// scale and zero-point pairs, results, flags and partial tiles.
+__device__ __forceinline__ const uint4* wq_at(const DecodeArgs& p, const uint4* ptr) {
+  return ld_at(ptr, p.Wq, (size_t)p.N * p.K / 32, p.err);
+}
+__device__ __forceinline__ const uint16_t* a_at(const DecodeArgs& p, const uint16_t* ptr) {
+  return ld_at(ptr, p.A, (size_t)p.M * p.K - 7, p.err);  // 16-byte copies
+}
+__device__ __forceinline__ const uint4* sp_at(const DecodeArgs& p, const uint4* ptr, int group_count) {
+  return ld_at(ptr, reinterpret_cast<const uint4*>(p.Sp2), (size_t)group_count * p.N / 8, p.err);
+}
+__device__ __forceinline__ const uint2* zp_at(const DecodeArgs& p, const uint2* ptr, int group_count) {
+  return ld_at(ptr, reinterpret_cast<const uint2*>(p.Zp), (size_t)group_count * p.N / 16, p.err);
+}
+__device__ __forceinline__ bool y_ok(const DecodeArgs& p, const uint16_t* ptr, size_t n) {
+  return in_buf(ptr, static_cast<const uint16_t*>(p.Y), n, p.err);
+}
+__device__ __forceinline__ float row_factor_at(const DecodeArgs& p, int tok) {
+  return p.row_scale ? *ld_at(p.row_scale + tok, p.row_scale, (size_t)p.M, p.err) : 1.0f;
+}
+__device__ __forceinline__ bool flag_ok(const DecodeArgs& p, const int* f) {
+  return in_buf(f, static_cast<const int*>(p.flags), (size_t)kDecodeMaxCtas, p.err);
+}
+__device__ __forceinline__ bool tile_ok(const DecodeArgs& p, const float* t) {
+  return in_buf(t, static_cast<const float*>(p.tiles), p.tile_floats, p.err);
+}
 
 // The bf16-activation instantiations live in their own translation unit.
 cudaError_t decode_dispatch_resident_bf16(const DecodeArgs& args, int mt, int nw, int apg_t, int ctas,
@@ -312,7 +341,7 @@ __device__ __forceinline__ void stage_act(uint4* slot, const DecodeArgs& p, int 
   for (int idx = threadIdx.x; idx < p.M * (kBatch * kAtomK / 8); idx += kThreads) {
     const int row = idx >> 6, c = idx & 63;
     if (c < pieces)
-      cp_async16(slot + row * kActRowVec + c, p.A + (size_t)row * p.K + (size_t)a0 * kAtomK + c * 8);
+      cp_async16(slot + row * kActRowVec + c, a_at(p, p.A + (size_t)row * p.K + (size_t)a0 * kAtomK + c * 8));
   }
 }
 
@@ -333,10 +362,10 @@ __device__ __forceinline__ void stage_meta(uint4* slot, const DecodeArgs& p, int
     const int w = idx / (NG * 3), r = idx - w * (NG * 3);
     const size_t base = (size_t)(blk * kWarps + w) * groups + grp0;
     if (r < 2 * NG) {  // scale pairs: two 16-byte pieces per group
-      if ((r >> 1) < ng) cp_async16(sp_dst + w * NG * 2 + r, sp_src + base * 2 + r);
+      if ((r >> 1) < ng) cp_async16(sp_dst + w * NG * 2 + r, sp_at(p, sp_src + base * 2 + r, groups));
     } else {           // zero-point pairs: 8 bytes per group
       const int g = r - 2 * NG;
-      if (g < ng) cp_async8(zp_dst + w * NG + g, zp_src + base + g);
+      if (g < ng) cp_async8(zp_dst + w * NG + g, zp_at(p, zp_src + base + g, groups));
     }
   }
 }
@@ -439,7 +468,7 @@ __device__ __forceinline__ void apply_group(float (&acc)[MT][4], const float (&p
 // predicated; otherwise atoms past cu.n are skipped and the refill loads
 // only the next unit's atoms.
 template <int MT, int APG, bool kFull, bool kB>
-__device__ __forceinline__ void unit_compute(float (&acc)[MT][4], uint4 (&w)[kBatch],
+__device__ __forceinline__ void unit_compute(const DecodeArgs& p, float (&acc)[MT][4], uint4 (&w)[kBatch],
                                              const Unit& cu, const Unit& nu, bool refill,
                                              const uint4* slot, const float* sb, int warp,
                                              int gq, int t) {
@@ -459,7 +488,7 @@ __device__ __forceinline__ void unit_compute(float (&acc)[MT][4], uint4 (&w)[kBa
     code_pairs<kB>(w[u].y, y);
     code_pairs<kB>(w[u].z, z);
     code_pairs<kB>(w[u].w, v);
-    if (refill && (kFull || u < nu.n)) w[u] = ldg_stream(nu.wp + u * 32);
+    if (refill && (kFull || u < nu.n)) w[u] = ldg_stream(wq_at(p, nu.wp + u * 32));
     if (compute && (kFull || u < cu.n)) {
       if (u % APG == 0)
         atom_mma<MT, true, kB>(pe, po, x, y, z, v, frag + u * 128);
@@ -517,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
     if (cu.active) {
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
-        if (u < cu.n) w[u] = ldg_stream(cu.wp + u * 32);
+        if (u < cu.n) w[u] = ldg_stream(wq_at(p, cu.wp + u * 32));
     }
     stage_meta<MT, NG, APG>(ring, p, sq.blk, sq.a0, cu.n, nstrips, groups);
     if (two) stage_meta<MT, NG, APG>(ring + SM::kSlotVecs, p, nq.blk, nq.a0, n1, nstrips, groups);
@@ -582,9 +611,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
     const uint4* cur = ring + slot * SM::kSlotVecs;
     const float* sb = sums + (i & 1) * SM::kSumFloats;
     if (cu.active && cu.n == kBatch && refill && nu.n == kBatch)
-      unit_compute<MT, APG, true, kB>(acc, w, cu, nu, true, cur, sb, warp, gq, t);
+      unit_compute<MT, APG, true, kB>(p, acc, w, cu, nu, true, cur, sb, warp, gq, t);
     else
-      unit_compute<MT, APG, false, kB>(acc, w, cu, nu, refill, cur, sb, warp, gq, t);
+      unit_compute<MT, APG, false, kB>(p, acc, w, cu, nu, refill, cur, sb, warp, gq, t);
 
     if (!has_next || nu.blk != cu.blk) {
       // ---- end of a segment: atoms [seg_a0, cu.a0 + cu.n) of block cu.blk
@@ -612,9 +641,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         __syncthreads();
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
-          if (col0 + col < N)
+          if (col0 + col < N && y_ok(p, p.Y + (size_t)tok * N + col0 + col, (size_t)M * N))
             p.Y[(size_t)tok * N + col0 + col] =
-                to_act<kB>(red[tok * kRedStride + col] * row_factor(p.row_scale, tok));
+                to_act<kB>(red[tok * kRedStride + col] * row_factor_at(p, tok));
         }
       } else if (head) {
         // finish the block: the later contributors' tiles, in CTA order
@@ -623,7 +652,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         bool ok = true;
         for (int j = threadIdx.x; j < others; j += kThreads) {
           int* f = p.flags + blockIdx.x + 1 + j;
-          if (wait_flag(f))
+          if (!flag_ok(p, f))
+            ok = false;
+          else if (wait_flag(f))
             *f = 0;  // lowered for the next call
           else
             ok = false;
@@ -648,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
 #pragma unroll
             for (int k = 0; k < kPerThread; ++k) {
               const int e = threadIdx.x + k * kThreads;
-              tv[jj][k] = (j0 + jj <= others && e < total) ? __ldcg(tile + e) : 0.f;
+              tv[jj][k] = (j0 + jj <= others && e < total && tile_ok(p, tile + e)) ? __ldcg(tile + e) : 0.f;
             }
           }
 #pragma unroll
@@ -661,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         for (int k = 0; k < kPerThread; ++k) {
           const int e = threadIdx.x + k * kThreads;
           const int col = e & (kDecodeBlockCols - 1);
-          if (e < total && col0 + col < N)
-            p.Y[(size_t)(e >> 7) * N + col0 + col] = to_act<kB>(v[k] * row_factor(p.row_scale, e >> 7));
+          if (e < total && col0 + col < N && y_ok(p, p.Y + (size_t)(e >> 7) * N + col0 + col, (size_t)M * N))
+            p.Y[(size_t)(e >> 7) * N + col0 + col] = to_act<kB>(v[k] * row_factor_at(p, e >> 7));
         }
       } else {
         // a run that starts inside block b: publish the partial tile, then
@@ -672,10 +703,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs p)
         float* my = p.tiles + (size_t)blockIdx.x * kTileFloats;
         for (int e = threadIdx.x; e < total; e += kThreads) {
           const int tok = e >> 7, col = e & (kDecodeBlockCols - 1);
-          my[e] = red[tok * kRedStride + col];
+          if (tile_ok(p, my + e)) my[e] = red[tok * kRedStride + col];
         }
         __syncthreads();
-        if (threadIdx.x == 0) st_release(p.flags + blockIdx.x, 1);
+        if (threadIdx.x == 0 && flag_ok(p, p.flags + blockIdx.x)) st_release(p.flags + blockIdx.x, 1);
       }
       __syncthreads();  // the partial tile buffer is reused by the next segment
       seg_a0 = nu.a0;
@@ -731,7 +762,7 @@ __device__ __forceinline__ void atom_mma_rows(float (&pe)[MT][4], float (&po)[MT
 // first group's pairs, sb its first atom's sums. The next unit's nn atoms are
 // loaded from nwp into w as the codes leave it (when refill).
 template <int MT, int APG, bool kFull, bool kB>
-__device__ __forceinline__ void resident_unit(float (&acc)[MT][4], uint4 (&w)[kBatch], int n, int nn,
+__device__ __forceinline__ void resident_unit(const DecodeArgs& p, float (&acc)[MT][4], uint4 (&w)[kBatch], int n, int nn,
                                            const uint4* nwp, bool refill, uint32_t fa, uint32_t fb,
                                            const uint32_t* sps, const uint8_t* zps, const float* sb,
                                            int t) {
@@ -743,7 +774,7 @@ __device__ __forceinline__ void resident_unit(float (&acc)[MT][4], uint4 (&w)[kB
     code_pairs<kB>(w[u].y, y);
     code_pairs<kB>(w[u].z, z);
     code_pairs<kB>(w[u].w, v);
-    if (refill && (kFull || u < nn)) w[u] = ldg_stream(nwp + u * 32);
+    if (refill && (kFull || u < nn)) w[u] = ldg_stream(wq_at(p, nwp + u * 32));
     if (kFull || u < n) {
       if (u % APG == 0)
         atom_mma_rows<MT, true, kB>(pe, po, x, y, z, v, fa + u * 128, fb + u * 128);
@@ -806,7 +837,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     if (g < run_end) {
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
-        if (u < n) w[u] = ldg_stream(wp + u * 32);
+        if (u < n) w[u] = ldg_stream(wq_at(p, wp + u * 32));
     }
     // group pairs of the CTA's strips, in virtual strip order: record
     // v G + grp of the stage is record gstrip(v) G + grp of Sp/Zp
@@ -818,9 +849,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       const int v = r / G;
       const size_t rg = (size_t)gstrip(v) * G + (r - v * G);  // its record in Sp/Zp
       if (i < 2 * nrec)
-        cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_src + rg * 2 + (i & 1));
+        cp_async16(reinterpret_cast<uint4*>(smem + p.meta_off) + i, sp_at(p, sp_src + rg * 2 + (i & 1), G));
       else
-        cp_async8(reinterpret_cast<uint2*>(smem + p.zp_off) + r, zp_src + rg);
+        cp_async8(reinterpret_cast<uint2*>(smem + p.zp_off) + r, zp_at(p, zp_src + rg, G));
     }
   };
   if (p.early_weights) prefetch();
@@ -833,7 +864,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     const int row_vecs = p.act_row / 16, per_row = K / 8;
     for (int i = threadIdx.x; i < M * per_row; i += (NW * 32)) {
       const int row = i / per_row, c = i - row * per_row;
-      cp_async16(act + row * row_vecs + c, p.A + (size_t)row * K + c * 8);
+      cp_async16(act + row * row_vecs + c, a_at(p, p.A + (size_t)row * K + c * 8));
     }
     for (int c = threadIdx.x; c < row_vecs; c += (NW * 32)) act[M * row_vecs + c] = make_uint4(0, 0, 0, 0);
   }
@@ -891,10 +922,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       for (int j = 0; j < 4; ++j) {
         const int tok = 8 * o + 2 * t + (j & 1);
         if (tok >= M) continue;  // rows past M hold nothing (the zero row)
-        const float val = v[o][j] * scale * row_factor(p.row_scale, tok);
+        const float val = v[o][j] * scale * row_factor_at(p, tok);
         if (kSilu)
           ytile[s * p.ytile_stride + tok * kStripCols + gq + 8 * (j >> 1)] = val;
-        else
+        else if (y_ok(p, p.Y + (size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1), (size_t)M * N))
           p.Y[(size_t)tok * N + gstrip(s) * kStripCols + gq + 8 * (j >> 1)] = to_act<kB>(val);
       }
   };
@@ -922,9 +953,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
     const float* sb = sums + a * MT * 8;
     const uint32_t fa = fa0 + a * 128, fb = fb0 + a * 128;
     if (n == kBatch && n2 == kBatch)
-      resident_unit<MT, APG, true, kB>(acc, w, n, n2, wp2, true, fa, fb, sps, zps, sb, t);
+      resident_unit<MT, APG, true, kB>(p, acc, w, n, n2, wp2, true, fa, fb, sps, zps, sb, t);
     else
-      resident_unit<MT, APG, false, kB>(acc, w, n, n2, wp2, has_next, fa, fb, sps, zps, sb, t);
+      resident_unit<MT, APG, false, kB>(p, acc, w, n, n2, wp2, has_next, fa, fb, sps, zps, sb, t);
     if (!has_next || s2 != strip) {
       // ---- end of a segment: atoms [seg_a0, a + n) of `strip`
       if (seg_a0 == 0 && a + n == natoms && !(kSilu && p.whole_in_red)) {
@@ -982,8 +1013,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) decode_resident_kernel(const
       const int tok = r / kStripCols, c = r - tok * kStripCols;
       const float gv = ytile[q * p.ytile_stride + tok * kStripCols + c];
       const float uv = ytile[(nu + q) * p.ytile_stride + tok * kStripCols + c];
-      p.Y[(size_t)tok * half + (u0 + q) * kStripCols + c] =
-          to_act<kB>(gv / (1.0f + expf(-gv)) * uv);
+      if (y_ok(p, p.Y + (size_t)tok * half + (u0 + q) * kStripCols + c, (size_t)M * half))
+        p.Y[(size_t)tok * half + (u0 + q) * kStripCols + c] = to_act<kB>(gv / (1.0f + expf(-gv)) * uv);
     }
   }
 }

@@ -35,7 +35,7 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 
 template <bool kB>
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ yfull, int M, int N,
-                                                       uint4* __restrict__ y) {
+                                                       uint4* __restrict__ y, int* err) {
   // launched with programmatic serialization: scheduled while the GEMM that
   // writes the product drains, it waits for that grid before reading it
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -44,8 +44,9 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
        i += (long)gridDim.x * blockDim.x) {
     const long m = i / hv, j = i - m * hv;
-    const uint4 g = yfull[m * (N / 8) + j];
-    const uint4 u = yfull[m * (N / 8) + hv + j];
+    const size_t nin = (size_t)M * (N / 8);
+    const uint4 g = *ld_at(yfull + m * (N / 8) + j, yfull, nin, err);
+    const uint4 u = *ld_at(yfull + m * (N / 8) + hv + j, yfull, nin, err);
     const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[4];
 #pragma unroll
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
       const float2 gf = to_float2<kB>(gw[k]), uf = to_float2<kB>(uw[k]);
       o[k] = from_float2<kB>(silu_times(gf.x, uf.x), silu_times(gf.y, uf.y));
     }
-    y[m * hv + j] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (in_buf(y + m * hv + j, y, (size_t)total, err)) y[m * hv + j] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -62,6 +63,9 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
 cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, bool bf16,
                             cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
+  int* err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
   const long vecs = (long)M * (N / 16);
   int blocks = (int)((vecs + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -76,8 +80,8 @@ cudaError_t launch_silu_mul(const uint16_t* Yfull, int M, int N, uint16_t* Y, bo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return bf16 ? cudaLaunchKernelEx(&cfg, silu_mul_kernel<true>, in, M, N, out)
-              : cudaLaunchKernelEx(&cfg, silu_mul_kernel<false>, in, M, N, out);
+  return bf16 ? cudaLaunchKernelEx(&cfg, silu_mul_kernel<true>, in, M, N, out, err)
+              : cudaLaunchKernelEx(&cfg, silu_mul_kernel<false>, in, M, N, out, err);
 }
 
 }  // namespace w4a16

@@ -79,6 +79,7 @@ struct TcParams {
   uint16_t* Y;
   int* counters;  // split > 1: one per output tile, zero between calls
   float* tiles;   // split > 1: fp32 partial tiles [tile][split][bt][128]
+  size_t tile_floats;  // extent of `tiles` (for the checked build)
   int M, N, K, group;
   int bt;          // token tile (MMA N): multiple of 16, 16..256
   int act_slots;   // activation ring depth (stages)
@@ -172,6 +173,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       auto codes = [&](int kb) {
         const int c = kb % ncode;
+        if (!in_smem(code_base + (uint32_t)c * code_bytes, code_bytes, raw, p.err)) return;
         mbar_expect_tx(code_full(c), code_bytes);
         tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, (kb0 + kb) * SA * 4,
                     n0 / kStripCols, code_full(c));
@@ -179,6 +181,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       auto acts = [&](int kb) {
         const int a = kb % nact;
         const uint32_t st = base + (uint32_t)a * act_bytes;
+        if (!in_smem(st, act_bytes, raw, p.err)) return;
         mbar_expect_tx(act_full(a), act_bytes);
 #pragma unroll
         for (int u = 0; u < SA; ++u)
@@ -234,11 +237,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t idesc = f16_idesc(kTileN, bt, kB);
       int a = 0, w = 0;
       uint32_t pw = 0;
-      bool ok = nk > 0 && mbar_wait(dq_full(0), 0, abort_flag, kErrMma, p.err);
+      bool ok = nk > 0 && in_tmem(0, (uint32_t)bt, (uint32_t)p.tmem_cols, p.err) &&
+                mbar_wait(dq_full(0), 0, abort_flag, kErrMma, p.err);
       for (int kb = 0; kb < nk && ok; ++kb) {
         tc_fence_after();
         const uint32_t bst = base + (uint32_t)a * act_bytes;
         const uint32_t acol = tmem_base + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
+        if (!in_smem(bst, act_bytes, raw, p.err) ||
+            !in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols), SA * kAtomCols, (uint32_t)p.tmem_cols, p.err)) {
+          ok = false;
+          break;
+        }
         const int w2 = w + 1 == ndq ? 0 : w + 1;
         const uint32_t pw2 = w2 == 0 ? pw ^ 1u : pw;
         bool ready = true;
@@ -292,8 +301,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (kb < nk && live) {
           const int grp = (int)(((long long)(kb0 + kb) * SA * kStageK + h * 128) / p.group);
           const size_t pg = (size_t)strip * G + grp;
-          const uint32_t sb = p.Sp[pg * 16 + 2 * cp + (hi ? 1 : 0)];
-          const uint32_t zb = reinterpret_cast<const uint8_t*>(p.Zp)[pg * 8 + cp];
+          const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp);
+          const uint32_t sb = *ld_at(p.Sp + pg * 16 + 2 * cp + (hi ? 1 : 0), p.Sp, (size_t)G * p.N, p.err);
+          const uint32_t zb = *ld_at(zp + pg * 8 + cp, zp, (size_t)G * p.N / 2, p.err);
           m.v[h] = sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
         }
       }
@@ -331,7 +341,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int l = 0; l < 4; ++l) {
             const uint32_t chunk = ((uint32_t)(4 * (cp & 1) + l)) ^ (row & 7u);  // 128-byte swizzle
-            const uint4 v = lds128(cb + row * 128u + (chunk << 4));
+            const uint32_t at = cb + row * 128u + (chunk << 4);
+            const uint4 v = lds128(in_smem(at, 16, raw, p.err) ? at : cb);
             wl[u][l] = hi ? v.y : v.x;
             wh[u][l] = hi ? v.w : v.z;
           }
@@ -365,7 +376,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               r[16 + 4 * l + j] = o1[j];
             }
           }
-          tmem_st32(tcol + (uint32_t)((u0 + u) * kAtomCols), r);
+          if (in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols + (u0 + u) * kAtomCols), kAtomCols,
+                      (uint32_t)p.tmem_cols, p.err))
+            tmem_st32(tcol + (uint32_t)((u0 + u) * kAtomCols), r);
         }
       }
       tmem_wait_st();
@@ -415,14 +428,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tmem_wait_ld();
         if (p.split > 1) {  // fp32 partial tile [token][column]
 #pragma unroll
-          for (int j = 0; j < 16; ++j) part[(16 * ch + j) * kTileN + 32 * q + lane] = __uint_as_float(r[j]);
+          for (int j = 0; j < 16; ++j) {
+            float* d = part + (16 * ch + j) * kTileN + 32 * q + lane;
+            if (in_buf(d, p.tiles, p.tile_floats, p.err)) *d = __uint_as_float(r[j]);
+          }
         } else if (n < p.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = m0 + 16 * ch + j;
-            if (tok < p.M)
-              p.Y[(size_t)tok * p.N + n] =
-                  to_out<kB>(__uint_as_float(r[j]) * (p.row_scale ? p.row_scale[tok] : 1.0f));
+            uint16_t* d = p.Y + (size_t)tok * p.N + n;
+            if (tok < p.M && in_buf(d, p.Y, (size_t)p.M * p.N, p.err))
+              *d = to_out<kB>(__uint_as_float(r[j]) *
+                              (p.row_scale ? *ld_at(p.row_scale + tok, p.row_scale, (size_t)p.M, p.err) : 1.0f));
           }
         }
       }
@@ -434,7 +451,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       epilogue_bar<Warps<NG>::kDqThreads>();  // every partial store issued; one release atomic covers them
       if (dw == 0 && lane == 0) {
         int old = 0;
-        if (*abort_flag == 0)
+        if (*abort_flag == 0 && in_buf(p.counters + tile, p.counters, kTcCounterBytes / sizeof(int), p.err))
           asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                        : "=r"(old)
                        : "l"(p.counters + tile)
@@ -458,7 +475,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
               const int e = e0 + u * Warps<NG>::kDqThreads;
-              v[u] = e < n4 ? __ldcg(tb + (size_t)z * (n4) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4* src = tb + (size_t)z * (n4) + e;
+              v[u] = e < n4 ? __ldcg(ld_at(src, reinterpret_cast<const float4*>(p.tiles), p.tile_floats / 4, p.err))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
@@ -473,15 +492,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int e = e0 + u * Warps<NG>::kDqThreads;
             const int tok = m0 + e / (kTileN / 4), n = n0 + (e % (kTileN / 4)) * 4;
             if (e < n4 && tok < p.M && n < p.N) {
-              const float f = p.row_scale ? p.row_scale[tok] : 1.0f;
+              const float f = p.row_scale ? *ld_at(p.row_scale + tok, p.row_scale, (size_t)p.M, p.err) : 1.0f;
               uint2 o;
               o.x = to_out2<kB>(acc[u].x * f, acc[u].y * f);
               o.y = to_out2<kB>(acc[u].z * f, acc[u].w * f);
-              *reinterpret_cast<uint2*>(p.Y + (size_t)tok * p.N + n) = o;
+              uint16_t* d = p.Y + (size_t)tok * p.N + n;
+              if (in_buf(d, p.Y, (size_t)p.M * p.N - 3, p.err)) *reinterpret_cast<uint2*>(d) = o;
             }
           }
         }
-        if (dw == 0 && lane == 0) p.counters[tile] = 0;
+        if (dw == 0 && lane == 0 && in_buf(p.counters + tile, p.counters, kTcCounterBytes / sizeof(int), p.err))
+          p.counters[tile] = 0;
       }
     }
   }
@@ -790,6 +811,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.counters = static_cast<int*>(workspace);
   prm.tiles = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kTcCounterBytes)
                         : nullptr;
+  prm.tile_floats = workspace ? (tc_workspace_bytes(M, N, prm.split) - kTcCounterBytes) / sizeof(float) : 0;
   const TcRings rings = tc_rings(bt, sa);
   prm.act_slots = rings.act;
   prm.code_slots = rings.code;

@@ -238,6 +238,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int tok0 = m0 + (int)rank * half;  // this CTA's half of the tile's tokens
       auto codes = [&](int kb) {
         const int c = kb % ncode;
+        if (!in_smem(code_base + (uint32_t)c * code_bytes, code_bytes, raw, p.err)) return;
         mbar_expect_tx(code_full(c), code_bytes);
         tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, kb * SA * 4, n0 / kStripCols,
                     code_full(c));
@@ -245,6 +246,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       auto acts = [&](int kb) {
         const int a = kb % nact;
         const uint32_t st = base + (uint32_t)a * act_bytes;
+        if (!in_smem(st, act_bytes, raw, p.err)) return;
         mbar_expect_tx(act_full(a), act_bytes);
 #pragma unroll
         for (int u = 0; u < SA; ++u)
@@ -306,11 +308,17 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t idesc = f16_idesc(2 * kCols, bt, kB);
       int a = 0, w = 0;
       uint32_t pw = 0;
-      bool ok = nk > 0 && mbar_wait_poll(dq_full(0), 0, abort_flag, kErrMma, p.err);
+      bool ok = nk > 0 && in_tmem(0, (uint32_t)bt, 512, p.err) &&
+                mbar_wait_poll(dq_full(0), 0, abort_flag, kErrMma, p.err);
       for (int kb = 0; kb < nk && ok; ++kb) {
         tc_fence_after();
         const uint32_t bst = base + (uint32_t)a * act_bytes;
         const uint32_t acol = tmem_base + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
+        if (!in_smem(bst, act_bytes, raw, p.err) ||
+            !in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols), SA * kAtomCols, 512, p.err)) {
+          ok = false;
+          break;
+        }
         const int w2 = w + 1 == ndq ? 0 : w + 1;
         const uint32_t pw2 = w2 == 0 ? pw ^ 1u : pw;
         bool ready = true;
@@ -358,8 +366,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (kb >= nk || !live) return 0u;
       const int grp = (int)((long long)kb * SA * kStageK / p.group);
       const size_t pg = (size_t)strip * G + grp;
-      const uint32_t sb = p.Sp[pg * 16 + 2 * cp + (hi ? 1 : 0)];
-      const uint32_t zb = reinterpret_cast<const uint8_t*>(p.Zp)[pg * 8 + cp];
+      const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp);
+      const uint32_t sb = *ld_at(p.Sp + pg * 16 + 2 * cp + (hi ? 1 : 0), p.Sp, (size_t)G * p.N, p.err);
+      const uint32_t zb = *ld_at(zp + pg * 8 + cp, zp, (size_t)G * p.N / 2, p.err);
       return sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
     };
     const uint32_t dq_remote0 = cluster_addr(dq_full(0), 0);  // the first CTA's dq_full(0)
@@ -385,7 +394,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int l = 0; l < 4; ++l) {
           const uint32_t chunk = ((uint32_t)(4 * (cp & 1) + l)) ^ (row & 7u);  // 128-byte swizzle
-          const uint4 v = lds128(cb + row * 128u + (chunk << 4));
+          const uint32_t at = cb + row * 128u + (chunk << 4);
+          const uint4 v = lds128(in_smem(at, 16, raw, p.err) ? at : cb);
           wl[u][l] = hi ? v.y : v.x;
           wh[u][l] = hi ? v.w : v.z;
         }
@@ -421,7 +431,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             r[16 + 4 * l + j] = o1[j];
           }
         }
-        tmem_st32(tcol + (uint32_t)(u * kAtomCols), r);
+        if (in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols + u * kAtomCols), kAtomCols, 512, p.err))
+          tmem_st32(tcol + (uint32_t)(u * kAtomCols), r);
       }
       tmem_wait_st();
       // this CTA's activations of the stage have landed (the MMAs read them too)
@@ -469,9 +480,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = m0 + 16 * ch + j;
-            if (tok < p.M)
-              p.Y[(size_t)tok * p.N + n] =
-                  to_out<kB>(__uint_as_float(r[j]) * (p.row_scale ? p.row_scale[tok] : 1.0f));
+            uint16_t* d = p.Y + (size_t)tok * p.N + n;
+            if (tok < p.M && in_buf(d, p.Y, (size_t)p.M * p.N, p.err))
+              *d = to_out<kB>(__uint_as_float(r[j]) *
+                              (p.row_scale ? *ld_at(p.row_scale + tok, p.row_scale, (size_t)p.M, p.err) : 1.0f));
           }
         }
       }

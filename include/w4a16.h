@@ -321,7 +321,10 @@ int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* Wq, const uint16_t* sc
                        uint16_t* Y, void* stream);
 
 /* Synchronizes `stream`, then reads and clears the library's device error
- * word (set by a kernel that gave up a bounded wait or failed a self-check).
+ * word (set by a kernel that gave up a bounded wait or failed a self-check;
+ * in the bounds-checked build of the library, compiled with -DW4A16_CHECKED,
+ * also by any global or shared-memory access outside its buffer, which the
+ * kernel then skips: bit 64).
  * Returns W4A16_OK or W4A16_ERR_DEVICE_CHECK (message: which check, where). */
 int w4a16_device_status(void* stream);
 

@@ -7,7 +7,7 @@ weights, one shared workspace), against the oracle on
 The oracle quantizes the whole weight itself from the same seeded fp32
 values; nothing it uses comes from the GPU. The worst err/bound ratio of every
 case is recorded (see conftest.py: printed at the end of the session and
-written to gpurun_out/parity_margins.json when that folder exists)."""
+written as JSON to the file W4A16_MARGINS_FILE names, if set)."""
 import numpy as np
 import pytest
 
