@@ -84,7 +84,9 @@ def peaks():
 PROFILED = {
     1: ("decode_resident_kernel", ["decode_impl.cuh", "decode.cu", "common.cuh"],
         "decode_resident_kernel_llama2-7b-decode.md"),
-    3: ("tc_gemm_kernel", ["tc_gemm.cu", "common.cuh"], "tc_gemm_kernel_llama2-7b-prefill.md"),
+    2: ("tc_gemm_kernel", ["tc_gemm.cu", "tc_ptx.cuh", "common.cuh"], "tc_gemm_kernel_llama2-13b-mid.md"),
+    3: ("tc_pair_kernel", ["tc_pair.cu", "tc_gemm.cu", "tc_ptx.cuh", "common.cuh"],
+        "tc_pair_kernel_llama2-7b-prefill.md"),
     4: ("tc_pair_kernel", ["tc_pair.cu", "tc_gemm.cu", "tc_ptx.cuh", "common.cuh"],
         "tc_pair_kernel_llama2-70b-sweep.md"),
 }
