@@ -255,11 +255,13 @@ TC_CONFIG_KEYS = ("token_tile", "stage_atoms", "act_slots", "code_slots", "dq_sl
                   "dequant_groups", "smem_bytes", "ctas_per_sm")
 
 
-def tc_config(M: int, K: int, group: int) -> dict:
-    """The one-SM tensor-core kernel's configuration for M rows (host-only)."""
-    out = (ctypes.c_int * 8)()
-    _check(lib().w4a16_tc_config(M, K, group, out, 8), "w4a16_tc_config")
-    return dict(zip(TC_CONFIG_KEYS, list(out)))
+def tc_config(M: int, K: int, group: int, pair: bool = False) -> dict:
+    """The one-SM tensor-core kernel's configuration for M rows, or with
+    `pair` the CTA-pair kernel's (per CTA; ctas_per_sm 1) (host-only)."""
+    out = (ctypes.c_int * 15)()
+    _check(lib().w4a16_tc_config(M, K, group, out, 15), "w4a16_tc_config")
+    vals = list(out)
+    return dict(zip(TC_CONFIG_KEYS, vals[8:15] + [1] if pair else vals[:8]))
 
 
 def gemm(A: torch.Tensor, pw: PackedWeight, out: Optional[torch.Tensor] = None,

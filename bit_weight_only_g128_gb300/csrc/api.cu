@@ -472,10 +472,12 @@ int w4a16_tc_config(int M, int K, int group, int* out, int n) {
   if (M < 1) return fail(W4A16_ERR_INVALID_ARG, "M=%d must be positive", M);
   if (!out || n < 8) return fail(W4A16_ERR_INVALID_ARG, "out must hold 8 values (n=%d)", n);
   if (int rc = check_kn(K, 16, group)) return rc;
-  int cfg[8];
+  int cfg[15];
   if (!tc_config(M, K, group, cfg))
     return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "no valid tensor-core configuration for M=%d K=%d", M, K);
-  for (int i = 0; i < 8; ++i) out[i] = cfg[i];
+  if (n >= 15 && !tc_pair_config(M, K, group, cfg + 8))
+    return fail(W4A16_ERR_UNSUPPORTED_SHAPE, "no valid CTA-pair configuration for M=%d K=%d", M, K);
+  for (int i = 0; i < (n >= 15 ? 15 : 8); ++i) out[i] = cfg[i];
   return ok();
 }
 

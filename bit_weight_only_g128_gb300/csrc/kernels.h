@@ -81,16 +81,19 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
                            int split, void* workspace, bool early_weights, bool bf16,
                            const float* row_scale, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int split);
-// Two-SM tensor-core GEMM for large M: clusters of two CTAs, each pair one
-// output tile of 256 columns x tc_pair_token_tile(M) tokens over all of K
-// (tcgen05.mma.cta_group::2); no workspace.
+// Two-SM tensor-core GEMM for large M: persistent clusters of two CTAs (as
+// many as are resident at once), each pair taking output tiles of 256
+// columns x tc_pair_token_tile(M) tokens over all of K in turn, the rings
+// running on across tiles (tcgen05.mma.cta_group::2); no workspace.
 cudaError_t launch_tc_pair(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
                            const uint32_t* Zp, uint16_t* Y, int M, int N, int K, int group,
                            bool early_weights, bool bf16, const float* row_scale,
                            cudaStream_t stream);
 int tc_pair_token_tile(int M);
 int tc_pair_stage_atoms(int K, int group);
-size_t tc_pair_smem_bytes(int bt, int sa, int* act_slots, int* dq_slots, int* code_slots);
+// The CTA-pair kernel's configuration for M rows (w4a16_tc_config's
+// out[8..14]); false if its rings would break the kernel's barrier invariants.
+bool tc_pair_config(int M, int K, int group, int out[7]);
 // 2-D tensor map of a row-major [dims1][dims0] array of `esize`-byte elements
 // with box [box1][box0], from a per-process cache keyed by pointer, shape,
 // box and type (encoding one costs a driver call); false if it cannot be

@@ -171,15 +171,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // each ring and issues whichever is free, so that neither ring waits for
     // the other's slots.
     if (lane == 0) {
-      auto codes = [&](int kb) {
-        const int c = kb % ncode;
+      auto codes = [&](int kb, int c) {
         if (!in_smem(code_base + (uint32_t)c * code_bytes, code_bytes, raw, p.err)) return;
         mbar_expect_tx(code_full(c), code_bytes);
         tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, (kb0 + kb) * SA * 4,
                     n0 / kStripCols, code_full(c));
       };
-      auto acts = [&](int kb) {
-        const int a = kb % nact;
+      auto acts = [&](int kb, int a) {
         const uint32_t st = base + (uint32_t)a * act_bytes;
         if (!in_smem(st, act_bytes, raw, p.err)) return;
         mbar_expect_tx(act_full(a), act_bytes);
@@ -188,21 +186,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tma_load_2d(st + u * atom_act, &tmA, ((kb0 + kb) * SA + u) * kStageK, m0, act_full(a));
       };
       int ci = 0, ai = 0;
+      RingPos cpos{0, 0u}, apos{0, 0u};  // ring positions of stages ci and ai
       // static weights: the first ring of codes goes out before the wait for
       // the previous grid (the slots are free: nothing has used them yet)
       if (p.early_weights)
-        for (; ci < nk && ci < ncode; ++ci) codes(ci);
+        for (; ci < nk && ci < ncode; ++ci, cpos.step(1, ncode)) codes(ci, cpos.slot);
       grid_dependency_wait();
       uint64_t t0 = globaltimer();
       uint32_t idle = 0;
       while (ci < nk || ai < nk) {
         bool progress = false;
-        if (ci < nk && mbar_test(code_empty(ci % ncode), ((uint32_t)(ci / ncode) & 1u) ^ 1u)) {
-          codes(ci++);
+        if (ci < nk && mbar_test(code_empty(cpos.slot), cpos.phase ^ 1u)) {
+          codes(ci++, cpos.slot);
+          cpos.step(1, ncode);
           progress = true;
         }
-        if (ai < nk && mbar_test(stage_done(ai % nact), ((uint32_t)(ai / nact) & 1u) ^ 1u)) {
-          acts(ai++);
+        if (ai < nk && mbar_test(stage_done(apos.slot), apos.phase ^ 1u)) {
+          acts(ai++, apos.slot);
+          apos.step(1, nact);
           progress = true;
         }
         if (progress) {
@@ -294,12 +295,32 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     struct Meta {
       uint32_t v[MH];
     };
-    auto load_meta = [&](int kb, Meta& m) {
+    // the stages' meta are loaded in order, NG stages apart: the group of
+    // stage mkb is followed without a division (gk = k of the stage's first
+    // atom, gend = k where the group after the stage's group starts)
+    int mkb = grp_id, mgrp = 0, mgend = p.group;
+    auto meta_step = [&]() {
+      mkb += NG;
+      const int gk = (kb0 + mkb) * SA * kStageK;
+      while (gk >= mgend) {
+        ++mgrp;
+        mgend += p.group;
+      }
+    };
+    {
+      const int gk = (kb0 + mkb) * SA * kStageK;
+      mgrp = gk / p.group;
+      mgend = (mgrp + 1) * p.group;
+    }
+    // loads the meta of stage mkb into m and steps to the group's next stage
+    auto load_meta = [&](Meta& m) {
 #pragma unroll
       for (int h = 0; h < MH; ++h) {
         m.v[h] = 0u;
-        if (kb < nk && live) {
-          const int grp = (int)(((long long)(kb0 + kb) * SA * kStageK + h * 128) / p.group);
+        if (mkb < nk && live) {
+          // SA >= 2: groups of 128 k or more, and the second 128 k of a stage
+          // starts a new group exactly when it reaches gend
+          const int grp = mgrp + ((h > 0 && (kb0 + mkb) * SA * kStageK + h * 128 >= mgend) ? 1 : 0);
           const size_t pg = (size_t)strip * G + grp;
           const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp);
           const uint32_t sb = *ld_at(p.Sp + pg * 16 + 2 * cp + (hi ? 1 : 0), p.Sp, (size_t)G * p.N, p.err);
@@ -307,21 +328,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           m.v[h] = sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
         }
       }
+      meta_step();
     };
     // one stage: wait for its codes, read this column's words, release the
     // codes; wait for the tensor-memory slot; dequantize and store; wait for
     // the stage's activations; arrive
+    // ring positions of this group's next stage kb (its stages are NG apart)
+    RingPos spos_code, spos_act;
+    spos_code.init(grp_id, ncode);
+    spos_act.init(grp_id, nact);
+    int sw = grp_id % ndq;
     auto stage = [&](int kb, const Meta& meta) -> bool {
-      const int cs = kb % ncode, a = kb % nact, w = kb % ndq;
-      if (!mbar_wait(code_full(cs), (uint32_t)(kb / ncode) & 1u, abort_flag, kErrDequant, p.err))
+      const int cs = spos_code.slot, a = spos_act.slot, w = sw;
+      const uint32_t code_par = spos_code.phase, act_par = spos_act.phase;
+      const RingPos prev = spos_act.before(ndq, nact);  // stage kb - dq_slots (dq_slots <= act_slots)
+      spos_code.step(NG, ncode);
+      spos_act.step(NG, nact);
+      sw += NG;
+      while (sw >= ndq) sw -= ndq;
+      if (!mbar_wait(code_full(cs), code_par, abort_flag, kErrDequant, p.err))
         return false;
       const uint32_t cb = code_base + (uint32_t)cs * code_bytes;
       // the slot's previous stage (kb - dq_slots) has completed its MMAs
       auto wait_slot = [&]() -> bool {
         if (kb < ndq) return true;
-        const int prev = kb - ndq;
-        if (!mbar_wait(stage_done(prev % nact), (uint32_t)(prev / nact) & 1u, abort_flag, kErrDequant,
-                       p.err))
+        if (!mbar_wait(stage_done(prev.slot), prev.phase, abort_flag, kErrDequant, p.err))
           return false;
         tc_fence_after();
         return true;
@@ -383,7 +414,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       tmem_wait_st();
       // the stage's activations have landed (the MMAs read them too)
-      if (!mbar_wait(act_full(a), (uint32_t)(kb / nact) & 1u, abort_flag, kErrDequant, p.err))
+      if (!mbar_wait(act_full(a), act_par, abort_flag, kErrDequant, p.err))
         return false;
       tc_fence_before();
       __syncwarp();
@@ -396,20 +427,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // wait for the previous grid (which orders this warp's stores of Y)
     Meta m0s, m1s, m2s;
     if (p.early_weights) {
-      load_meta(grp_id, m0s);
-      load_meta(grp_id + NG, m1s);
+      load_meta(m0s);  // stage grp_id
+      load_meta(m1s);  // stage grp_id + NG
     }
     grid_dependency_wait();
     if (!p.early_weights) {
-      load_meta(grp_id, m0s);
-      load_meta(grp_id + NG, m1s);
+      load_meta(m0s);
+      load_meta(m1s);
     }
     for (int kb = grp_id; kb < nk; kb += 3 * NG) {
-      load_meta(kb + 2 * NG, m2s);
+      load_meta(m2s);  // stage kb + 2 NG
       if (!stage(kb, m0s) || kb + NG >= nk) break;
-      load_meta(kb + 3 * NG, m0s);
+      load_meta(m0s);  // kb + 3 NG
       if (!stage(kb + NG, m1s) || kb + 2 * NG >= nk) break;
-      load_meta(kb + 4 * NG, m1s);
+      load_meta(m1s);  // kb + 4 NG
       if (!stage(kb + 2 * NG, m2s)) break;
     }
 

@@ -47,6 +47,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -63,6 +66,19 @@ constexpr int kAtomCols = kStageK / 2;           // tensor-memory columns of one
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBarBytes = 1024;
 
+// Stage s of a cluster's sequence as (its tile's index in the sequence,
+// stage kb of that tile), stepped forward without a division.
+struct SeqPos {
+  int kb, tile;
+  __device__ __forceinline__ void step(int d, int nk) {
+    kb += d;
+    while (kb >= nk) {
+      kb -= nk;
+      ++tile;
+    }
+  }
+};
+
 template <int NG>
 struct PairWarps {
   static constexpr int kThreads = 64 + 128 * NG;
@@ -74,6 +90,8 @@ struct PairParams {
   uint16_t* Y;
   int M, N, K, group;
   int bt;          // tokens per tile (MMA N over the pair): 128 or 256
+  int tiles;       // output tiles of the launch: column pairs x token tiles
+  int tiles_m;     // token tiles (the fastest index of a tile)
   int act_slots;   // activation ring depth (stages)
   int code_slots;  // packed-code ring depth (stages)
   int dq_slots;    // dequantized-operand ring depth (stages), at most act_slots
@@ -171,6 +189,18 @@ __device__ __forceinline__ void pair_commit_both(uint32_t bar) {
 
 // SA: 64-k atoms per pipeline stage (2 when K and the group are multiples of
 // 128, else 1); NG: dequant groups.
+//
+// Persistent: the grid is one cluster per TPC (at most), and cluster c takes
+// the tiles c, c + clusters, ... in raster order (token tiles fastest). The
+// rings run on across tiles: stage s of the cluster's sequence is stage
+// s % nk of its tile s / nk, so the copies and conversions of a tile's first
+// stages proceed while the previous tile's last MMAs and epilogue run. The
+// single accumulator is handed over with two more barriers: accum_full (both
+// CTAs; committed after a tile's last MMA) and accum_empty (first CTA; every
+// dequant warp of both CTAs arrives once it has stored its part of the tile);
+// the MMA thread waits for accum_empty before the next tile's first MMA.
+// A group stores its part of tile i right after converting its first stage of
+// a later tile (whose operands then wait in the rings), or at its end.
 template <int SA, bool kB, int NG>
 __global__ void __launch_bounds__(PairWarps<NG>::kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -192,19 +222,29 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto dq_full = [&](int w) { return bars + 8u * (2 * nact + w); };
   auto code_full = [&](int c) { return bars + 8u * (2 * nact + ndq + c); };
   auto code_empty = [&](int c) { return bars + 8u * (2 * nact + ndq + ncode + c); };
-  const uint32_t accum_bar = bars + 8u * (2 * nact + ndq + 2 * ncode);
-  const uint32_t tmem_slot = accum_bar + 8u;
+  const uint32_t accum_full = bars + 8u * (2 * nact + ndq + 2 * ncode);
+  const uint32_t accum_empty = accum_full + 8u;  // used in the first CTA
+  const uint32_t drain_bar = accum_empty + 8u;   // the MMAs issued before an abort completed
+  const uint32_t tmem_slot = drain_bar + 8u;
   uint8_t* gen_base = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gen_base + (tmem_slot + 4u - base));
 
   const uint32_t rank = cluster_rank();  // 0: the CTA that issues the MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid: x = 2 * token tile + column half (the pair: two consecutive x; token
-  // tiles fastest, so the token tiles of one column pair run together and its
-  // weights are read from DRAM once), y = column pair
-  const int n0 = (2 * blockIdx.y + (blockIdx.x & 1)) * kCols;  // this CTA's 128 weight columns
-  const int m0 = (blockIdx.x >> 1) * bt;                        // the pair's tokens
-  const int nk = p.K / (kStageK * SA);                          // stages
+  const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const int nk = p.K / (kStageK * SA);  // stages of one tile
+  // this cluster's tiles: cluster, cluster + clusters, ...
+  const int ntl = cluster < p.tiles ? (p.tiles - 1 - cluster) / clusters + 1 : 0;
+  const int total = ntl * nk;  // stages of the cluster's sequence
+  // tile i of the sequence: this CTA's 128 weight columns and the pair's tokens
+  auto tile_n0 = [&](int i) {
+    const int t = cluster + i * clusters;
+    return (2 * (t / p.tiles_m) + (int)rank) * kCols;
+  };
+  auto tile_m0 = [&](int i) {
+    const int t = cluster + i * clusters;
+    return (t % p.tiles_m) * bt;
+  };
 
   if (threadIdx.x == 0) {
     for (int a = 0; a < nact; ++a) {
@@ -214,9 +254,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int w = 0; w < ndq; ++w) mbar_init(dq_full(w), 8);  // used in the first CTA: a group of both CTAs
     for (int c = 0; c < ncode; ++c) {
       mbar_init(code_full(c), 1);
-      mbar_init(code_empty(c), 4);
+      mbar_init(code_empty(c), 4);  // the warps of the group that converts the stage
     }
-    mbar_init(accum_bar, 1);
+    mbar_init(accum_full, 1);
+    mbar_init(accum_empty, 2 * 4 * NG);  // every dequant warp of both CTAs
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -235,39 +277,55 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // One thread keeps both rings full: it polls the slot of the next copy of
     // each ring and issues whichever is free.
     if (lane == 0) {
-      const int tok0 = m0 + (int)rank * half;  // this CTA's half of the tile's tokens
-      auto codes = [&](int kb) {
-        const int c = kb % ncode;
-        if (!in_smem(code_base + (uint32_t)c * code_bytes, code_bytes, raw, p.err)) return;
-        mbar_expect_tx(code_full(c), code_bytes);
-        tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, kb * SA * 4, n0 / kStripCols,
-                    code_full(c));
-      };
-      auto acts = [&](int kb) {
-        const int a = kb % nact;
-        const uint32_t st = base + (uint32_t)a * act_bytes;
-        if (!in_smem(st, act_bytes, raw, p.err)) return;
-        mbar_expect_tx(act_full(a), act_bytes);
-#pragma unroll
-        for (int u = 0; u < SA; ++u)
-          tma_load_2d(st + u * atom_act, &tmA, (kb * SA + u) * kStageK, tok0, act_full(a));
-      };
+      // the next copy of each ring: its stage, tile position, ring slot and
+      // the tile's strip (codes) or this CTA's first token (activations)
       int ci = 0, ai = 0;
+      SeqPos cseq{0, 0}, aseq{0, 0};
+      RingPos cpos{0, 0u}, apos{0, 0u};
+      int cstrip = tile_n0(0) / kStripCols;
+      int atok = tile_m0(0) + (int)rank * half;  // this CTA's half of the tile's tokens
+      auto codes = [&]() {
+        const int c = cpos.slot;
+        if (in_smem(code_base + (uint32_t)c * code_bytes, code_bytes, raw, p.err)) {
+          mbar_expect_tx(code_full(c), code_bytes);
+          tma_load_3d(code_base + (uint32_t)c * code_bytes, &tmW, 0, cseq.kb * SA * 4, cstrip, code_full(c));
+        }
+        ++ci;
+        cpos.step(1, ncode);
+        const int tl = cseq.tile;
+        cseq.step(1, nk);
+        if (cseq.tile != tl && ci < total) cstrip = tile_n0(cseq.tile) / kStripCols;
+      };
+      auto acts = [&]() {
+        const int a = apos.slot;
+        const uint32_t st = base + (uint32_t)a * act_bytes;
+        if (in_smem(st, act_bytes, raw, p.err)) {
+          mbar_expect_tx(act_full(a), act_bytes);
+#pragma unroll
+          for (int u = 0; u < SA; ++u)
+            tma_load_2d(st + u * atom_act, &tmA, (aseq.kb * SA + u) * kStageK, atok, act_full(a));
+        }
+        ++ai;
+        apos.step(1, nact);
+        const int tl = aseq.tile;
+        aseq.step(1, nk);
+        if (aseq.tile != tl && ai < total) atok = tile_m0(aseq.tile) + (int)rank * half;
+      };
       // static weights: the first ring of codes before the wait for the
       // previous grid (the slots are free: nothing has used them yet)
       if (p.early_weights)
-        for (; ci < nk && ci < ncode; ++ci) codes(ci);
+        while (ci < total && ci < ncode) codes();
       grid_dependency_wait();
       uint64_t t0 = globaltimer();
       uint32_t idle = 0;
-      while (ci < nk || ai < nk) {
+      while (ci < total || ai < total) {
         bool progress = false;
-        if (ci < nk && mbar_test(code_empty(ci % ncode), ((uint32_t)(ci / ncode) & 1u) ^ 1u)) {
-          codes(ci++);
+        if (ci < total && mbar_test(code_empty(cpos.slot), cpos.phase ^ 1u)) {
+          codes();
           progress = true;
         }
-        if (ai < nk && mbar_test(stage_done(ai % nact), ((uint32_t)(ai / nact) & 1u) ^ 1u)) {
-          acts(ai++);
+        if (ai < total && mbar_test(stage_done(apos.slot), apos.phase ^ 1u)) {
+          acts();
           progress = true;
         }
         if (progress) {
@@ -285,14 +343,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA leaves
-        for (int kb = (ai > nact ? ai - nact : 0); kb < ai; ++kb)
-          mbar_drain(act_full(kb % nact), (uint32_t)(kb / nact) & 1u, p.err);
-        for (int kb = (ci > ncode ? ci - ncode : 0); kb < ci; ++kb)
-          mbar_drain(code_full(kb % ncode), (uint32_t)(kb / ncode) & 1u, p.err);
+        for (int s = (ai > nact ? ai - nact : 0); s < ai; ++s)
+          mbar_drain(act_full(s % nact), (uint32_t)(s / nact) & 1u, p.err);
+        for (int s = (ci > ncode ? ci - ncode : 0); s < ci; ++s)
+          mbar_drain(code_full(s % ncode), (uint32_t)(s / ncode) & 1u, p.err);
       } else {
         // the pair's last commits have reached this CTA: none is still on its way
-        for (int kb = (nk > nact ? nk - nact : 0); kb < nk; ++kb)
-          if (!mbar_wait_poll(stage_done(kb % nact), (uint32_t)(kb / nact) & 1u, abort_flag,
+        for (int s = (total > nact ? total - nact : 0); s < total; ++s)
+          if (!mbar_wait_poll(stage_done(s % nact), (uint32_t)(s / nact) & 1u, abort_flag,
                               kErrProducer, p.err))
             break;
       }
@@ -304,88 +362,141 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // warp after its tensor-memory stores completed and its own CTA's
       // activations of the stage landed: one test covers both operands of
       // both CTAs. The next stage's barrier is tested between this stage's
-      // MMAs, while the tensor core works through the queued ones.
+      // MMAs, while the tensor core works through the queued ones. A tile's
+      // first MMA waits for the previous tile's accumulator to be stored.
       const uint32_t idesc = f16_idesc(2 * kCols, bt, kB);
       int a = 0, w = 0;
       uint32_t pw = 0;
-      bool ok = nk > 0 && in_tmem(0, (uint32_t)bt, 512, p.err) &&
+      bool ok = total > 0 && in_tmem(0, (uint32_t)bt, 512, p.err) &&
                 mbar_wait_poll(dq_full(0), 0, abort_flag, kErrMma, p.err);
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        tc_fence_after();
-        const uint32_t bst = base + (uint32_t)a * act_bytes;
-        const uint32_t acol = tmem_base + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
-        if (!in_smem(bst, act_bytes, raw, p.err) ||
-            !in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols), SA * kAtomCols, 512, p.err)) {
-          ok = false;
+      // one loop per tile: the hand-over of the accumulator stays out of the
+      // loop that issues the MMAs (a branch there cost about 10% of the stage
+      // rate: this thread's issue is on the critical path)
+      for (int tl = 0; tl < ntl && ok; ++tl) {
+        if (tl > 0 && !(ok = mbar_wait_poll(accum_empty, (uint32_t)(tl - 1) & 1u, abort_flag, kErrMma, p.err)))
           break;
-        }
-        const int w2 = w + 1 == ndq ? 0 : w + 1;
-        const uint32_t pw2 = w2 == 0 ? pw ^ 1u : pw;
-        bool ready = true;
-#pragma unroll
-        for (int u = 0; u < SA; ++u) {
-          const uint64_t bdesc = sw128_kmajor_desc(bst + u * atom_act);
-#pragma unroll
-          for (int kk = 0; kk < kStageK / 16; ++kk) {  // 16 k per MMA: 8 columns of A, 32 bytes of B
-            pair_mma_f16_ts(tmem_base, acol + (uint32_t)(u * kAtomCols + 8 * kk), bdesc + 2u * kk, idesc,
-                            (kb | u | kk) != 0);
-            if (u == 0 && kk == 1 && kb + 1 < nk) ready = mbar_test(dq_full(w2), pw2);
+        const bool more = tl + 1 < ntl;  // another tile's stages follow this tile's last
+        for (int kb = 0; kb < nk && ok; ++kb) {
+          tc_fence_after();
+          const uint32_t bst = base + (uint32_t)a * act_bytes;
+          const uint32_t acol = tmem_base + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
+          if (!in_smem(bst, act_bytes, raw, p.err) ||
+              !in_tmem((uint32_t)(p.dq_col0 + w * SA * kAtomCols), SA * kAtomCols, 512, p.err)) {
+            ok = false;
+            break;
           }
+          const bool next = kb + 1 < nk || more;
+          const int w2 = w + 1 == ndq ? 0 : w + 1;
+          const uint32_t pw2 = w2 == 0 ? pw ^ 1u : pw;
+          bool ready = true;
+#pragma unroll
+          for (int u = 0; u < SA; ++u) {
+            const uint64_t bdesc = sw128_kmajor_desc(bst + u * atom_act);
+#pragma unroll
+            for (int kk = 0; kk < kStageK / 16; ++kk) {  // 16 k per MMA: 8 columns of A, 32 bytes of B
+              pair_mma_f16_ts(tmem_base, acol + (uint32_t)(u * kAtomCols + 8 * kk), bdesc + 2u * kk, idesc,
+                              (kb | u | kk) != 0);
+              if (u == 0 && kk == 1 && next) ready = mbar_test(dq_full(w2), pw2);
+            }
+          }
+          pair_commit_both(stage_done(a));
+          a = a + 1 == nact ? 0 : a + 1;
+          w = w2;
+          pw = pw2;
+          if (next && !ready) ok = mbar_wait_poll(dq_full(w), pw, abort_flag, kErrMma, p.err);
         }
-        pair_commit_both(stage_done(a));
-        a = a + 1 == nact ? 0 : a + 1;
-        w = w2;
-        pw = pw2;
-        if (kb + 1 < nk && !ready) ok = mbar_wait_poll(dq_full(w), pw, abort_flag, kErrMma, p.err);
+        if (ok) pair_commit_both(accum_full);  // the tile's accumulator is complete
       }
-      pair_commit_both(accum_bar);  // fires once every MMA issued above has completed
-      if (!ok) mbar_drain(accum_bar, 0, p.err);  // no MMA may run past the release of tensor memory
+      if (!ok) {
+        // no MMA may run past the release of tensor memory: one more commit,
+        // to both CTAs' drain barriers, fires once every MMA issued has completed
+        pair_commit_both(drain_bar);
+        mbar_drain(drain_bar, 0, p.err);
+      }
     }
   } else {
     // ---------------------------------------------------------- dequant + epilogue
-    // NG groups of four warps; group g converts the stages g, g + NG, ...
-    // Thread (lane quarter q, lane) owns weight column 32 q + lane of this
-    // CTA's 128: tensor-memory lane 32 q + lane, strip 2 q + lane / 16,
-    // column c = lane % 16 of the strip. In the packed format the 16 bytes at
-    // 64 (c % 8) + 16 l (l = 0..3) of a strip's atom hold the words of
-    // k-octets l and 4 + l of columns c % 8 (words 0, 2) and c % 8 + 8 (words
-    // 1, 3).
+    // NG groups of four warps; group g converts the stages g, g + NG, ... of
+    // the cluster's sequence. Thread (lane quarter q, lane) owns weight column
+    // 32 q + lane of this CTA's 128: tensor-memory lane 32 q + lane, strip
+    // 2 q + lane / 16, column c = lane % 16 of the strip. In the packed format
+    // the 16 bytes at 64 (c % 8) + 16 l (l = 0..3) of a strip's atom hold the
+    // words of k-octets l and 4 + l of columns c % 8 (words 0, 2) and c % 8 + 8
+    // (words 1, 3).
     const int dw = warp - 2;
     const int grp_id = dw >> 2;
     const int q = warp & 3;
     const int ls = 2 * q + (lane >> 4);
     const int c = lane & 15, cp = c & 7;
     const bool hi = c >= 8;
-    const int strip = n0 / kStripCols + ls;
-    const bool live = strip < p.N / kStripCols;
     const int G = p.K / p.group;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     // scale bits (low half) and zero point (bits 16..19) of this column for a
-    // stage (one group per stage)
-    auto load_meta = [&](int kb) -> uint32_t {
-      if (kb >= nk || !live) return 0u;
-      const int grp = (int)((long long)kb * SA * kStageK / p.group);
-      const size_t pg = (size_t)strip * G + grp;
-      const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp);
-      const uint32_t sb = *ld_at(p.Sp + pg * 16 + 2 * cp + (hi ? 1 : 0), p.Sp, (size_t)G * p.N, p.err);
-      const uint32_t zb = *ld_at(zp + pg * 8 + cp, zp, (size_t)G * p.N / 2, p.err);
-      return sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
+    // stage (one group per stage). The stages' meta are loaded in order, NG
+    // stages apart; the stage's tile, strip and group are followed without a
+    // division (mgend: the k where the group after the stage's group starts).
+    int mi = grp_id;  // stage of the sequence whose meta loads next
+    SeqPos mseq{grp_id, 0};
+    mseq.step(0, nk);
+    int mstrip = tile_n0(mseq.tile) / kStripCols + ls;
+    int mgrp = mseq.kb * SA * kStageK / p.group;
+    int mgend = (mgrp + 1) * p.group;
+    auto load_meta = [&]() -> uint32_t {
+      uint32_t v = 0u;
+      if (mi < total && mstrip < p.N / kStripCols) {
+        const size_t pg = (size_t)mstrip * G + mgrp;
+        const uint8_t* zp = reinterpret_cast<const uint8_t*>(p.Zp);
+        const uint32_t sb = *ld_at(p.Sp + pg * 16 + 2 * cp + (hi ? 1 : 0), p.Sp, (size_t)G * p.N, p.err);
+        const uint32_t zb = *ld_at(zp + pg * 8 + cp, zp, (size_t)G * p.N / 2, p.err);
+        v = sb | (((zb >> (hi ? 4 : 0)) & 15u) << 16);
+      }
+      mi += NG;
+      const int tl = mseq.tile;
+      mseq.step(NG, nk);
+      if (mseq.tile != tl) {
+        if (mi < total) mstrip = tile_n0(mseq.tile) / kStripCols + ls;
+        mgrp = 0;
+        mgend = p.group;
+      }
+      while (mseq.kb * SA * kStageK >= mgend) {
+        ++mgrp;
+        mgend += p.group;
+      }
+      return v;
     };
-    const uint32_t dq_remote0 = cluster_addr(dq_full(0), 0);  // the first CTA's dq_full(0)
+    const uint32_t dq_remote0 = cluster_addr(dq_full(0), 0);          // the first CTA's dq_full(0)
+    const uint32_t empty_remote = cluster_addr(accum_empty, 0);       // the first CTA's accum_empty
     // a wait that every lane of the warp passes or every lane gives up on:
-    // the tensor-memory stores that follow are .sync.aligned
-    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool poll) -> bool {
-      const bool ok = poll ? mbar_wait_poll(bar, parity, abort_flag, kErrDequant, p.err)
-                           : mbar_wait(bar, parity, abort_flag, kErrDequant, p.err);
+    // the tensor-memory stores and loads that follow are .sync.aligned
+    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool poll, int code) -> bool {
+      const bool ok = poll ? mbar_wait_poll(bar, parity, abort_flag, code, p.err)
+                           : mbar_wait(bar, parity, abort_flag, code, p.err);
       return __all_sync(0xffffffffu, ok);
     };
     // one stage: wait for its codes, read this column's words, release the
     // codes; wait for the tensor-memory slot (its previous stage's MMAs, a
     // commit from the first CTA); dequantize and store; wait for this CTA's
     // activations of the stage; arrive on the first CTA's dq_full
-    auto stage = [&](int kb, uint32_t meta) -> bool {
-      const int cs = kb % ncode, a = kb % nact, w = kb % ndq;
-      if (!warp_wait(code_full(cs), (uint32_t)(kb / ncode) & 1u, false)) return false;
+    // ring positions and tile of this group's next stage (its stages are NG
+    // apart); stile: the tile of the stage converted last
+    RingPos spos_code, spos_act;
+    spos_code.init(grp_id, ncode);
+    spos_act.init(grp_id, nact);
+    int sw = grp_id % ndq;
+    SeqPos sseq{grp_id, 0};
+    sseq.step(0, nk);
+    int stile = 0;
+    auto stage = [&](int s, uint32_t meta) -> bool {
+      const int cs = spos_code.slot, a = spos_act.slot, w = sw;
+      const uint32_t code_par = spos_code.phase, act_par = spos_act.phase;
+      const RingPos prev = spos_act.before(ndq, nact);  // stage s - dq_slots (dq_slots <= act_slots)
+      stile = sseq.tile;
+      spos_code.step(NG, ncode);
+      spos_act.step(NG, nact);
+      sw += NG;
+      while (sw >= ndq) sw -= ndq;
+      sseq.step(NG, nk);
+      if (!warp_wait(code_full(cs), code_par, false, kErrDequant)) return false;
       const uint32_t cb = code_base + (uint32_t)cs * code_bytes;
       uint32_t wl[SA][4], wh[SA][4];  // k-octets l and 4 + l of each atom
 #pragma unroll
@@ -402,13 +513,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(code_empty(cs));  // the codes are in registers
-      if (kb >= ndq) {
-        const int prev = kb - ndq;
-        if (!warp_wait(stage_done(prev % nact), (uint32_t)(prev / nact) & 1u, true)) return false;
+      if (s >= ndq) {
+        if (!warp_wait(stage_done(prev.slot), prev.phase, true, kErrDequant)) return false;
         tc_fence_after();
       }
       const uint32_t z = (meta >> 16) & 15u;
-      const uint16_t s = (uint16_t)(meta & 0xffffu);
+      const uint16_t sc = (uint16_t)(meta & 0xffffu);
       const uint32_t tcol = tmem_base + tlane + (uint32_t)(p.dq_col0 + w * SA * kAtomCols);
 #pragma unroll
       for (int u = 0; u < SA; ++u) {
@@ -417,11 +527,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int l = 0; l < 4; ++l) {
           uint32_t o0[4], o1[4];
           if (kB) {
-            const DeqConstBf16 dc = make_deq_const_bf16(z, s);
+            const DeqConstBf16 dc = make_deq_const_bf16(z, sc);
             dequant_word_bf16(wl[u][l], dc, o0);
             dequant_word_bf16(wh[u][l], dc, o1);
           } else {
-            const DeqConst dc = make_deq_const(z, s);
+            const DeqConst dc = make_deq_const(z, sc);
             dequant_word(wl[u][l], dc, o0);
             dequant_word(wh[u][l], dc, o1);
           }
@@ -436,45 +546,23 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       tmem_wait_st();
       // this CTA's activations of the stage have landed (the MMAs read them too)
-      if (!warp_wait(act_full(a), (uint32_t)(kb / nact) & 1u, false)) return false;
+      if (!warp_wait(act_full(a), act_par, false, kErrDequant)) return false;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(dq_remote0 + 8u * w);
       return true;
     };
-    // scales and zero points: three register sets in rotation, each loaded two
-    // of this group's stages before its own (no stage waits for its loads).
-    // They are weights: with static weights the first sets are read before the
-    // wait for the previous grid (which orders this warp's stores of Y)
-    uint32_t m0s = 0, m1s = 0, m2s = 0;
-    if (p.early_weights) {
-      m0s = load_meta(grp_id);
-      m1s = load_meta(grp_id + NG);
-    }
-    grid_dependency_wait();
-    if (!p.early_weights) {
-      m0s = load_meta(grp_id);
-      m1s = load_meta(grp_id + NG);
-    }
-    for (int kb = grp_id; kb < nk; kb += 3 * NG) {
-      m2s = load_meta(kb + 2 * NG);
-      if (!stage(kb, m0s) || kb + NG >= nk) break;
-      m0s = load_meta(kb + 3 * NG);
-      if (!stage(kb + NG, m1s) || kb + 2 * NG >= nk) break;
-      m1s = load_meta(kb + 4 * NG);
-      if (!stage(kb + 2 * NG, m2s)) break;
-    }
-
-    // epilogue: tensor-memory lanes 32q..32q+31 are this CTA's columns, its
-    // columns are the pair's BT tokens (the first CTA's half, then the second's)
-    const bool have_accum = mbar_wait_poll(accum_bar, 0, abort_flag, kErrEpilogue, p.err);
-    __syncwarp();
-    if (__all_sync(0xffffffffu, have_accum)) {  // warp-uniform: tcgen05.ld is .aligned
+    // this warp's part of tile i's epilogue: tensor-memory lanes 32q..32q+31
+    // are this CTA's columns, its columns the pair's BT tokens (the first
+    // CTA's half, then the second's); then the accumulator is free for the
+    // first CTA's next tile
+    auto epilogue = [&](int i) -> bool {
+      if (!warp_wait(accum_full, (uint32_t)i & 1u, true, kErrEpilogue)) return false;
       tc_fence_after();
-      const int n = n0 + 32 * q + lane;
+      const int n = tile_n0(i) + 32 * q + lane, m0 = tile_m0(i);
       for (int ch = grp_id; ch < bt / 16; ch += NG) {
         uint32_t r[16];
-        tmem_ld16(tmem_base + tlane + (uint32_t)(16 * ch), r);
+        if (in_tmem((uint32_t)(16 * ch), 16, 512, p.err)) tmem_ld16(tmem_base + tlane + (uint32_t)(16 * ch), r);
         tmem_wait_ld();
         if (n < p.N) {
 #pragma unroll
@@ -487,12 +575,48 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(empty_remote);
+      return true;
+    };
+    // scales and zero points, loaded two of this group's stages before their
+    // own (m0s: this stage's, m1s: the next one's). They are weights: with
+    // static weights the first ones are read before the wait for the previous
+    // grid (which orders this warp's stores of Y)
+    uint32_t m0s = 0, m1s = 0;
+    if (p.early_weights) {
+      m0s = load_meta();  // stage grp_id
+      m1s = load_meta();  // stage grp_id + NG
     }
+    grid_dependency_wait();
+    if (!p.early_weights) {
+      m0s = load_meta();
+      m1s = load_meta();
+    }
+    // the tiles whose epilogue this warp has done: [0, done). One call site
+    // each for the stage and the epilogue keeps the loop's code small.
+    int done = 0;
+    bool ok = true;
+    for (int s = grp_id; s < total && ok; s += NG) {
+      const uint32_t m2s = load_meta();  // stage s + 2 NG
+      ok = stage(s, m0s);
+      // the epilogues of the tiles before the converted stage's tile
+      for (; ok && done < stile; ++done) ok = epilogue(done);
+      m0s = m1s;
+      m1s = m2s;
+    }
+    // the remaining epilogues (normally the last tile's)
+    for (; ok && done < ntl; ++done) ok = epilogue(done);
   }
 
-  // an epilogue that gave up still lets the pair's last commit land here
-  // before the CTA can leave (immediate in a normal run)
-  if (threadIdx.x == 64) mbar_drain(accum_bar, 0, p.err);
+  // the pair's last commit has landed here before the CTA can leave: the last
+  // tile's accumulator commit in a normal run (already waited for by the
+  // epilogue), the drain commit after an abort
+  if (threadIdx.x == 64) {
+    if (*abort_flag == 0) mbar_drain(accum_full, (uint32_t)(ntl - 1) & 1u, p.err);
+    else mbar_drain(drain_bar, 0, p.err);
+  }
   __syncwarp();
   tc_fence_before();
   cluster_sync();  // both CTAs done with the tensor memory and each other's barriers
@@ -532,18 +656,57 @@ PairRings pair_rings(int bt, int sa) {
   return r;
 }
 
+// Besides the one-SM kernel's invariants, the dequantized slots are at least
+// the groups: a group's conversion of a stage then waits only for MMAs of
+// tiles whose accumulator it has already stored (its previous stage came at
+// most `groups` stages earlier), so a tile's epilogue never waits for itself.
 bool pair_rings_valid(const PairRings& r) {
-  return r.dq >= 1 && r.dq <= r.act && r.act >= r.groups && r.code % r.groups == 0;
+  return r.dq >= r.groups && r.dq <= r.act && r.act >= r.groups && r.code % r.groups == 0;
+}
+
+// Clusters of a kernel and launch shape that are resident at once
+// (cudaOccupancyMaxActiveClusters, kept per kernel, device and shared-memory
+// size). A cluster's two CTAs sit on the two SMs of one TPC within one GPC,
+// so GPCs with an odd number of usable SMs leave an SM out and the count can
+// be below SMs / 2; a persistent grid larger than it would run its last
+// clusters after the others, each with its whole share of the tiles.
+cudaError_t max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg, int* out) {
+  struct Entry {
+    const void* kernel;
+    int device;
+    size_t smem;
+    int clusters;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> known;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& k : known)
+      if (k.kernel == kernel && k.device == dev && k.smem == cfg.dynamicSmemBytes) {
+        *out = k.clusters;
+        return cudaSuccess;
+      }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  std::lock_guard<std::mutex> lock(mu);
+  known.push_back({kernel, dev, cfg.dynamicSmemBytes, n});
+  *out = n;
+  return cudaSuccess;
 }
 
 template <int SA, bool kB, int NG>
 cudaError_t launch_pair_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, const PairParams& prm,
-                               dim3 grid, size_t smem, cudaStream_t stream) {
-  cudaError_t e =
-      set_max_smem_once(reinterpret_cast<const void*>(tc_pair_kernel<SA, kB, NG>), kSmemLimit);
+                               size_t smem, cudaStream_t stream) {
+  const void* kern = reinterpret_cast<const void*>(tc_pair_kernel<SA, kB, NG>);
+  cudaError_t e = set_max_smem_once(kern, kSmemLimit);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
   cfg.blockDim = dim3(PairWarps<NG>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -555,18 +718,27 @@ cudaError_t launch_pair_kernel(const CUtensorMap& tmA, const CUtensorMap& tmW, c
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  cfg.numAttrs = 1;           // the occupancy query takes the cluster shape only
+  cfg.gridDim = dim3(2, 1, 1);  // and a grid of whole clusters
+  int resident = 0;
+  e = max_active_clusters(kern, cfg, &resident);
+  if (e != cudaSuccess) return e;
+  // persistent: as many clusters as are resident at once (at most one per
+  // tile), each taking every clusters-th tile
+  const int clusters = prm.tiles < resident ? prm.tiles : resident;
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tc_pair_kernel<SA, kB, NG>, tmA, tmW, prm);
 }
 
 template <bool kB>
 cudaError_t launch_pair_sa(int sa, int ng, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                           const PairParams& prm, dim3 grid, size_t smem, cudaStream_t stream) {
+                           const PairParams& prm, size_t smem, cudaStream_t stream) {
   if (ng == 4)
-    return sa == 2 ? launch_pair_kernel<2, kB, 4>(tmA, tmW, prm, grid, smem, stream)
-                   : launch_pair_kernel<1, kB, 4>(tmA, tmW, prm, grid, smem, stream);
-  return sa == 2 ? launch_pair_kernel<2, kB, 2>(tmA, tmW, prm, grid, smem, stream)
-                 : launch_pair_kernel<1, kB, 2>(tmA, tmW, prm, grid, smem, stream);
+    return sa == 2 ? launch_pair_kernel<2, kB, 4>(tmA, tmW, prm, smem, stream)
+                   : launch_pair_kernel<1, kB, 4>(tmA, tmW, prm, smem, stream);
+  return sa == 2 ? launch_pair_kernel<2, kB, 2>(tmA, tmW, prm, smem, stream)
+                 : launch_pair_kernel<1, kB, 2>(tmA, tmW, prm, smem, stream);
 }
 
 }  // namespace
@@ -575,12 +747,18 @@ int tc_pair_token_tile(int M) { return M > 128 ? 256 : 128; }
 
 int tc_pair_stage_atoms(int K, int group) { return K % 128 == 0 && group % 128 == 0 ? 2 : 1; }
 
-size_t tc_pair_smem_bytes(int bt, int sa, int* act_slots, int* dq_slots, int* code_slots) {
+bool tc_pair_config(int M, int K, int group, int out[7]) {
+  const int bt = tc_pair_token_tile(M);
+  const int sa = tc_pair_stage_atoms(K, group);
   const PairRings r = pair_rings(bt, sa);
-  if (act_slots) *act_slots = r.act;
-  if (dq_slots) *dq_slots = r.dq;
-  if (code_slots) *code_slots = r.code;
-  return r.smem;
+  out[0] = bt;
+  out[1] = sa;
+  out[2] = r.act;
+  out[3] = r.code;
+  out[4] = r.dq;
+  out[5] = r.groups;
+  out[6] = (int)r.smem;
+  return pair_rings_valid(r);
 }
 
 cudaError_t launch_tc_pair(const uint16_t* A, const uint32_t* Wq, const uint16_t* Sp,
@@ -613,9 +791,10 @@ cudaError_t launch_tc_pair(const uint16_t* A, const uint32_t* Wq, const uint16_t
   prm.row_scale = row_scale;
   cudaError_t e = device_error_word(&prm.err);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(2 * ((M + bt - 1) / bt)), (unsigned)((N + 2 * kCols - 1) / (2 * kCols)), 1);
-  return bf16 ? launch_pair_sa<true>(sa, rings.groups, tmA, tmW, prm, grid, rings.smem, stream)
-              : launch_pair_sa<false>(sa, rings.groups, tmA, tmW, prm, grid, rings.smem, stream);
+  prm.tiles_m = (M + bt - 1) / bt;
+  prm.tiles = prm.tiles_m * ((N + 2 * kCols - 1) / (2 * kCols));
+  return bf16 ? launch_pair_sa<true>(sa, rings.groups, tmA, tmW, prm, rings.smem, stream)
+              : launch_pair_sa<false>(sa, rings.groups, tmA, tmW, prm, rings.smem, stream);
 }
 
 }  // namespace w4a16

@@ -22,6 +22,35 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 // role whose wait gave up)
 constexpr int kErrProducer = 1, kErrMma = 2, kErrDequant = 4, kErrEpilogue = 8, kErrDrain = 16;
 
+// Slot and phase parity of a stage in a ring of n slots (slot = s % n,
+// phase = (s / n) & 1), stepped forward without a division: the rings' depths
+// are launch arguments, and a runtime division costs about twenty issue slots
+// in warps whose issue slots bound the stage time.
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ void init(int s, int n) {
+    slot = s % n;
+    phase = (uint32_t)(s / n) & 1u;
+  }
+  __device__ __forceinline__ void step(int d, int n) {
+    slot += d;
+    while (slot >= n) {
+      slot -= n;
+      phase ^= 1u;
+    }
+  }
+  // the position `back` stages earlier (0 < back <= n)
+  __device__ __forceinline__ RingPos before(int back, int n) const {
+    RingPos r{slot - back, phase};
+    if (r.slot < 0) {
+      r.slot += n;
+      r.phase ^= 1u;
+    }
+    return r;
+  }
+};
+
 // ------------------------------------------------------------------ PTX
 
 __device__ __forceinline__ uint64_t globaltimer() {

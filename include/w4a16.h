@@ -106,10 +106,11 @@ extern "C" {
 #define W4A16_PATH_DECODE_RESIDENT 3
 #define W4A16_PATH_DECODE_STREAMK 4
 /* The tensor-core GEMM on pairs of SMs (tcgen05.mma.cta_group::2): clusters
- * of two CTAs, each pair one output tile of 256 columns x 256 tokens (128
- * when M <= 128) over all of K; each CTA dequantizes its 128 columns into
- * its tensor memory (the MMA's A operand) and stages half of the tokens, and
- * the pair's MMAs read both halves. The same
+ * of two CTAs, as many as are resident at once, each taking output tiles of
+ * 256 columns x 256 tokens (128 when M <= 128) over all of K in turn; each
+ * CTA dequantizes its 128 columns into its tensor memory (the MMA's A
+ * operand) and stages half of the tokens, and the pair's MMAs read both
+ * halves. The same
  * arithmetic as W4A16_PATH_TENSOR (RNE_fp16((q - z) s) operands, fp32
  * accumulation); no K split and no workspace of its own. */
 #define W4A16_PATH_TENSOR_PAIR 5
@@ -291,7 +292,11 @@ int w4a16_plan(int M, int N, int K, int group, int* path, int* parts);
  * N), out[1] 64-k atoms per pipeline stage, out[2] activation ring slots,
  * out[3] packed-code ring slots, out[4] dequantized-operand ring slots (in
  * tensor memory), out[5] dequantizing warp groups, out[6] dynamic shared
- * memory bytes, out[7] CTAs per SM. `n` is the length of `out` (at least 8).
+ * memory bytes, out[7] CTAs per SM. With n >= 15, out[8..14] hold the same
+ * for the CTA-pair kernel (W4A16_PATH_TENSOR_PAIR), per CTA: token tile of
+ * the pair (the MMA's N), atoms per stage, activation, code and dequantized
+ * ring slots, dequantizing warp groups, dynamic shared memory bytes.
+ * `n` is the length of `out` (at least 8).
  * Host-only (no device is touched); W4A16_ERR_INVALID_ARG for M < 1, a null
  * `out` or n < 8, and the shape errors of w4a16_gemm. */
 int w4a16_tc_config(int M, int K, int group, int* out, int n);
