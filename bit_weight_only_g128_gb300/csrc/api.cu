@@ -79,25 +79,25 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 // The path for M rows, from measurements on GB300 (CUDA graphs of 20 launches
 // over weight copies larger than L2; the full tables are kept with the design
 // notes).
-// Decode GEMV up to 16 rows; on wide layers (N >= 16384) up to 24 rows, and
-// up to 32 rows (two 16-row passes over the weights) where the layer has at
-// most 2^28 weights (us, decode / one-SM tensor cores):
-//   7B gate_up (4096 x 22016):  16 rows 16.2 / 31.2, 24 rows 26.9 / 31.8, 32 rows 32.0 / 31.7
-//   13B gate_up (5120 x 27648): 16 rows 22.7 / 44.9, 32 rows 44.3 / 51.6, 48 rows 66.0 / 51.6
-//   70B gate_up (8192 x 57344): 24 rows 133.2 / 144.4, 32 rows 154.2 / 145.7
-//   13B qkv (5120 x 15360):     16 rows 16.3 / 27.1, 20 rows 26.5 / 27.5, 32 rows 31.4 / 27.5
+// Decode GEMV up to 16 rows; on wide layers (N >= 16384) of at most 2^28
+// weights up to 24 rows (two 16-row passes over the weights) (us, decode /
+// one-SM tensor cores):
+//   7B gate_up (4096 x 22016):  16 rows 16.3 / 27.3, 24 rows 26.8 / 28.0, 32 rows 32.2 / 28.1
+//   13B gate_up (5120 x 27648): 16 rows 22.7 / 40.7, 24 rows 38.2 / 39.7, 32 rows 44.7 / 39.4
+//   70B gate_up (8192 x 57344): 16 rows 77.9 / 110.0, 20 rows 116.1 / 108.6
+//   13B o_proj (5120 x 5120):   16 rows 11.7 / 11.8, 20 rows 18.6 / 12.1
 // Above, the tensor cores: a CTA pair per 256-column tile (tcgen05.mma
 // cta_group::2) from 256 rows where the pairs' CTAs make at least 80 (they
 // have no K split), else one SM per tile (TFLOP/s, one SM / pair):
-//   256 rows: 70B gate_up 1374 / 1633, 70B qkv 829 / 982, 70B o_proj 951 / 804
-//   512 rows: 70B down 1323 / 1674, 13B o_proj 757 / 886, 7B o_proj 751 / 697
-//   4096 rows: 70B gate_up 1344 / 1457, 7B o_proj 1176 / 1277, 7B qkv 1317 / 1275
-//   128 rows: 13B qkv 701 / 686, 70B qkv 550 / 513, 7B qkv 472 / 535
+//   256 rows: 70B gate_up 1629 / 1775, 70B qkv 898 / 1003, 70B o_proj 1068 / 818
+//   512 rows: 70B down 1476 / 1724, 13B o_proj 888 / 893, 7B o_proj 775 / 710
+//   4096 rows: 70B gate_up 1452 / 1583, 7B o_proj 1275 / 1398, 7B qkv 1390 / 1545
+//   128 rows: 13B qkv 778 / 680, 70B qkv 587 / 513, 7B qkv 488 / 530
 int choose_path(int M, int N, int K, int group) {
   const long long nk = (long long)N * K;
   // (group sizes the decode kernel does not take go to the tensor cores)
   const bool wide = N >= 16384;
-  if ((M <= 16 || (wide && (M <= 24 || (M <= 32 && nk <= (1LL << 28))))) &&
+  if ((M <= 16 || (wide && M <= 24 && nk <= (1LL << 28))) &&
       decode_units(N, K, group) > 0)
     return W4A16_PATH_DECODE;
   const long long pair_ctas = 2LL * ((N + 255) / 256) * ((M + 255) / 256);

@@ -249,8 +249,8 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
 /* Y [M][N] = A [M][K] . dequant(Wq, scales, zeros) with fp32 accumulation.
  * The path and its grid are chosen from M, N, K, the group and the device's
  * SM count, by rules measured on GB300: the decode GEMV for M <= 16 (for
- * layers with N >= 16384 up to 24 rows, and up to 32 rows when N*K <= 2^28,
- * in two passes over the weights), else the tensor-core GEMM, on SM pairs
+ * layers with N >= 16384 and N*K <= 2^28 up to 24 rows, in two passes over
+ * the weights), else the tensor-core GEMM, on SM pairs
  * (W4A16_PATH_TENSOR_PAIR) for M >= 256 when the pairs make at least 80
  * CTAs (2 x ceil(N/256) x ceil(M/256)), on single SMs otherwise; group sizes
  * the decode kernel does not take always go to the tensor cores. `workspace` (256-byte

@@ -242,8 +242,8 @@ def test_path_constants_match_the_header():
 
 def test_plan_follows_the_measured_path_rules(lib):
     """w4a16_plan (host only) reports the paths of the measured dispatch
-    rules: decode up to 16 rows, on wide layers (N >= 16384) up to 24 rows
-    and up to 32 rows for at most 2^28 weights; the CTA-pair kernel from 256
+    rules: decode up to 16 rows, on wide layers (N >= 16384) of at most 2^28
+    weights up to 24 rows; the CTA-pair kernel from 256
     rows where the pairs make at least 80 CTAs; single-SM tensor-core tiles
     otherwise; tensor cores whenever the decode kernel does not take the
     group size."""
@@ -251,12 +251,13 @@ def test_plan_follows_the_measured_path_rules(lib):
         return w4.plan(M, N, K, g)[0]
     assert path(1, 12288, 4096).startswith("decode")
     assert path(16, 4096, 4096).startswith("decode")
-    assert path(32, 22016, 4096).startswith("decode")        # 7B gate_up: two decode passes
-    assert path(32, 27648, 5120).startswith("decode")        # 13B gate_up
-    assert path(24, 57344, 8192).startswith("decode")        # 70B gate_up: up to 24 rows
-    assert path(32, 57344, 8192) == "tensor"                 # above 2^28 weights
+    assert path(24, 22016, 4096).startswith("decode")        # 7B gate_up: two decode passes
+    assert path(24, 27648, 5120).startswith("decode")        # 13B gate_up
+    assert path(25, 27648, 5120) == "tensor"
+    assert path(32, 22016, 4096) == "tensor"
+    assert path(16, 57344, 8192).startswith("decode")        # 70B gate_up
+    assert path(17, 57344, 8192) == "tensor"                 # above 2^28 weights
     assert path(20, 15360, 5120) == "tensor"                 # 13B qkv
-    assert path(33, 22016, 4096) == "tensor"
     assert path(128, 57344, 8192) == "tensor"                # pairs from 256 rows
     assert path(256, 10240, 8192) == "tensor-pair"           # 2 x 40 pair CTAs
     assert path(256, 8192, 8192) == "tensor"                 # 2 x 32: too few

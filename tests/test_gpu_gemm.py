@@ -72,7 +72,8 @@ def test_decode_path_picks_a_variant(M, K, N, group):
                                          (24, 1024, 16384, 128), (32, 512, 16400, 128),
                                          (9, 768, 256, 192)])
 def test_auto_path(M, K, N, group):
-    # (24 and 32 rows of a wide layer: two decode passes; group 192: tensor cores)
+    # (24 rows of a wide layer: two decode passes; 32 rows: tensor cores;
+    # group 192: tensor cores)
     run_and_check(M, K, N, group, seed=M + K + N)
 
 
