@@ -100,13 +100,14 @@ __device__ __forceinline__ void epilogue_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-// SA: atoms (64 k) per pipeline stage, 1, 2 or 4. Larger stages cut the
-// barrier hand-offs per weight byte; SA >= 2 needs K and the group to be
-// multiples of 128 (one scale and zero point per 128 k). NG: dequant groups.
+// SA: atoms (64 k) per pipeline stage, 1 or 2. Larger stages cut the
+// barrier hand-offs per weight byte; SA = 2 needs K and the group to be
+// multiples of 128 (one scale and zero point per stage). NG: dequant groups.
 template <int SA, bool kB, int NG>
 __global__ void __launch_bounds__(Warps<NG>::kThreads, NG == 2 ? 2 : 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const TcParams p) {
+  static_assert(SA == 1 || SA == 2, "stages of one or two 64-k atoms");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -649,7 +650,7 @@ bool tc_config(int M, int K, int group, int out[8]) {
   out[5] = r.groups;
   out[6] = (int)r.smem;
   out[7] = tc_ctas_per_sm(bt);
-  return tc_rings_valid(r) && !(sa == 4 && r.groups != 4);
+  return tc_rings_valid(r);
 }
 
 size_t tc_workspace_bytes(int M, int N, int split) {
@@ -738,7 +739,6 @@ cudaError_t launch_sa(int sa, int ng, const CUtensorMap& tmA, const CUtensorMap&
   if (ng == 2)
     return sa == 2 ? launch_kernel<2, kB, 2>(tmA, tmW, prm, grid, smem, stream)
                    : launch_kernel<1, kB, 2>(tmA, tmW, prm, grid, smem, stream);
-  if (sa == 4) return launch_kernel<4, kB, 4>(tmA, tmW, prm, grid, smem, stream);
   return sa == 2 ? launch_kernel<2, kB, 4>(tmA, tmW, prm, grid, smem, stream)
                  : launch_kernel<1, kB, 4>(tmA, tmW, prm, grid, smem, stream);
 }
@@ -853,7 +853,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, const uint32_t* Wq, const uint16_t
   const dim3 grid((unsigned)((M + bt - 1) / bt), (unsigned)((N + kTileN - 1) / kTileN),
                   (unsigned)prm.split);
   const int ng = rings.groups;
-  if (!tc_rings_valid(rings) || (sa == 4 && ng != 4)) return cudaErrorInvalidValue;
+  if (!tc_rings_valid(rings)) return cudaErrorInvalidValue;
   return bf16 ? launch_sa<true>(sa, ng, tmA, tmW, prm, grid, smem, stream)
               : launch_sa<false>(sa, ng, tmA, tmW, prm, grid, smem, stream);
 }

@@ -41,8 +41,7 @@ def configs():
 def test_token_tile_and_stage_atoms(configs):
     for (M, K, group), c in configs.items():
         assert c["token_tile"] == (256 if M >= 256 else (M + 15) // 16 * 16)
-        want = 2 if K % 128 == 0 and group % 128 == 0 else 1
-        assert c["stage_atoms"] in (want, 4) and (c["stage_atoms"] != 4 or want == 2)
+        assert c["stage_atoms"] == (2 if K % 128 == 0 and group % 128 == 0 else 1)
         assert c["ctas_per_sm"] == (2 if c["token_tile"] <= 64 else 1)
 
 
