@@ -25,8 +25,9 @@ and `roofline_by_bound` both groups.
 
 The end-to-end figure (`e2e`) runs the same step through the public API with
 every step's input copied in from pinned host memory and its result copied
-back, double-buffered on a second stream as a serving loop would (step i
-overlaps step i+1's input copy and step i-1's result copy).
+back, double-buffered on two more streams (one per copy direction) as a
+serving loop would (step i overlaps step i+1's input copy and step i-1's
+result copy).
 
 Under torchrun (WORLD_SIZE > 1) every rank runs its own replica of the
 workload on its own GPU (independent problems, no collective on the data
@@ -616,11 +617,12 @@ def run_ours(args, wl, dist, rank, world, local):
 
     # end to end through the public API: every step's activations copied in
     # from pinned host memory and every step's results read back (weights are
-    # resident model state). The copies are double-buffered on a second
-    # stream, as a serving loop would run them: during step i the next step's
-    # input goes in and the previous step's result comes out, and the timed
-    # region also holds the first step's input copy and the last step's
-    # result copy.
+    # resident model state). The copies are double-buffered on two more
+    # streams, one per direction (host-to-device and device-to-host copies then
+    # run at once: 9.0 against 13.0 ms for 1 GB in and 1.6 GB out on GB300), as
+    # a serving loop would run them: during step i the next step's input goes
+    # in and the previous step's result comes out, and the timed region also
+    # holds the first step's input copy and the last step's result copy.
     a_host = torch.empty_like(a_flat, device="cpu").pin_memory()
     a_host.copy_(a_flat)
     y_host = torch.empty_like(y_flat, device="cpu").pin_memory()
@@ -628,7 +630,7 @@ def run_ours(args, wl, dist, rank, world, local):
     y_flat2, y_views2 = _aligned_views(torch, [(c.M, c.N) for c in cases], y_flat.dtype, device)
     a_bufs, y_bufs = (a_flat, a_flat2), (y_flat, y_flat2)
     a_sets, y_sets = (a_views, a_views2), (y_views, y_views2)
-    io = torch.cuda.Stream(device)
+    io_in, io_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     e2e_graphs = {}
     for b in (0, 1):
         for ri, r in enumerate(rot):
@@ -636,16 +638,20 @@ def run_ours(args, wl, dist, rank, world, local):
             with torch.cuda.graph(g, stream=stream):
                 fork = torch.cuda.Event()
                 fork.record(stream)
-                io.wait_event(fork)
-                with torch.cuda.stream(io):
+                io_in.wait_event(fork)
+                io_out.wait_event(fork)
+                with torch.cuda.stream(io_in):
                     a_bufs[1 - b].copy_(a_host, non_blocking=True)   # the next step's input
+                with torch.cuda.stream(io_out):
                     y_host.copy_(y_bufs[1 - b], non_blocking=True)   # the previous step's result
-                join = torch.cuda.Event()
-                join.record(io)
+                join_in, join_out = torch.cuda.Event(), torch.cuda.Event()
+                join_in.record(io_in)
+                join_out.record(io_out)
                 for c, A, Y in zip(cases, a_sets[b], y_sets[b]):
                     w4.gemm(A, r[c.key], out=Y, workspace=r["workspace"], static_weights=True,
                             **GEMM_KW)
-                stream.wait_event(join)
+                stream.wait_event(join_in)
+                stream.wait_event(join_out)
             e2e_graphs[(b, ri)] = g
 
     def time_e2e(steps):
@@ -689,8 +695,8 @@ def run_ours(args, wl, dist, rank, world, local):
         "roofline": roofline,
         "roofline_by_bound": groups,
         "e2e": {"value": e2e_value, "unit": unit,
-                "copies": "double-buffered on a second stream: step i overlaps the input copy "
-                          "of step i+1 and the result copy of step i-1",
+                "copies": "double-buffered on one stream per direction: step i overlaps the "
+                          "input copy of step i+1 and the result copy of step i-1",
                 "h2d_bytes_per_step": sum(2 * c.M * c.K for c in cases),
                 "d2h_bytes_per_step": sum(2 * c.M * c.N for c in cases)},
         "gpu_launches": launches,
