@@ -42,6 +42,17 @@ def expected(A64, q, s, z, group, bf16, silu, a8):
 def test_flag_combinations(path, M, K, N, group, bf16, silu, a8):
     if path == "tensor" and M < 17:
         M += 16  # the tensor path is for more than 16 rows
+    check_flags(path, M, K, N, group, bf16, silu, a8)
+
+
+@pytest.mark.parametrize("bf16,silu,a8", list(itertools.product([False, True], repeat=3)))
+def test_flag_combinations_persistent_pairs(bf16, silu, a8):
+    """The CTA-pair kernel with more tiles than resident clusters (9 token
+    tiles x 13 column pairs), so that clusters take several tiles in turn."""
+    check_flags("tensor-pair", 2304, 128, 3328, 128, bf16, silu, a8)
+
+
+def check_flags(path, M, K, N, group, bf16, silu, a8):
     W = synthetic.small_weights(K, N, seed=M + K + N)
     (q, s, z), pw = prepare(W, group)
     A = synthetic.small_activations(M, K, seed=M * K)

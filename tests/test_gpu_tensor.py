@@ -116,6 +116,11 @@ PAIR_CASES = [
     (700, 2048, 272, 2048),
     (1024, 1088, 512, 64),   # K not a multiple of 128
     (4096, 512, 768, 128),
+    # persistent clusters (76 on GB300) taking several tiles each
+    (4000, 128, 2000, 128),  # 128 tiles; ragged last token tile and column pair
+    (2304, 64, 4096, 64),    # one stage per tile: the accumulator changes hands every stage
+    (1500, 192, 3104, 64),   # 78 tiles: two clusters take a second tile; the last pair has 32 columns
+    (8192, 128, 4096, 128),  # about seven tiles per cluster
 ]
 
 
