@@ -93,6 +93,10 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 //   512 rows: 70B down 1476 / 1724, 13B o_proj 888 / 893, 7B o_proj 775 / 710
 //   4096 rows: 70B gate_up 1452 / 1583, 7B o_proj 1275 / 1398, 7B qkv 1390 / 1545
 //   128 rows: 13B qkv 778 / 680, 70B qkv 587 / 513, 7B qkv 488 / 530
+// and, on wide layers of at most 2^28 weights, from 65 to 128 rows (us, one
+// SM / pair): 7B gate_up 80 rows 45.4 / 41.6, 128 rows 47.7 / 41.8; 13B
+// gate_up 80 rows 53.2 / 51.1, 128 rows 55.7 / 51.2; 70B gate_up (above 2^28)
+// 128 rows 114.0 / 118.3; 13B qkv (narrower) 128 rows 25.7 / 29.4
 int choose_path(int M, int N, int K, int group) {
   const long long nk = (long long)N * K;
   // (group sizes the decode kernel does not take go to the tensor cores)
@@ -102,6 +106,8 @@ int choose_path(int M, int N, int K, int group) {
     return W4A16_PATH_DECODE;
   const long long pair_ctas = 2LL * ((N + 255) / 256) * ((M + 255) / 256);
   if (M >= 256 && pair_ctas >= 80) return W4A16_PATH_TENSOR_PAIR;
+  // wide layers of at most 2^28 weights at 65-128 rows: pairs of 128-token tiles
+  if (M > 64 && M <= 128 && wide && nk <= (1LL << 28)) return W4A16_PATH_TENSOR_PAIR;
   return W4A16_PATH_TENSOR;
 }
 

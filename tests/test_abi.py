@@ -243,7 +243,8 @@ def test_path_constants_match_the_header():
 def test_plan_follows_the_measured_path_rules(lib):
     """w4a16_plan (host only) reports the paths of the measured dispatch
     rules: decode up to 16 rows, on wide layers (N >= 16384) of at most 2^28
-    weights up to 24 rows; the CTA-pair kernel from 256
+    weights up to 24 rows; the CTA-pair kernel on such wide layers at 65-128
+    rows and from 256
     rows where the pairs make at least 80 CTAs; single-SM tensor-core tiles
     otherwise; tensor cores whenever the decode kernel does not take the
     group size."""
@@ -258,7 +259,12 @@ def test_plan_follows_the_measured_path_rules(lib):
     assert path(16, 57344, 8192).startswith("decode")        # 70B gate_up
     assert path(17, 57344, 8192) == "tensor"                 # above 2^28 weights
     assert path(20, 15360, 5120) == "tensor"                 # 13B qkv
-    assert path(128, 57344, 8192) == "tensor"                # pairs from 256 rows
+    assert path(128, 57344, 8192) == "tensor"                # above 2^28 weights: one SM
+    assert path(128, 22016, 4096) == "tensor-pair"           # 7B gate_up, 65-128 rows
+    assert path(65, 27648, 5120) == "tensor-pair"            # 13B gate_up
+    assert path(64, 27648, 5120) == "tensor"
+    assert path(128, 15360, 5120) == "tensor"                # narrower than 16384
+    assert path(129, 22016, 4096) == "tensor"                # pairs again from 256 rows
     assert path(256, 10240, 8192) == "tensor-pair"           # 2 x 40 pair CTAs
     assert path(256, 8192, 8192) == "tensor"                 # 2 x 32: too few
     assert path(512, 4096, 11008) == "tensor"                # 2 x 16 x 2
