@@ -96,7 +96,9 @@ int decode_ctas(int M, int N, int K, int group, int requested) {
 // and, on wide layers of at most 2^28 weights, from 65 to 128 rows (us, one
 // SM / pair): 7B gate_up 80 rows 45.4 / 41.6, 128 rows 47.7 / 41.8; 13B
 // gate_up 80 rows 53.2 / 51.1, 128 rows 55.7 / 51.2; 70B gate_up (above 2^28)
-// 128 rows 114.0 / 118.3; 13B qkv (narrower) 128 rows 25.7 / 29.4
+// 128 rows 114.0 / 118.3; 13B qkv (narrower) 128 rows 25.7 / 29.4; and on
+// wide layers from 193 to 255 rows: 7B gate_up 208 rows 48.6 / 44.5, 13B
+// gate_up 224 rows 60.0 / 54.6, 70B gate_up 240 rows 147.7 / 137.6
 int choose_path(int M, int N, int K, int group) {
   const long long nk = (long long)N * K;
   // (group sizes the decode kernel does not take go to the tensor cores)
@@ -108,6 +110,9 @@ int choose_path(int M, int N, int K, int group) {
   if (M >= 256 && pair_ctas >= 80) return W4A16_PATH_TENSOR_PAIR;
   // wide layers of at most 2^28 weights at 65-128 rows: pairs of 128-token tiles
   if (M > 64 && M <= 128 && wide && nk <= (1LL << 28)) return W4A16_PATH_TENSOR_PAIR;
+  // wide layers at 193-255 rows, where the one-SM kernel's 208-256-token
+  // tiles leave room for two dequant groups only
+  if (M > 192 && M < 256 && wide) return W4A16_PATH_TENSOR_PAIR;
   return W4A16_PATH_TENSOR;
 }
 

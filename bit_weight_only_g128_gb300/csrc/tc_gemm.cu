@@ -614,6 +614,14 @@ TcRings tc_rings(int bt, int sa) {
   const size_t act_slot = (size_t)sa * bt * 128;
   const size_t code_slot = (size_t)sa * kCodeAtomBytes;
   int act = (int)((budget - (size_t)r.code * code_slot) / act_slot);
+  // one CTA per SM: a shorter code ring (down to 4 slots) where it buys the
+  // fourth activation slot, and with it four dequant groups instead of two
+  // (176-token tiles: 5-18% faster on the Llama layers)
+  while (!two && act < 4 && r.code > 4 &&
+         (int)((budget - (size_t)(r.code / 2) * code_slot) / act_slot) >= 4) {
+    r.code /= 2;
+    act = (int)((budget - (size_t)r.code * code_slot) / act_slot);
+  }
   r.act = act > 16 / sa ? 16 / sa : act;
   r.groups = !two && r.act >= 4 ? 4 : 2;
   r.tmem_cols = two ? 256 : 512;

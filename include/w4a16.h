@@ -252,8 +252,9 @@ int w4a16_workspace_size_ex(int M, int N, int K, int group, int path, int parts,
  * layers with N >= 16384 and N*K <= 2^28 up to 24 rows, in two passes over
  * the weights), else the tensor-core GEMM, on SM pairs
  * (W4A16_PATH_TENSOR_PAIR) for M >= 256 when the pairs make at least 80
- * CTAs (2 x ceil(N/256) x ceil(M/256)) and for 64 < M <= 128 on layers with
- * N >= 16384 and N*K <= 2^28, on single SMs otherwise; group sizes
+ * CTAs (2 x ceil(N/256) x ceil(M/256)), for 64 < M <= 128 on layers with
+ * N >= 16384 and N*K <= 2^28, and for 192 < M < 256 on layers with
+ * N >= 16384, on single SMs otherwise; group sizes
  * the decode kernel does not take always go to the tensor cores. `workspace` (256-byte
  * aligned, zero-filled before first use) may be NULL when
  * w4a16_workspace_size reports 0; W4A16_ERR_WORKSPACE_TOO_SMALL otherwise.

@@ -244,7 +244,7 @@ def test_plan_follows_the_measured_path_rules(lib):
     """w4a16_plan (host only) reports the paths of the measured dispatch
     rules: decode up to 16 rows, on wide layers (N >= 16384) of at most 2^28
     weights up to 24 rows; the CTA-pair kernel on such wide layers at 65-128
-    rows and from 256
+    rows, on every wide layer at 193-255 rows, and from 256
     rows where the pairs make at least 80 CTAs; single-SM tensor-core tiles
     otherwise; tensor cores whenever the decode kernel does not take the
     group size."""
@@ -264,7 +264,11 @@ def test_plan_follows_the_measured_path_rules(lib):
     assert path(65, 27648, 5120) == "tensor-pair"            # 13B gate_up
     assert path(64, 27648, 5120) == "tensor"
     assert path(128, 15360, 5120) == "tensor"                # narrower than 16384
-    assert path(129, 22016, 4096) == "tensor"                # pairs again from 256 rows
+    assert path(129, 22016, 4096) == "tensor"
+    assert path(192, 22016, 4096) == "tensor"
+    assert path(193, 22016, 4096) == "tensor-pair"           # wide layers, 193-255 rows
+    assert path(255, 57344, 8192) == "tensor-pair"
+    assert path(224, 15360, 5120) == "tensor"                # narrower than 16384
     assert path(256, 10240, 8192) == "tensor-pair"           # 2 x 40 pair CTAs
     assert path(256, 8192, 8192) == "tensor"                 # 2 x 32: too few
     assert path(512, 4096, 11008) == "tensor"                # 2 x 16 x 2
